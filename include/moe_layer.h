@@ -1,0 +1,251 @@
+/*
+ * moe_layer.h -- C ABI of the GB300 fused MoE expert layer (libmoe_layer.so).
+ *
+ * The layer is six calls issued in order on one CUDA stream:
+ *
+ *   moe_topk_route -> moe_permute_align -> moe_gemm1_swiglu
+ *     -> (optional) mxfp8_quantize_block32 -> moe_gemm2
+ *     -> moe_unpermute_topk_reduce | moe_batched_weight_reduce
+ *
+ * following the decomposition of the vLLM design doc "Fused MoE Modular
+ * Kernel", section "apply()": Permute, Matmul with W1, Act + Mul,
+ * Quantisation, Matmul with W2, Unpermute, TopK weight application + reduce.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every array argument is a DEVICE pointer to caller-owned memory.  The
+ *   library never allocates, frees or synchronises; it only launches kernels
+ *   on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
+ *   stream).  All calls are asynchronous.
+ * - Matrices are row-major and dense (the last index is contiguous).
+ * - Element types: MOE_F32 (binary32), MOE_BF16 (bfloat16), MOE_E4M3
+ *   (OCP E4M3FN codes, one byte each, always paired with one E8M0 scale byte
+ *   per 32 consecutive elements along the contraction dimension).
+ * - Expert ids are int32; -1 marks a padding slot that every step skips
+ *   (transformers PR 49606 analysis "DeepGEMM Mega MoE as an EP
+ *   implementation", section 2: padded slots carry expert id -1, weight 0).
+ * - Return value: MOE_OK, or an error status found on the host before any
+ *   launch (nothing is launched then).  moe_last_error() gives a message for
+ *   the calling thread's last failure.
+ * - Errors that depend on device data never trap.  Kernels OR bits into
+ *   *err_word (a device int32 the caller zeroes and reads when it likes;
+ *   err_word may be NULL where documented): MOE_DEVERR_ID_RANGE for an id
+ *   outside [-1, E), MOE_DEVERR_CAPACITY for a batched expert over capacity,
+ *   MOE_DEVERR_TIMEOUT when a pipeline wait inside a GEMM gave up (the
+ *   kernel then returns early and its outputs are unspecified).
+ * - Sizes are int64 where they can exceed 2^31 elements.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (host) ---- */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1         /* null pointer, bad size or enum */
+#define MOE_ERR_UNSUPPORTED 2         /* dtype/layout combination, or no sm_103a device */
+#define MOE_ERR_ALIGNMENT 3           /* pointer or row pitch not 16-byte aligned, or a size not a multiple of 32 */
+#define MOE_ERR_WORKSPACE_TOO_SMALL 4
+#define MOE_ERR_LAUNCH 5              /* a CUDA runtime call failed */
+
+/* ---- device error bits (OR-ed into *err_word) ---- */
+#define MOE_DEVERR_ID_RANGE 1
+#define MOE_DEVERR_CAPACITY 2
+#define MOE_DEVERR_TIMEOUT 4
+
+/* ---- element types ---- */
+#define MOE_F32 0
+#define MOE_BF16 1
+#define MOE_E4M3 2
+
+/* ---- activation layouts ("Fused MoE Modular Kernel", Introduction) ---- */
+#define MOE_LAYOUT_CONTIGUOUS 0       /* (M, K) rows grouped by expert */
+#define MOE_LAYOUT_BATCHED 1          /* (E, max_tokens, K) + expert_num_tokens[E] */
+
+/* ---- W1 row layouts ---- */
+#define MOE_W1_GATE_UP 0              /* W1[e] = [gate rows 0..I-1 ; up rows 0..I-1] */
+#define MOE_W1_INTERLEAVE16 1         /* rows in groups of 32: 16 gate rows then the 16 matching up rows
+                                         ("Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2,
+                                         _interleave_gate_up_16 "After") */
+
+/* ---- GEMM implementations ---- */
+#define MOE_IMPL_AUTO 0               /* tcgen05 tiles; swap-AB when routes/expert are few; SIMT for fp32 */
+#define MOE_IMPL_TCGEN05 1            /* tcgen05 tiles, tokens on the MMA M side (128 rows per tile) */
+#define MOE_IMPL_TCGEN05_SWAP_AB 2    /* tcgen05 tiles, weight rows on the MMA M side, tokens on N
+                                         (AWS blog "MoE kernel engineering on SageMaker AI", Swap-AB:
+                                         C^T = B^T A^T when M < 64) */
+#define MOE_IMPL_SIMT 3               /* CUDA-core FMA tiles (fp32 path, any shape) */
+
+/* Message describing the calling thread's last failed call ("" if none). */
+MOE_API const char* moe_last_error(void);
+
+/* Library version, (major << 16) | minor. */
+MOE_API int moe_version(void);
+
+/* Upper bound on the rows of the contiguous layout:
+ * T*top_k + E*(block_m - 1) = max over routings of sum_e ceil(count_e/block_m)*block_m. */
+MOE_API int64_t moe_max_padded_rows(int64_t T, int top_k, int E, int block_m);
+
+/* Bytes of scratch moe_permute_align needs for T tokens, top_k slots, E experts
+ * (the two workspaces declared up front in "Fused MoE Modular Kernel",
+ * workspace_shapes()). */
+MOE_API size_t moe_permute_workspace_size(int64_t T, int top_k, int E);
+
+/*
+ * moe_topk_route -- per token, the top_k largest of E router logits and their
+ * weights.  The weights are softmax over all E, restricted to the chosen
+ * experts and renormalised to sum 1 (renormalize != 0), or the plain softmax
+ * probabilities (renormalize == 0).  Selection compares the fp32 logits
+ * (softmax is monotone); ties go to the lower expert index.
+ * ("Fused MoE Modular Kernel", How-To: select_experts and the TopK ids dtype.)
+ *
+ *   logits        (T, E) fp32
+ *   topk_ids      (T, top_k) int32 out, in decreasing logit order
+ *   topk_weights  (T, top_k) fp32 out
+ * Limits: 1 <= top_k <= min(E, 32), E <= 1024.  T may be 0 (no launch).
+ */
+MOE_API int moe_topk_route(const float* logits, int64_t T, int E, int top_k, int renormalize,
+                   int32_t* topk_ids, float* topk_weights, void* stream);
+
+/*
+ * moe_permute_align -- groups the routes r = t*top_k + j into expert-major
+ * rows ("Fused MoE Modular Kernel", apply(): Permute; Introduction: the
+ * Contiguous and Batched formats).  Within an expert, rows follow increasing
+ * route index (a stable order), so the result is unique.
+ *
+ *   topk_ids        (T, top_k) int32; -1 = padding, skipped; other ids
+ *                   outside [0, E) set MOE_DEVERR_ID_RANGE and are skipped.
+ *   layout          MOE_LAYOUT_CONTIGUOUS:
+ *                     expert_counts[e]   = routes of expert e
+ *                     expert_offsets[e]  = sum_{e'<e} ceil(count_e'/block_m)*block_m, E+1 entries
+ *                     row_route[s]       = the route in row s, -1 in padding rows; rows_cap entries,
+ *                                          entries at and beyond expert_offsets[E] are not written
+ *                     rows_cap >= moe_max_padded_rows(T, top_k, E, block_m)
+ *                   MOE_LAYOUT_BATCHED (rows (e, q) at e*max_tokens + q):
+ *                     expert_counts[e]   = expert_num_tokens[e] = min(count_e, max_tokens);
+ *                                          routes beyond max_tokens are dropped and set
+ *                                          MOE_DEVERR_CAPACITY
+ *                     expert_offsets[e]  = e*max_tokens, E+1 entries
+ *                     row_route[s]       = route or -1, all E*max_tokens entries written
+ *                     rows_cap == E*max_tokens; block_m is ignored
+ *   route_row       (T*top_k) int32 out: the row of each route, -1 for skipped ones
+ *   x, x_dtype, K   optional (x may be NULL): (T, K) activations (F32 or BF16) to
+ *                   gather into x_out (rows_cap, K); rows holding no route are not written.
+ *                   K*element size must be a multiple of 16 bytes.
+ *   workspace       >= moe_permute_workspace_size(T, top_k, E) bytes, 256-byte aligned;
+ *                   its contents on entry do not matter.
+ *   err_word        device int32, may be NULL.
+ */
+MOE_API int moe_permute_align(const int32_t* topk_ids, int64_t T, int top_k, int E,
+                      int layout, int block_m, int max_tokens,
+                      const void* x, int x_dtype, int64_t K, void* x_out, int64_t rows_cap,
+                      int32_t* expert_counts, int32_t* expert_offsets,
+                      int32_t* row_route, int32_t* route_row,
+                      void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream);
+
+/*
+ * moe_gemm1_swiglu -- grouped GEMM with W1 fused with SiLU-and-mul
+ * ("Fused MoE Modular Kernel", apply(): Matmul with W1, Act + Mul).
+ * For every valid row s of expert e:
+ *     g_i = sum_k a[s,k] W1[e, gate_row(i), k],  u_i likewise with up_row(i),
+ *     h[s, i] = silu(g_i) * u_i = g_i / (1 + exp(-g_i)) * u_i,   i < I.
+ *
+ *   a             rows of activations, element type a_dtype (F32 or BF16)
+ *                   contiguous: (rows_cap, K); expert e owns rows
+ *                     [expert_offsets[e], expert_offsets[e] + expert_counts[e])
+ *                   batched: (E, max_tokens, K); expert e owns rows [0, expert_counts[e])
+ *   w1            (E, 2I, K) of w_dtype (F32, BF16 or E4M3); rows per w1_layout
+ *   w1_scale      (E, 2I, K/32) E8M0 bytes when w_dtype == MOE_E4M3, else NULL
+ *   h             same row indexing as `a`, (rows, I) of h_dtype (F32 or BF16);
+ *                 only valid rows are written.
+ *   impl          MOE_IMPL_*; the tcgen05 paths need BF16 activations, BF16 or E4M3
+ *                 weights, K % 64 == 0 and I % 64 == 0 (MOE_ERR_UNSUPPORTED otherwise).
+ * Counts and offsets stay on the device: the call needs no host synchronisation.
+ */
+MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, int layout,
+                     const int32_t* expert_counts, const int32_t* expert_offsets,
+                     int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
+                     const void* w1, const uint8_t* w1_scale, int w_dtype, int w1_layout,
+                     int impl, void* h, int h_dtype, int32_t* err_word, void* stream);
+
+/*
+ * moe_gemm2 -- grouped GEMM with W2 ("Fused MoE Modular Kernel", apply():
+ * Matmul with W2), whose epilogue multiplies by the route weight (optional)
+ * and writes each result straight to its (token, top-k slot) row ("Cake
+ * MegaMoE EP16" FlashInfer PR 5148 analysis, section 3: FC2 results returned
+ * directly to the source (token, top-k slot) buffer).
+ * For every valid row s of expert e:  y_s[n] = w * sum_i h[s,i] W2[e, n, i],  n < K.
+ *
+ *   h             (rows, I) of h_dtype (BF16, or F32 for the SIMT path), row indexing as
+ *                 in moe_gemm1_swiglu
+ *   w2            (E, K, I) of w_dtype; w2_scale (E, K, I/32) E8M0 for E4M3, else NULL
+ *   contiguous:   row s goes to y[row_route[s]] (rows with row_route -1 are skipped);
+ *                 y is (y_rows, K) with y_rows = T*top_k; route_weights, if not NULL,
+ *                 is (T*top_k) fp32 indexed by route.
+ *   batched:      row s goes to y[s]; y is (E*max_tokens, K); route_weights, if not
+ *                 NULL, is (E*max_tokens) indexed by row; row_route may be NULL.
+ *   y             y_dtype F32 or BF16.
+ */
+MOE_API int moe_gemm2(const void* h, int h_dtype, int layout,
+              const int32_t* expert_counts, const int32_t* expert_offsets,
+              int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
+              const void* w2, const uint8_t* w2_scale, int w_dtype,
+              const int32_t* row_route, const float* route_weights,
+              int impl, void* y, int y_dtype, int64_t y_rows, int32_t* err_word, void* stream);
+
+/*
+ * moe_unpermute_topk_reduce -- ordered TopK weight-and-reduce
+ * ("Fused MoE Modular Kernel", TopKWeightAndReduce, Contiguous; "Cake
+ * MegaMoE EP16" analysis, section 4: a separate ordered Top-K reduce kernel).
+ *     out[t, n] = sum_{j = 0..top_k-1, 0 <= topk_ids[t,j] < E} w[t,j] * y[t*top_k + j, n]
+ * summed in fp32 in increasing j (run-to-run bit-identical); w = 1 when
+ * topk_weights is NULL (weights already applied by moe_gemm2).  A token with
+ * no valid slot gets +0.0.
+ *   y    (T*top_k, K) of y_dtype (F32 or BF16); out (T, K) of out_dtype (F32 or BF16).
+ *   K*element size must be a multiple of 16 bytes.
+ */
+MOE_API int moe_unpermute_topk_reduce(const void* y, int y_dtype, const int32_t* topk_ids, const float* topk_weights,
+                              int64_t T, int top_k, int E, int64_t K, void* out, int out_dtype, void* stream);
+
+/*
+ * moe_batched_weight_reduce -- naive-batched weight application
+ * ("Fused MoE Modular Kernel", TopKWeightAndReduce, NaiveBatched), read as a
+ * per-row weight in place of the batched layout:
+ *     out[e, q, :] = w[e, q] * y[e, q, :]   for q < expert_num_tokens[e]
+ * (w = 1 when row_weights is NULL).  Rows q >= expert_num_tokens[e] are
+ * neither read nor written.  y, out: (E, max_tokens, K); out may equal y.
+ */
+MOE_API int moe_batched_weight_reduce(const void* y, int y_dtype, const int32_t* expert_num_tokens,
+                              const float* row_weights, int E, int max_tokens, int64_t K,
+                              void* out, int out_dtype, void* stream);
+
+/*
+ * mxfp8_quantize_block32 -- MXFP8 block-32 quantisation along rows
+ * ("Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2,
+ * _quantize_mxfp8_block32 "After").  For each block of 32 consecutive
+ * elements of a row with m = max |x|:
+ *     code  = 0 if m == 0, else clamp(ceil(log2(m/448)) + 127, 0, 254)
+ *     q[i]  = E4M3(x[i] / 2^(code-127)), round to nearest even, saturating, sign kept.
+ *   x       (rows, cols) F32 or BF16; cols % 32 == 0
+ *   codes   (rows, cols) uint8 out;  scales (rows, cols/32) uint8 out.
+ * The codes and scales are exact (they depend on no rounding order).
+ */
+MOE_API int mxfp8_quantize_block32(const void* x, int x_dtype, int64_t rows, int64_t cols,
+                           uint8_t* codes, uint8_t* scales, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYER_H */

@@ -1,0 +1,519 @@
+// tcgen05 grouped GEMMs for sm_103a: persistent, warp-specialised CTAs
+// (one per SM).
+//
+//   warp 0      TMA producer: one thread streams 64-wide k-blocks of the A and
+//               B tiles into a 4-stage shared-memory ring (128-byte swizzle),
+//               completing a "full" mbarrier per stage.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (kind::f16, bf16 in,
+//               fp32 accumulate) into one of two TMEM accumulators and frees
+//               each stage with tcgen05.commit on its "empty" mbarrier.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//               32*(w%4)...), apply SiLU-and-mul (GEMM 1) or route weight +
+//               scatter to the (token, slot) row (GEMM 2), store to global.
+// The two accumulators let the epilogue of one tile overlap the MMAs of the
+// next.  Tiles are listed per expert on the device (ExpertTable).
+//
+// Normal tiles (tokens on the MMA M side): 128 token rows x 256 weight rows.
+//   GEMM 1: the 256 weight rows are 128 units as [gate16, up16] x 8, so each
+//   epilogue thread holds matching gate and up columns side by side.  The
+//   [gate; up] W1 layout is read through a 5-D tensor map (k, 16, 2, I/16, E)
+//   that produces this order; the interleave-16 layout is read as stored.
+// Swap-AB tiles (AWS "MoE kernel engineering on SageMaker AI", Swap-AB:
+//   C^T = B^T A^T when tokens per expert are few): 128 weight rows on M and
+//   the expert's tokens (up to 256, loaded as 16-row boxes) on N, so a weight
+//   tile is read once for all of the expert's tokens.  Weight loads carry an
+//   L2 evict-first hint (the weights are streamed once).
+//
+// Every mbarrier wait is bounded (2 s of globaltimer); on expiry the kernel
+// records MOE_DEVERR_TIMEOUT, lets its copies in flight land, frees TMEM and
+// returns.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;           // MMA M
+constexpr int BK = 64;            // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_ROWS = 256;
+constexpr int B_BYTES = B_ROWS * BK * 2;    // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 512;
+constexpr int kThreads = 192;
+constexpr int TOK_BOX = 16;                 // swap-AB token rows per TMA box
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct __align__(8) Ctrl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile int abort;
+};
+
+struct TcParams {
+    int gemm;            // 1 or 2
+    int swap;            // 0 normal, 1 swap-AB
+    int layout;
+    int E;
+    int max_tokens;
+    int64_t rows_cap;
+    int nkb;             // k-blocks per tile
+    int nt;              // normal: n-tiles per m-tile; swap: weight blocks per expert
+    int w_mode;          // weights map: 0 = 3-D (k, rows, E), 1 = 5-D gate/up interleaving view
+    int64_t I, K;
+    const int32_t* counts;
+    const int32_t* offsets;
+    const int32_t* row_route;
+    const float* route_w;
+    void* out;
+    int out_dtype;
+    int64_t out_rows;    // GEMM 2, contiguous: rows of y (routes)
+    int32_t* err_word;
+};
+
+MOE_DEVICE bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl& c, int32_t* err_word) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t deadline = ptx::globaltimer() + kWaitNs;
+    if (ptx::mbar_wait_bounded(bar, parity, deadline, &c.abort)) return true;
+    if (!c.abort) {
+        c.abort = 1;
+        report(err_word, MOE_DEVERR_TIMEOUT);
+    }
+    return false;
+}
+
+// Tile -> (expert, rows, n-tile / weight block, tokens) decoding, shared by all roles.
+struct Tile {
+    int e;
+    int64_t row0;     // first activation row of the tile
+    int rows;         // valid activation rows (normal: <= 128; swap: tokens <= 256)
+    int nb;           // normal: n-tile; swap: weight block
+};
+
+MOE_DEVICE Tile decode_tile(const ExpertTable& tab, const TcParams& p, int32_t t) {
+    Tile tl;
+    tl.e = find_expert(tab, p.E, t);
+    const int32_t local = t - tiles_before(tab, tl.e);
+    const int32_t seg = local / p.nt;
+    tl.nb = local - seg * p.nt;
+    const int span = p.swap ? 256 : BM;
+    tl.row0 = int64_t(tab.start[tl.e]) + int64_t(seg) * span;
+    tl.rows = min(span, tab.count[tl.e] - seg * span);
+    return tl;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
+                   const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ ExpertTable tab;
+    __shared__ Ctrl ctrl;
+
+    // 1024-byte aligned stage buffers (the 128-byte swizzle pattern repeats every 1024 bytes)
+    const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&ctrl.full[s], 1);
+            ptx::mbar_init(&ctrl.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&ctrl.acc_full[b], 1);
+            ptx::mbar_init(&ctrl.acc_empty[b], 4);
+        }
+        ptx::mbar_init(&ctrl.drain, 1);
+        ctrl.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tm_act);
+        ptx::prefetch_tmap(&tm_w);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&ctrl.tmem_base, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    const int span = p.swap ? 256 : BM;
+    const int ntl = p.nt;
+    build_expert_table(tab, p.E, p.counts, p.offsets, p.max_tokens, p.rows_cap,
+                       [span, ntl](int32_t c) { return ((c + span - 1) / span) * ntl; });
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = ctrl.tmem_base;
+    const int32_t total = tab.total;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_a = ptx::policy_evict_last();
+            uint32_t it = 0;
+            for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
+                const Tile tl = decode_tile(tab, p, t);
+                const int nbox = p.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
+                const uint32_t bytes = p.swap ? uint32_t(A_BYTES + nbox * TOK_BOX * BK * 2) : uint32_t(STAGE_BYTES);
+                for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!wait_bar(&ctrl.empty[s], ph ^ 1, ctrl, p.err_word)) break;
+                    uint8_t* sa = smem + s * STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    ptx::mbar_arrive_expect_tx(&ctrl.full[s], bytes);
+                    const int k0 = kb * BK;
+                    // weights: normal -> B operand (256 rows); swap -> A operand (128 rows)
+                    uint8_t* wdst = p.swap ? sa : sb;
+                    const int wrows = p.swap ? 128 : 256;
+                    const int row_w = tl.nb * wrows;          // first weight row (interleaved order)
+                    if (p.w_mode == 1)
+                        ptx::tma_load_5d(wdst, &tm_w, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_w);
+                    else
+                        ptx::tma_load_3d(wdst, &tm_w, &ctrl.full[s], k0, row_w, tl.e, pol_w);
+                    if (p.swap) {
+                        for (int b = 0; b < nbox; ++b)
+                            ptx::tma_load_2d(sb + b * TOK_BOX * BK * 2, &tm_act, &ctrl.full[s], k0,
+                                             int32_t(tl.row0 + b * TOK_BOX), pol_a);
+                    } else {
+                        ptx::tma_load_2d(sa, &tm_act, &ctrl.full[s], k0, int32_t(tl.row0), pol_a);
+                    }
+                }
+            }
+            // let every copy issued so far land before the CTA can exit
+            const uint32_t issued = it;
+            for (uint32_t j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
+                const int s = j % STAGES;
+                const uint64_t deadline = ptx::globaltimer() + kWaitNs / 4;
+                volatile int never = 0;
+                ptx::mbar_wait_bounded(&ctrl.full[s], (j / STAGES) & 1, deadline, &never);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, tc = 0;
+            for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x, ++tc) {
+                const Tile tl = decode_tile(tab, p, t);
+                const int buf = tc & 1;
+                const uint32_t aph = (tc >> 1) & 1;
+                if (!wait_bar(&ctrl.acc_empty[buf], aph ^ 1, ctrl, p.err_word)) break;
+                ptx::tc_fence_after();
+                int n_mma = 256;
+                if (p.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
+                const uint32_t idesc = ptx::idesc_bf16(BM, n_mma);
+                const uint32_t d_tmem = tmem_base + uint32_t(buf * ACC_COLS);
+                bool ok = true;
+                for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
+                        const uint64_t bd = ptx::smem_desc_sw128(sb + kk * UMMA_K * 2);
+                        ptx::mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                    }
+                    ptx::mma_commit(&ctrl.empty[s]);
+                }
+                if (!ok) break;
+                ptx::mma_commit(&ctrl.acc_full[buf]);
+            }
+            // all MMAs issued by this thread complete before TMEM is released
+            ptx::mma_commit(&ctrl.drain);
+            const uint64_t deadline = ptx::globaltimer() + kWaitNs / 4;
+            volatile int never = 0;
+            ptx::mbar_wait_bounded(&ctrl.drain, 0, deadline, &never);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const uint32_t lane_base = uint32_t(q * 32) << 16;
+        uint32_t tc = 0;
+        for (int32_t t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            const Tile tl = decode_tile(tab, p, t);
+            const int buf = tc & 1;
+            const uint32_t aph = (tc >> 1) & 1;
+            if (!wait_bar(&ctrl.acc_full[buf], aph, ctrl, p.err_word)) break;
+            ptx::tc_fence_after();
+            const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * ACC_COLS);
+            if (!p.swap) {
+                const int r = q * 32 + lane;                  // tile row of this thread
+                const bool valid = r < tl.rows;
+                const int64_t row = tl.row0 + r;
+                if (p.gemm == 1) {
+                    uint16_t* h = static_cast<uint16_t*>(p.out);
+#pragma unroll 1
+                    for (int c = 0; c < ACC_COLS / 32; ++c) {
+                        uint32_t v[32];
+                        ptx::tmem_ld_32x32b_x32(tacc + c * 32, v);
+                        ptx::tmem_ld_wait();
+                        if (valid) {
+                            uint32_t o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float h0 = silu_mul(__uint_as_float(v[2 * i]), __uint_as_float(v[16 + 2 * i]));
+                                const float h1 =
+                                    silu_mul(__uint_as_float(v[2 * i + 1]), __uint_as_float(v[16 + 2 * i + 1]));
+                                o[i] = pack_bf16x2(h0, h1);
+                            }
+                            const int64_t unit = int64_t(tl.nb) * 128 + c * 16;
+                            uint4* dst = reinterpret_cast<uint4*>(h + row * p.I + unit);
+                            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                        }
+                    }
+                } else {
+                    int64_t dst_row = -1;
+                    float wt = 1.f;
+                    if (valid) {
+                        if (p.layout == MOE_LAYOUT_CONTIGUOUS) {
+                            const int32_t route = p.row_route[row];
+                            if (route >= 0 && route < p.out_rows) {
+                                dst_row = route;
+                                if (p.route_w) wt = p.route_w[route];
+                            }
+                        } else {
+                            dst_row = row;
+                            if (p.route_w) wt = p.route_w[row];
+                        }
+                    }
+#pragma unroll 1
+                    for (int c = 0; c < ACC_COLS / 32; ++c) {
+                        uint32_t v[32];
+                        ptx::tmem_ld_32x32b_x32(tacc + c * 32, v);
+                        ptx::tmem_ld_wait();
+                        if (dst_row >= 0) {
+                            const int64_t col = int64_t(tl.nb) * 256 + c * 32;
+                            if (p.out_dtype == MOE_BF16) {
+                                uint32_t o[16];
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    o[i] = pack_bf16x2(wt * __uint_as_float(v[2 * i]), wt * __uint_as_float(v[2 * i + 1]));
+                                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + dst_row * p.K + col);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                            } else {
+                                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + dst_row * p.K + col);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    dst[i] = make_float4(wt * __uint_as_float(v[4 * i]), wt * __uint_as_float(v[4 * i + 1]),
+                                                         wt * __uint_as_float(v[4 * i + 2]), wt * __uint_as_float(v[4 * i + 3]));
+                            }
+                        }
+                    }
+                }
+            } else {
+                // swap-AB: TMEM lane = weight row of the tile, column = token
+                const int n_tok = tl.rows;
+                const int n_chunks = (n_tok + 15) / 16;
+                if (p.gemm == 1) {
+                    // lanes 0..15: gate of unit u, lanes 16..31: up of unit u, u = 64*nb + 16*q + (lane & 15)
+                    const int64_t unit = int64_t(tl.nb) * 64 + q * 16 + (lane & 15);
+                    uint16_t* h = static_cast<uint16_t*>(p.out);
+#pragma unroll 1
+                    for (int cb = 0; cb < n_chunks; ++cb) {
+                        uint32_t v[16];
+                        ptx::tmem_ld_32x32b_x16(tacc + cb * 16, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float mine = __uint_as_float(v[i]);
+                            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+                            const float g = lane < 16 ? mine : other;
+                            const float u = lane < 16 ? other : mine;
+                            const int n = cb * 16 + i;
+                            // lanes 0..15 store even tokens, 16..31 odd tokens of each pair
+                            if (((i & 1) == (lane >> 4)) && n < n_tok)
+                                h[(tl.row0 + n) * p.I + unit] = float_to_bf16_bits(silu_mul(g, u));
+                        }
+                    }
+                } else {
+                    const int64_t col = int64_t(tl.nb) * 128 + q * 32 + lane;   // output hidden index
+#pragma unroll 1
+                    for (int cb = 0; cb < n_chunks; ++cb) {
+                        uint32_t v[16];
+                        ptx::tmem_ld_32x32b_x16(tacc + cb * 16, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int n = cb * 16 + i;
+                            if (n >= n_tok) break;
+                            const int64_t row = tl.row0 + n;
+                            int64_t dst_row;
+                            float wt = 1.f;
+                            if (p.layout == MOE_LAYOUT_CONTIGUOUS) {
+                                const int32_t route = p.row_route[row];
+                                if (route < 0 || route >= p.out_rows) continue;
+                                dst_row = route;
+                                if (p.route_w) wt = p.route_w[route];
+                            } else {
+                                dst_row = row;
+                                if (p.route_w) wt = p.route_w[row];
+                            }
+                            const float val = wt * __uint_as_float(v[i]);
+                            if (p.out_dtype == MOE_BF16)
+                                static_cast<uint16_t*>(p.out)[dst_row * p.K + col] = float_to_bf16_bits(val);
+                            else
+                                static_cast<float*>(p.out)[dst_row * p.K + col] = val;
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&ctrl.acc_empty[buf]);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---- host: tensor maps -------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+             const cuuint32_t* box, const char* what) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base), dims,
+                    strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MOE_ERR_ALIGNMENT, std::string("cuTensorMapEncodeTiled failed for ") + what + " (CUresult " +
+                                           std::to_string(int(r)) + ")");
+    return MOE_OK;
+}
+
+constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024;
+
+}  // namespace
+
+int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
+    if (g.a_dtype != MOE_BF16 || g.w_dtype != MOE_BF16)
+        return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: bf16 activations and bf16 weights only");
+    if (g.gemm == 1 && g.out_dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 GEMM 1 writes bf16 h");
+    const int64_t kdim = g.gemm == 1 ? g.K : g.I;
+    if (kdim % BK != 0) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: contraction length must be a multiple of 64");
+    const int64_t wrows = g.gemm == 1 ? 2 * g.I : g.K;   // weight rows per expert
+    const int wtile = swap ? 128 : 256;
+    if (wrows % wtile != 0)
+        return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: weight rows per expert must be a multiple of the tile");
+    if (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP && g.I % 16 != 0)
+        return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: I must be a multiple of 16");
+    if (g.rows_cap >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: too many rows");
+    if (g.rows_cap == 0) return MOE_OK;   // no rows, nothing to do
+
+    CUtensorMap tm_act, tm_w;
+    {
+        cuuint64_t dims[2] = {cuuint64_t(kdim), cuuint64_t(g.rows_cap)};
+        cuuint64_t str[1] = {cuuint64_t(kdim * 2)};
+        cuuint32_t box[2] = {BK, cuuint32_t(swap ? TOK_BOX : BM)};
+        int rc = make_map(&tm_act, g.a, 2, dims, str, box, "activations");
+        if (rc) return rc;
+    }
+    int w_mode = 0;
+    if (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) {
+        // view W1[e] (2I, K) as (K, 16, 2, I/16): row = half*I + 16*blk + q
+        w_mode = 1;
+        cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
+        cuuint64_t str[4] = {cuuint64_t(g.K * 2), cuuint64_t(g.I * g.K * 2), cuuint64_t(16 * g.K * 2),
+                             cuuint64_t(2 * g.I * g.K * 2)};
+        cuuint32_t box[5] = {BK, 16, 2, cuuint32_t(wtile / 32), 1};
+        int rc = make_map(&tm_w, g.w, 5, dims, str, box, "W1 (gate/up view)");
+        if (rc) return rc;
+    } else {
+        cuuint64_t dims[3] = {cuuint64_t(kdim), cuuint64_t(wrows), cuuint64_t(g.E)};
+        cuuint64_t str[2] = {cuuint64_t(kdim * 2), cuuint64_t(wrows * kdim * 2)};
+        cuuint32_t box[3] = {BK, cuuint32_t(wtile), 1};
+        int rc = make_map(&tm_w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2");
+        if (rc) return rc;
+    }
+
+    TcParams p;
+    p.gemm = g.gemm;
+    p.swap = swap ? 1 : 0;
+    p.layout = g.layout;
+    p.E = g.E;
+    p.max_tokens = g.max_tokens;
+    p.rows_cap = g.rows_cap;
+    p.nkb = int(kdim / BK);
+    p.nt = int(wrows / wtile);
+    p.w_mode = w_mode;
+    p.I = g.I;
+    p.K = g.K;
+    p.counts = g.counts;
+    p.offsets = g.offsets;
+    p.row_route = g.row_route;
+    p.route_w = g.route_w;
+    p.out = g.out;
+    p.out_dtype = g.out_dtype;
+    p.out_rows = g.out_rows;
+    p.err_word = g.err_word;
+
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+                cudaSuccess)
+                return fail(MOE_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem) failed");
+            attr_set[dev] = true;
+        }
+    }
+    // upper bound on the tiles, then one CTA per SM at most
+    const int span = swap ? 256 : BM;
+    int64_t segs;
+    if (g.layout == MOE_LAYOUT_CONTIGUOUS) segs = (g.rows_cap + span - 1) / span + g.E;
+    else segs = int64_t(g.E) * ((g.max_tokens + span - 1) / span);
+    const int64_t tiles = segs * p.nt;
+    if (tiles == 0) return MOE_OK;
+    const int grid = int(std::min<int64_t>(tiles, num_sms()));
+    gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_act, tm_w, p);
+    return check_launch("gemm_tc_kernel");
+}
+
+}  // namespace moe

@@ -1,0 +1,66 @@
+// Host-side launchers shared between the translation units of libmoe_layer.
+// Arguments are validated in api.cu before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace moe {
+
+// Records a message for moe_last_error() and returns `status`.
+int fail(int status, const std::string& msg);
+// Checks cudaGetLastError() after a launch; returns MOE_OK or MOE_ERR_LAUNCH.
+int check_launch(const char* what);
+
+int num_sms();
+int device_cc();   // major*10 + minor of the current device, 0 if none
+
+cudaError_t launch_topk_route(const float* logits, int64_t T, int E, int top_k, int renorm, int32_t* ids,
+                              float* weights, cudaStream_t s);
+
+size_t permute_workspace_bytes(int64_t T, int top_k, int E);
+cudaError_t launch_permute(const int32_t* ids, int64_t T, int top_k, int E, int layout, int block_m,
+                           int max_tokens, int32_t* counts, int32_t* offsets, int32_t* row_route,
+                           int32_t* route_row, void* ws, int32_t* err_word, cudaStream_t s);
+cudaError_t launch_gather_rows(const void* x, int esize, int64_t K, const int32_t* row_route, int top_k,
+                               const int32_t* offsets, int E, int64_t rows_cap, void* x_out, cudaStream_t s);
+
+cudaError_t launch_topk_reduce(const void* y, int y_dtype, const int32_t* ids, const float* w, int64_t T,
+                               int top_k, int E, int64_t K, void* out, int out_dtype, cudaStream_t s);
+cudaError_t launch_batched_weight(const void* y, int y_dtype, const int32_t* counts, const float* w, int E,
+                                  int max_tokens, int64_t K, void* out, int out_dtype, cudaStream_t s);
+
+cudaError_t launch_mxfp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, uint8_t* codes,
+                                  uint8_t* scales, cudaStream_t s);
+
+struct GemmArgs {
+    int gemm;               // 1: gate/up + SiLU-and-mul, 2: down projection
+    const void* a;          // activations (gemm 1) or h (gemm 2)
+    int a_dtype;
+    int layout;
+    const int32_t* counts;
+    const int32_t* offsets; // contiguous layout; NULL for batched
+    int max_tokens;
+    int64_t rows_cap;
+    int E;
+    int64_t K, I;
+    const void* w;
+    const uint8_t* w_scale;
+    int w_dtype;
+    int w1_layout;
+    const int32_t* row_route;   // gemm 2, contiguous
+    const float* route_w;       // gemm 2, optional
+    void* out;
+    int out_dtype;
+    int64_t out_rows;
+    int32_t* err_word;
+};
+
+cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t s);
+// Returns MOE_OK or a status (with message) when the tcgen05 path cannot run.
+int launch_gemm_tc(const GemmArgs& g, bool swap_ab, cudaStream_t s);
+
+}  // namespace moe

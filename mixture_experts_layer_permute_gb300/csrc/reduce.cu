@@ -1,0 +1,92 @@
+// moe_unpermute_topk_reduce and moe_batched_weight_reduce: HBM-bound
+// elementwise passes.  Each thread owns 8 consecutive elements of one output
+// row (one 16-byte bf16 vector), reads the top_k slot rows in increasing j and
+// sums in fp32 in that fixed order, so the result is bit-identical run to run.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+template <int YDT, int ODT>
+__global__ void __launch_bounds__(256) topk_reduce_kernel(const void* __restrict__ y,
+                                                          const int32_t* __restrict__ ids,
+                                                          const float* __restrict__ w, int64_t T, int top_k, int E,
+                                                          int64_t K, void* __restrict__ out) {
+    const int64_t vec_per_row = K / 8;
+    const int64_t n = T * vec_per_row;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = i / vec_per_row;
+        const int64_t col = (i - t * vec_per_row) * 8;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < top_k; ++j) {
+            const int e = ids[t * top_k + j];
+            if (e < 0 || e >= E) continue;
+            const float wj = w ? w[t * top_k + j] : 1.0f;
+            float v[8];
+            load8<YDT>(y, (t * top_k + j) * K + col, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj, v[q], acc[q]);
+        }
+        store8<ODT>(out, t * K + col, acc);
+    }
+}
+
+template <int YDT, int ODT>
+__global__ void __launch_bounds__(256) batched_weight_kernel(const void* __restrict__ y,
+                                                             const int32_t* __restrict__ counts,
+                                                             const float* __restrict__ w, int E, int max_tokens,
+                                                             int64_t K, void* out) {
+    const int64_t vec_per_row = K / 8;
+    const int64_t n = int64_t(E) * max_tokens * vec_per_row;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t row = i / vec_per_row;
+        const int e = int(row / max_tokens), q = int(row - int64_t(e) * max_tokens);
+        if (q >= counts[e]) continue;
+        const int64_t col = (i - row * vec_per_row) * 8;
+        const float wr = w ? w[row] : 1.0f;
+        float v[8];
+        load8<YDT>(y, row * K + col, v);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = wr * v[c];
+        store8<ODT>(out, row * K + col, v);
+    }
+}
+
+unsigned grid_for(int64_t n) {
+    int64_t blocks = (n + 255) / 256;
+    int64_t cap = int64_t(num_sms()) * 8;
+    if (blocks > cap) blocks = cap;
+    return unsigned(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_topk_reduce(const void* y, int y_dtype, const int32_t* ids, const float* w, int64_t T,
+                               int top_k, int E, int64_t K, void* out, int out_dtype, cudaStream_t s) {
+    if (T == 0 || K == 0) return cudaSuccess;
+    const unsigned g = grid_for(T * (K / 8));
+#define MOE_REDUCE(YD, OD) topk_reduce_kernel<YD, OD><<<g, 256, 0, s>>>(y, ids, w, T, top_k, E, K, out)
+    if (y_dtype == MOE_BF16 && out_dtype == MOE_BF16) MOE_REDUCE(MOE_BF16, MOE_BF16);
+    else if (y_dtype == MOE_BF16 && out_dtype == MOE_F32) MOE_REDUCE(MOE_BF16, MOE_F32);
+    else if (y_dtype == MOE_F32 && out_dtype == MOE_BF16) MOE_REDUCE(MOE_F32, MOE_BF16);
+    else MOE_REDUCE(MOE_F32, MOE_F32);
+#undef MOE_REDUCE
+    return cudaGetLastError();
+}
+
+cudaError_t launch_batched_weight(const void* y, int y_dtype, const int32_t* counts, const float* w, int E,
+                                  int max_tokens, int64_t K, void* out, int out_dtype, cudaStream_t s) {
+    if (E == 0 || max_tokens == 0 || K == 0) return cudaSuccess;
+    const unsigned g = grid_for(int64_t(E) * max_tokens * (K / 8));
+#define MOE_BW(YD, OD) batched_weight_kernel<YD, OD><<<g, 256, 0, s>>>(y, counts, w, E, max_tokens, K, out)
+    if (y_dtype == MOE_BF16 && out_dtype == MOE_BF16) MOE_BW(MOE_BF16, MOE_BF16);
+    else if (y_dtype == MOE_BF16 && out_dtype == MOE_F32) MOE_BW(MOE_BF16, MOE_F32);
+    else if (y_dtype == MOE_F32 && out_dtype == MOE_BF16) MOE_BW(MOE_F32, MOE_BF16);
+    else MOE_BW(MOE_F32, MOE_F32);
+#undef MOE_BW
+    return cudaGetLastError();
+}
+
+}  // namespace moe

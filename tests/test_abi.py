@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host (no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_permute_gb300 as m
+from mixture_experts_layer_permute_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return m.load()
+
+
+def _declared():
+    names = []
+    for f in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"MOE_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(names) == sorted(m.EXPORTED)
+
+
+def test_library_is_built_for_sm103a():
+    # the build passes exactly one -gencode for sm_103a
+    assert build_mod.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_version_and_sizes(lib):
+    assert m.moe_version() >> 16 == 1
+    assert m.moe_max_padded_rows(4096, 8, 128, 128) == 4096 * 8 + 128 * 127
+    assert m.moe_max_padded_rows(0, 8, 128, 1) == 0
+    assert m.moe_max_padded_rows(1, 0, 1, 1) == -1
+    assert m.moe_permute_workspace_size(4096, 8, 128) >= 4096 * 8 * 4
+
+
+def _status(fn, *args):
+    return fn(*args), lib_error()
+
+
+def lib_error():
+    return m.load().moe_last_error().decode()
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, 4, 8, 9, 1, None, None, None), 1),        # top_k > E
+    ((None, 4, 2000, 2, 1, None, None, None), 1),     # E > 1024
+    ((None, -1, 8, 2, 1, None, None, None), 1),       # T < 0
+    ((None, 4, 8, 2, 1, None, None, None), 1),        # null pointers
+])
+def test_route_validation(lib, args, expect):
+    assert lib.moe_topk_route(*args) == expect
+    assert lib_error().startswith("moe_topk_route")
+
+
+def test_route_T0_is_a_no_op(lib):
+    assert lib.moe_topk_route(None, 0, 8, 2, 1, None, None, None) == 0
+
+
+def test_permute_validation(lib):
+    fake = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
+    # rows_cap too small for the padding
+    rc = lib.moe_permute_align(fake, 4, 2, 8, 0, 16, 0, None, 1, 0, None, 8, fake, fake, fake, fake, fake,
+                               1 << 20, None, None)
+    assert rc == 1 and "rows_cap" in lib_error()
+    # workspace too small
+    rc = lib.moe_permute_align(fake, 4, 2, 8, 0, 1, 0, None, 1, 0, None, 8, fake, fake, fake, fake, fake, 0,
+                               None, None)
+    assert rc == 4
+    # misaligned workspace
+    rc = lib.moe_permute_align(fake, 4, 2, 8, 0, 1, 0, None, 1, 0, None, 8, fake, fake, fake, fake,
+                               ctypes.c_void_p(0x1004), 1 << 20, None, None)
+    assert rc == 3
+    # batched rows_cap must be E*max_tokens
+    rc = lib.moe_permute_align(fake, 4, 2, 8, 1, 1, 16, None, 1, 0, None, 100, fake, fake, fake, fake, fake,
+                               1 << 20, None, None)
+    assert rc == 1
+    # gather with a K that breaks 16-byte rows
+    rc = lib.moe_permute_align(fake, 4, 2, 8, 0, 1, 0, fake, 1, 12, fake, 8, fake, fake, fake, fake, fake,
+                               1 << 20, None, None)
+    assert rc == 3
+
+
+def test_gemm_validation(lib):
+    fake = ctypes.c_void_p(0x1000)
+    # K not a multiple of 32
+    rc = lib.moe_gemm1_swiglu(fake, 1, 0, fake, fake, 0, 64, 4, 100, 64, fake, None, 1, 0, 0, fake, 1, None, None)
+    assert rc == 3 and "multiples of 32" in lib_error()
+    # E4M3 weights without scales
+    rc = lib.moe_gemm1_swiglu(fake, 1, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 2, 0, 0, fake, 1, None, None)
+    assert rc == 1
+    # misaligned activations
+    rc = lib.moe_gemm1_swiglu(ctypes.c_void_p(0x1002), 1, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, 0, 0,
+                              fake, 1, None, None)
+    assert rc == 3
+    # contiguous gemm2 needs row_route
+    rc = lib.moe_gemm2(fake, 1, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, None, None, 0, fake, 1, 10, None,
+                       None)
+    assert rc == 1 and "row_route" in lib_error()
+    # unknown layout
+    rc = lib.moe_gemm2(fake, 1, 7, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, fake, None, 0, fake, 1, 10, None,
+                       None)
+    assert rc == 1
+
+
+def test_reduce_and_quant_validation(lib):
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.moe_unpermute_topk_reduce(fake, 1, fake, None, 4, 2, 8, 12, fake, 1, None) == 3   # K % 8
+    assert lib.moe_unpermute_topk_reduce(fake, 2, fake, None, 4, 2, 8, 16, fake, 1, None) == 2   # E4M3 y
+    assert lib.moe_batched_weight_reduce(fake, 1, fake, None, 0, 4, 16, fake, 1, None) == 1      # E = 0
+    assert lib.mxfp8_quantize_block32(fake, 1, 4, 33, fake, fake, None) == 3                     # cols % 32
+    assert lib.mxfp8_quantize_block32(fake, 2, 4, 32, fake, fake, None) == 2                     # E4M3 input
+    assert lib.mxfp8_quantize_block32(None, 1, 0, 32, None, None, None) == 0                     # empty: no-op

@@ -1,0 +1,425 @@
+"""GPU parity: every call of the C ABI against the CPU oracle on the same seeded inputs.
+
+Bit-exact: routing ids, permutation (counts, offsets, rows, inverse map),
+gathered rows, MXFP8 codes and scales, device error bits.  Floats: the
+tolerances of tests/helpers.py (rel-RMS and max-abs relative to max|ref|,
+1e-5 for fp32, 2e-2 for bf16).  Sizes span several tiles and ragged tails;
+full-size workloads are checked on sampled tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_permute_gb300 import workloads as wl
+from helpers import TOL_BF16, TOL_F32, assert_close, compact_experts, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+IMPLS_BF16 = ["tcgen05", "swap_ab", "simt"]
+
+
+def _impl(m, name):
+    return {"tcgen05": m.MOE_IMPL_TCGEN05, "swap_ab": m.MOE_IMPL_TCGEN05_SWAP_AB, "simt": m.MOE_IMPL_SIMT,
+            "auto": m.MOE_IMPL_AUTO}[name]
+
+
+# ----------------------------------------------------------------------------
+# routing
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,E,k,renorm", [(16, 8, 2, True), (64, 128, 8, True), (4096, 128, 8, True),
+                                          (33, 512, 8, True), (100, 40, 5, False), (7, 1024, 32, True),
+                                          (5, 3, 3, False)])
+def test_route_bit_exact(moe, T, E, k, renorm):
+    w = wl.scaled(wl.decode(T), E=E, top_k=k)
+    logits = wl.router_logits(w, seed=T + E)
+    if E == 40:
+        logits = torch.round(logits * 2) / 2          # exact ties: lower index must win
+    ids, wts = moe.moe_topk_route(logits.to(DEV), k, renormalize=renorm)
+    rids, rw = oracle.topk_route(logits.numpy(), k, renormalize=renorm)
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+
+
+def test_route_zipf_prefill(moe):
+    w = wl.prefill()
+    logits = wl.router_logits(w, 0)
+    ids, wts = moe.moe_topk_route(logits.to(DEV), w.top_k)
+    rids, rw = oracle.topk_route(logits.numpy(), w.top_k)
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+
+
+# ----------------------------------------------------------------------------
+# permute / align
+# ----------------------------------------------------------------------------
+
+def _ids(T, k, E, seed, pad=0.0, bad=0):
+    g = torch.Generator().manual_seed(seed)
+    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    if pad:
+        ids[torch.rand(T, k, generator=g) < pad] = -1
+    if bad:
+        flat = ids.view(-1)
+        pos = torch.randperm(flat.numel(), generator=g)[:bad]
+        flat[pos[: bad // 2]] = E + 3
+        flat[pos[bad // 2:]] = -5
+    return ids
+
+
+@pytest.mark.parametrize("T,k,E,bm,pad", [(16, 2, 8, 1, 0.0), (64, 8, 128, 1, 0.1), (128, 8, 128, 16, 0.0),
+                                          (4096, 8, 128, 128, 0.05), (9000, 8, 64, 4, 0.2),
+                                          (3, 1, 1, 1, 0.0), (1, 8, 1024, 128, 0.0)])
+def test_permute_contiguous_bit_exact(moe, T, k, E, bm, pad):
+    ids = _ids(T, k, E, seed=T * 7 + E, pad=pad) if E >= k else torch.zeros(T, k, dtype=torch.int32)
+    K = 64
+    x = wl._normal((T, K), 1.0, 5, "x", 0, "cpu", torch.bfloat16)
+    res = moe.moe_permute_align(ids.to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, bm, x=x.to(DEV))
+    ref = oracle.permute_contiguous(ids.numpy(), E, bm)
+    off = res["offsets"].cpu().numpy()
+    assert np.array_equal(res["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(off, ref["offsets"])
+    rows = off[E]
+    assert np.array_equal(res["row_route"][:rows].cpu().numpy(), ref["sorted_route"])
+    assert np.array_equal(res["route_row"].cpu().numpy(), ref["route_row"])
+    # gathered rows are the token rows, bit for bit
+    xo = res["x_out"][:rows].cpu()
+    valid = ref["sorted_route"] >= 0
+    src = torch.from_numpy(ref["sorted_route"][valid] // k).long()
+    assert torch.equal(xo[torch.from_numpy(valid)].view(torch.int16), x[src].view(torch.int16))
+
+
+def test_permute_chunked_rounds(moe):
+    """More routes than 64 chunks x 1024: each CTA takes several rounds."""
+    T, k, E = 12000, 8, 96
+    ids = _ids(T, k, E, seed=3, pad=0.1)
+    res = moe.moe_permute_align(ids.to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 8)
+    ref = oracle.permute_contiguous(ids.numpy(), E, 8)
+    rows = ref["offsets"][E]
+    assert np.array_equal(res["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(res["row_route"][:rows].cpu().numpy(), ref["sorted_route"])
+    assert np.array_equal(res["route_row"].cpu().numpy(), ref["route_row"])
+
+
+@pytest.mark.parametrize("T", [40, 3000])
+def test_permute_bad_ids_flagged(moe, T):
+    E, k = 16, 4
+    ids = _ids(T, k, E, seed=9, pad=0.1, bad=10)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    res = moe.moe_permute_align(ids.to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, err_word=err)
+    ref = oracle.permute_contiguous(ids.numpy(), E, 1)
+    assert int(err.item()) == moe.MOE_DEVERR_ID_RANGE == ref["err"]
+    assert np.array_equal(res["route_row"].cpu().numpy(), ref["route_row"])
+    assert np.array_equal(res["counts"].cpu().numpy(), ref["counts"])
+
+
+@pytest.mark.parametrize("T,k,E,cap", [(50, 4, 8, 32), (2000, 2, 16, 200), (100, 2, 4, 0)])
+def test_permute_batched_bit_exact(moe, T, k, E, cap):
+    ids = _ids(T, k, E, seed=T + cap, pad=0.1)
+    K = 32
+    x = wl._normal((T, K), 1.0, 6, "x", 0, "cpu", torch.float32)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    res = moe.moe_permute_align(ids.to(DEV), E, moe.MOE_LAYOUT_BATCHED, 1, cap, x=x.to(DEV), err_word=err)
+    ref = oracle.permute_batched(ids.numpy(), E, cap)
+    assert int(err.item()) == ref["err"]
+    assert np.array_equal(res["counts"].cpu().numpy(), ref["expert_num_tokens"])
+    assert np.array_equal(res["offsets"].cpu().numpy(), np.arange(E + 1) * cap)
+    assert np.array_equal(res["row_route"][:E * cap].cpu().numpy(), ref["row_route"].reshape(-1))
+    assert np.array_equal(res["route_row"].cpu().numpy(), ref["route_row"])
+    xo = res["x_out"].cpu().reshape(E, cap, K) if cap else None
+    for e in range(E):
+        for q in range(ref["expert_num_tokens"][e]):
+            r = ref["row_route"][e, q]
+            assert torch.equal(xo[e, q], x[r // k])
+
+
+# ----------------------------------------------------------------------------
+# MXFP8 quantisation
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_mxfp8_quantize_bit_exact(moe, dtype):
+    g = torch.Generator().manual_seed(1)
+    x = torch.randn(300, 512, generator=g) * 0.02
+    x[0, :64] = 0.0                                        # zero blocks
+    x[1, :32] = -0.0
+    x[2, :32] *= 1e-36                                      # clamps the code at 0
+    x[3, :32] = 448.0                                       # exact boundary: code 127
+    x[4, :32] = torch.randn(32, generator=g) * 1e30         # large
+    x[5] = torch.exp(torch.randn(512, generator=g) * 8)     # wide dynamic range inside blocks
+    x[6, 5] = 1.75 * 2.0 ** -120                            # f exactly 1.75 in a tiny block
+    x = x.to(dtype)
+    codes, scales = moe.mxfp8_quantize_block32(x.to(DEV))
+    rc, rs = oracle.mxfp8_quantize(wl.to_numpy(x))
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+# ----------------------------------------------------------------------------
+# reduce
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ydt,odt,weighted", [(torch.bfloat16, torch.bfloat16, True),
+                                              (torch.float32, torch.float32, True),
+                                              (torch.bfloat16, torch.float32, False)])
+def test_topk_reduce(moe, ydt, odt, weighted):
+    T, k, K, E = 37, 8, 4096, 64
+    g = torch.Generator().manual_seed(2)
+    ids = _ids(T, k, E, seed=4, pad=0.2)
+    ids[5] = -1                                            # a token made only of padding
+    y = torch.randn(T * k, K, generator=g).to(ydt)
+    w = torch.rand(T, k, generator=g)
+    out = moe.moe_unpermute_topk_reduce(y.to(DEV), ids.to(DEV), E, w.to(DEV) if weighted else None,
+                                        out_dtype=moe.MOE_F32 if odt == torch.float32 else moe.MOE_BF16)
+    ref = oracle.topk_reduce(wl.to_numpy(y), ids.numpy(), w.numpy() if weighted else None)
+    tol = TOL_F32 if (ydt == torch.float32 and odt == torch.float32) else TOL_BF16
+    assert_close(to_f64(out), ref, tol, "topk_reduce")
+    o5 = out[5].cpu()
+    assert torch.all(o5 == 0) and not torch.any(torch.signbit(o5.float()))   # +0.0
+    again = moe.moe_unpermute_topk_reduce(y.to(DEV), ids.to(DEV), E, w.to(DEV) if weighted else None,
+                                          out_dtype=moe.MOE_F32 if odt == torch.float32 else moe.MOE_BF16)
+    assert torch.equal(out.view(torch.uint8), again.view(torch.uint8))       # fixed order: same bits
+
+
+def test_batched_weight_reduce(moe):
+    E, maxT, K = 6, 40, 256
+    g = torch.Generator().manual_seed(3)
+    counts = torch.tensor([0, 40, 7, 13, 1, 39], dtype=torch.int32)
+    y = torch.randn(E, maxT, K, generator=g).to(torch.bfloat16)
+    w = torch.rand(E, maxT, generator=g)
+    out = torch.full((E, maxT, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    moe.moe_batched_weight_reduce(y.to(DEV), counts.to(DEV), w.to(DEV), out=out)
+    out = out.cpu()
+    for e in range(E):
+        c = int(counts[e])
+        ref = y[e, :c].double() * w[e, :c].double()[:, None]
+        assert_close(to_f64(out[e, :c]), ref.numpy(), TOL_BF16, "batched weight")
+        assert torch.all(out[e, c:] == 7.0)
+
+
+# ----------------------------------------------------------------------------
+# grouped GEMMs
+# ----------------------------------------------------------------------------
+
+GEMM_SHAPES = [  # T, k, E, K, I, block_m
+    (96, 4, 8, 512, 256, 1),
+    (300, 2, 16, 256, 384, 128),
+    (600, 1, 2, 256, 256, 1),        # ~300 rows per expert: several m-tiles / two token segments
+    (5, 8, 128, 512, 128, 1),        # decode-like: a few tokens per expert
+]
+
+
+def _routed(T, k, E, K, seed):
+    w = wl.scaled(wl.decode(T), T=T, K=K, E=E, top_k=k)
+    logits = wl.router_logits(w, seed)
+    ids, weights = oracle.topk_route(logits.numpy(), k)
+    x = wl.activations(w, seed)
+    return w, x, ids, weights
+
+
+@pytest.mark.parametrize("impl", IMPLS_BF16)
+@pytest.mark.parametrize("shape", GEMM_SHAPES)
+@pytest.mark.parametrize("w1_layout", [0, 1])
+def test_gemm1_swiglu(moe, impl, shape, w1_layout):
+    T, k, E, K, I, bm = shape
+    w, x, ids, _ = _routed(T, k, E, K, seed=T + E)
+    wI = wl.scaled(w, I=I)
+    W1 = wl.expert_weights(wI, "W1", 1)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, bm, x=x.to(DEV))
+    h = moe.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1.to(DEV), I, w1_layout=w1_layout,
+                             impl=_impl(moe, impl))
+    flat = ids.reshape(-1)
+    href = oracle.expert_gate_up(wl.to_numpy(x)[np.arange(T * k) // k], flat, wl.to_numpy(W1),
+                                 w1_layout=w1_layout)
+    rr = res["route_row"].cpu().numpy().reshape(-1)
+    got = to_f64(h.cpu()[torch.from_numpy(rr).long()])
+    assert_close(got, href, TOL_BF16, f"gemm1 {impl}")
+
+
+@pytest.mark.parametrize("impl", IMPLS_BF16)
+@pytest.mark.parametrize("shape", GEMM_SHAPES)
+@pytest.mark.parametrize("weighted", [True, False])
+def test_gemm2(moe, impl, shape, weighted):
+    T, k, E, K, I, bm = shape
+    w, _, ids, weights = _routed(T, k, E, K, seed=T + 2 * E)
+    wI = wl.scaled(w, I=I)
+    W2 = wl.expert_weights(wI, "W2", 2)
+    R = T * k
+    hsrc = wl._normal((R, I), 1.0, 7, "h", 0, "cpu", torch.bfloat16)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, bm)
+    rr = res["route_row"].view(-1).long()
+    hperm = torch.zeros((res["rows_cap"], I), dtype=torch.bfloat16, device=DEV)
+    hperm[rr] = hsrc.to(DEV)                                   # test plumbing: rows placed as routed
+    wt = torch.from_numpy(weights).to(DEV).reshape(-1)
+    y = moe.moe_gemm2(hperm, res["counts"], res["offsets"], W2.to(DEV), R, row_route=res["row_route"],
+                      route_weights=wt if weighted else None, impl=_impl(moe, impl))
+    yref = oracle.expert_down(wl.to_numpy(hsrc), ids.reshape(-1), wl.to_numpy(W2))
+    if weighted:
+        yref = yref * weights.reshape(-1, 1).astype(np.float64)
+    assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 {impl}")
+
+
+def test_gemm_unsupported_shape_falls_back_under_auto(moe):
+    """K not a multiple of 64: AUTO uses the CUDA-core tiles; forcing tcgen05 reports UNSUPPORTED."""
+    T, k, E, K, I = 20, 2, 4, 96, 64
+    w, x, ids, _ = _routed(T, k, E, K, seed=1)
+    W1 = wl.expert_weights(wl.scaled(w, I=I), "W1", 1)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1.to(DEV), I,
+                             impl=moe.MOE_IMPL_TCGEN05)
+    assert ei.value.status == 2
+    h = moe.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1.to(DEV), I, impl=moe.MOE_IMPL_AUTO)
+    href = oracle.expert_gate_up(wl.to_numpy(x)[np.arange(T * k) // k], ids.reshape(-1), wl.to_numpy(W1))
+    rr = res["route_row"].cpu().numpy().reshape(-1)
+    assert_close(to_f64(h.cpu()[torch.from_numpy(rr).long()]), href, TOL_BF16, "auto fallback")
+
+
+# ----------------------------------------------------------------------------
+# whole layer
+# ----------------------------------------------------------------------------
+
+def test_layer_tiny_fp32(moe):
+    """The fp32 configuration: T=16, K=128, I=256, E=8, top_k=2 -- tolerance 1e-5."""
+    w = wl.tiny()
+    x, logits = wl.activations(w, 0), wl.router_logits(w, 0)
+    W1, W2 = wl.expert_weights(w, "W1", 0), wl.expert_weights(w, "W2", 0)
+    for weight_in_gemm2 in (True, False):
+        layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=torch.float32,
+                             weight_in_gemm2=weight_in_gemm2, device=DEV)
+        out = layer.forward(x.to(DEV), W1.to(DEV), W2.to(DEV), logits=logits.to(DEV))
+        ids, weights = oracle.topk_route(logits.numpy(), w.top_k)
+        assert np.array_equal(layer.ids.cpu().numpy(), ids)
+        ref, _ = oracle.moe_layer(x.numpy(), ids, weights, W1.numpy(), W2.numpy())
+        assert_close(to_f64(out.cpu()), ref, TOL_F32, "tiny fp32 layer")
+        assert layer.device_errors() == 0
+
+
+@pytest.mark.parametrize("impl", IMPLS_BF16 + ["auto"])
+@pytest.mark.parametrize("bm", [1, 128])
+def test_layer_bf16_small(moe, impl, bm):
+    w = wl.scaled(wl.decode(64), T=200, K=512, I=256, E=16, top_k=4)
+    x, logits = wl.activations(w, 3), wl.router_logits(w, 3)
+    W1, W2 = wl.expert_weights(w, "W1", 3), wl.expert_weights(w, "W2", 3)
+    layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, block_m=bm, impl=_impl(moe, impl), device=DEV)
+    out = layer.forward(x.to(DEV), W1.to(DEV), W2.to(DEV), logits=logits.to(DEV))
+    ids, weights = oracle.topk_route(logits.numpy(), w.top_k)
+    ref, _ = oracle.moe_layer(wl.to_numpy(x), ids, weights, wl.to_numpy(W1), wl.to_numpy(W2))
+    assert_close(to_f64(out.cpu()), ref, TOL_BF16, f"layer {impl} bm={bm}")
+    first = out.clone()
+    layer.forward(x.to(DEV), W1.to(DEV), W2.to(DEV), logits=logits.to(DEV))
+    assert torch.equal(first.view(torch.int16), out.view(torch.int16))          # run-to-run identical
+    assert layer.device_errors() == 0
+
+
+def test_layer_padding_tokens(moe):
+    """Tokens whose slots are all padding (id -1, weight 0) come out as +0.0."""
+    w = wl.scaled(wl.decode(64), T=24, K=256, I=128, E=8, top_k=2)
+    x = wl.activations(w, 4)
+    ids, weights = oracle.topk_route(wl.router_logits(w, 4).numpy(), w.top_k)
+    ids_t, w_t = wl.padding_tokens(torch.from_numpy(ids), torch.from_numpy(weights), 8)
+    x_all = torch.cat([x, wl._normal((8, w.K), 1.0, 9, "xp", 0, "cpu", torch.bfloat16)])
+    ids_t[3, 1], w_t[3, 1] = -1, 0.0
+    W1, W2 = wl.expert_weights(w, "W1", 4), wl.expert_weights(w, "W2", 4)
+    T = x_all.shape[0]
+    for impl in ("tcgen05", "swap_ab"):
+        layer = moe.MoELayer(T, w.K, w.I, w.E, w.top_k, impl=_impl(moe, impl), device=DEV)
+        out = layer.forward(x_all.to(DEV), W1.to(DEV), W2.to(DEV), topk_ids=ids_t.to(DEV),
+                            topk_weights=w_t.to(DEV)).cpu()
+        ref, _ = oracle.moe_layer(wl.to_numpy(x_all), ids_t.numpy(), w_t.numpy(), wl.to_numpy(W1),
+                                  wl.to_numpy(W2))
+        assert_close(to_f64(out), ref, TOL_BF16, "padding")
+        assert torch.all(out[-8:] == 0) and not torch.any(torch.signbit(out[-8:].float()))
+
+
+def test_layer_decode_full_size_sampled(moe):
+    """Decode configuration at full size (K=4096, I=1536, E=128, top_k=8), T=8; oracle on 2 tokens."""
+    w = wl.decode(8)
+    x, logits = wl.activations(w, 0, DEV), wl.router_logits(w, 0, DEV)
+    W1, W2 = wl.expert_weights(w, "W1", 0, DEV), wl.expert_weights(w, "W2", 0, DEV)
+    for impl in ("auto", "tcgen05"):
+        layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, impl=_impl(moe, impl), device=DEV)
+        out = layer.forward(x, W1, W2, logits=logits)
+        ids, weights = oracle.topk_route(logits.cpu().numpy(), w.top_k)
+        assert np.array_equal(layer.ids.cpu().numpy(), ids)
+        for t in (0, 5):
+            cids, (w1h, w2h, _, _) = compact_experts(ids[t:t + 1], W1, W2)
+            ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, weights[t:t + 1], w1h, w2h)
+            assert_close(to_f64(out[t:t + 1]), ref, TOL_BF16, f"decode token {t} {impl}")
+
+
+def test_layer_prefill_full_size_sampled(moe):
+    """Skewed prefill at full size (T=4096, bm=128); oracle on 2 tokens, one of them routed to the hottest expert."""
+    w = wl.prefill()
+    x, logits = wl.activations(w, 0, DEV), wl.router_logits(w, 0, DEV)
+    W1, W2 = wl.expert_weights(w, "W1", 0, DEV), wl.expert_weights(w, "W2", 0, DEV)
+    layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, block_m=w.block_m, device=DEV)
+    out = layer.forward(x, W1, W2, logits=logits)
+    ids, weights = oracle.topk_route(logits.cpu().numpy(), w.top_k)
+    assert np.array_equal(layer.ids.cpu().numpy(), ids)
+    ref_perm = oracle.permute_contiguous(ids, w.E, w.block_m)
+    assert np.array_equal(layer.offsets.cpu().numpy(), ref_perm["offsets"])
+    assert np.array_equal(layer.row_route[:ref_perm["offsets"][-1]].cpu().numpy(), ref_perm["sorted_route"])
+    for t in (0, 4095):
+        cids, (w1h, w2h, _, _) = compact_experts(ids[t:t + 1], W1, W2)
+        ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, weights[t:t + 1], w1h, w2h)
+        assert_close(to_f64(out[t:t + 1]), ref, TOL_BF16, f"prefill token {t}")
+    assert layer.device_errors() == 0
+
+
+def _mxfp8_weights(moe, w, which, seed):
+    rows = 2 * w.I if which == "W1" else w.K
+    cols = w.K if which == "W1" else w.I
+    codes = torch.empty((w.E, rows, cols), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((w.E, rows, cols // 32), dtype=torch.uint8, device=DEV)
+    for e in range(w.E):
+        Wf = wl.expert_weights(w, which, seed, DEV, experts=[e])[0]
+        moe.mxfp8_quantize_block32(Wf, codes=codes[e], scales=scales[e])
+    return codes, scales
+
+
+def test_layer_mxfp8_full_size_sampled(moe):
+    """MXFP8 weights (E=512, K=7168, I=2048, interleave-16 W1, affine routing); oracle on 2 tokens."""
+    w = wl.mxfp8()
+    x = wl.activations(w, 0, DEV)
+    ids_t, w_t = wl.affine_routing(w)
+    c1, s1 = _mxfp8_weights(moe, w, "W1", 0)
+    c2, s2 = _mxfp8_weights(moe, w, "W2", 0)
+    # the GPU codes of one expert equal the oracle's codes of the same fp32 draw
+    W1e = wl.expert_weights(w, "W1", 0, DEV, experts=[19])[0].cpu()
+    rc, rs = oracle.mxfp8_quantize(W1e.numpy())
+    assert np.array_equal(c1[19].cpu().numpy(), rc) and np.array_equal(s1[19].cpu().numpy(), rs)
+    layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, device=DEV)
+    out = layer.forward(x, c1, c2, topk_ids=ids_t.to(DEV), topk_weights=w_t.to(DEV), w1_scale=s1, w2_scale=s2,
+                        w1_layout=moe.MOE_W1_INTERLEAVE16)
+    ids = ids_t.numpy()
+    for t in (0, 511):
+        cids, (w1h, w2h, s1h, s2h) = compact_experts(ids[t:t + 1], c1, c2, s1, s2)
+        ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, w_t[t:t + 1].numpy(), w1h, w2h, w1_scale=s1h,
+                                  w2_scale=s2h, w1_layout=1)
+        assert_close(to_f64(out[t:t + 1]), ref, TOL_BF16, f"mxfp8 token {t}")
+
+
+@pytest.mark.parametrize("garbage", ["nan", "big"])
+def test_layer_batched_full_size_sampled(moe, garbage):
+    """Batched layout (E=32, max_tokens=256, K=6144, I=4096); garbage rows ignored; oracle on sampled rows."""
+    w = wl.batched(garbage)
+    xb, counts, rw = wl.batched_inputs(w, 0, DEV)
+    W1, W2 = wl.expert_weights(w, "W1", 0, DEV), wl.expert_weights(w, "W2", 0, DEV)
+    layer = moe.MoELayer(0, w.K, w.I, w.E, 1, layout=moe.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens, device=DEV)
+    layer.out.fill_(3.0)
+    out = layer.forward(xb, W1, W2, expert_num_tokens=counts, row_weights=rw)
+    cnt = counts.cpu().numpy()
+    for e in (int(np.argmax(cnt)), int(np.argmin(np.where(cnt > 0, cnt, 999)))):
+        c = int(cnt[e])
+        rows = sorted({0, c - 1, c // 2})
+        sub = xb[e, rows][None]                             # (1, len(rows), K)
+        ref, _ = oracle.moe_layer_batched(wl.to_numpy(sub), np.array([len(rows)], np.int32),
+                                          rw[e, rows][None].cpu().numpy(), wl.to_numpy(W1[e:e + 1]),
+                                          wl.to_numpy(W2[e:e + 1]))
+        assert_close(to_f64(out[e, rows]), ref[0], TOL_BF16, f"batched expert {e}")
+        if c < w.max_tokens:
+            assert torch.all(out[e, c:] == 3.0)             # rows beyond the count untouched
+    assert torch.isfinite(out.float()).sum() > 0

@@ -1,0 +1,541 @@
+"""Throughput of the fused MoE expert layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One "step" is one pass of the whole layer (route, permute, gate/up + SiLU-and-
+mul, down projection with the route weight, ordered top-k reduce) over one
+batch of synthetic input resident in HBM.  The default workload is the decode
+sweep: the layer at T = 1, 8, 32 and 64 tokens (K=4096, I=1536, E=128,
+top_k=8, bf16), all four passes forming one step.  Other workloads (prefill,
+mxfp8, batched, tiny) can be selected with --workload.
+
+Rank 0 prints ONE JSON line.  Under torchrun (N > 1) each rank runs an
+independent replica of the workload on its GPU (the layer has no exchange
+step), a barrier brackets the timed region and the max time over ranks is
+used; value = routed tokens of all ranks / that time.
+
+--impl reference times the CPU oracle (the plain fp64 C reference) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/s per MoE layer on 1 GB300; % of HBM (decode) / tensor (prefill) roofline"
+UNIT = "routed tokens/s"
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+
+def workload_list(name):
+    from mixture_experts_layer_permute_gb300 import workloads as wl
+    if name == "decode":
+        return [wl.decode(T) for T in (1, 8, 32, 64)]
+    if name.startswith("decode"):
+        return [wl.decode(int(name[len("decode"):]))]
+    return [{"prefill": wl.prefill, "mxfp8": wl.mxfp8, "batched": wl.batched, "tiny": wl.tiny}[name]()]
+
+
+def describe(name, ws):
+    if name == "decode":
+        return "decode bf16 sweep T in {1,8,32,64}: K=4096, I=1536, E=128, top_k=8, contiguous, swap-AB tiles"
+    w = ws[0]
+    return (f"{w.name}: T={w.T}, K={w.K}, I={w.I}, E={w.E}, top_k={w.top_k}, act={w.act}, weights={w.weight}, "
+            f"layout={w.layout}, block_m={w.block_m}, max_tokens={w.max_tokens}")
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0.0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class Instance:
+    """Device inputs and the layer object of one workload."""
+
+    def __init__(self, w, seed, device):
+        import torch
+        import mixture_experts_layer_permute_gb300 as m
+        from mixture_experts_layer_permute_gb300 import workloads as wl
+        self.w = w
+        self.m = m
+        dev = torch.device(device)
+        self.routes_fixed = None
+        if w.layout == "batched":
+            self.xb, self.counts, self.rw = wl.batched_inputs(w, seed, dev)
+            self.W1 = wl.expert_weights(w, "W1", seed, dev)
+            self.W2 = wl.expert_weights(w, "W2", seed, dev)
+            self.layer = m.MoELayer(0, w.K, w.I, w.E, 1, layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens,
+                                    device=dev)
+            self.s1 = self.s2 = None
+            self.routes = int(self.counts.sum().item())
+            self.used_experts = int((self.counts > 0).sum().item())
+            return
+        self.x = wl.activations(w, seed, dev)
+        if w.routing == "affine":
+            self.ids, self.tw = [t.to(dev) for t in wl.affine_routing(w)]
+            self.logits = None
+        else:
+            self.logits = wl.router_logits(w, seed, dev)
+        if w.weight == "mxfp8":
+            self.W1, self.s1 = self._mxfp8(w, "W1", seed, dev)
+            self.W2, self.s2 = self._mxfp8(w, "W2", seed, dev)
+        else:
+            self.W1 = wl.expert_weights(w, "W1", seed, dev)
+            self.W2 = wl.expert_weights(w, "W2", seed, dev)
+            self.s1 = self.s2 = None
+        self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
+                                device=dev)
+        self.forward()
+        torch.cuda.synchronize()
+        ids = self.layer.ids if self.logits is not None else self.ids
+        self.routes = int((ids >= 0).sum().item())
+        self.used_experts = int(torch.unique(ids[ids >= 0]).numel())
+
+    def _mxfp8(self, w, which, seed, dev):
+        import torch
+        from mixture_experts_layer_permute_gb300 import workloads as wl
+        rows, cols = (2 * w.I, w.K) if which == "W1" else (w.K, w.I)
+        codes = torch.empty((w.E, rows, cols), dtype=torch.uint8, device=dev)
+        scales = torch.empty((w.E, rows, cols // 32), dtype=torch.uint8, device=dev)
+        for e in range(w.E):
+            self.m.mxfp8_quantize_block32(wl.expert_weights(w, which, seed, dev, experts=[e])[0], codes=codes[e],
+                                          scales=scales[e])
+        return codes, scales
+
+    def forward(self, x=None, logits=None, gemm1_events=None):
+        L = self.layer
+        w1_layout = self.w.w1_layout
+        if self.w.layout == "batched":
+            return L.forward(self.xb, self.W1, self.W2, expert_num_tokens=self.counts, row_weights=self.rw,
+                             gemm1_events=gemm1_events)
+        x = self.x if x is None else x
+        if self.logits is not None:
+            lg = self.logits if logits is None else logits
+            return L.forward(x, self.W1, self.W2, logits=lg, w1_scale=self.s1, w2_scale=self.s2,
+                             w1_layout=w1_layout, gemm1_events=gemm1_events)
+        return L.forward(x, self.W1, self.W2, topk_ids=self.ids, topk_weights=self.tw, w1_scale=self.s1,
+                         w2_scale=self.s2, w1_layout=w1_layout, gemm1_events=gemm1_events)
+
+    def launches(self):
+        if self.w.layout == "batched":
+            return 2
+        R = self.w.T * self.w.top_k
+        n = 1 + (1 if R <= 1024 else 2) + 1 + 1 + 1 + 1     # (route) permute gather gemm1 gemm2 reduce
+        return n if self.logits is not None else n - 1
+
+    # algorithmic bytes / FLOPs (touched weights + scales + activations in + output; 6 K I flops per route)
+    def gemm1_bytes(self):
+        w = self.w
+        wb = 2 * w.I * w.K * (1 if w.weight == "mxfp8" else 2)
+        sb = (2 * w.I * w.K // 32) if w.weight == "mxfp8" else 0
+        act = 2 if w.act == "bf16" else 4
+        return self.used_experts * (wb + sb) + self.routes * (w.K + w.I) * act
+
+    def layer_bytes(self):
+        w = self.w
+        per_w = 3 * w.I * w.K * (1 if w.weight == "mxfp8" else (4 if w.weight == "f32" else 2))
+        if w.weight == "mxfp8":
+            per_w += 3 * w.I * w.K // 32
+        act = 2 if w.act == "bf16" else 4
+        if w.layout == "batched":
+            return self.used_experts * per_w + 2 * self.routes * w.K * act
+        return self.used_experts * per_w + 2 * w.T * w.K * act
+
+    def layer_flops(self):
+        return 6.0 * self.w.K * self.w.I * self.routes
+
+    def gemm1_flops(self):
+        return 4.0 * self.w.K * self.w.I * self.routes
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# traffic from the committed ncu summary (valid only for the kernel source it was taken on)
+# ----------------------------------------------------------------------------
+
+def kernel_source_hash():
+    p = os.path.join(ROOT, "mixture_experts_layer_permute_gb300", "csrc", "gemm_tc.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = d.get(workload)
+    if not rec or rec.get("gemm_tc_sha") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    ws = workload_list(args.workload)
+    insts = [Instance(w, args.seed, dev) for w in ws]
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        for n, inst in enumerate(insts):
+            inst.forward(gemm1_events=None if ev is None else ev[n])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # per-launch events on the launching stream bracket GEMM 1 (the dominant kernel)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)] for _ in insts]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            step([e[s] for e in ev])
+        end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms_total = start.elapsed_time(end)
+    clocks = clk.summary()
+
+    routes_per_step = sum(i.routes for i in insts)
+    t_max = ms_total
+    total_routes = routes_per_step * args.steps
+    if world > 1:
+        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+        rr = torch.tensor([total_routes], dtype=torch.float64, device=dev)
+        dist.all_reduce(rr, op=dist.ReduceOp.SUM)
+        total_routes = float(rr.item())
+    value = total_routes / (t_max / 1e3)
+
+    # GEMM 1 roofline (HBM bound for decode/mxfp8/batched, tensor bound for prefill)
+    hbm, tf_burst, tf_sust, peak_kind = read_peaks()
+    g1_ms = [sum(a.elapsed_time(b) for a, b in e) / args.steps for e in ev]
+    g1_bytes = [i.gemm1_bytes() for i in insts]
+    g1_flops = [i.gemm1_flops() for i in insts]
+    prefill = args.workload == "prefill"
+    if prefill:
+        achieved = sum(g1_flops) / (sum(g1_ms) / 1e3) / 1e12
+        peak = tf_sust or tf_burst
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4)}
+    else:
+        achieved = sum(g1_bytes) / (sum(g1_ms) / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4)}
+    roof["kernel"] = "gemm_tc_kernel (moe_gemm1_swiglu)"
+    roof["peak_source"] = f"MEASURED_PEAKS.json ({peak_kind})" + (", sustained bf16" if prefill else "")
+    roof["traffic"] = recorded_traffic(args.workload)
+    roof["algorithmic_per_launch"] = [int(b) for b in (g1_flops if prefill else g1_bytes)]
+    roof["launch_ms"] = [round(x, 4) for x in g1_ms]
+
+    # whole-layer roofline per pass: max(flops / tensor peak, bytes / HBM peak)
+    sweep = []
+    for n, inst in enumerate(insts):
+        t_roof = max(inst.layer_flops() / (tf_burst * 1e12), inst.layer_bytes() / (hbm * 1e9)) * 1e3
+        sweep.append({"workload": inst.w.name, "routes": inst.routes, "experts_touched": inst.used_experts,
+                      "layer_bytes": inst.layer_bytes(), "layer_flops": inst.layer_flops(),
+                      "gemm1_ms": round(g1_ms[n], 4), "roofline_ms": round(t_roof, 4)})
+
+    e2e = run_e2e(args, insts, dev) if rank == 0 or world > 1 else None
+    launches = sum(i.launches() for i in insts) * args.steps
+    cpu = cpu_baseline(args, insts) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": insts[0].w.act, "data": "synthetic",
+            "config": {"workload": describe(args.workload, ws), "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (touched expert weights exceed 129 MB every pass)",
+                       "routes_per_step": routes_per_step},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, insts, dev):
+    """Same metric through the public API with host buffers: H2D of x and logits, layer, D2H of the output."""
+    import torch
+    host = []
+    for inst in insts:
+        hx = inst.x.cpu().pin_memory() if inst.w.layout != "batched" else inst.xb.cpu().pin_memory()
+        hl = inst.logits.cpu().pin_memory() if getattr(inst, "logits", None) is not None else None
+        out = inst.layer.out
+        ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        dx = torch.empty_like(inst.x if inst.w.layout != "batched" else inst.xb)
+        dl = torch.empty_like(inst.logits) if hl is not None else None
+        host.append((hx, hl, ho, dx, dl))
+
+    def step():
+        for inst, (hx, hl, ho, dx, dl) in zip(insts, host):
+            dx.copy_(hx, non_blocking=True)
+            if hl is not None:
+                dl.copy_(hl, non_blocking=True)
+            if inst.w.layout == "batched":
+                out = inst.layer.forward(dx, inst.W1, inst.W2, expert_num_tokens=inst.counts, row_weights=inst.rw)
+            else:
+                out = inst.forward(x=dx, logits=dl)
+            ho.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    routes = sum(i.routes for i in insts) * args.steps
+    h2d = sum(h[0].numel() * h[0].element_size() + (h[1].numel() * h[1].element_size() if h[1] is not None else 0)
+              for h in host)
+    d2h = sum(h[2].numel() * h[2].element_size() for h in host)
+    return {"value": round(routes / dt, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(ws, seed, device_inputs=None):
+    """Host inputs for a bounded oracle sample: one token of each pass of the workload (every route of it)."""
+    import numpy as np
+    import torch
+    import oracle
+    from mixture_experts_layer_permute_gb300 import workloads as wl
+    samples = []
+    for n, w in enumerate(ws):
+        if w.layout == "batched":
+            if device_inputs is not None:
+                inst = device_inputs[n]
+                e = int(torch.argmax(inst.counts).item())
+                xb = wl.to_numpy(inst.xb[e:e + 1, :1])
+                W1 = wl.to_numpy(inst.W1[e:e + 1])
+                W2 = wl.to_numpy(inst.W2[e:e + 1])
+            else:
+                g = wl.scaled(w, E=1, max_tokens=1)
+                xb = wl.to_numpy(wl._normal((1, 1, w.K), 1.0, seed, "xb", 0, "cpu", torch.bfloat16))
+                W1 = wl.to_numpy(wl.expert_weights(g, "W1", seed))
+                W2 = wl.to_numpy(wl.expert_weights(g, "W2", seed))
+            samples.append(("batched", xb, W1, W2, None, None, 1))
+            continue
+        if device_inputs is not None:
+            inst = device_inputs[n]
+            x = wl.to_numpy(inst.x[:1])
+            if inst.logits is not None:
+                ids, wts = oracle.topk_route(inst.logits[:1].cpu().numpy(), w.top_k)
+            else:
+                ids, wts = inst.ids[:1].cpu().numpy(), inst.tw[:1].cpu().numpy()
+            used = sorted({int(e) for e in ids.reshape(-1)})
+            sel = torch.tensor(used, device=inst.W1.device)
+            W1 = wl.to_numpy(inst.W1.index_select(0, sel))
+            W2 = wl.to_numpy(inst.W2.index_select(0, sel))
+            S1 = None if inst.s1 is None else wl.to_numpy(inst.s1.index_select(0, sel))
+            S2 = None if inst.s2 is None else wl.to_numpy(inst.s2.index_select(0, sel))
+        else:
+            x = wl.to_numpy(wl.activations(wl.scaled(w, T=1), seed))
+            if w.routing == "affine":
+                it, iw = wl.affine_routing(wl.scaled(w, T=1))
+                ids, wts = it.numpy(), iw.numpy()
+            else:
+                ids, wts = oracle.topk_route(wl.router_logits(wl.scaled(w, T=1), seed).numpy(), w.top_k)
+            used = sorted({int(e) for e in ids.reshape(-1)})
+            W1t = wl.expert_weights(w, "W1", seed, experts=used)
+            W2t = wl.expert_weights(w, "W2", seed, experts=used)
+            if w.weight == "mxfp8":
+                W1, S1 = oracle.mxfp8_quantize(W1t.numpy())
+                W2, S2 = oracle.mxfp8_quantize(W2t.numpy())
+            else:
+                W1, W2, S1, S2 = wl.to_numpy(W1t), wl.to_numpy(W2t), None, None
+        remap = {e: i for i, e in enumerate(used)}
+        cids = np.vectorize(lambda e: remap[int(e)])(ids).astype(np.int32)
+        samples.append(("contig", x, W1, W2, (cids, wts, S1, S2, w.w1_layout), None, int(ids.size)))
+    return samples
+
+
+def run_oracle_samples(samples):
+    import oracle
+    routes = 0
+    for kind, x, W1, W2, extra, _, n in samples:
+        if kind == "batched":
+            oracle.moe_layer_batched(x, [1], None, W1, W2)
+        else:
+            cids, wts, S1, S2, w1l = extra
+            oracle.moe_layer(x, cids, wts, W1, W2, w1_scale=S1, w2_scale=S2, w1_layout=w1l)
+        routes += n
+    return routes
+
+
+def cpu_baseline(args, insts):
+    import oracle
+    oracle.build()
+    samples = oracle_sample([i.w for i in insts], args.seed, insts)
+    t0 = time.perf_counter()
+    routes, reps = 0, 0
+    while True:
+        routes += run_oracle_samples(samples)
+        reps += 1
+        if time.perf_counter() - t0 > args.cpu_seconds or reps >= 50:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(routes / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} x (one token of each pass of the workload, all its routes; single-threaded C "
+                      f"oracle, fp64), {routes} routes in {dt:.1f} s on the host"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    ws = workload_list(args.workload)
+    samples = oracle_sample(ws, args.seed)
+    # each step: one token of one pass of the workload, rotating through the passes
+    for i in range(args.warmup):
+        run_oracle_samples([samples[i % len(samples)]])
+    t0 = time.perf_counter()
+    routes = 0
+    for i in range(args.steps):
+        routes += run_oracle_samples([samples[i % len(samples)]])
+    dt = time.perf_counter() - t0
+    value = routes / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(args.workload, ws),
+                   "sample": "each step: one token (all its routes) of one pass of the workload, passes in "
+                             "rotation, through the CPU oracle"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "one token of one pass per step, single-threaded fp64 C oracle"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -125,8 +125,9 @@ int moe_permute_align(const int32_t* topk_ids, int64_t T, int top_k, int E, int 
         MOE_REQUIRE(is_float_dtype(x_dtype), MOE_ERR_UNSUPPORTED, "moe_permute_align: x must be F32 or BF16");
         MOE_REQUIRE(K > 0 && (K * esize(x_dtype)) % 16 == 0, MOE_ERR_ALIGNMENT,
                     "moe_permute_align: K * element size must be a multiple of 16 bytes");
-        MOE_REQUIRE(x_out && aligned16(x) && aligned16(x_out), MOE_ERR_ALIGNMENT,
-                    "moe_permute_align: x and x_out must be non-null and 16-byte aligned");
+        MOE_REQUIRE(x_out || rows_cap == 0, MOE_ERR_INVALID_ARG, "moe_permute_align: x given without x_out");
+        MOE_REQUIRE(aligned16(x) && aligned16(x_out), MOE_ERR_ALIGNMENT,
+                    "moe_permute_align: x and x_out must be 16-byte aligned");
     }
     cudaStream_t s = as_stream(stream);
     int rc = launch_status(launch_permute(topk_ids, T, top_k, E, layout, block_m, max_tokens, expert_counts,

@@ -56,10 +56,11 @@ class MoELayer:
                 topk_ids: Optional[torch.Tensor] = None, topk_weights: Optional[torch.Tensor] = None,
                 w1_scale=None, w2_scale=None, w1_layout: int = B.MOE_W1_GATE_UP,
                 expert_num_tokens: Optional[torch.Tensor] = None, row_weights: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
+                stream=None, gemm1_events=None) -> torch.Tensor:
+        """Runs the layer; ``gemm1_events`` = (start, end) CUDA events recorded around the gate/up GEMM."""
         if self.layout == B.MOE_LAYOUT_BATCHED:
             return self._forward_batched(x, w1, w2, expert_num_tokens, row_weights, w1_scale, w2_scale, w1_layout,
-                                         stream)
+                                         stream, gemm1_events)
         if logits is not None:
             B.moe_topk_route(logits, self.top_k, True, self.ids, self.weights, stream=stream)
             ids, weights = self.ids, self.weights
@@ -69,8 +70,12 @@ class MoELayer:
                             rows_cap=self.rows_cap, expert_counts=self.counts, expert_offsets=self.offsets,
                             row_route=self.row_route, route_row=self.route_row, workspace=self.workspace,
                             err_word=self.err, stream=stream)
+        if gemm1_events is not None:
+            gemm1_events[0].record(stream)
         B.moe_gemm1_swiglu(self.x_perm, self.counts, self.offsets, w1, self.I, w1_scale=w1_scale,
                            w1_layout=w1_layout, impl=self.impl, h=self.h, err_word=self.err, stream=stream)
+        if gemm1_events is not None:
+            gemm1_events[1].record(stream)
         B.moe_gemm2(self.h, self.counts, self.offsets, w2, self.T * self.top_k, w2_scale=w2_scale,
                     row_route=self.row_route, route_weights=weights if self.weight_in_gemm2 else None,
                     impl=self.impl, y=self.y, err_word=self.err, stream=stream)
@@ -78,10 +83,15 @@ class MoELayer:
                                     stream=stream)
         return self.out
 
-    def _forward_batched(self, xb, w1, w2, counts, row_weights, w1_scale, w2_scale, w1_layout, stream):
+    def _forward_batched(self, xb, w1, w2, counts, row_weights, w1_scale, w2_scale, w1_layout, stream,
+                         gemm1_events=None):
+        if gemm1_events is not None:
+            gemm1_events[0].record(stream)
         B.moe_gemm1_swiglu(xb, counts, None, w1, self.I, layout=B.MOE_LAYOUT_BATCHED, max_tokens=self.max_tokens,
                            w1_scale=w1_scale, w1_layout=w1_layout, impl=self.impl, h=self.h, err_word=self.err,
                            stream=stream)
+        if gemm1_events is not None:
+            gemm1_events[1].record(stream)
         if self.weight_in_gemm2:
             B.moe_gemm2(self.h, counts, None, w2, self.rows_cap, layout=B.MOE_LAYOUT_BATCHED,
                         max_tokens=self.max_tokens, w2_scale=w2_scale, route_weights=row_weights, impl=self.impl,

@@ -155,6 +155,29 @@ MOE_API int moe_permute_align(const int32_t* topk_ids, int64_t T, int top_k, int
                       void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream);
 
 /*
+ * moe_permute_align_static -- moe_permute_align for callers that cannot
+ * allocate device memory.  The sources describe no such variant; it exists for
+ * callers with no allocator to hand: plugins inside a host framework that owns
+ * all device memory, request paths where cudaMalloc/cudaFree (which can
+ * synchronise the device) are forbidden, or deployments whose memory budget is
+ * fixed at start-up.  Arguments and results are those of moe_permute_align,
+ * without workspace and workspace_bytes: the scratch is a 2 MiB array built
+ * into the library, reserved on every GPU that loads it until the process
+ * exits.  This call allocates nothing.
+ *   - Routings needing more than 2 MiB of scratch (moe_permute_workspace_size
+ *     > 2 MiB, about 450k routes) return MOE_ERR_WORKSPACE_TOO_SMALL.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race and must be serialised by the caller.
+ */
+MOE_API int moe_permute_align_static(const int32_t* topk_ids, int64_t T, int top_k, int E,
+                                     int layout, int block_m, int max_tokens,
+                                     const void* x, int x_dtype, int64_t K, void* x_out, int64_t rows_cap,
+                                     int32_t* expert_counts, int32_t* expert_offsets,
+                                     int32_t* row_route, int32_t* route_row, int32_t* err_word, void* stream);
+
+/*
  * moe_gemm1_swiglu -- grouped GEMM with W1 fused with SiLU-and-mul
  * ("Fused MoE Modular Kernel", apply(): Matmul with W1, Act + Mul).
  * For every valid row s of expert e:

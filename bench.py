@@ -172,57 +172,120 @@ class Instance:
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples SM clock and clock-event reasons of one GPU while the timed region runs.
+
+    Polls NVML (libnvidia-ml, loaded with ctypes) every 2 ms from a thread, so
+    that even a timed region of a few tens of milliseconds gets many samples;
+    falls back to `nvidia-smi -lms 100` when NVML cannot be loaded.  Reads only.
+    """
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+        self.samples = []
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        self._smi = None
+
+    def _nvml(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        try:   # the CUDA device's PCI address (NVML numbers GPUs its own way)
+            import torch
+            pr = torch.cuda.get_device_properties(self.gpu)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) == 0
+        except (AttributeError, RuntimeError):
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            return None
+        return lib, h
 
     def __enter__(self):
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
+        import ctypes
+        import threading
+        nv = self._nvml()
+        if nv is None:
+            fd, self._path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=open(self._path, "w"), stderr=subprocess.DEVNULL)
+            except OSError:
+                self._smi = None
+            return self
+        lib, h = nv
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM = 1
+            self.max_mhz = float(mx.value)
+        self._stop = threading.Event()
+
+        def poll():
+            clk = ctypes.c_uint()
+            rs = ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                ok1 = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0
+                ok2 = lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0
+                if ok1:
+                    self.samples.append((float(clk.value), int(rs.value) if ok2 else 0))
+                time.sleep(0.002)
+
+        self._thread = threading.Thread(target=poll, daemon=True)
+        self._thread.start()
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=2)
+        if self._smi is not None:
+            self._smi.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._smi.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-
-    def summary(self):
-        rows = []
-        try:
-            with open(self.path) as f:
-                for line in f:
-                    parts = [p.strip() for p in line.split(",")]
-                    if len(parts) >= 9:
-                        rows.append(parts)
-        except OSError:
-            pass
-        finally:
+                self._smi.kill()
             try:
-                os.remove(self.path)
+                with open(self._path) as f:
+                    for line in f:
+                        parts = [p.strip() for p in line.split(",")]
+                        if len(parts) >= 6 and parts[0].replace(".", "").isdigit():
+                            bits = 0
+                            for b, v in zip((0x8, 0x40, 0x20, 0x4), parts[2:6]):
+                                if v.lower().startswith("active"):
+                                    bits |= b
+                            self.samples.append((float(parts[0]), bits))
+                            if parts[1].replace(".", "").isdigit():
+                                self.max_mhz = float(parts[1])
+                os.remove(self._path)
             except OSError:
                 pass
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
+        bits = 0
+        for _, b in self.samples:
+            bits |= b
+        reasons = sorted(name for b, name in self.REASONS.items() if bits & b)
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples),
+                "source": "nvml" if self._smi is None else "nvidia-smi"}
 
 
 # ----------------------------------------------------------------------------
@@ -259,6 +322,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
     ws = workload_list(args.workload)
+    if args.experts:
+        from mixture_experts_layer_permute_gb300 import workloads as wl
+        ws = [wl.scaled(w, E=args.experts) for w in ws]
     insts = [Instance(w, args.seed, dev) for w in ws]
     stream = torch.cuda.current_stream()
 
@@ -329,7 +395,7 @@ def run_ours(args, rank, world, local_rank):
                       "layer_bytes": inst.layer_bytes(), "layer_flops": inst.layer_flops(),
                       "gemm1_ms": round(g1_ms[n], 4), "roofline_ms": round(t_roof, 4)})
 
-    e2e = run_e2e(args, insts, dev) if rank == 0 or world > 1 else None
+    e2e = None if args.no_e2e else run_e2e(args, insts, dev)
     launches = sum(i.launches() for i in insts) * args.steps
     cpu = cpu_baseline(args, insts) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     if rank == 0:
@@ -515,6 +581,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling only: fewer experts than the workload (a small case for ncu)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -136,11 +136,7 @@ class Instance:
                          w2_scale=self.s2, w1_layout=w1_layout, gemm1_events=gemm1_events)
 
     def launches(self):
-        if self.w.layout == "batched":
-            return 2
-        R = self.w.T * self.w.top_k
-        n = 1 + (1 if R <= 1024 else 2) + 1 + 1 + 1 + 1     # (route) permute gather gemm1 gemm2 reduce
-        return n if self.logits is not None else n - 1
+        return self.layer.launches_per_forward()
 
     # algorithmic bytes / FLOPs (touched weights + scales + activations in + output; 6 K I flops per route)
     def gemm1_bytes(self):
@@ -336,17 +332,38 @@ def run_ours(args, rank, world, local_rank):
         step()
     torch.cuda.synchronize()
 
-    # per-launch events on the launching stream bracket GEMM 1 (the dominant kernel)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    # The K timed steps run as one captured CUDA graph (the launch sequence of a
+    # decode server), with external timing events around every GEMM 1 launch;
+    # --eager issues them from Python instead.
+    mode = "eager" if args.eager else "cuda_graph"
+    graph = None
+    ev = [[(torch.cuda.Event(enable_timing=True, external=not args.eager),
+            torch.cuda.Event(enable_timing=True, external=not args.eager))
            for _ in range(args.steps)] for _ in insts]
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for s in range(args.steps):
+                    step([e[s] for e in ev])
+            graph.replay()            # untimed: uploads the graph
+            torch.cuda.synchronize()
+        except Exception as exc:      # capture unavailable: time the same launches eagerly
+            print(f"bench: graph capture failed ({exc}); timing eagerly", file=sys.stderr)
+            graph, mode = None, "eager (capture failed)"
+            ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)] for _ in insts]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         start.record(stream)
-        for s in range(args.steps):
-            step([e[s] for e in ev])
+        if graph is not None:
+            graph.replay()
+        else:
+            for s in range(args.steps):
+                step([e[s] for e in ev])
         end.record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -404,6 +421,7 @@ def run_ours(args, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": insts[0].w.act, "data": "synthetic",
             "config": {"workload": describe(args.workload, ws), "parallelism": f"replicas x{world}",
+                       "launch": mode,
                        "l2": "inputs larger than L2 (touched expert weights exceed 129 MB every pass)",
                        "routes_per_step": routes_per_step},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
@@ -582,6 +600,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="issue the timed steps from Python, not as a CUDA graph")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: fewer experts than the workload (a small case for ncu)")
     args = ap.parse_args()

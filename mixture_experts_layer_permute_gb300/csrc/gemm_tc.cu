@@ -30,6 +30,7 @@
 #include <cuda.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 #include "internal.h"
@@ -427,6 +428,36 @@ int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
 
 constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024;
 
+// Tensor maps depend only on pointers and shapes, which repeat call after call:
+// they are encoded once and kept (up to 256 shapes; the cache is cleared when full).
+struct MapKey {
+    int dev;
+    const void* a;
+    const void* w;
+    int64_t kdim, rows_cap, wrows, I, K;
+    int E, gemm, swap, w_mode;
+    bool operator==(const MapKey& o) const {
+        return dev == o.dev && a == o.a && w == o.w && kdim == o.kdim && rows_cap == o.rows_cap && wrows == o.wrows && I == o.I &&
+               K == o.K && E == o.E && gemm == o.gemm && swap == o.swap && w_mode == o.w_mode;
+    }
+};
+
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        size_t h = std::hash<const void*>()(k.a) * 31 + std::hash<const void*>()(k.w);
+        h = h * 31 + std::hash<int64_t>()(k.kdim * 1000003 + k.rows_cap);
+        h = h * 31 + std::hash<int64_t>()(k.wrows * 7 + k.I * 13 + k.K * 17 + k.E);
+        return h * 31 + size_t(k.gemm * 8 + k.swap * 4 + k.w_mode + k.dev * 64);
+    }
+};
+
+struct MapPair {
+    CUtensorMap act, w;
+};
+
+std::mutex g_map_mu;
+std::unordered_map<MapKey, MapPair, MapKeyHash> g_maps;
+
 }  // namespace
 
 int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
@@ -444,30 +475,47 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     if (g.rows_cap >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: too many rows");
     if (g.rows_cap == 0) return MOE_OK;   // no rows, nothing to do
 
+    const int w_mode = (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    const MapKey key{dev_id, g.a, g.w, kdim, g.rows_cap, wrows, g.I, g.K, g.E, g.gemm, swap ? 1 : 0, w_mode};
     CUtensorMap tm_act, tm_w;
+    bool cached = false;
     {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            tm_act = it->second.act;
+            tm_w = it->second.w;
+            cached = true;
+        }
+    }
+    if (!cached) {
         cuuint64_t dims[2] = {cuuint64_t(kdim), cuuint64_t(g.rows_cap)};
         cuuint64_t str[1] = {cuuint64_t(kdim * 2)};
         cuuint32_t box[2] = {BK, cuuint32_t(swap ? TOK_BOX : BM)};
         int rc = make_map(&tm_act, g.a, 2, dims, str, box, "activations");
         if (rc) return rc;
     }
-    int w_mode = 0;
-    if (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) {
+    if (!cached && w_mode == 1) {
         // view W1[e] (2I, K) as (K, 16, 2, I/16): row = half*I + 16*blk + q
-        w_mode = 1;
         cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
         cuuint64_t str[4] = {cuuint64_t(g.K * 2), cuuint64_t(g.I * g.K * 2), cuuint64_t(16 * g.K * 2),
                              cuuint64_t(2 * g.I * g.K * 2)};
         cuuint32_t box[5] = {BK, 16, 2, cuuint32_t(wtile / 32), 1};
         int rc = make_map(&tm_w, g.w, 5, dims, str, box, "W1 (gate/up view)");
         if (rc) return rc;
-    } else {
+    } else if (!cached) {
         cuuint64_t dims[3] = {cuuint64_t(kdim), cuuint64_t(wrows), cuuint64_t(g.E)};
         cuuint64_t str[2] = {cuuint64_t(kdim * 2), cuuint64_t(wrows * kdim * 2)};
         cuuint32_t box[3] = {BK, cuuint32_t(wtile), 1};
         int rc = make_map(&tm_w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2");
         if (rc) return rc;
+    }
+    if (!cached) {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        if (g_maps.size() >= 256) g_maps.clear();
+        g_maps[key] = MapPair{tm_act, tm_w};
     }
 
     TcParams p;

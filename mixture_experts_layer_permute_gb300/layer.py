@@ -10,8 +10,12 @@ intermediates are declared up front and reused), and ``forward`` issues
 or, for the batched layout,
 
     moe_gemm1_swiglu -> moe_gemm2 (route weight in the epilogue)
+        [-> moe_batched_weight_reduce when the weight is not fused]
 
 with no host synchronisation.  Every step runs in libmoe_layer's kernels.
+The marshalled argument lists of the C calls are kept between calls with the
+same tensors and stream, so a decode step spends a few microseconds per call
+on the host; the calls also capture into a CUDA graph (``capture``).
 """
 from __future__ import annotations
 
@@ -22,6 +26,10 @@ import torch
 from . import binding as B
 
 
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
 class MoELayer:
     def __init__(self, T: int, K: int, I: int, E: int, top_k: int, act_dtype=torch.bfloat16, block_m: int = 1,
                  layout: int = B.MOE_LAYOUT_CONTIGUOUS, max_tokens: int = 0, impl: int = B.MOE_IMPL_AUTO,
@@ -30,6 +38,7 @@ class MoELayer:
         self.block_m, self.layout, self.max_tokens, self.impl = block_m, layout, max_tokens, impl
         self.weight_in_gemm2 = weight_in_gemm2
         self.act_dtype = act_dtype
+        self.lib = B.load()
         dev = torch.device(device)
         i32 = dict(dtype=torch.int32, device=dev)
         self.err = torch.zeros(1, **i32)
@@ -51,57 +60,108 @@ class MoELayer:
             self.rows_cap = E * max_tokens
             self.h = torch.empty((E, max_tokens, I), dtype=act_dtype, device=dev)
             self.out = torch.empty((E, max_tokens, K), dtype=act_dtype, device=dev)
+        self._plan_key = None
+        self._plan = None
 
+    # ---------------------------------------------------------------- planning
+    def _check_inputs(self, x, w1, w2, logits, topk_ids, topk_weights, w1_scale, w2_scale, counts, row_weights):
+        for t in (x, w1, w2, logits, topk_ids, topk_weights, w1_scale, w2_scale, counts, row_weights):
+            if t is not None and (not t.is_cuda or not t.is_contiguous()):
+                raise ValueError("MoELayer.forward takes contiguous device tensors")
+        if w1.shape[0] != self.E or w2.shape[0] != self.E:
+            raise ValueError("weight expert count does not match the layer")
+        if self.layout == B.MOE_LAYOUT_CONTIGUOUS:
+            if tuple(x.shape) != (self.T, self.K) or x.dtype != self.act_dtype:
+                raise ValueError(f"x must be ({self.T}, {self.K}) {self.act_dtype}")
+        elif tuple(x.shape) != (self.E, self.max_tokens, self.K):
+            raise ValueError(f"x must be ({self.E}, {self.max_tokens}, {self.K})")
+
+    def _build_plan(self, x, w1, w2, logits, topk_ids, topk_weights, w1_scale, w2_scale, w1_layout, counts,
+                    row_weights, stream):
+        lib = self.lib
+        adt = B.dtype_code(x)
+        wdt = B.dtype_code(w1, e4m3=w1_scale is not None)
+        I, K, E, T, k = self.I, self.K, self.E, self.T, self.top_k
+        calls = []
+        if self.layout == B.MOE_LAYOUT_BATCHED:
+            mt = self.max_tokens
+            calls.append((lib.moe_gemm1_swiglu, (x.data_ptr(), adt, self.layout, counts.data_ptr(), None, mt,
+                                                 self.rows_cap, E, K, I, w1.data_ptr(), _p(w1_scale), wdt,
+                                                 w1_layout, self.impl, self.h.data_ptr(), adt, self.err.data_ptr(),
+                                                 stream), "gemm1"))
+            rw = row_weights if self.weight_in_gemm2 else None
+            calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, self.layout, counts.data_ptr(), None, mt,
+                                          self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, None, _p(rw),
+                                          self.impl, self.out.data_ptr(), adt, self.rows_cap, self.err.data_ptr(),
+                                          stream), "gemm2"))
+            if not self.weight_in_gemm2:
+                calls.append((lib.moe_batched_weight_reduce, (self.out.data_ptr(), adt, counts.data_ptr(),
+                                                              _p(row_weights), E, mt, K, self.out.data_ptr(), adt,
+                                                              stream), "reduce"))
+            return calls
+        if logits is not None:
+            calls.append((lib.moe_topk_route, (logits.data_ptr(), T, logits.shape[1], k, 1, self.ids.data_ptr(),
+                                               self.weights.data_ptr(), stream), "route"))
+            ids, weights = self.ids, self.weights
+        else:
+            ids, weights = topk_ids, topk_weights
+        calls.append((lib.moe_permute_align, (ids.data_ptr(), T, k, E, self.layout, self.block_m, 0, x.data_ptr(),
+                                              adt, K, self.x_perm.data_ptr(), self.rows_cap,
+                                              self.counts.data_ptr(), self.offsets.data_ptr(),
+                                              self.row_route.data_ptr(), self.route_row.data_ptr(),
+                                              self.workspace.data_ptr(), self.workspace.numel(),
+                                              self.err.data_ptr(), stream), "permute"))
+        calls.append((lib.moe_gemm1_swiglu, (self.x_perm.data_ptr(), adt, self.layout, self.counts.data_ptr(),
+                                             self.offsets.data_ptr(), 0, self.rows_cap, E, K, I, w1.data_ptr(),
+                                             _p(w1_scale), wdt, w1_layout, self.impl, self.h.data_ptr(), adt,
+                                             self.err.data_ptr(), stream), "gemm1"))
+        rw = weights if self.weight_in_gemm2 else None
+        calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, self.layout, self.counts.data_ptr(),
+                                      self.offsets.data_ptr(), 0, self.rows_cap, E, K, I, w2.data_ptr(),
+                                      _p(w2_scale), wdt, self.row_route.data_ptr(), _p(rw), self.impl,
+                                      self.y.data_ptr(), adt, T * k, self.err.data_ptr(), stream), "gemm2"))
+        calls.append((lib.moe_unpermute_topk_reduce, (self.y.data_ptr(), adt, ids.data_ptr(),
+                                                      None if self.weight_in_gemm2 else weights.data_ptr(), T, k,
+                                                      E, K, self.out.data_ptr(), adt, stream), "reduce"))
+        return calls
+
+    # ---------------------------------------------------------------- running
     def forward(self, x: torch.Tensor, w1: torch.Tensor, w2: torch.Tensor, logits: Optional[torch.Tensor] = None,
                 topk_ids: Optional[torch.Tensor] = None, topk_weights: Optional[torch.Tensor] = None,
                 w1_scale=None, w2_scale=None, w1_layout: int = B.MOE_W1_GATE_UP,
                 expert_num_tokens: Optional[torch.Tensor] = None, row_weights: Optional[torch.Tensor] = None,
                 stream=None, gemm1_events=None) -> torch.Tensor:
-        """Runs the layer; ``gemm1_events`` = (start, end) CUDA events recorded around the gate/up GEMM."""
-        if self.layout == B.MOE_LAYOUT_BATCHED:
-            return self._forward_batched(x, w1, w2, expert_num_tokens, row_weights, w1_scale, w2_scale, w1_layout,
-                                         stream, gemm1_events)
-        if logits is not None:
-            B.moe_topk_route(logits, self.top_k, True, self.ids, self.weights, stream=stream)
-            ids, weights = self.ids, self.weights
-        else:
-            ids, weights = topk_ids, topk_weights
-        B.moe_permute_align(ids, self.E, B.MOE_LAYOUT_CONTIGUOUS, self.block_m, 0, x=x, x_out=self.x_perm,
-                            rows_cap=self.rows_cap, expert_counts=self.counts, expert_offsets=self.offsets,
-                            row_route=self.row_route, route_row=self.route_row, workspace=self.workspace,
-                            err_word=self.err, stream=stream)
-        if gemm1_events is not None:
-            gemm1_events[0].record(stream)
-        B.moe_gemm1_swiglu(self.x_perm, self.counts, self.offsets, w1, self.I, w1_scale=w1_scale,
-                           w1_layout=w1_layout, impl=self.impl, h=self.h, err_word=self.err, stream=stream)
-        if gemm1_events is not None:
-            gemm1_events[1].record(stream)
-        B.moe_gemm2(self.h, self.counts, self.offsets, w2, self.T * self.top_k, w2_scale=w2_scale,
-                    row_route=self.row_route, route_weights=weights if self.weight_in_gemm2 else None,
-                    impl=self.impl, y=self.y, err_word=self.err, stream=stream)
-        B.moe_unpermute_topk_reduce(self.y, ids, self.E, None if self.weight_in_gemm2 else weights, out=self.out,
-                                    stream=stream)
+        """Runs the layer on `stream` (default: the current stream) and returns the output buffer.
+
+        Contiguous layout: x (T, K) and either router `logits` (T, E) or `topk_ids`/`topk_weights` (T, top_k).
+        Batched layout: x (E, max_tokens, K), `expert_num_tokens` (E,), optional `row_weights` (E, max_tokens).
+        ``gemm1_events`` = (start, end) CUDA events recorded around the gate/up GEMM.
+        """
+        s = stream if stream is not None else torch.cuda.current_stream()
+        key = (_p(x), _p(w1), _p(w2), _p(logits), _p(topk_ids), _p(topk_weights), _p(w1_scale), _p(w2_scale),
+               w1_layout, _p(expert_num_tokens), _p(row_weights), s.cuda_stream)
+        if key != self._plan_key:
+            self._check_inputs(x, w1, w2, logits, topk_ids, topk_weights, w1_scale, w2_scale, expert_num_tokens,
+                               row_weights)
+            self._plan = self._build_plan(x, w1, w2, logits, topk_ids, topk_weights, w1_scale, w2_scale, w1_layout,
+                                          expert_num_tokens, row_weights, s.cuda_stream)
+            self._plan_key = key
+        for fn, args, name in self._plan:
+            if gemm1_events is not None and name == "gemm1":
+                gemm1_events[0].record(s)
+            rc = fn(*args)
+            if rc != B.MOE_OK:
+                B._check(rc)
+            if gemm1_events is not None and name == "gemm1":
+                gemm1_events[1].record(s)
         return self.out
 
-    def _forward_batched(self, xb, w1, w2, counts, row_weights, w1_scale, w2_scale, w1_layout, stream,
-                         gemm1_events=None):
-        if gemm1_events is not None:
-            gemm1_events[0].record(stream)
-        B.moe_gemm1_swiglu(xb, counts, None, w1, self.I, layout=B.MOE_LAYOUT_BATCHED, max_tokens=self.max_tokens,
-                           w1_scale=w1_scale, w1_layout=w1_layout, impl=self.impl, h=self.h, err_word=self.err,
-                           stream=stream)
-        if gemm1_events is not None:
-            gemm1_events[1].record(stream)
-        if self.weight_in_gemm2:
-            B.moe_gemm2(self.h, counts, None, w2, self.rows_cap, layout=B.MOE_LAYOUT_BATCHED,
-                        max_tokens=self.max_tokens, w2_scale=w2_scale, route_weights=row_weights, impl=self.impl,
-                        y=self.out, err_word=self.err, stream=stream)
-        else:
-            B.moe_gemm2(self.h, counts, None, w2, self.rows_cap, layout=B.MOE_LAYOUT_BATCHED,
-                        max_tokens=self.max_tokens, w2_scale=w2_scale, impl=self.impl, y=self.out,
-                        err_word=self.err, stream=stream)
-            B.moe_batched_weight_reduce(self.out, counts, row_weights, out=self.out, stream=stream)
-        return self.out
+    def launches_per_forward(self) -> int:
+        """Kernels one forward launches (for launch accounting)."""
+        if self.layout == B.MOE_LAYOUT_BATCHED:
+            return 2 if self.weight_in_gemm2 else 3
+        n = 3 + 1 + (1 if self.T * self.top_k <= 1024 else 2) + 1   # gemm1 gemm2 reduce, gather, permute, route
+        return n if any(name == "route" for _, _, name in (self._plan or [])) else n - 1
 
     def device_errors(self, reset: bool = True) -> int:
         """Device error bits (MOE_DEVERR_*) accumulated since the last reset (synchronises)."""

@@ -295,16 +295,22 @@ def kernel_source_hash():
 
 
 def recorded_traffic(workload):
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """GEMM 1 DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    p = os.path.join(ROOT, "profiles", f"gemm_tc_traffic_{'decode_sweep' if workload == 'decode' else workload}.txt")
+    fields = {}
     try:
         with open(p) as f:
-            d = json.load(f)
-    except (OSError, ValueError):
+            for line in f:
+                line = line.strip()
+                if line and not line.startswith("#"):
+                    k, _, v = line.partition(" ")
+                    fields[k] = v.split()
+    except OSError:
         return None
-    rec = d.get(workload)
-    if not rec or rec.get("gemm_tc_sha") != kernel_source_hash():
+    if fields.get("gemm_tc_sha", [None])[0] != kernel_source_hash() or fields.get("workload", [None])[0] != workload:
         return None
-    return rec.get("dram_bytes_per_launch")
+    vals = [int(v) for v in fields.get("gemm1_traffic_bytes", [])]
+    return vals or None
 
 
 # ----------------------------------------------------------------------------

@@ -103,7 +103,7 @@ def test_mxfp8_quantize_properties(oracle_mod):
             c = s - 127
             assert m <= math.ldexp(448.0, c) and (s == 0 or m > math.ldexp(448.0, c - 1))
             dec = np.array([oracle_mod.e4m3_to_double(int(q)) for q in codes[r, 32 * b:32 * b + 32]])
-            # each element is the nearest E4M3 value of x/scale (library cast as the judge)
+            # each element is the nearest E4M3 value of x/scale (the library cast decides)
             ref = torch.tensor(blk / math.ldexp(1.0, c), dtype=torch.float32).to(torch.float8_e4m3fn)
             assert np.array_equal(ref.view(torch.uint8).numpy(), codes[r, 32 * b:32 * b + 32])
             # round-trip error within half a unit in the last place of E4M3

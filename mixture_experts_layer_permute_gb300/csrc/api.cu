@@ -170,11 +170,14 @@ int validate_gemm(const GemmArgs& g, const char* name) {
 }
 
 int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
-    const bool tc_ok = g.a_dtype == MOE_BF16 && g.w_dtype == MOE_BF16 && device_cc() >= 100;
+    const bool tc_ok = g.a_dtype == MOE_BF16 && (g.w_dtype == MOE_BF16 || g.w_dtype == MOE_E4M3) &&
+                       g.out_dtype == MOE_BF16 && device_cc() >= 100;
     int chosen = impl;
     if (impl == MOE_IMPL_AUTO) {
         if (!tc_ok) {
             chosen = MOE_IMPL_SIMT;
+        } else if (g.w_dtype == MOE_E4M3) {
+            chosen = MOE_IMPL_TCGEN05_SWAP_AB;     // E4M3 weights are decoded on swap-AB tiles
         } else {
             // few routes per expert (decode): weight rows on the MMA M side
             int64_t rows = g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens;

@@ -24,6 +24,14 @@
 //   tile is read once for all of the expert's tokens.  Weight loads carry an
 //   L2 evict-first hint (the weights are streamed once).
 //
+// MXFP8 weights (E4M3 codes + one E8M0 scale per 32 along the contraction;
+//   "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): swap-AB tiles
+//   only.  TMA streams the raw codes (1 byte per weight, each read once), and
+//   eight converter warps (warps 6..13) decode them exactly to bf16
+//   (e4m3x2 -> f16x2 -> f32 x 2^(scale-127) -> bf16x2), writing the 128-byte
+//   swizzled A tile the MMA reads; a "converted" mbarrier per stage hands the
+//   tile to the MMA issuer.  Tokens per tile are capped at 64 here.
+//
 // Every mbarrier wait is bounded (2 s of globaltimer); on expiry the kernel
 // records MOE_DEVERR_TIMEOUT, lets its copies in flight land, frees TMEM and
 // returns.
@@ -43,20 +51,33 @@ namespace {
 constexpr int BM = 128;           // MMA M
 constexpr int BK = 64;            // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_ROWS = 256;
-constexpr int B_BYTES = B_ROWS * BK * 2;    // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
-constexpr int kThreads = 192;
 constexpr int TOK_BOX = 16;                 // swap-AB token rows per TMA box
+constexpr int MAX_STAGES = 6;
+constexpr int kConvThreads = 256;           // E4M3 converter warps 6..13
 constexpr uint64_t kWaitNs = 2000000000ull;
 
+// Per weight type: stage ring layout and CTA shape.
+//   bf16:  [A 16 KB][B 32 KB] x 4 stages, 192 threads, up to 256 tokens per swap-AB tile
+//   E4M3:  [A 16 KB (bf16, written by the converters)][B tokens 8 KB][codes 8 KB] x 6 stages,
+//          448 threads, up to 64 tokens per tile
+template <bool W8>
+struct Cfg {
+    static constexpr int STAGES = W8 ? 6 : 4;
+    static constexpr int B_BYTES = W8 ? 64 * BK * 2 : 256 * BK * 2;
+    static constexpr int CODE_OFF = A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = W8 ? A_BYTES + B_BYTES + BM * BK : A_BYTES + B_BYTES;
+    static constexpr int THREADS = W8 ? 192 + kConvThreads : 192;
+    static constexpr int TOK_SPAN = W8 ? 64 : 256;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+};
+
 struct __align__(8) Ctrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
+    uint64_t conv[MAX_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -83,6 +104,10 @@ struct TcParams {
     int out_dtype;
     int64_t out_rows;    // GEMM 2, contiguous: rows of y (routes)
     int32_t* err_word;
+    int span;            // activation rows per tile (normal: 128; swap: token segment)
+    const uint8_t* w_scale;   // E4M3 weights: E8M0 scales (E, wrows, kdim/32)
+    int64_t wrows;       // weight rows per expert
+    int64_t nsb;         // scale bytes per weight row (kdim / 32)
 };
 
 MOE_DEVICE bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl& c, int32_t* err_word) {
@@ -110,15 +135,53 @@ MOE_DEVICE Tile decode_tile(const ExpertTable& tab, const TcParams& p, int32_t t
     const int32_t local = t - tiles_before(tab, tl.e);
     const int32_t seg = local / p.nt;
     tl.nb = local - seg * p.nt;
-    const int span = p.swap ? 256 : BM;
-    tl.row0 = int64_t(tab.start[tl.e]) + int64_t(seg) * span;
-    tl.rows = min(span, tab.count[tl.e] - seg * span);
+    tl.row0 = int64_t(tab.start[tl.e]) + int64_t(seg) * p.span;
+    tl.rows = min(p.span, tab.count[tl.e] - seg * p.span);
     return tl;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Weight row (within the expert) held by row r of a 128-row swap-AB weight tile nb.
+MOE_DEVICE int64_t tile_weight_row(const TcParams& p, int nb, int r) {
+    if (p.w_mode == 1) {   // [gate; up] rows seen through the interleave-16 view
+        const int64_t unit = int64_t(nb) * 64 + (r >> 5) * 16 + (r & 15);
+        return ((r >> 4) & 1) * p.I + unit;
+    }
+    return int64_t(nb) * 128 + r;
+}
+
+// 32 E4M3 codes (one scale block) -> 32 bf16, exact: e4m3x2 -> f16x2, each half to
+// f32, times 2^(scale-127) (packed f32x2 multiply), rounded to bf16x2.
+MOE_DEVICE void dequant32(const uint4 (&c)[2], float scale, uint32_t (&o)[16]) {
+    const uint32_t w[8] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w};
+    uint64_t s2;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(scale));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint16_t pair = uint16_t(w[i] >> (16 * half));
+            uint32_t f16x2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+            float lo, hi;
+            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+                : "=f"(lo), "=f"(hi)
+                : "r"(f16x2));
+            uint64_t v2, r2;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(v2) : "f"(lo), "f"(hi));
+            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r2) : "l"(v2), "l"(s2));
+            float a, b;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r2));
+            o[2 * i + half] = pack_bf16x2(a, b);
+        }
+    }
+}
+
+template <bool W8>
+__global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
                    const TcParams p) {
+    constexpr int STAGES = Cfg<W8>::STAGES;
+    constexpr int STAGE_BYTES = Cfg<W8>::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
     __shared__ ExpertTable tab;
     __shared__ Ctrl ctrl;
@@ -133,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&ctrl.full[s], 1);
             ptx::mbar_init(&ctrl.empty[s], 1);
+            ptx::mbar_init(&ctrl.conv[s], kConvThreads);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&ctrl.acc_full[b], 1);
@@ -150,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(&ctrl.tmem_base, TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    const int span = p.swap ? 256 : BM;
+    const int span = p.span;
     const int ntl = p.nt;
     build_expert_table(tab, p.E, p.counts, p.offsets, p.max_tokens, p.rows_cap,
                        [span, ntl](int32_t c) { return ((c + span - 1) / span) * ntl; });
@@ -169,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
                 const Tile tl = decode_tile(tab, p, t);
                 const int nbox = p.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
-                const uint32_t bytes = p.swap ? uint32_t(A_BYTES + nbox * TOK_BOX * BK * 2) : uint32_t(STAGE_BYTES);
+                const uint32_t wbytes = W8 ? uint32_t(BM * BK) : uint32_t(A_BYTES);
+                const uint32_t bytes = p.swap ? wbytes + uint32_t(nbox * TOK_BOX * BK * 2) : uint32_t(STAGE_BYTES);
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -178,8 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sb = sa + A_BYTES;
                     ptx::mbar_arrive_expect_tx(&ctrl.full[s], bytes);
                     const int k0 = kb * BK;
-                    // weights: normal -> B operand (256 rows); swap -> A operand (128 rows)
-                    uint8_t* wdst = p.swap ? sa : sb;
+                    // weights: normal -> B operand (256 rows); swap -> A operand (128 rows);
+                    // E4M3 codes -> the converters' staging area
+                    uint8_t* wdst = W8 ? sa + Cfg<W8>::CODE_OFF : (p.swap ? sa : sb);
                     const int wrows = p.swap ? 128 : 256;
                     const int row_w = tl.nb * wrows;          // first weight row (interleaved order)
                     if (p.w_mode == 1)
@@ -224,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
+                    if (W8 && !wait_bar(&ctrl.conv[s], ph, ctrl, p.err_word)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
@@ -245,6 +312,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_wait_bounded(&ctrl.drain, 0, deadline, &never);
         }
         __syncwarp();
+    } else if (W8 && warp >= 6) {
+        // ------------------------------------------------------------ E4M3 converters
+        // thread ct: row r = ct / 2 of the 128-row weight tile, scale block h = ct % 2 of each k-block
+        const int ct = int(threadIdx.x) - 192, r = ct >> 1, h = ct & 1;
+        uint32_t it = 0;
+        for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
+            const Tile tl = decode_tile(tab, p, t);
+            const uint8_t* srow =
+                p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb + h;
+            bool ok = true;
+            for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+                if ((kb & 15) == 0 && kb + 16 < p.nkb)
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 2 * (kb + 16)));
+                const uint32_t code = __ldg(srow + 2 * kb);
+                const float scale = __uint_as_float(code ? code << 23 : 0x00400000u);   // 2^(code-127)
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
+                uint8_t* st = smem + s * STAGE_BYTES;
+                const uint4* src = reinterpret_cast<const uint4*>(st + Cfg<W8>::CODE_OFF + r * BK + h * 32);
+                uint4 c[2] = {src[0], src[1]};
+                uint32_t o[16];
+                dequant32(c, scale, o);
+                // bf16 row r, 16-byte chunks 4h..4h+3, 128-byte swizzle: chunk j lands at (j ^ (r % 8))
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int chunk = (4 * h + j) ^ (r & 7);
+                    *reinterpret_cast<uint4*>(st + r * 128 + chunk * 16) =
+                        make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                ptx::mbar_arrive(&ctrl.conv[s]);
+            }
+            if (!ok) break;
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
@@ -413,12 +515,14 @@ EncodeTiledFn encode_fn() {
 }
 
 int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
-             const cuuint32_t* box, const char* what) {
+             const cuuint32_t* box, const char* what, bool bytes = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(MOE_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base), dims,
-                    strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    // bf16 operands land 128-byte swizzled for the MMA; E4M3 codes land as plain rows for the converters
+    CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank),
+                    const_cast<void*>(base), dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(MOE_ERR_ALIGNMENT, std::string("cuTensorMapEncodeTiled failed for ") + what + " (CUresult " +
@@ -426,7 +530,6 @@ int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
     return MOE_OK;
 }
 
-constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024;
 
 // Tensor maps depend only on pointers and shapes, which repeat call after call:
 // they are encoded once and kept (up to 256 shapes; the cache is cleared when full).
@@ -460,9 +563,28 @@ std::unordered_map<MapKey, MapPair, MapKeyHash> g_maps;
 
 }  // namespace
 
+template <bool W8>
+int set_smem_attr() {
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && !done[dev]) {
+        if (cudaFuncSetAttribute(gemm_tc_kernel<W8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<W8>::SMEM) !=
+            cudaSuccess)
+            return fail(MOE_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem) failed");
+        done[dev] = true;
+    }
+    return MOE_OK;
+}
+
 int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
-    if (g.a_dtype != MOE_BF16 || g.w_dtype != MOE_BF16)
-        return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: bf16 activations and bf16 weights only");
+    const bool w8 = g.w_dtype == MOE_E4M3;
+    if (g.a_dtype != MOE_BF16 || (g.w_dtype != MOE_BF16 && !w8))
+        return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: bf16 activations with bf16 or E4M3 weights only");
+    if (w8 && !swap) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: E4M3 weights run on swap-AB tiles only");
+    if (w8 && !g.w_scale) return fail(MOE_ERR_INVALID_ARG, "tcgen05 path: E4M3 weights need scales");
     if (g.gemm == 1 && g.out_dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 GEMM 1 writes bf16 h");
     const int64_t kdim = g.gemm == 1 ? g.K : g.I;
     if (kdim % BK != 0) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: contraction length must be a multiple of 64");
@@ -478,7 +600,8 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     const int w_mode = (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0;
     int dev_id = 0;
     cudaGetDevice(&dev_id);
-    const MapKey key{dev_id, g.a, g.w, kdim, g.rows_cap, wrows, g.I, g.K, g.E, g.gemm, swap ? 1 : 0, w_mode};
+    const MapKey key{dev_id, g.a, g.w, kdim, g.rows_cap, wrows, g.I, g.K, g.E, g.gemm, (swap ? 1 : 0) | (w8 ? 2 : 0),
+                     w_mode};
     CUtensorMap tm_act, tm_w;
     bool cached = false;
     {
@@ -499,17 +622,19 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     }
     if (!cached && w_mode == 1) {
         // view W1[e] (2I, K) as (K, 16, 2, I/16): row = half*I + 16*blk + q
+        const int64_t es = w8 ? 1 : 2;
         cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
-        cuuint64_t str[4] = {cuuint64_t(g.K * 2), cuuint64_t(g.I * g.K * 2), cuuint64_t(16 * g.K * 2),
-                             cuuint64_t(2 * g.I * g.K * 2)};
+        cuuint64_t str[4] = {cuuint64_t(g.K * es), cuuint64_t(g.I * g.K * es), cuuint64_t(16 * g.K * es),
+                             cuuint64_t(2 * g.I * g.K * es)};
         cuuint32_t box[5] = {BK, 16, 2, cuuint32_t(wtile / 32), 1};
-        int rc = make_map(&tm_w, g.w, 5, dims, str, box, "W1 (gate/up view)");
+        int rc = make_map(&tm_w, g.w, 5, dims, str, box, "W1 (gate/up view)", w8);
         if (rc) return rc;
     } else if (!cached) {
+        const int64_t es = w8 ? 1 : 2;
         cuuint64_t dims[3] = {cuuint64_t(kdim), cuuint64_t(wrows), cuuint64_t(g.E)};
-        cuuint64_t str[2] = {cuuint64_t(kdim * 2), cuuint64_t(wrows * kdim * 2)};
+        cuuint64_t str[2] = {cuuint64_t(kdim * es), cuuint64_t(wrows * kdim * es)};
         cuuint32_t box[3] = {BK, cuuint32_t(wtile), 1};
-        int rc = make_map(&tm_w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2");
+        int rc = make_map(&tm_w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2", w8);
         if (rc) return rc;
     }
     if (!cached) {
@@ -538,29 +663,25 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     p.out_dtype = g.out_dtype;
     p.out_rows = g.out_rows;
     p.err_word = g.err_word;
+    p.span = swap ? (w8 ? Cfg<true>::TOK_SPAN : Cfg<false>::TOK_SPAN) : BM;
+    p.w_scale = g.w_scale;
+    p.wrows = wrows;
+    p.nsb = kdim / 32;
 
-    static std::mutex mu;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 64 && !attr_set[dev]) {
-            if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-                cudaSuccess)
-                return fail(MOE_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem) failed");
-            attr_set[dev] = true;
-        }
-    }
+    int rc = w8 ? set_smem_attr<true>() : set_smem_attr<false>();
+    if (rc) return rc;
     // upper bound on the tiles, then one CTA per SM at most
-    const int span = swap ? 256 : BM;
+    const int span = p.span;
     int64_t segs;
     if (g.layout == MOE_LAYOUT_CONTIGUOUS) segs = (g.rows_cap + span - 1) / span + g.E;
     else segs = int64_t(g.E) * ((g.max_tokens + span - 1) / span);
     const int64_t tiles = segs * p.nt;
     if (tiles == 0) return MOE_OK;
     const int grid = int(std::min<int64_t>(tiles, num_sms()));
-    gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_act, tm_w, p);
+    if (w8)
+        gemm_tc_kernel<true><<<grid, Cfg<true>::THREADS, Cfg<true>::SMEM, s>>>(tm_act, tm_w, p);
+    else
+        gemm_tc_kernel<false><<<grid, Cfg<false>::THREADS, Cfg<false>::SMEM, s>>>(tm_act, tm_w, p);
     return check_launch("gemm_tc_kernel");
 }
 

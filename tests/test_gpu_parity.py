@@ -261,6 +261,74 @@ def test_gemm2(moe, impl, shape, weighted):
     assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 {impl}")
 
 
+E4M3_SHAPES = [  # T, k, E, K, I
+    (96, 4, 8, 512, 256),            # ~48 tokens per expert
+    (300, 1, 2, 256, 128),           # ~150 tokens per expert: three 64-token segments
+    (5, 8, 64, 512, 128),            # decode-like
+]
+
+
+def _e4m3_weights(moe, W):
+    """Quantise fp32 weights with the library (codes are checked bit-exact elsewhere) and by the oracle."""
+    W = W.clone()
+    W[0, 3, :64] = 0.0                                  # an all-zero block and zero codes
+    W[0, 5, :32] *= 1e-3                                # subnormal codes next to normal ones
+    W[0, 5, 7] = 2.0
+    codes, scales = moe.mxfp8_quantize_block32(W.to(DEV))
+    rc, rs = oracle.mxfp8_quantize(W.numpy())
+    assert np.array_equal(codes.cpu().numpy(), rc) and np.array_equal(scales.cpu().numpy(), rs)
+    return codes, scales, rc, rs
+
+
+@pytest.mark.parametrize("impl", ["swap_ab", "auto", "simt"])
+@pytest.mark.parametrize("shape", E4M3_SHAPES)
+@pytest.mark.parametrize("w1_layout", [0, 1])
+def test_gemm1_swiglu_e4m3(moe, impl, shape, w1_layout):
+    T, k, E, K, I = shape
+    w, x, ids, _ = _routed(T, k, E, K, seed=T + 3 * E)
+    W1 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8"), "W1", 5)
+    c1, s1, rc1, rs1 = _e4m3_weights(moe, W1)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    h = moe.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], c1, I, w1_scale=s1,
+                             w1_layout=w1_layout, impl=_impl(moe, impl))
+    href = oracle.expert_gate_up(wl.to_numpy(x)[np.arange(T * k) // k], ids.reshape(-1), rc1, w1_scale=rs1,
+                                 w1_layout=w1_layout)
+    rr = res["route_row"].cpu().numpy().reshape(-1)
+    assert_close(to_f64(h.cpu()[torch.from_numpy(rr).long()]), href, TOL_BF16, f"gemm1 e4m3 {impl}")
+
+
+@pytest.mark.parametrize("impl", ["swap_ab", "simt"])
+@pytest.mark.parametrize("shape", E4M3_SHAPES)
+def test_gemm2_e4m3(moe, impl, shape):
+    T, k, E, K, I = shape
+    w, _, ids, weights = _routed(T, k, E, K, seed=T + 4 * E)
+    W2 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8"), "W2", 6)
+    c2, s2, rc2, rs2 = _e4m3_weights(moe, W2)
+    R = T * k
+    hsrc = wl._normal((R, I), 1.0, 8, "h", 0, "cpu", torch.bfloat16)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1)
+    hperm = torch.zeros((res["rows_cap"], I), dtype=torch.bfloat16, device=DEV)
+    hperm[res["route_row"].view(-1).long()] = hsrc.to(DEV)
+    wt = torch.from_numpy(weights).to(DEV).reshape(-1)
+    y = moe.moe_gemm2(hperm, res["counts"], res["offsets"], c2, R, w2_scale=s2, row_route=res["row_route"],
+                      route_weights=wt, impl=_impl(moe, impl))
+    yref = oracle.expert_down(wl.to_numpy(hsrc), ids.reshape(-1), rc2, w2_scale=rs2)
+    yref = yref * weights.reshape(-1, 1).astype(np.float64)
+    assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 e4m3 {impl}")
+
+
+def test_e4m3_normal_tiles_unsupported_but_auto_works(moe):
+    T, k, E, K, I = 64, 2, 4, 256, 128
+    w, x, ids, _ = _routed(T, k, E, K, seed=11)
+    W1 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8"), "W1", 7)
+    c1, s1 = moe.mxfp8_quantize_block32(W1.to(DEV))
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], c1, I, w1_scale=s1,
+                             impl=moe.MOE_IMPL_TCGEN05)
+    assert ei.value.status == 2
+
+
 def test_gemm_unsupported_shape_falls_back_under_auto(moe):
     """K not a multiple of 64: AUTO uses the CUDA-core tiles; forcing tcgen05 reports UNSUPPORTED."""
     T, k, E, K, I = 20, 2, 4, 96, 64

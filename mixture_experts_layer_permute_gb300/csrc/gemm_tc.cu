@@ -27,10 +27,13 @@
 // MXFP8 weights (E4M3 codes + one E8M0 scale per 32 along the contraction;
 //   "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): swap-AB tiles
 //   only.  TMA streams the raw codes (1 byte per weight, each read once), and
-//   eight converter warps (warps 6..13) decode them exactly to bf16
+//   sixteen converter warps (warps 6..21) decode them exactly to bf16
 //   (e4m3x2 -> f16x2 -> f32 x 2^(scale-127) -> bf16x2), writing the 128-byte
 //   swizzled A tile the MMA reads; a "converted" mbarrier per stage hands the
-//   tile to the MMA issuer.  Tokens per tile are capped at 64 here.
+//   tile to the MMA issuer.  Tokens per tile are capped at 64 here.  Each
+//   converter thread owns one 16-byte chunk (16 codes) of the k-block, so the
+//   chunk reads are consecutive across a warp, and it keeps the E8M0 scales
+//   of its row for 8 k-blocks in registers, loading the next 8 ahead.
 //
 // Every mbarrier wait is bounded (2 s of globaltimer); on expiry the kernel
 // records MOE_DEVERR_TIMEOUT, lets its copies in flight land, frees TMEM and
@@ -56,13 +59,13 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int TOK_BOX = 16;                 // swap-AB token rows per TMA box
 constexpr int MAX_STAGES = 6;
-constexpr int kConvThreads = 256;           // E4M3 converter warps 6..13
+constexpr int kConvThreads = 512;           // E4M3 converter warps 6..21
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // Per weight type: stage ring layout and CTA shape.
 //   bf16:  [A 16 KB][B 32 KB] x 4 stages, 192 threads, up to 256 tokens per swap-AB tile
 //   E4M3:  [A 16 KB (bf16, written by the converters)][B tokens 8 KB][codes 8 KB] x 6 stages,
-//          448 threads, up to 64 tokens per tile
+//          704 threads, up to 64 tokens per tile
 template <bool W8>
 struct Cfg {
     static constexpr int STAGES = W8 ? 6 : 4;
@@ -149,14 +152,14 @@ MOE_DEVICE int64_t tile_weight_row(const TcParams& p, int nb, int r) {
     return int64_t(nb) * 128 + r;
 }
 
-// 32 E4M3 codes (one scale block) -> 32 bf16, exact: e4m3x2 -> f16x2, each half to
-// f32, times 2^(scale-127) (packed f32x2 multiply), rounded to bf16x2.
-MOE_DEVICE void dequant32(const uint4 (&c)[2], float scale, uint32_t (&o)[16]) {
-    const uint32_t w[8] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w};
+// 16 E4M3 codes -> 16 bf16, exact: e4m3x2 -> f16x2, each half to f32, times
+// 2^(scale-127) (packed f32x2 multiply), rounded to bf16x2.
+MOE_DEVICE void dequant16(const uint4 c, float scale, uint32_t (&o)[8]) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
     uint64_t s2;
     asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(scale));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const uint16_t pair = uint16_t(w[i] >> (16 * half));
@@ -174,6 +177,10 @@ MOE_DEVICE void dequant32(const uint4 (&c)[2], float scale, uint32_t (&o)[16]) {
             o[2 * i + half] = pack_bf16x2(a, b);
         }
     }
+}
+
+MOE_DEVICE float e8m0_scale(uint32_t code) {   // 2^(code-127); code 0 is the subnormal 2^-127
+    return __uint_as_float(code ? code << 23 : 0x00400000u);
 }
 
 template <bool W8>
@@ -314,31 +321,46 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters
-        // thread ct: row r = ct / 2 of the 128-row weight tile, scale block h = ct % 2 of each k-block
-        const int ct = int(threadIdx.x) - 192, r = ct >> 1, h = ct & 1;
+        // thread ct owns 16-byte chunk ct of the 128 x 64-byte code tile: row r = ct / 4, codes
+        // 16*(ct % 4) .. +15, which belong to scale block h = (ct % 4) / 2 of the k-block
+        const int ct = int(threadIdx.x) - 192, r = ct >> 2, sub = ct & 3, h = sub >> 1;
+        const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows
         uint32_t it = 0;
         for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
             const Tile tl = decode_tile(tab, p, t);
-            const uint8_t* srow =
-                p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb + h;
+            const uint8_t* srow = p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb;
+            // scales of 8 k-blocks (16 bytes) per register group; the next group is loaded one group ahead
+            uint4 cur = make_uint4(0, 0, 0, 0), nxt = make_uint4(0, 0, 0, 0);
+            if (vec_scales) {
+                cur = __ldg(reinterpret_cast<const uint4*>(srow));
+                if (p.nkb > 8) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 16));
+            }
             bool ok = true;
             for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                if ((kb & 15) == 0 && kb + 16 < p.nkb)
-                    asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 2 * (kb + 16)));
-                const uint32_t code = __ldg(srow + 2 * kb);
-                const float scale = __uint_as_float(code ? code << 23 : 0x00400000u);   // 2^(code-127)
+                uint32_t code;
+                if (vec_scales) {
+                    const int j = 2 * (kb & 7) + h;
+                    const uint32_t word = j < 4 ? cur.x : (j < 8 ? cur.y : (j < 12 ? cur.z : cur.w));
+                    code = (word >> (8 * (j & 3))) & 0xFFu;
+                    if ((kb & 7) == 7) {
+                        cur = nxt;
+                        if (kb + 9 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 2 * (kb + 9)));
+                    }
+                } else {
+                    code = __ldg(srow + 2 * kb + h);
+                }
+                const float scale = e8m0_scale(code);
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
                 uint8_t* st = smem + s * STAGE_BYTES;
-                const uint4* src = reinterpret_cast<const uint4*>(st + Cfg<W8>::CODE_OFF + r * BK + h * 32);
-                uint4 c[2] = {src[0], src[1]};
-                uint32_t o[16];
-                dequant32(c, scale, o);
-                // bf16 row r, 16-byte chunks 4h..4h+3, 128-byte swizzle: chunk j lands at (j ^ (r % 8))
+                const uint4 c = reinterpret_cast<const uint4*>(st + Cfg<W8>::CODE_OFF)[ct];
+                uint32_t o[8];
+                dequant16(c, scale, o);
+                // bf16 row r, 16-byte chunks 2*sub and 2*sub+1, 128-byte swizzle: chunk j lands at j ^ (r % 8)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int chunk = (4 * h + j) ^ (r & 7);
+                for (int j = 0; j < 2; ++j) {
+                    const int chunk = (2 * sub + j) ^ (r & 7);
                     *reinterpret_cast<uint4*>(st + r * 128 + chunk * 16) =
                         make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
                 }

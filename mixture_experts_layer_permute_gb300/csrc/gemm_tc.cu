@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&ctrl.full[s], 1);
             ptx::mbar_init(&ctrl.empty[s], 1);
-            ptx::mbar_init(&ctrl.conv[s], kConvThreads);
+            ptx::mbar_init(&ctrl.conv[s], kConvThreads / 32);   // one arrive per converter warp
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&ctrl.acc_full[b], 1);
@@ -364,8 +364,11 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     *reinterpret_cast<uint4*>(st + r * 128 + chunk * 16) =
                         make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
                 }
+                // each thread makes its generic-proxy writes visible to the tensor core, then one
+                // lane per warp arrives (512 arrivals on one barrier word would serialise)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                ptx::mbar_arrive(&ctrl.conv[s]);
+                __syncwarp();
+                if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&ctrl.conv[s]);
             }
             if (!ok) break;
         }

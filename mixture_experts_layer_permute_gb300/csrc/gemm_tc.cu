@@ -26,14 +26,16 @@
 //
 // MXFP8 weights (E4M3 codes + one E8M0 scale per 32 along the contraction;
 //   "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): swap-AB tiles
-//   only.  TMA streams the raw codes (1 byte per weight, each read once), and
-//   sixteen converter warps (warps 6..21) decode them exactly to bf16
-//   (e4m3x2 -> f16x2 -> f32 x 2^(scale-127) -> bf16x2), writing the 128-byte
-//   swizzled A tile the MMA reads; a "converted" mbarrier per stage hands the
-//   tile to the MMA issuer.  Tokens per tile are capped at 64 here.  Each
-//   converter thread owns one 16-byte chunk (16 codes) of the k-block, so the
-//   chunk reads are consecutive across a warp, and it keeps the E8M0 scales
-//   of its row for 8 k-blocks in registers, loading the next 8 ahead.
+//   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
+//   12-stage ring, as four 16-byte-wide column boxes per k-block so that the
+//   rows of one 16-code column are contiguous.  Sixteen converter warps
+//   (warps 6..21) decode them exactly to bf16 (e4m3x2 -> f16x2 -> f32 x
+//   2^(scale-127) -> bf16x2) and store the tile straight into tensor memory
+//   with tcgen05.st; the MMA takes its A operand from TMEM.  Warp w may only
+//   reach TMEM lanes 32*(w%4)..+31, so it converts those 32 rows' column
+//   (w-6)/4.  A "converted" mbarrier per stage hands the tile to the MMA
+//   issuer.  Each thread keeps the E8M0 scales of its row for 8 k-blocks in
+//   registers, loading the next 8 ahead.  Tokens per tile are capped at 64.
 //
 // Every mbarrier wait is bounded (2 s of globaltimer); on expiry the kernel
 // records MOE_DEVERR_TIMEOUT, lets its copies in flight land, frees TMEM and
@@ -58,23 +60,27 @@ constexpr int A_BYTES = BM * BK * 2;        // 16 KB
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int TOK_BOX = 16;                 // swap-AB token rows per TMA box
-constexpr int MAX_STAGES = 6;
+constexpr int MAX_STAGES = 12;
 constexpr int kConvThreads = 512;           // E4M3 converter warps 6..21
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// Per weight type: stage ring layout and CTA shape.
-//   bf16:  [A 16 KB][B 32 KB] x 4 stages, 192 threads, up to 256 tokens per swap-AB tile
-//   E4M3:  [A 16 KB (bf16, written by the converters)][B tokens 8 KB][codes 8 KB] x 6 stages,
-//          704 threads, up to 64 tokens per tile
+// Per weight type: stage ring layout, TMEM map and CTA shape.
+//   bf16:  smem [A 16 KB][B 32 KB] x 4 stages; TMEM: two 256-column accumulators;
+//          192 threads; up to 256 tokens per swap-AB tile
+//   E4M3:  smem [codes 8 KB = 4 column boxes of 128 rows x 16 B][B tokens 8 KB] x 12 stages;
+//          TMEM: two 64-column accumulators, then 12 bf16 A tiles of 32 columns;
+//          704 threads; up to 64 tokens per tile
 template <bool W8>
 struct Cfg {
-    static constexpr int STAGES = W8 ? 6 : 4;
+    static constexpr int STAGES = W8 ? 12 : 4;
+    static constexpr int B_OFF = W8 ? BM * BK : A_BYTES;        // tokens (swap) / weights (normal)
     static constexpr int B_BYTES = W8 ? 64 * BK * 2 : 256 * BK * 2;
-    static constexpr int CODE_OFF = A_BYTES + B_BYTES;
-    static constexpr int STAGE_BYTES = W8 ? A_BYTES + B_BYTES + BM * BK : A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
     static constexpr int THREADS = W8 ? 192 + kConvThreads : 192;
     static constexpr int TOK_SPAN = W8 ? 64 : 256;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+    static constexpr int ACC_STRIDE = W8 ? 64 : ACC_COLS;       // TMEM columns per accumulator
+    static constexpr int A_TMEM = 2 * ACC_STRIDE;               // E4M3: first A tile column
 };
 
 struct __align__(8) Ctrl {
@@ -241,24 +247,30 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 const Tile tl = decode_tile(tab, p, t);
                 const int nbox = p.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
                 const uint32_t wbytes = W8 ? uint32_t(BM * BK) : uint32_t(A_BYTES);
-                const uint32_t bytes = p.swap ? wbytes + uint32_t(nbox * TOK_BOX * BK * 2) : uint32_t(STAGE_BYTES);
+                const uint32_t bytes =
+                    p.swap ? wbytes + uint32_t(nbox * TOK_BOX * BK * 2) : uint32_t(A_BYTES + Cfg<W8>::B_BYTES);
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!wait_bar(&ctrl.empty[s], ph ^ 1, ctrl, p.err_word)) break;
                     uint8_t* sa = smem + s * STAGE_BYTES;
-                    uint8_t* sb = sa + A_BYTES;
+                    uint8_t* sb = sa + Cfg<W8>::B_OFF;
                     ptx::mbar_arrive_expect_tx(&ctrl.full[s], bytes);
                     const int k0 = kb * BK;
                     // weights: normal -> B operand (256 rows); swap -> A operand (128 rows);
-                    // E4M3 codes -> the converters' staging area
-                    uint8_t* wdst = W8 ? sa + Cfg<W8>::CODE_OFF : (p.swap ? sa : sb);
+                    // E4M3 codes -> four 16-code column boxes for the converters
+                    uint8_t* wdst = W8 ? sa : (p.swap ? sa : sb);
                     const int wrows = p.swap ? 128 : 256;
                     const int row_w = tl.nb * wrows;          // first weight row (interleaved order)
-                    if (p.w_mode == 1)
-                        ptx::tma_load_5d(wdst, &tm_w, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_w);
-                    else
-                        ptx::tma_load_3d(wdst, &tm_w, &ctrl.full[s], k0, row_w, tl.e, pol_w);
+#pragma unroll 1
+                    for (int cbox = 0; cbox < (W8 ? 4 : 1); ++cbox) {
+                        const int kc = k0 + cbox * 16;
+                        uint8_t* dst = wdst + cbox * (BM * 16);
+                        if (p.w_mode == 1)
+                            ptx::tma_load_5d(dst, &tm_w, &ctrl.full[s], kc, 0, 0, row_w / 32, tl.e, pol_w);
+                        else
+                            ptx::tma_load_3d(dst, &tm_w, &ctrl.full[s], kc, row_w, tl.e, pol_w);
+                    }
                     if (p.swap) {
                         for (int b = 0; b < nbox; ++b)
                             ptx::tma_load_2d(sb + b * TOK_BOX * BK * 2, &tm_act, &ctrl.full[s], k0,
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 int n_mma = 256;
                 if (p.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
                 const uint32_t idesc = ptx::idesc_bf16(BM, n_mma);
-                const uint32_t d_tmem = tmem_base + uint32_t(buf * ACC_COLS);
+                const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg<W8>::ACC_STRIDE);
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -300,12 +312,18 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     if (W8 && !wait_bar(&ctrl.conv[s], ph, ctrl, p.err_word)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t sb = sa + Cfg<W8>::B_OFF;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
                         const uint64_t bd = ptx::smem_desc_sw128(sb + kk * UMMA_K * 2);
-                        ptx::mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        if constexpr (W8) {
+                            // A from TMEM: 16 bf16 of a row = 8 columns per k step
+                            const uint32_t a_tmem = tmem_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2) + kk * 8);
+                            ptx::mma_f16_tmem_a(d_tmem, a_tmem, bd, idesc, (kb | kk) != 0);
+                        } else {
+                            const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
+                            ptx::mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        }
                     }
                     ptx::mma_commit(&ctrl.empty[s]);
                 }
@@ -321,9 +339,10 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters
-        // thread ct owns 16-byte chunk ct of the 128 x 64-byte code tile: row r = ct / 4, codes
-        // 16*(ct % 4) .. +15, which belong to scale block h = (ct % 4) / 2 of the k-block
-        const int ct = int(threadIdx.x) - 192, r = ct >> 2, sub = ct & 3, h = sub >> 1;
+        // warp w converts column box (w-6)/4 (codes 16*cb .. +15 of the k-block) of the 32 rows in
+        // its TMEM lane quarter: row r = 32*(w%4) + lane, scale block h = cb / 2 of the k-block
+        const int q = warp & 3, cb = (warp - 6) >> 2, r = q * 32 + lane, h = cb >> 1;
+        const uint32_t lane_base = uint32_t(q * 32) << 16;
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows
         uint32_t it = 0;
         for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
@@ -353,22 +372,14 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                uint8_t* st = smem + s * STAGE_BYTES;
-                const uint4 c = reinterpret_cast<const uint4*>(st + Cfg<W8>::CODE_OFF)[ct];
+                const uint4 c = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + cb * (BM * 16))[r];
                 uint32_t o[8];
                 dequant16(c, scale, o);
-                // bf16 row r, 16-byte chunks 2*sub and 2*sub+1, 128-byte swizzle: chunk j lands at j ^ (r % 8)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int chunk = (2 * sub + j) ^ (r & 7);
-                    *reinterpret_cast<uint4*>(st + r * 128 + chunk * 16) =
-                        make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                }
-                // each thread makes its generic-proxy writes visible to the tensor core, then one
-                // lane per warp arrives (512 arrivals on one barrier word would serialise)
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                ptx::tmem_st_32x32b_x8(tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2) + cb * 8), o);
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
                 __syncwarp();
-                if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&ctrl.conv[s]);
+                if (lane == 0) ptx::mbar_arrive(&ctrl.conv[s]);
             }
             if (!ok) break;
         }
@@ -383,7 +394,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             const uint32_t aph = (tc >> 1) & 1;
             if (!wait_bar(&ctrl.acc_full[buf], aph, ctrl, p.err_word)) break;
             ptx::tc_fence_after();
-            const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * ACC_COLS);
+            const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * Cfg<W8>::ACC_STRIDE);
             if (!p.swap) {
                 const int r = q * 32 + lane;                  // tile row of this thread
                 const bool valid = r < tl.rows;
@@ -651,14 +662,14 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
         cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
         cuuint64_t str[4] = {cuuint64_t(g.K * es), cuuint64_t(g.I * g.K * es), cuuint64_t(16 * g.K * es),
                              cuuint64_t(2 * g.I * g.K * es)};
-        cuuint32_t box[5] = {BK, 16, 2, cuuint32_t(wtile / 32), 1};
+        cuuint32_t box[5] = {cuuint32_t(w8 ? 16 : BK), 16, 2, cuuint32_t(wtile / 32), 1};
         int rc = make_map(&tm_w, g.w, 5, dims, str, box, "W1 (gate/up view)", w8);
         if (rc) return rc;
     } else if (!cached) {
         const int64_t es = w8 ? 1 : 2;
         cuuint64_t dims[3] = {cuuint64_t(kdim), cuuint64_t(wrows), cuuint64_t(g.E)};
         cuuint64_t str[2] = {cuuint64_t(kdim * es), cuuint64_t(wrows * kdim * es)};
-        cuuint32_t box[3] = {BK, cuuint32_t(wtile), 1};
+        cuuint32_t box[3] = {cuuint32_t(w8 ? 16 : BK), cuuint32_t(wtile), 1};
         int rc = make_map(&tm_w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2", w8);
         if (rc) return rc;
     }

@@ -27,15 +27,17 @@
 // MXFP8 weights (E4M3 codes + one E8M0 scale per 32 along the contraction;
 //   "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): swap-AB tiles
 //   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
-//   12-stage ring, as four 16-byte-wide column boxes per k-block so that the
-//   rows of one 16-code column are contiguous.  Sixteen converter warps
-//   (warps 6..21) decode them exactly to bf16 (e4m3x2 -> f16x2 -> f32 x
-//   2^(scale-127) -> bf16x2) and store the tile straight into tensor memory
-//   with tcgen05.st; the MMA takes its A operand from TMEM.  Warp w may only
-//   reach TMEM lanes 32*(w%4)..+31, so it converts those 32 rows' column
-//   (w-6)/4.  A "converted" mbarrier per stage hands the tile to the MMA
-//   issuer.  Each thread keeps the E8M0 scales of its row for 8 k-blocks in
-//   registers, loading the next 8 ahead.  Tokens per tile are capped at 64.
+//   12-stage ring.  Four converter warps (warps 6..9) decode them exactly to
+//   bf16 and store the tile straight into tensor memory with tcgen05.st; the
+//   MMA takes its A operand from TMEM.  Warp w may only reach TMEM lanes
+//   32*(w%4)..+31, so thread (w, lane) owns row 32*(w%4)+lane: 64 codes and 2
+//   scales per k-block.  Decoding needs no conversion instruction: the E4M3
+//   bits placed into bf16 bit positions (sign to bit 15, exponent and
+//   mantissa to bits 10..4) give exactly code * 2^-120 for normal, subnormal
+//   and zero codes alike, and one bf16x2 multiply by 2^(scale-7) restores the
+//   value (two multiplies when that factor would leave bf16's range).  A
+//   "converted" mbarrier per stage hands the tile to the MMA issuer.  Tokens
+//   per tile are capped at 64.
 //
 // Every mbarrier wait is bounded (2 s of globaltimer); on expiry the kernel
 // records MOE_DEVERR_TIMEOUT, lets its copies in flight land, frees TMEM and
@@ -61,15 +63,15 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int TOK_BOX = 16;                 // swap-AB token rows per TMA box
 constexpr int MAX_STAGES = 12;
-constexpr int kConvThreads = 512;           // E4M3 converter warps 6..21
+constexpr int kConvThreads = 128;           // E4M3 converter warps 6..9
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // Per weight type: stage ring layout, TMEM map and CTA shape.
 //   bf16:  smem [A 16 KB][B 32 KB] x 4 stages; TMEM: two 256-column accumulators;
 //          192 threads; up to 256 tokens per swap-AB tile
-//   E4M3:  smem [codes 8 KB = 4 column boxes of 128 rows x 16 B][B tokens 8 KB] x 12 stages;
+//   E4M3:  smem [codes 128 rows x 64 B][B tokens 8 KB] x 12 stages;
 //          TMEM: two 64-column accumulators, then 12 bf16 A tiles of 32 columns;
-//          704 threads; up to 64 tokens per tile
+//          320 threads; up to 64 tokens per tile
 template <bool W8>
 struct Cfg {
     static constexpr int STAGES = W8 ? 12 : 4;
@@ -158,35 +160,30 @@ MOE_DEVICE int64_t tile_weight_row(const TcParams& p, int nb, int r) {
     return int64_t(nb) * 128 + r;
 }
 
-// 16 E4M3 codes -> 16 bf16, exact: e4m3x2 -> f16x2, each half to f32, times
-// 2^(scale-127) (packed f32x2 multiply), rounded to bf16x2.
-MOE_DEVICE void dequant16(const uint4 c, float scale, uint32_t (&o)[8]) {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    uint64_t s2;
-    asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(scale));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint16_t pair = uint16_t(w[i] >> (16 * half));
-            uint32_t f16x2;
-            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
-            float lo, hi;
-            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
-                : "=f"(lo), "=f"(hi)
-                : "r"(f16x2));
-            uint64_t v2, r2;
-            asm("mov.b64 %0, {%1, %2};" : "=l"(v2) : "f"(lo), "f"(hi));
-            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r2) : "l"(v2), "l"(s2));
-            float a, b;
-            asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r2));
-            o[2 * i + half] = pack_bf16x2(a, b);
-        }
-    }
+// bf16x2 factors that turn code * 2^-120 into code * 2^(scale-127): f1 = 2^(scale-7) when that is a
+// bf16 normal (scale <= 134), else f1 = 2^(scale-127) and f2 = 2^120.
+MOE_DEVICE void e8m0_factors(uint32_t code, uint32_t& f1, uint32_t& f2) {
+    const uint32_t e1 = code <= 134u ? code + 120u : code;   // bf16 exponent field of f1
+    f1 = (e1 << 7) | (e1 << 23);
+    f2 = code <= 134u ? 0u : ((247u << 7) | (247u << 23));
 }
 
-MOE_DEVICE float e8m0_scale(uint32_t code) {   // 2^(code-127); code 0 is the subnormal 2^-127
-    return __uint_as_float(code ? code << 23 : 0x00400000u);
+// 4 E4M3 codes (one 32-bit word) -> 2 bf16x2 words (codes 0,1 and 2,3), scaled.
+// prmt copies each code into the low byte of a 16-bit half and its sign into the high byte;
+// shifting by 4 moves exponent+mantissa to bits 10..4 and the sign bits to 15..12 (and 19..16,
+// outside the half); the mask keeps bits 15 and 10..4 of each half.
+MOE_DEVICE void dequant4(uint32_t w, uint32_t f1, uint32_t f2, uint32_t& lo, uint32_t& hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));   // [sx(c1) c1 sx(c0) c0]
+    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));   // [sx(c3) c3 sx(c2) c2]
+    a = (a << 4) & 0x87F087F0u;
+    b = (b << 4) & 0x87F087F0u;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(f1));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(f1));
+    if (f2) {
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(lo), "r"(f2));
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(hi), "r"(f2));
+    }
 }
 
 template <bool W8>
@@ -258,19 +255,14 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     ptx::mbar_arrive_expect_tx(&ctrl.full[s], bytes);
                     const int k0 = kb * BK;
                     // weights: normal -> B operand (256 rows); swap -> A operand (128 rows);
-                    // E4M3 codes -> four 16-code column boxes for the converters
+                    // E4M3 codes -> row-major 64-byte rows for the converters
                     uint8_t* wdst = W8 ? sa : (p.swap ? sa : sb);
                     const int wrows = p.swap ? 128 : 256;
                     const int row_w = tl.nb * wrows;          // first weight row (interleaved order)
-#pragma unroll 1
-                    for (int cbox = 0; cbox < (W8 ? 4 : 1); ++cbox) {
-                        const int kc = k0 + cbox * 16;
-                        uint8_t* dst = wdst + cbox * (BM * 16);
-                        if (p.w_mode == 1)
-                            ptx::tma_load_5d(dst, &tm_w, &ctrl.full[s], kc, 0, 0, row_w / 32, tl.e, pol_w);
-                        else
-                            ptx::tma_load_3d(dst, &tm_w, &ctrl.full[s], kc, row_w, tl.e, pol_w);
-                    }
+                    if (p.w_mode == 1)
+                        ptx::tma_load_5d(wdst, &tm_w, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_w);
+                    else
+                        ptx::tma_load_3d(wdst, &tm_w, &ctrl.full[s], k0, row_w, tl.e, pol_w);
                     if (p.swap) {
                         for (int b = 0; b < nbox; ++b)
                             ptx::tma_load_2d(sb + b * TOK_BOX * BK * 2, &tm_act, &ctrl.full[s], k0,
@@ -339,9 +331,9 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters
-        // warp w converts column box (w-6)/4 (codes 16*cb .. +15 of the k-block) of the 32 rows in
-        // its TMEM lane quarter: row r = 32*(w%4) + lane, scale block h = cb / 2 of the k-block
-        const int q = warp & 3, cb = (warp - 6) >> 2, r = q * 32 + lane, h = cb >> 1;
+        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile: its 64 codes
+        // per k-block (scale blocks 0 and 1) go to TMEM lane r, 32 columns of the stage's A tile
+        const int q = warp & 3, r = q * 32 + lane;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows
         uint32_t it = 0;
@@ -356,26 +348,39 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             }
             bool ok = true;
             for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                uint32_t code;
+                uint32_t sc0, sc1;
                 if (vec_scales) {
-                    const int j = 2 * (kb & 7) + h;
-                    const uint32_t word = j < 4 ? cur.x : (j < 8 ? cur.y : (j < 12 ? cur.z : cur.w));
-                    code = (word >> (8 * (j & 3))) & 0xFFu;
-                    if ((kb & 7) == 7) {
+                    const int j = kb & 7;   // this k-block's two scales: bytes 2j, 2j+1 of the group
+                    const uint32_t word = j < 2 ? cur.x : (j < 4 ? cur.y : (j < 6 ? cur.z : cur.w));
+                    const uint32_t pair = (word >> (16 * (j & 1))) & 0xFFFFu;
+                    sc0 = pair & 0xFFu;
+                    sc1 = pair >> 8;
+                    if (j == 7) {
                         cur = nxt;
                         if (kb + 9 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 2 * (kb + 9)));
                     }
                 } else {
-                    code = __ldg(srow + 2 * kb + h);
+                    sc0 = __ldg(srow + 2 * kb);
+                    sc1 = __ldg(srow + 2 * kb + 1);
                 }
-                const float scale = e8m0_scale(code);
+                uint32_t f1a, f2a, f1b, f2b;
+                e8m0_factors(sc0, f1a, f2a);
+                e8m0_factors(sc1, f1b, f2b);
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                const uint4 c = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + cb * (BM * 16))[r];
-                uint32_t o[8];
-                dequant16(c, scale, o);
-                ptx::tmem_st_32x32b_x8(tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2) + cb * 8), o);
+                const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * BK);
+                uint32_t o[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {   // 16 codes per chunk; chunks 0,1 use scale 0, chunks 2,3 scale 1
+                    const uint4 v = src[c];
+                    const uint32_t f1 = c < 2 ? f1a : f1b, f2 = c < 2 ? f2a : f2b;
+                    dequant4(v.x, f1, f2, o[8 * c + 0], o[8 * c + 1]);
+                    dequant4(v.y, f1, f2, o[8 * c + 2], o[8 * c + 3]);
+                    dequant4(v.z, f1, f2, o[8 * c + 4], o[8 * c + 5]);
+                    dequant4(v.w, f1, f2, o[8 * c + 6], o[8 * c + 7]);
+                }
+                ptx::tmem_st_32x32b_x32(tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2)), o);
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -662,14 +667,14 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
         cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
         cuuint64_t str[4] = {cuuint64_t(g.K * es), cuuint64_t(g.I * g.K * es), cuuint64_t(16 * g.K * es),
                              cuuint64_t(2 * g.I * g.K * es)};
-        cuuint32_t box[5] = {cuuint32_t(w8 ? 16 : BK), 16, 2, cuuint32_t(wtile / 32), 1};
+        cuuint32_t box[5] = {BK, 16, 2, cuuint32_t(wtile / 32), 1};
         int rc = make_map(&tm_w, g.w, 5, dims, str, box, "W1 (gate/up view)", w8);
         if (rc) return rc;
     } else if (!cached) {
         const int64_t es = w8 ? 1 : 2;
         cuuint64_t dims[3] = {cuuint64_t(kdim), cuuint64_t(wrows), cuuint64_t(g.E)};
         cuuint64_t str[2] = {cuuint64_t(kdim * es), cuuint64_t(wrows * kdim * es)};
-        cuuint32_t box[3] = {cuuint32_t(w8 ? 16 : BK), cuuint32_t(wtile), 1};
+        cuuint32_t box[3] = {BK, cuuint32_t(wtile), 1};
         int rc = make_map(&tm_w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2", w8);
         if (rc) return rc;
     }

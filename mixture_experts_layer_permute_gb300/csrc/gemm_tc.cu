@@ -27,11 +27,12 @@
 // MXFP8 weights (E4M3 codes + one E8M0 scale per 32 along the contraction;
 //   "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): swap-AB tiles
 //   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
-//   12-stage ring.  Four converter warps (warps 6..9) decode them exactly to
+//   12-stage ring.  Eight converter warps (warps 6..13) decode them exactly to
 //   bf16 and store the tile straight into tensor memory with tcgen05.st; the
 //   MMA takes its A operand from TMEM.  Warp w may only reach TMEM lanes
-//   32*(w%4)..+31, so thread (w, lane) owns row 32*(w%4)+lane: 64 codes and 2
-//   scales per k-block.  Decoding needs no conversion instruction: the E4M3
+//   32*(w%4)..+31, so thread (w, lane) owns row 32*(w%4)+lane and scale block
+//   (w-6)/4 of each k-block: 32 codes and one scale.  Decoding needs no
+//   conversion instruction: the E4M3
 //   bits placed into bf16 bit positions (sign to bit 15, exponent and
 //   mantissa to bits 10..4) give exactly code * 2^-120 for normal, subnormal
 //   and zero codes alike, and one bf16x2 multiply by 2^(scale-7) restores the
@@ -63,7 +64,7 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int TOK_BOX = 16;                 // swap-AB token rows per TMA box
 constexpr int MAX_STAGES = 12;
-constexpr int kConvThreads = 128;           // E4M3 converter warps 6..9
+constexpr int kConvThreads = 256;           // E4M3 converter warps 6..13
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // Per weight type: stage ring layout, TMEM map and CTA shape.
@@ -71,7 +72,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 //          192 threads; up to 256 tokens per swap-AB tile
 //   E4M3:  smem [codes 128 rows x 64 B][B tokens 8 KB] x 12 stages;
 //          TMEM: two 64-column accumulators, then 12 bf16 A tiles of 32 columns;
-//          320 threads; up to 64 tokens per tile
+//          448 threads; up to 64 tokens per tile
 template <bool W8>
 struct Cfg {
     static constexpr int STAGES = W8 ? 12 : 4;
@@ -168,11 +169,11 @@ MOE_DEVICE void e8m0_factors(uint32_t code, uint32_t& f1, uint32_t& f2) {
     f2 = code <= 134u ? 0u : ((247u << 7) | (247u << 23));
 }
 
-// 4 E4M3 codes (one 32-bit word) -> 2 bf16x2 words (codes 0,1 and 2,3), scaled.
+// 4 E4M3 codes (one 32-bit word) -> 2 bf16x2 words (codes 0,1 and 2,3) times f1.
 // prmt copies each code into the low byte of a 16-bit half and its sign into the high byte;
 // shifting by 4 moves exponent+mantissa to bits 10..4 and the sign bits to 15..12 (and 19..16,
 // outside the half); the mask keeps bits 15 and 10..4 of each half.
-MOE_DEVICE void dequant4(uint32_t w, uint32_t f1, uint32_t f2, uint32_t& lo, uint32_t& hi) {
+MOE_DEVICE void dequant4(uint32_t w, uint32_t f1, uint32_t& lo, uint32_t& hi) {
     uint32_t a, b;
     asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));   // [sx(c1) c1 sx(c0) c0]
     asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));   // [sx(c3) c3 sx(c2) c2]
@@ -180,10 +181,12 @@ MOE_DEVICE void dequant4(uint32_t w, uint32_t f1, uint32_t f2, uint32_t& lo, uin
     b = (b << 4) & 0x87F087F0u;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(f1));
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(f1));
-    if (f2) {
-        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(lo), "r"(f2));
-        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(hi), "r"(f2));
-    }
+}
+
+MOE_DEVICE uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 template <bool W8>
@@ -331,9 +334,10 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters
-        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile: its 64 codes
-        // per k-block (scale blocks 0 and 1) go to TMEM lane r, 32 columns of the stage's A tile
-        const int q = warp & 3, r = q * 32 + lane;
+        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile and scale block
+        // h = (w-6)/4: codes 32h..32h+31 of each k-block go to TMEM lane r, columns 16h..16h+15 of the
+        // stage's A tile
+        const int q = warp & 3, h = (warp - 6) >> 2, r = q * 32 + lane;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows
         uint32_t it = 0;
@@ -348,39 +352,42 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             }
             bool ok = true;
             for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                uint32_t sc0, sc1;
+                uint32_t sc;
                 if (vec_scales) {
-                    const int j = kb & 7;   // this k-block's two scales: bytes 2j, 2j+1 of the group
-                    const uint32_t word = j < 2 ? cur.x : (j < 4 ? cur.y : (j < 6 ? cur.z : cur.w));
-                    const uint32_t pair = (word >> (16 * (j & 1))) & 0xFFFFu;
-                    sc0 = pair & 0xFFu;
-                    sc1 = pair >> 8;
-                    if (j == 7) {
+                    const int j = 2 * (kb & 7) + h;     // byte of this k-block's scale in the group
+                    const uint32_t word = j < 4 ? cur.x : (j < 8 ? cur.y : (j < 12 ? cur.z : cur.w));
+                    sc = (word >> (8 * (j & 3))) & 0xFFu;
+                    if ((kb & 7) == 7) {
                         cur = nxt;
                         if (kb + 9 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 2 * (kb + 9)));
                     }
                 } else {
-                    sc0 = __ldg(srow + 2 * kb);
-                    sc1 = __ldg(srow + 2 * kb + 1);
+                    sc = __ldg(srow + 2 * kb + h);
                 }
-                uint32_t f1a, f2a, f1b, f2b;
-                e8m0_factors(sc0, f1a, f2a);
-                e8m0_factors(sc1, f1b, f2b);
+                // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that factor
+                // leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
+                const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
+                const uint32_t f1 = (e1 << 7) | (e1 << 23);
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * BK);
-                uint32_t o[32];
+                const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * BK + h * 32);
+                const uint4 v0 = src[0], v1 = src[1];
+                uint32_t o[16];
+                dequant4(v0.x, f1, o[0], o[1]);
+                dequant4(v0.y, f1, o[2], o[3]);
+                dequant4(v0.z, f1, o[4], o[5]);
+                dequant4(v0.w, f1, o[6], o[7]);
+                dequant4(v1.x, f1, o[8], o[9]);
+                dequant4(v1.y, f1, o[10], o[11]);
+                dequant4(v1.z, f1, o[12], o[13]);
+                dequant4(v1.w, f1, o[14], o[15]);
+                if (sc > 134u) {
+                    const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {   // 16 codes per chunk; chunks 0,1 use scale 0, chunks 2,3 scale 1
-                    const uint4 v = src[c];
-                    const uint32_t f1 = c < 2 ? f1a : f1b, f2 = c < 2 ? f2a : f2b;
-                    dequant4(v.x, f1, f2, o[8 * c + 0], o[8 * c + 1]);
-                    dequant4(v.y, f1, f2, o[8 * c + 2], o[8 * c + 3]);
-                    dequant4(v.z, f1, f2, o[8 * c + 4], o[8 * c + 5]);
-                    dequant4(v.w, f1, f2, o[8 * c + 6], o[8 * c + 7]);
+                    for (int i = 0; i < 16; ++i) o[i] = bf16x2_mul(o[i], f2);
                 }
-                ptx::tmem_st_32x32b_x32(tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2)), o);
+                ptx::tmem_st_32x32b_x16(tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2) + h * 16), o);
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();

@@ -350,48 +350,60 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 cur = __ldg(reinterpret_cast<const uint4*>(srow));
                 if (p.nkb > 8) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 16));
             }
+            // k-blocks are converted two at a time: both tiles are stored to TMEM before one wait for
+            // the stores, so the store latency of the first overlaps the decoding of the second
             bool ok = true;
-            for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                uint32_t sc;
-                if (vec_scales) {
-                    const int j = 2 * (kb & 7) + h;     // byte of this k-block's scale in the group
-                    const uint32_t word = j < 4 ? cur.x : (j < 8 ? cur.y : (j < 12 ? cur.z : cur.w));
-                    sc = (word >> (8 * (j & 3))) & 0xFFu;
-                    if ((kb & 7) == 7) {
-                        cur = nxt;
-                        if (kb + 9 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 2 * (kb + 9)));
+            for (int kb0 = 0; kb0 < p.nkb; kb0 += 2) {
+                const int nk = min(2, p.nkb - kb0);
+                int stage[2];
+                for (int u = 0; u < nk; ++u) {
+                    const int kb = kb0 + u;
+                    uint32_t sc;
+                    if (vec_scales) {
+                        const int j = 2 * (kb & 7) + h;     // byte of this k-block's scale in the group
+                        const uint32_t word = j < 4 ? cur.x : (j < 8 ? cur.y : (j < 12 ? cur.z : cur.w));
+                        sc = (word >> (8 * (j & 3))) & 0xFFu;
+                        if ((kb & 7) == 7) {
+                            cur = nxt;
+                            if (kb + 9 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 2 * (kb + 9)));
+                        }
+                    } else {
+                        sc = __ldg(srow + 2 * kb + h);
                     }
-                } else {
-                    sc = __ldg(srow + 2 * kb + h);
-                }
-                // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that factor
-                // leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
-                const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
-                const uint32_t f1 = (e1 << 7) | (e1 << 23);
-                const int s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1;
-                if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * BK + h * 32);
-                const uint4 v0 = src[0], v1 = src[1];
-                uint32_t o[16];
-                dequant4(v0.x, f1, o[0], o[1]);
-                dequant4(v0.y, f1, o[2], o[3]);
-                dequant4(v0.z, f1, o[4], o[5]);
-                dequant4(v0.w, f1, o[6], o[7]);
-                dequant4(v1.x, f1, o[8], o[9]);
-                dequant4(v1.y, f1, o[10], o[11]);
-                dequant4(v1.z, f1, o[12], o[13]);
-                dequant4(v1.w, f1, o[14], o[15]);
-                if (sc > 134u) {
-                    const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
+                    // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that
+                    // factor leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
+                    const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
+                    const uint32_t f1 = (e1 << 7) | (e1 << 23);
+                    const int s = (it + u) % STAGES;
+                    const uint32_t ph = ((it + u) / STAGES) & 1;
+                    stage[u] = s;
+                    if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
+                    const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * BK + h * 32);
+                    const uint4 v0 = src[0], v1 = src[1];
+                    uint32_t o[16];
+                    dequant4(v0.x, f1, o[0], o[1]);
+                    dequant4(v0.y, f1, o[2], o[3]);
+                    dequant4(v0.z, f1, o[4], o[5]);
+                    dequant4(v0.w, f1, o[6], o[7]);
+                    dequant4(v1.x, f1, o[8], o[9]);
+                    dequant4(v1.y, f1, o[10], o[11]);
+                    dequant4(v1.z, f1, o[12], o[13]);
+                    dequant4(v1.w, f1, o[14], o[15]);
+                    if (sc > 134u) {
+                        const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = bf16x2_mul(o[i], f2);
+                        for (int i = 0; i < 16; ++i) o[i] = bf16x2_mul(o[i], f2);
+                    }
+                    ptx::tmem_st_32x32b_x16(
+                        tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2) + h * 16), o);
                 }
-                ptx::tmem_st_32x32b_x16(tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2) + h * 16), o);
+                if (!ok) break;
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&ctrl.conv[s]);
+                if (lane == 0)
+                    for (int u = 0; u < nk; ++u) ptx::mbar_arrive(&ctrl.conv[stage[u]]);
+                it += nk;
             }
             if (!ok) break;
         }

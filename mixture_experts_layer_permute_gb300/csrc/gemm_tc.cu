@@ -27,11 +27,13 @@
 // MXFP8 weights (E4M3 codes + one E8M0 scale per 32 along the contraction;
 //   "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): swap-AB tiles
 //   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
-//   12-stage ring.  Eight converter warps (warps 6..13) decode them exactly to
+//   6-stage ring of 128-wide k slices (full 128-byte lines; two MMA k-blocks per
+//   hand-off halve the per-byte cost of the single-thread producer and MMA
+//   loops).  Eight converter warps (warps 6..13) decode them exactly to
 //   bf16 and store the tile straight into tensor memory with tcgen05.st; the
 //   MMA takes its A operand from TMEM.  Warp w may only reach TMEM lanes
-//   32*(w%4)..+31, so thread (w, lane) owns row 32*(w%4)+lane and scale block
-//   (w-6)/4 of each k-block: 32 codes and one scale.  Decoding needs no
+//   32*(w%4)..+31, so thread (w, lane) owns row 32*(w%4)+lane and half (w-6)/4
+//   of each 128-wide slice: 64 codes and two scales.  Decoding needs no
 //   conversion instruction: the E4M3
 //   bits placed into bf16 bit positions (sign to bit 15, exponent and
 //   mantissa to bits 10..4) give exactly code * 2^-120 for normal, subnormal
@@ -70,20 +72,23 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // Per weight type: stage ring layout, TMEM map and CTA shape.
 //   bf16:  smem [A 16 KB][B 32 KB] x 4 stages; TMEM: two 256-column accumulators;
 //          192 threads; up to 256 tokens per swap-AB tile
-//   E4M3:  smem [codes 128 rows x 64 B][B tokens 8 KB] x 12 stages;
-//          TMEM: two 64-column accumulators, then 12 bf16 A tiles of 32 columns;
+//   E4M3:  stages of 128 k (two 64-wide k-blocks): smem [codes 128 rows x 128 B][B tokens 2 x 8 KB]
+//          x 6 stages; TMEM: two 64-column accumulators, then 6 bf16 A tiles of 64 columns;
 //          448 threads; up to 64 tokens per tile
 template <bool W8>
 struct Cfg {
-    static constexpr int STAGES = W8 ? 12 : 4;
-    static constexpr int B_OFF = W8 ? BM * BK : A_BYTES;        // tokens (swap) / weights (normal)
-    static constexpr int B_BYTES = W8 ? 64 * BK * 2 : 256 * BK * 2;
+    static constexpr int KSUB = W8 ? 2 : 1;                     // 64-wide k-blocks per stage
+    static constexpr int STAGES = W8 ? 6 : 4;
+    static constexpr int B_OFF = W8 ? BM * BK * KSUB : A_BYTES; // tokens (swap) / weights (normal)
+    static constexpr int B_SUB = W8 ? 64 * BK * 2 : 256 * BK * 2;   // B bytes per 64-wide k-block
+    static constexpr int B_BYTES = B_SUB * KSUB;
     static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
     static constexpr int THREADS = W8 ? 192 + kConvThreads : 192;
     static constexpr int TOK_SPAN = W8 ? 64 : 256;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
     static constexpr int ACC_STRIDE = W8 ? 64 : ACC_COLS;       // TMEM columns per accumulator
     static constexpr int A_TMEM = 2 * ACC_STRIDE;               // E4M3: first A tile column
+    static constexpr int A_COLS = KSUB * BK / 2;                // E4M3: TMEM columns per stage
 };
 
 struct __align__(8) Ctrl {
@@ -246,9 +251,10 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
                 const Tile tl = decode_tile(tab, p, t);
                 const int nbox = p.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
-                const uint32_t wbytes = W8 ? uint32_t(BM * BK) : uint32_t(A_BYTES);
-                const uint32_t bytes =
-                    p.swap ? wbytes + uint32_t(nbox * TOK_BOX * BK * 2) : uint32_t(A_BYTES + Cfg<W8>::B_BYTES);
+                constexpr int KSUB = Cfg<W8>::KSUB;
+                const uint32_t wbytes = W8 ? uint32_t(BM * BK * KSUB) : uint32_t(A_BYTES);
+                const uint32_t bytes = p.swap ? wbytes + uint32_t(KSUB * nbox * TOK_BOX * BK * 2)
+                                              : uint32_t(A_BYTES + Cfg<W8>::B_BYTES);
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -256,7 +262,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     uint8_t* sa = smem + s * STAGE_BYTES;
                     uint8_t* sb = sa + Cfg<W8>::B_OFF;
                     ptx::mbar_arrive_expect_tx(&ctrl.full[s], bytes);
-                    const int k0 = kb * BK;
+                    const int k0 = kb * BK * KSUB;
                     // weights: normal -> B operand (256 rows); swap -> A operand (128 rows);
                     // E4M3 codes -> row-major 64-byte rows for the converters
                     uint8_t* wdst = W8 ? sa : (p.swap ? sa : sb);
@@ -267,9 +273,10 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     else
                         ptx::tma_load_3d(wdst, &tm_w, &ctrl.full[s], k0, row_w, tl.e, pol_w);
                     if (p.swap) {
-                        for (int b = 0; b < nbox; ++b)
-                            ptx::tma_load_2d(sb + b * TOK_BOX * BK * 2, &tm_act, &ctrl.full[s], k0,
-                                             int32_t(tl.row0 + b * TOK_BOX), pol_a);
+                        for (int sub = 0; sub < KSUB; ++sub)
+                            for (int b = 0; b < nbox; ++b)
+                                ptx::tma_load_2d(sb + sub * Cfg<W8>::B_SUB + b * TOK_BOX * BK * 2, &tm_act,
+                                                 &ctrl.full[s], k0 + sub * BK, int32_t(tl.row0 + b * TOK_BOX), pol_a);
                     } else {
                         ptx::tma_load_2d(sa, &tm_act, &ctrl.full[s], k0, int32_t(tl.row0), pol_a);
                     }
@@ -309,11 +316,13 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
                     const uint32_t sb = sa + Cfg<W8>::B_OFF;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t bd = ptx::smem_desc_sw128(sb + kk * UMMA_K * 2);
+                    for (int kk = 0; kk < Cfg<W8>::KSUB * BK / UMMA_K; ++kk) {
+                        const int sub = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
+                        const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<W8>::B_SUB + kq * UMMA_K * 2);
                         if constexpr (W8) {
                             // A from TMEM: 16 bf16 of a row = 8 columns per k step
-                            const uint32_t a_tmem = tmem_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2) + kk * 8);
+                            const uint32_t a_tmem =
+                                tmem_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + kk * 8);
                             ptx::mma_f16_tmem_a(d_tmem, a_tmem, bd, idesc, (kb | kk) != 0);
                         } else {
                             const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
@@ -334,76 +343,71 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters
-        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile and scale block
-        // h = (w-6)/4: codes 32h..32h+31 of each k-block go to TMEM lane r, columns 16h..16h+15 of the
-        // stage's A tile
+        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile and half
+        // h = (w-6)/4 of each 128-wide slice: codes 64h..64h+63 (scale blocks 2h, 2h+1) go to TMEM lane
+        // r, columns 32h..32h+31 of the stage's A tile
         const int q = warp & 3, h = (warp - 6) >> 2, r = q * 32 + lane;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
-        const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows
+        const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows (4 slices per 16 B)
         uint32_t it = 0;
         for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
             const Tile tl = decode_tile(tab, p, t);
             const uint8_t* srow = p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb;
-            // scales of 8 k-blocks (16 bytes) per register group; the next group is loaded one group ahead
+            // scales of 4 slices (16 bytes) per register group; the next group is loaded one group ahead
             uint4 cur = make_uint4(0, 0, 0, 0), nxt = make_uint4(0, 0, 0, 0);
             if (vec_scales) {
                 cur = __ldg(reinterpret_cast<const uint4*>(srow));
-                if (p.nkb > 8) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 16));
+                if (p.nkb > 4) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 16));
             }
-            // k-blocks are converted two at a time: both tiles are stored to TMEM before one wait for
-            // the stores, so the store latency of the first overlaps the decoding of the second
             bool ok = true;
-            for (int kb0 = 0; kb0 < p.nkb; kb0 += 2) {
-                const int nk = min(2, p.nkb - kb0);
-                int stage[2];
-                for (int u = 0; u < nk; ++u) {
-                    const int kb = kb0 + u;
-                    uint32_t sc;
-                    if (vec_scales) {
-                        const int j = 2 * (kb & 7) + h;     // byte of this k-block's scale in the group
-                        const uint32_t word = j < 4 ? cur.x : (j < 8 ? cur.y : (j < 12 ? cur.z : cur.w));
-                        sc = (word >> (8 * (j & 3))) & 0xFFu;
-                        if ((kb & 7) == 7) {
-                            cur = nxt;
-                            if (kb + 9 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 2 * (kb + 9)));
-                        }
-                    } else {
-                        sc = __ldg(srow + 2 * kb + h);
+            for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+                uint32_t sc[2];
+                if (vec_scales) {
+                    const int j = kb & 3;   // slice j of the group: scale bytes 4j..4j+3, this thread's 4j+2h, +1
+                    const uint32_t word = j == 0 ? cur.x : (j == 1 ? cur.y : (j == 2 ? cur.z : cur.w));
+                    sc[0] = (word >> (16 * h)) & 0xFFu;
+                    sc[1] = (word >> (16 * h + 8)) & 0xFFu;
+                    if (j == 3) {
+                        cur = nxt;
+                        if (kb + 5 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 4 * (kb + 5)));
                     }
+                } else {
+                    sc[0] = __ldg(srow + 4 * kb + 2 * h);
+                    sc[1] = __ldg(srow + 4 * kb + 2 * h + 1);
+                }
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
+                const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * (BK * 2) + h * 64);
+                uint32_t o[32];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
                     // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that
                     // factor leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
-                    const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
+                    const uint32_t e1 = sc[b] <= 134u ? sc[b] + 120u : sc[b];
                     const uint32_t f1 = (e1 << 7) | (e1 << 23);
-                    const int s = (it + u) % STAGES;
-                    const uint32_t ph = ((it + u) / STAGES) & 1;
-                    stage[u] = s;
-                    if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                    const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * BK + h * 32);
-                    const uint4 v0 = src[0], v1 = src[1];
-                    uint32_t o[16];
-                    dequant4(v0.x, f1, o[0], o[1]);
-                    dequant4(v0.y, f1, o[2], o[3]);
-                    dequant4(v0.z, f1, o[4], o[5]);
-                    dequant4(v0.w, f1, o[6], o[7]);
-                    dequant4(v1.x, f1, o[8], o[9]);
-                    dequant4(v1.y, f1, o[10], o[11]);
-                    dequant4(v1.z, f1, o[12], o[13]);
-                    dequant4(v1.w, f1, o[14], o[15]);
-                    if (sc > 134u) {
+                    const uint4 v0 = src[2 * b], v1 = src[2 * b + 1];
+                    uint32_t* ob = o + 16 * b;
+                    dequant4(v0.x, f1, ob[0], ob[1]);
+                    dequant4(v0.y, f1, ob[2], ob[3]);
+                    dequant4(v0.z, f1, ob[4], ob[5]);
+                    dequant4(v0.w, f1, ob[6], ob[7]);
+                    dequant4(v1.x, f1, ob[8], ob[9]);
+                    dequant4(v1.y, f1, ob[10], ob[11]);
+                    dequant4(v1.z, f1, ob[12], ob[13]);
+                    dequant4(v1.w, f1, ob[14], ob[15]);
+                    if (sc[b] > 134u) {
                         const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] = bf16x2_mul(o[i], f2);
+                        for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], f2);
                     }
-                    ptx::tmem_st_32x32b_x16(
-                        tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * (BK / 2) + h * 16), o);
                 }
-                if (!ok) break;
+                ptx::tmem_st_32x32b_x32(tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + h * 32),
+                                        o);
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    for (int u = 0; u < nk; ++u) ptx::mbar_arrive(&ctrl.conv[stage[u]]);
-                it += nk;
+                if (lane == 0) ptx::mbar_arrive(&ctrl.conv[s]);
             }
             if (!ok) break;
         }
@@ -648,6 +652,8 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     if (g.gemm == 1 && g.out_dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 GEMM 1 writes bf16 h");
     const int64_t kdim = g.gemm == 1 ? g.K : g.I;
     if (kdim % BK != 0) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: contraction length must be a multiple of 64");
+    if (w8 && kdim % (BK * Cfg<true>::KSUB) != 0)
+        return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: E4M3 weights need a contraction length multiple of 128");
     const int64_t wrows = g.gemm == 1 ? 2 * g.I : g.K;   // weight rows per expert
     const int wtile = swap ? 128 : 256;
     if (wrows % wtile != 0)
@@ -686,14 +692,14 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
         cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
         cuuint64_t str[4] = {cuuint64_t(g.K * es), cuuint64_t(g.I * g.K * es), cuuint64_t(16 * g.K * es),
                              cuuint64_t(2 * g.I * g.K * es)};
-        cuuint32_t box[5] = {BK, 16, 2, cuuint32_t(wtile / 32), 1};
+        cuuint32_t box[5] = {cuuint32_t(w8 ? BK * Cfg<true>::KSUB : BK), 16, 2, cuuint32_t(wtile / 32), 1};
         int rc = make_map(&tm_w, g.w, 5, dims, str, box, "W1 (gate/up view)", w8);
         if (rc) return rc;
     } else if (!cached) {
         const int64_t es = w8 ? 1 : 2;
         cuuint64_t dims[3] = {cuuint64_t(kdim), cuuint64_t(wrows), cuuint64_t(g.E)};
         cuuint64_t str[2] = {cuuint64_t(kdim * es), cuuint64_t(wrows * kdim * es)};
-        cuuint32_t box[3] = {BK, cuuint32_t(wtile), 1};
+        cuuint32_t box[3] = {cuuint32_t(w8 ? BK * Cfg<true>::KSUB : BK), cuuint32_t(wtile), 1};
         int rc = make_map(&tm_w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2", w8);
         if (rc) return rc;
     }
@@ -710,7 +716,7 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     p.E = g.E;
     p.max_tokens = g.max_tokens;
     p.rows_cap = g.rows_cap;
-    p.nkb = int(kdim / BK);
+    p.nkb = int(kdim / (BK * (w8 ? Cfg<true>::KSUB : 1)));   // stages per tile
     p.nt = int(wrows / wtile);
     p.w_mode = w_mode;
     p.I = g.I;

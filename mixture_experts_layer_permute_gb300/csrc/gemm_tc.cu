@@ -29,11 +29,11 @@
 //   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
 //   6-stage ring of 128-wide k slices (full 128-byte lines; two MMA k-blocks per
 //   hand-off halve the per-byte cost of the single-thread producer and MMA
-//   loops).  Eight converter warps (warps 6..13) decode them exactly to
+//   loops).  Sixteen converter warps (warps 6..13) decode them exactly to
 //   bf16 and store the tile straight into tensor memory with tcgen05.st; the
 //   MMA takes its A operand from TMEM.  Warp w may only reach TMEM lanes
-//   32*(w%4)..+31, so thread (w, lane) owns row 32*(w%4)+lane and half (w-6)/4
-//   of each 128-wide slice: 64 codes and two scales.  Decoding needs no
+//   32*(w%4)..+31, so thread (w, lane) owns row 32*(w%4)+lane and quarter
+//   (w-6)/4 of each 128-wide slice: 32 codes and one scale.  Decoding needs no
 //   conversion instruction: the E4M3
 //   bits placed into bf16 bit positions (sign to bit 15, exponent and
 //   mantissa to bits 10..4) give exactly code * 2^-120 for normal, subnormal
@@ -66,7 +66,7 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int TOK_BOX = 16;                 // swap-AB token rows per TMA box
 constexpr int MAX_STAGES = 12;
-constexpr int kConvThreads = 256;           // E4M3 converter warps 6..13
+constexpr int kConvThreads = 512;           // E4M3 converter warps 6..21
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // Per weight type: stage ring layout, TMEM map and CTA shape.
@@ -74,7 +74,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 //          192 threads; up to 256 tokens per swap-AB tile
 //   E4M3:  stages of 128 k (two 64-wide k-blocks): smem [codes 128 rows x 128 B][B tokens 2 x 8 KB]
 //          x 6 stages; TMEM: two 64-column accumulators, then 6 bf16 A tiles of 64 columns;
-//          448 threads; up to 64 tokens per tile
+//          704 threads; up to 64 tokens per tile
 template <bool W8>
 struct Cfg {
     static constexpr int KSUB = W8 ? 2 : 1;                     // 64-wide k-blocks per stage
@@ -343,9 +343,9 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters
-        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile and half
-        // h = (w-6)/4 of each 128-wide slice: codes 64h..64h+63 (scale blocks 2h, 2h+1) go to TMEM lane
-        // r, columns 32h..32h+31 of the stage's A tile
+        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile and scale block
+        // h = (w-6)/4 of each 128-wide slice: codes 32h..32h+31 go to TMEM lane r, columns 16h..16h+15 of
+        // the stage's A tile
         const int q = warp & 3, h = (warp - 6) >> 2, r = q * 32 + lane;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows (4 slices per 16 B)
@@ -361,49 +361,43 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             }
             bool ok = true;
             for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                uint32_t sc[2];
+                uint32_t sc;
                 if (vec_scales) {
-                    const int j = kb & 3;   // slice j of the group: scale bytes 4j..4j+3, this thread's 4j+2h, +1
+                    const int j = kb & 3;   // slice j of the group: scale bytes 4j..4j+3, this thread's 4j+h
                     const uint32_t word = j == 0 ? cur.x : (j == 1 ? cur.y : (j == 2 ? cur.z : cur.w));
-                    sc[0] = (word >> (16 * h)) & 0xFFu;
-                    sc[1] = (word >> (16 * h + 8)) & 0xFFu;
+                    sc = (word >> (8 * h)) & 0xFFu;
                     if (j == 3) {
                         cur = nxt;
                         if (kb + 5 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 4 * (kb + 5)));
                     }
                 } else {
-                    sc[0] = __ldg(srow + 4 * kb + 2 * h);
-                    sc[1] = __ldg(srow + 4 * kb + 2 * h + 1);
+                    sc = __ldg(srow + 4 * kb + h);
                 }
+                // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that factor
+                // leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
+                const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
+                const uint32_t f1 = (e1 << 7) | (e1 << 23);
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * (BK * 2) + h * 64);
-                uint32_t o[32];
+                const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * (BK * 2) + h * 32);
+                const uint4 v0 = src[0], v1 = src[1];
+                uint32_t o[16];
+                dequant4(v0.x, f1, o[0], o[1]);
+                dequant4(v0.y, f1, o[2], o[3]);
+                dequant4(v0.z, f1, o[4], o[5]);
+                dequant4(v0.w, f1, o[6], o[7]);
+                dequant4(v1.x, f1, o[8], o[9]);
+                dequant4(v1.y, f1, o[10], o[11]);
+                dequant4(v1.z, f1, o[12], o[13]);
+                dequant4(v1.w, f1, o[14], o[15]);
+                if (sc > 134u) {
+                    const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that
-                    // factor leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
-                    const uint32_t e1 = sc[b] <= 134u ? sc[b] + 120u : sc[b];
-                    const uint32_t f1 = (e1 << 7) | (e1 << 23);
-                    const uint4 v0 = src[2 * b], v1 = src[2 * b + 1];
-                    uint32_t* ob = o + 16 * b;
-                    dequant4(v0.x, f1, ob[0], ob[1]);
-                    dequant4(v0.y, f1, ob[2], ob[3]);
-                    dequant4(v0.z, f1, ob[4], ob[5]);
-                    dequant4(v0.w, f1, ob[6], ob[7]);
-                    dequant4(v1.x, f1, ob[8], ob[9]);
-                    dequant4(v1.y, f1, ob[10], ob[11]);
-                    dequant4(v1.z, f1, ob[12], ob[13]);
-                    dequant4(v1.w, f1, ob[14], ob[15]);
-                    if (sc[b] > 134u) {
-                        const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], f2);
-                    }
+                    for (int i = 0; i < 16; ++i) o[i] = bf16x2_mul(o[i], f2);
                 }
-                ptx::tmem_st_32x32b_x32(tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + h * 32),
-                                        o);
+                ptx::tmem_st_32x32b_x16(
+                    tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + h * 16), o);
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();

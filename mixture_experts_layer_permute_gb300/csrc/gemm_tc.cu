@@ -47,6 +47,7 @@
 // returns.
 #include <cuda.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <unordered_map>
 
@@ -125,6 +126,7 @@ struct TcParams {
     const uint8_t* w_scale;   // E4M3 weights: E8M0 scales (E, wrows, kdim/32)
     int64_t wrows;       // weight rows per expert
     int64_t nsb;         // scale bytes per weight row (kdim / 32)
+    int skip_first_copy; // test hook: CTA 0 never issues its first weight copy (see timeout_test_hook)
 };
 
 MOE_DEVICE bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl& c, int32_t* err_word) {
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     uint8_t* sa = smem + s * STAGE_BYTES;
                     uint8_t* sb = sa + Cfg<W8>::B_OFF;
                     ptx::mbar_arrive_expect_tx(&ctrl.full[s], bytes);
+                    if (p.skip_first_copy && blockIdx.x == 0 && it == 0) continue;   // bytes that never arrive
                     const int k0 = kb * BK * KSUB;
                     // weights: normal -> B operand (256 rows); swap -> A operand (128 rows);
                     // E4M3 codes -> row-major 64-byte rows for the converters
@@ -621,6 +624,18 @@ std::unordered_map<MapKey, MapPair, MapKeyHash> g_maps;
 
 }  // namespace
 
+// Test hook for the bounded waits: when the environment variable MOE_TEST_SKIP_FIRST_COPY is 1 at the
+// first launch, CTA 0 of every tcgen05 GEMM announces its first stage's bytes but never issues the copy,
+// so that stage's "full" barrier never completes.  The MMA issuer's wait then runs out after 2 s, the
+// kernel records MOE_DEVERR_TIMEOUT and returns; nothing faults or hangs.  Off unless set.
+bool timeout_test_hook() {
+    static const bool on = [] {
+        const char* v = std::getenv("MOE_TEST_SKIP_FIRST_COPY");
+        return v && v[0] == '1';
+    }();
+    return on;
+}
+
 template <bool W8>
 int set_smem_attr() {
     static std::mutex mu;
@@ -727,6 +742,7 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     p.w_scale = g.w_scale;
     p.wrows = wrows;
     p.nsb = kdim / 32;
+    p.skip_first_copy = timeout_test_hook() ? 1 : 0;
 
     int rc = w8 ? set_smem_attr<true>() : set_smem_attr<false>();
     if (rc) return rc;

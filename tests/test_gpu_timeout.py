@@ -1,0 +1,52 @@
+"""Failure detection on the GPU without a fault: a pipeline wait that runs out.
+
+A child process sets MOE_TEST_SKIP_FIRST_COPY=1, so CTA 0 of the tcgen05 GEMM never
+issues its first weight copy and that stage's barrier never completes (a flag nothing
+sets).  The bounded wait gives up after ~2 s: the kernel must report
+MOE_DEVERR_TIMEOUT in err_word, free its tensor memory and return, leaving the CUDA
+context usable -- the same process then runs routing and checks it against the oracle.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import sys, time
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import mixture_experts_layer_permute_gb300 as m
+import oracle
+from mixture_experts_layer_permute_gb300 import workloads as wl
+w = wl.scaled(wl.decode(64), T=64, K=256, I=128, E=4, top_k=2)
+x, logits = wl.activations(w, 0).cuda(), wl.router_logits(w, 0)
+W1 = wl.expert_weights(w, "W1", 0).cuda()
+ids, _ = m.moe_topk_route(logits.cuda(), 2)
+res = m.moe_permute_align(ids, 4, m.MOE_LAYOUT_CONTIGUOUS, 1, x=x)
+err = torch.zeros(1, dtype=torch.int32, device="cuda")
+t0 = time.time()
+m.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1, 128, impl=m.MOE_IMPL_{impl}, err_word=err)
+torch.cuda.synchronize()
+dt = time.time() - t0
+print("ERR", int(err.item()), "SECONDS", round(dt, 2))
+ids2, w2 = m.moe_topk_route(logits.cuda(), 2)          # the context still works
+rids, rw = oracle.topk_route(logits.numpy(), 2)
+print("ROUTE_OK", bool(np.array_equal(ids2.cpu().numpy(), rids)))
+"""
+
+
+@pytest.mark.parametrize("impl", ["TCGEN05", "TCGEN05_SWAP_AB"])
+def test_gemm_wait_runs_out_and_reports(moe, impl):
+    env = dict(os.environ, MOE_TEST_SKIP_FIRST_COPY="1")
+    r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT, impl=impl)], env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    fields = dict(zip(r.stdout.split()[::2], r.stdout.split()[1::2]))
+    assert int(fields["ERR"]) & moe.MOE_DEVERR_TIMEOUT
+    assert 1.0 <= float(fields["SECONDS"]) <= 30.0
+    assert fields["ROUTE_OK"] == "True"

@@ -80,12 +80,15 @@ extern "C" {
                                          _interleave_gate_up_16 "After") */
 
 /* ---- GEMM implementations ---- */
-#define MOE_IMPL_AUTO 0               /* tcgen05 tiles; swap-AB when routes/expert are few; SIMT for fp32 */
+#define MOE_IMPL_AUTO 0               /* swap-AB tiles when routes/expert are few, else mixed tiles;
+                                         E4M3 weights on swap-AB tiles; CUDA cores for fp32 */
 #define MOE_IMPL_TCGEN05 1            /* tcgen05 tiles, tokens on the MMA M side (128 rows per tile) */
 #define MOE_IMPL_TCGEN05_SWAP_AB 2    /* tcgen05 tiles, weight rows on the MMA M side, tokens on N
                                          (AWS blog "MoE kernel engineering on SageMaker AI", Swap-AB:
                                          C^T = B^T A^T when M < 64) */
 #define MOE_IMPL_SIMT 3               /* CUDA-core FMA tiles (fp32 path, any shape) */
+#define MOE_IMPL_TCGEN05_MIXED 4      /* tcgen05: full 128-row tiles per expert, and a swap-AB tile for an
+                                         expert's tail of fewer than 64 rows (bf16 weights) */
 
 /* Message describing the calling thread's last failed call ("" if none). */
 MOE_API const char* moe_last_error(void);

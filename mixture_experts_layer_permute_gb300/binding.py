@@ -24,7 +24,7 @@ MOE_OK = 0
 MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_LAYOUT_CONTIGUOUS, MOE_LAYOUT_BATCHED = 0, 1
 MOE_W1_GATE_UP, MOE_W1_INTERLEAVE16 = 0, 1
-MOE_IMPL_AUTO, MOE_IMPL_TCGEN05, MOE_IMPL_TCGEN05_SWAP_AB, MOE_IMPL_SIMT = 0, 1, 2, 3
+MOE_IMPL_AUTO, MOE_IMPL_TCGEN05, MOE_IMPL_TCGEN05_SWAP_AB, MOE_IMPL_SIMT, MOE_IMPL_TCGEN05_MIXED = 0, 1, 2, 3, 4
 MOE_DEVERR_ID_RANGE, MOE_DEVERR_CAPACITY, MOE_DEVERR_TIMEOUT = 1, 2, 4
 
 EXPORTED = [

@@ -183,14 +183,17 @@ int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
             int64_t rows = g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens;
             int64_t per_expert = rows / std::max(1, g.E);
             if (g.layout == MOE_LAYOUT_BATCHED) per_expert = g.max_tokens / 2;
-            chosen = per_expert < 64 ? MOE_IMPL_TCGEN05_SWAP_AB : MOE_IMPL_TCGEN05;
+            chosen = per_expert < 64 ? MOE_IMPL_TCGEN05_SWAP_AB : MOE_IMPL_TCGEN05_MIXED;
         }
     }
     if (chosen == MOE_IMPL_SIMT) return launch_status(launch_gemm_simt(g, s), name);
-    MOE_REQUIRE(chosen == MOE_IMPL_TCGEN05 || chosen == MOE_IMPL_TCGEN05_SWAP_AB, MOE_ERR_INVALID_ARG,
-                std::string(name) + ": unknown impl");
+    MOE_REQUIRE(chosen == MOE_IMPL_TCGEN05 || chosen == MOE_IMPL_TCGEN05_SWAP_AB ||
+                    chosen == MOE_IMPL_TCGEN05_MIXED,
+                MOE_ERR_INVALID_ARG, std::string(name) + ": unknown impl");
     MOE_REQUIRE(device_cc() >= 100, MOE_ERR_UNSUPPORTED, std::string(name) + ": tcgen05 needs an sm_100+ device");
-    int rc = launch_gemm_tc(g, chosen == MOE_IMPL_TCGEN05_SWAP_AB, s);
+    const int mode = chosen == MOE_IMPL_TCGEN05_SWAP_AB ? TC_SWAP : (chosen == MOE_IMPL_TCGEN05_MIXED ? TC_MIXED
+                                                                                                      : TC_NORMAL);
+    int rc = launch_gemm_tc(g, mode, s);
     if (rc != MOE_OK && impl == MOE_IMPL_AUTO && rc == MOE_ERR_UNSUPPORTED) {
         // shape outside the tcgen05 tiles: the CUDA-core kernel covers every shape
         g_last_error.clear();

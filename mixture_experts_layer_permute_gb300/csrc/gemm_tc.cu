@@ -42,6 +42,11 @@
 //   "converted" mbarrier per stage hands the tile to the MMA issuer.  Tokens
 //   per tile are capped at 64.
 //
+// Mixed tiles (bf16): one launch serves every expert with full 128-row normal
+// tiles and puts an expert's tail of fewer than 64 rows (or a whole small
+// expert) on a swap-AB tile, so a skewed routing does not pay a mostly empty
+// 128-row tile per expert.
+//
 // Every mbarrier wait is bounded (2 s of globaltimer); on expiry the kernel
 // records MOE_DEVERR_TIMEOUT, lets its copies in flight land, frees TMEM and
 // returns.
@@ -123,6 +128,8 @@ struct TcParams {
     int64_t out_rows;    // GEMM 2, contiguous: rows of y (routes)
     int32_t* err_word;
     int span;            // activation rows per tile (normal: 128; swap: token segment)
+    int mixed;           // 1: normal tiles plus a swap-AB tile for each expert's short tail
+    int nt_n, nt_s;      // mixed: weight tiles per m-tile (normal, 256 rows) and per segment (swap, 128 rows)
     const uint8_t* w_scale;   // E4M3 weights: E8M0 scales (E, wrows, kdim/32)
     int64_t wrows;       // weight rows per expert
     int64_t nsb;         // scale bytes per weight row (kdim / 32)
@@ -142,16 +149,40 @@ MOE_DEVICE bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl& c, int32_t* err_w
 
 // Tile -> (expert, rows, n-tile / weight block, tokens) decoding, shared by all roles.
 struct Tile {
+    int swap;         // this tile puts weights on the MMA M side
     int e;
     int64_t row0;     // first activation row of the tile
     int rows;         // valid activation rows (normal: <= 128; swap: tokens <= 256)
     int nb;           // normal: n-tile; swap: weight block
 };
 
+// Mixed mode: an expert with c rows gets n_norm normal m-tiles (a last partial one only when it holds at
+// least 64 rows) and, for a shorter tail, one swap-AB segment.
+MOE_DEVICE int mixed_normal_tiles(int32_t c) { return (c & 127) >= 64 ? (c >> 7) + 1 : (c >> 7); }
+MOE_DEVICE int32_t mixed_tail(int32_t c) { return (c & 127) >= 64 ? 0 : (c & 127); }
+
 MOE_DEVICE Tile decode_tile(const ExpertTable& tab, const TcParams& p, int32_t t) {
     Tile tl;
     tl.e = find_expert(tab, p.E, t);
     const int32_t local = t - tiles_before(tab, tl.e);
+    if (p.mixed) {
+        const int32_t c = tab.count[tl.e];
+        const int32_t nn = mixed_normal_tiles(c);
+        if (local < nn * p.nt_n) {
+            const int32_t m = local / p.nt_n;
+            tl.swap = 0;
+            tl.nb = local - m * p.nt_n;
+            tl.row0 = int64_t(tab.start[tl.e]) + int64_t(m) * BM;
+            tl.rows = min(BM, c - m * BM);
+        } else {
+            tl.swap = 1;
+            tl.nb = local - nn * p.nt_n;
+            tl.row0 = int64_t(tab.start[tl.e]) + int64_t(c >> 7) * BM;
+            tl.rows = mixed_tail(c);
+        }
+        return tl;
+    }
+    tl.swap = p.swap;
     const int32_t seg = local / p.nt;
     tl.nb = local - seg * p.nt;
     tl.row0 = int64_t(tab.start[tl.e]) + int64_t(seg) * p.span;
@@ -199,7 +230,10 @@ MOE_DEVICE uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 template <bool W8>
 __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
+                   const __grid_constant__ CUtensorMap tm_act_s, const __grid_constant__ CUtensorMap tm_w_s,
                    const TcParams p) {
+    // tm_act/tm_w: boxes of normal tiles (or of every tile when all tiles are of one kind);
+    // tm_act_s/tm_w_s: boxes of the swap-AB tiles of a mixed launch
     constexpr int STAGES = Cfg<W8>::STAGES;
     constexpr int STAGE_BYTES = Cfg<W8>::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
@@ -229,15 +263,21 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tm_act);
         ptx::prefetch_tmap(&tm_w);
+        if (p.mixed) {
+            ptx::prefetch_tmap(&tm_act_s);
+            ptx::prefetch_tmap(&tm_w_s);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(&ctrl.tmem_base, TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    const int span = p.span;
-    const int ntl = p.nt;
+    const int span = p.span, ntl = p.nt, mixed = p.mixed, ntn = p.nt_n, nts = p.nt_s;
     build_expert_table(tab, p.E, p.counts, p.offsets, p.max_tokens, p.rows_cap,
-                       [span, ntl](int32_t c) { return ((c + span - 1) / span) * ntl; });
+                       [span, ntl, mixed, ntn, nts](int32_t c) {
+                           if (mixed) return mixed_normal_tiles(c) * ntn + (mixed_tail(c) > 0 ? nts : 0);
+                           return ((c + span - 1) / span) * ntl;
+                       });
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -252,10 +292,12 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             uint32_t it = 0;
             for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
                 const Tile tl = decode_tile(tab, p, t);
-                const int nbox = p.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
+                const int nbox = tl.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
+                const CUtensorMap* mact = (p.mixed && tl.swap) ? &tm_act_s : &tm_act;
+                const CUtensorMap* mw = (p.mixed && tl.swap) ? &tm_w_s : &tm_w;
                 constexpr int KSUB = Cfg<W8>::KSUB;
                 const uint32_t wbytes = W8 ? uint32_t(BM * BK * KSUB) : uint32_t(A_BYTES);
-                const uint32_t bytes = p.swap ? wbytes + uint32_t(KSUB * nbox * TOK_BOX * BK * 2)
+                const uint32_t bytes = tl.swap ? wbytes + uint32_t(KSUB * nbox * TOK_BOX * BK * 2)
                                               : uint32_t(A_BYTES + Cfg<W8>::B_BYTES);
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -268,20 +310,20 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     const int k0 = kb * BK * KSUB;
                     // weights: normal -> B operand (256 rows); swap -> A operand (128 rows);
                     // E4M3 codes -> row-major 64-byte rows for the converters
-                    uint8_t* wdst = W8 ? sa : (p.swap ? sa : sb);
-                    const int wrows = p.swap ? 128 : 256;
+                    uint8_t* wdst = W8 ? sa : (tl.swap ? sa : sb);
+                    const int wrows = tl.swap ? 128 : 256;
                     const int row_w = tl.nb * wrows;          // first weight row (interleaved order)
                     if (p.w_mode == 1)
-                        ptx::tma_load_5d(wdst, &tm_w, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_w);
+                        ptx::tma_load_5d(wdst, mw, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_w);
                     else
-                        ptx::tma_load_3d(wdst, &tm_w, &ctrl.full[s], k0, row_w, tl.e, pol_w);
-                    if (p.swap) {
+                        ptx::tma_load_3d(wdst, mw, &ctrl.full[s], k0, row_w, tl.e, pol_w);
+                    if (tl.swap) {
                         for (int sub = 0; sub < KSUB; ++sub)
                             for (int b = 0; b < nbox; ++b)
-                                ptx::tma_load_2d(sb + sub * Cfg<W8>::B_SUB + b * TOK_BOX * BK * 2, &tm_act,
+                                ptx::tma_load_2d(sb + sub * Cfg<W8>::B_SUB + b * TOK_BOX * BK * 2, mact,
                                                  &ctrl.full[s], k0 + sub * BK, int32_t(tl.row0 + b * TOK_BOX), pol_a);
                     } else {
-                        ptx::tma_load_2d(sa, &tm_act, &ctrl.full[s], k0, int32_t(tl.row0), pol_a);
+                        ptx::tma_load_2d(sa, mact, &ctrl.full[s], k0, int32_t(tl.row0), pol_a);
                     }
                 }
             }
@@ -306,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 if (!wait_bar(&ctrl.acc_empty[buf], aph ^ 1, ctrl, p.err_word)) break;
                 ptx::tc_fence_after();
                 int n_mma = 256;
-                if (p.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
+                if (tl.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
                 const uint32_t idesc = ptx::idesc_bf16(BM, n_mma);
                 const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg<W8>::ACC_STRIDE);
                 bool ok = true;
@@ -420,7 +462,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             if (!wait_bar(&ctrl.acc_full[buf], aph, ctrl, p.err_word)) break;
             ptx::tc_fence_after();
             const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * Cfg<W8>::ACC_STRIDE);
-            if (!p.swap) {
+            if (!tl.swap) {
                 const int r = q * 32 + lane;                  // tile row of this thread
                 const bool valid = r < tl.rows;
                 const int64_t row = tl.row0 + r;
@@ -615,12 +657,12 @@ struct MapKeyHash {
     }
 };
 
-struct MapPair {
-    CUtensorMap act, w;
+struct MapSet {
+    CUtensorMap act, w, act_s, w_s;
 };
 
 std::mutex g_map_mu;
-std::unordered_map<MapKey, MapPair, MapKeyHash> g_maps;
+std::unordered_map<MapKey, MapSet, MapKeyHash> g_maps;
 
 }  // namespace
 
@@ -652,7 +694,36 @@ int set_smem_attr() {
     return MOE_OK;
 }
 
-int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
+// Tensor maps of one tile kind: activation rows (128 per normal tile, 16-row boxes for swap-AB) and
+// weight rows (256 per normal tile, 128 per swap-AB tile; E4M3 codes as plain bytes).
+int build_maps(const GemmArgs& g, bool swap, bool w8, int64_t kdim, int64_t wrows, CUtensorMap* act,
+               CUtensorMap* w) {
+    const int wtile = swap ? 128 : 256;
+    {
+        cuuint64_t dims[2] = {cuuint64_t(kdim), cuuint64_t(g.rows_cap)};
+        cuuint64_t str[1] = {cuuint64_t(kdim * 2)};
+        cuuint32_t box[2] = {BK, cuuint32_t(swap ? TOK_BOX : BM)};
+        int rc = make_map(act, g.a, 2, dims, str, box, "activations");
+        if (rc) return rc;
+    }
+    const int64_t es = w8 ? 1 : 2;
+    const cuuint32_t kbox = cuuint32_t(w8 ? BK * Cfg<true>::KSUB : BK);
+    if (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) {
+        // view W1[e] (2I, K) as (K, 16, 2, I/16): row = half*I + 16*blk + q
+        cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
+        cuuint64_t str[4] = {cuuint64_t(g.K * es), cuuint64_t(g.I * g.K * es), cuuint64_t(16 * g.K * es),
+                             cuuint64_t(2 * g.I * g.K * es)};
+        cuuint32_t box[5] = {kbox, 16, 2, cuuint32_t(wtile / 32), 1};
+        return make_map(w, g.w, 5, dims, str, box, "W1 (gate/up view)", w8);
+    }
+    cuuint64_t dims[3] = {cuuint64_t(kdim), cuuint64_t(wrows), cuuint64_t(g.E)};
+    cuuint64_t str[2] = {cuuint64_t(kdim * es), cuuint64_t(wrows * kdim * es)};
+    cuuint32_t box[3] = {kbox, cuuint32_t(wtile), 1};
+    return make_map(w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2", w8);
+}
+
+int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
+    const bool swap = mode == TC_SWAP, mixed = mode == TC_MIXED;
     const bool w8 = g.w_dtype == MOE_E4M3;
     if (g.a_dtype != MOE_BF16 || (g.w_dtype != MOE_BF16 && !w8))
         return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: bf16 activations with bf16 or E4M3 weights only");
@@ -675,47 +746,31 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     const int w_mode = (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0;
     int dev_id = 0;
     cudaGetDevice(&dev_id);
-    const MapKey key{dev_id, g.a, g.w, kdim, g.rows_cap, wrows, g.I, g.K, g.E, g.gemm, (swap ? 1 : 0) | (w8 ? 2 : 0),
-                     w_mode};
-    CUtensorMap tm_act, tm_w;
+    const MapKey key{dev_id, g.a, g.w, kdim, g.rows_cap, wrows, g.I, g.K, g.E, g.gemm,
+                     mode | (w8 ? 4 : 0), w_mode};
+    MapSet maps;
     bool cached = false;
     {
         std::lock_guard<std::mutex> lock(g_map_mu);
         auto it = g_maps.find(key);
         if (it != g_maps.end()) {
-            tm_act = it->second.act;
-            tm_w = it->second.w;
+            maps = it->second;
             cached = true;
         }
     }
     if (!cached) {
-        cuuint64_t dims[2] = {cuuint64_t(kdim), cuuint64_t(g.rows_cap)};
-        cuuint64_t str[1] = {cuuint64_t(kdim * 2)};
-        cuuint32_t box[2] = {BK, cuuint32_t(swap ? TOK_BOX : BM)};
-        int rc = make_map(&tm_act, g.a, 2, dims, str, box, "activations");
+        int rc = build_maps(g, swap, w8, kdim, wrows, &maps.act, &maps.w);
         if (rc) return rc;
-    }
-    if (!cached && w_mode == 1) {
-        // view W1[e] (2I, K) as (K, 16, 2, I/16): row = half*I + 16*blk + q
-        const int64_t es = w8 ? 1 : 2;
-        cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
-        cuuint64_t str[4] = {cuuint64_t(g.K * es), cuuint64_t(g.I * g.K * es), cuuint64_t(16 * g.K * es),
-                             cuuint64_t(2 * g.I * g.K * es)};
-        cuuint32_t box[5] = {cuuint32_t(w8 ? BK * Cfg<true>::KSUB : BK), 16, 2, cuuint32_t(wtile / 32), 1};
-        int rc = make_map(&tm_w, g.w, 5, dims, str, box, "W1 (gate/up view)", w8);
-        if (rc) return rc;
-    } else if (!cached) {
-        const int64_t es = w8 ? 1 : 2;
-        cuuint64_t dims[3] = {cuuint64_t(kdim), cuuint64_t(wrows), cuuint64_t(g.E)};
-        cuuint64_t str[2] = {cuuint64_t(kdim * es), cuuint64_t(wrows * kdim * es)};
-        cuuint32_t box[3] = {cuuint32_t(w8 ? BK * Cfg<true>::KSUB : BK), cuuint32_t(wtile), 1};
-        int rc = make_map(&tm_w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2", w8);
-        if (rc) return rc;
-    }
-    if (!cached) {
+        if (mixed) {
+            rc = build_maps(g, true, w8, kdim, wrows, &maps.act_s, &maps.w_s);
+            if (rc) return rc;
+        } else {
+            maps.act_s = maps.act;
+            maps.w_s = maps.w;
+        }
         std::lock_guard<std::mutex> lock(g_map_mu);
         if (g_maps.size() >= 256) g_maps.clear();
-        g_maps[key] = MapPair{tm_act, tm_w};
+        g_maps[key] = maps;
     }
 
     TcParams p;
@@ -727,6 +782,9 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     p.rows_cap = g.rows_cap;
     p.nkb = int(kdim / (BK * (w8 ? Cfg<true>::KSUB : 1)));   // stages per tile
     p.nt = int(wrows / wtile);
+    p.mixed = mixed ? 1 : 0;
+    p.nt_n = int(wrows / 256);
+    p.nt_s = int(wrows / 128);
     p.w_mode = w_mode;
     p.I = g.I;
     p.K = g.K;
@@ -751,13 +809,15 @@ int launch_gemm_tc(const GemmArgs& g, bool swap, cudaStream_t s) {
     int64_t segs;
     if (g.layout == MOE_LAYOUT_CONTIGUOUS) segs = (g.rows_cap + span - 1) / span + g.E;
     else segs = int64_t(g.E) * ((g.max_tokens + span - 1) / span);
-    const int64_t tiles = segs * p.nt;
+    const int64_t tiles = segs * p.nt + (mixed ? int64_t(g.E) * p.nt_s : 0);
     if (tiles == 0) return MOE_OK;
     const int grid = int(std::min<int64_t>(tiles, num_sms()));
     if (w8)
-        gemm_tc_kernel<true><<<grid, Cfg<true>::THREADS, Cfg<true>::SMEM, s>>>(tm_act, tm_w, p);
+        gemm_tc_kernel<true><<<grid, Cfg<true>::THREADS, Cfg<true>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
+                                                                                 maps.w_s, p);
     else
-        gemm_tc_kernel<false><<<grid, Cfg<false>::THREADS, Cfg<false>::SMEM, s>>>(tm_act, tm_w, p);
+        gemm_tc_kernel<false><<<grid, Cfg<false>::THREADS, Cfg<false>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
+                                                                                   maps.w_s, p);
     return check_launch("gemm_tc_kernel");
 }
 

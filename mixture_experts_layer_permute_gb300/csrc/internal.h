@@ -60,7 +60,9 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t s);
+// tcgen05 tile kinds: tokens on the MMA M side, weights on M (swap-AB), or both in one launch.
+enum { TC_NORMAL = 0, TC_SWAP = 1, TC_MIXED = 2 };
 // Returns MOE_OK or a status (with message) when the tcgen05 path cannot run.
-int launch_gemm_tc(const GemmArgs& g, bool swap_ab, cudaStream_t s);
+int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s);
 
 }  // namespace moe

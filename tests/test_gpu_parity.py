@@ -17,12 +17,12 @@ from helpers import TOL_BF16, TOL_F32, assert_close, compact_experts, to_f64
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-IMPLS_BF16 = ["tcgen05", "swap_ab", "simt"]
+IMPLS_BF16 = ["tcgen05", "swap_ab", "mixed", "simt"]
 
 
 def _impl(m, name):
     return {"tcgen05": m.MOE_IMPL_TCGEN05, "swap_ab": m.MOE_IMPL_TCGEN05_SWAP_AB, "simt": m.MOE_IMPL_SIMT,
-            "auto": m.MOE_IMPL_AUTO}[name]
+            "mixed": m.MOE_IMPL_TCGEN05_MIXED, "auto": m.MOE_IMPL_AUTO}[name]
 
 
 # ----------------------------------------------------------------------------
@@ -208,12 +208,15 @@ GEMM_SHAPES = [  # T, k, E, K, I, block_m
     (300, 2, 16, 256, 384, 128),
     (600, 1, 2, 256, 256, 1),        # ~300 rows per expert: several m-tiles / two token segments
     (5, 8, 128, 512, 128, 1),        # decode-like: a few tokens per expert
+    (700, 2, 6, 256, 128, 1),        # skewed below: full tiles, long and short tails, tiny experts
 ]
 
 
 def _routed(T, k, E, K, seed):
     w = wl.scaled(wl.decode(T), T=T, K=K, E=E, top_k=k)
     logits = wl.router_logits(w, seed)
+    if E == 6:   # a steep per-expert bias: counts from hundreds down to a handful
+        logits = logits + torch.tensor([6.0, 4.0, 2.5, 1.0, -1.0, -3.0])
     ids, weights = oracle.topk_route(logits.numpy(), k)
     x = wl.activations(w, seed)
     return w, x, ids, weights

@@ -87,8 +87,8 @@ extern "C" {
                                          (AWS blog "MoE kernel engineering on SageMaker AI", Swap-AB:
                                          C^T = B^T A^T when M < 64) */
 #define MOE_IMPL_SIMT 3               /* CUDA-core FMA tiles (fp32 path, any shape) */
-#define MOE_IMPL_TCGEN05_MIXED 4      /* tcgen05: full 128-row tiles per expert, and a swap-AB tile for an
-                                         expert's tail of fewer than 64 rows (bf16 weights) */
+#define MOE_IMPL_TCGEN05_MIXED 4      /* tcgen05: 128-row tiles for experts of 64 rows or more and a swap-AB
+                                         tile for each smaller expert, in one launch (bf16 weights) */
 
 /* Message describing the calling thread's last failed call ("" if none). */
 MOE_API const char* moe_last_error(void);

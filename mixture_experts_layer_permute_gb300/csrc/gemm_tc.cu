@@ -42,10 +42,9 @@
 //   "converted" mbarrier per stage hands the tile to the MMA issuer.  Tokens
 //   per tile are capped at 64.
 //
-// Mixed tiles (bf16): one launch serves every expert with full 128-row normal
-// tiles and puts an expert's tail of fewer than 64 rows (or a whole small
-// expert) on a swap-AB tile, so a skewed routing does not pay a mostly empty
-// 128-row tile per expert.
+// Mixed tiles (bf16): one launch serves experts of 64 rows or more with
+// normal 128-row tiles and smaller experts with a swap-AB tile, so a skewed
+// routing does not pay a mostly empty 128-row tile per small expert.
 //
 // Every mbarrier wait is bounded (2 s of globaltimer); on expiry the kernel
 // records MOE_DEVERR_TIMEOUT, lets its copies in flight land, frees TMEM and
@@ -156,10 +155,11 @@ struct Tile {
     int nb;           // normal: n-tile; swap: weight block
 };
 
-// Mixed mode: an expert with c rows gets n_norm normal m-tiles (a last partial one only when it holds at
-// least 64 rows) and, for a shorter tail, one swap-AB segment.
-MOE_DEVICE int mixed_normal_tiles(int32_t c) { return (c & 127) >= 64 ? (c >> 7) + 1 : (c >> 7); }
-MOE_DEVICE int32_t mixed_tail(int32_t c) { return (c & 127) >= 64 ? 0 : (c & 127); }
+// Mixed mode: an expert with at least 64 rows gets normal 128-row m-tiles (the last one padded); a smaller
+// expert gets one swap-AB segment instead.  Either way each expert's weights are streamed once: a swap-AB
+// tile for the tail of a large expert would stream them a second time, which costs more than the padding.
+MOE_DEVICE int mixed_normal_tiles(int32_t c) { return c >= 64 ? (c + BM - 1) / BM : 0; }
+MOE_DEVICE int32_t mixed_tail(int32_t c) { return c >= 64 ? 0 : c; }
 
 MOE_DEVICE Tile decode_tile(const ExpertTable& tab, const TcParams& p, int32_t t) {
     Tile tl;
@@ -177,7 +177,7 @@ MOE_DEVICE Tile decode_tile(const ExpertTable& tab, const TcParams& p, int32_t t
         } else {
             tl.swap = 1;
             tl.nb = local - nn * p.nt_n;
-            tl.row0 = int64_t(tab.start[tl.e]) + int64_t(c >> 7) * BM;
+            tl.row0 = int64_t(tab.start[tl.e]);
             tl.rows = mixed_tail(c);
         }
         return tl;

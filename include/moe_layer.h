@@ -80,7 +80,7 @@ extern "C" {
                                          _interleave_gate_up_16 "After") */
 
 /* ---- GEMM implementations ---- */
-#define MOE_IMPL_AUTO 0               /* swap-AB tiles when routes/expert are few, else mixed tiles;
+#define MOE_IMPL_AUTO 0               /* swap-AB tiles when routes/expert are few, else normal tiles;
                                          E4M3 weights on swap-AB tiles; CUDA cores for fp32 */
 #define MOE_IMPL_TCGEN05 1            /* tcgen05 tiles, tokens on the MMA M side (128 rows per tile) */
 #define MOE_IMPL_TCGEN05_SWAP_AB 2    /* tcgen05 tiles, weight rows on the MMA M side, tokens on N

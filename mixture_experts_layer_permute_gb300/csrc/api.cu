@@ -183,7 +183,7 @@ int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
             int64_t rows = g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens;
             int64_t per_expert = rows / std::max(1, g.E);
             if (g.layout == MOE_LAYOUT_BATCHED) per_expert = g.max_tokens / 2;
-            chosen = per_expert < 64 ? MOE_IMPL_TCGEN05_SWAP_AB : MOE_IMPL_TCGEN05_MIXED;
+            chosen = per_expert < 64 ? MOE_IMPL_TCGEN05_SWAP_AB : MOE_IMPL_TCGEN05;
         }
     }
     if (chosen == MOE_IMPL_SIMT) return launch_status(launch_gemm_simt(g, s), name);

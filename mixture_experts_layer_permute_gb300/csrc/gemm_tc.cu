@@ -287,14 +287,18 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t pol_w = ptx::policy_evict_first();
-            const uint64_t pol_a = ptx::policy_evict_last();
+            // L2 hints: swap-AB weights are streamed once (evict first); normal-tile weights are reused by
+            // every m-tile of the expert and activation rows by every n-tile (keep them)
+            const uint64_t pol_stream = ptx::policy_evict_first();
+            const uint64_t pol_keep = ptx::policy_evict_last();
+            const uint64_t pol_a = pol_keep;
             uint32_t it = 0;
             for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
                 const Tile tl = decode_tile(tab, p, t);
                 const int nbox = tl.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
                 const CUtensorMap* mact = (p.mixed && tl.swap) ? &tm_act_s : &tm_act;
                 const CUtensorMap* mw = (p.mixed && tl.swap) ? &tm_w_s : &tm_w;
+                const uint64_t pol_w = tl.swap ? pol_stream : pol_keep;
                 constexpr int KSUB = Cfg<W8>::KSUB;
                 const uint32_t wbytes = W8 ? uint32_t(BM * BK * KSUB) : uint32_t(A_BYTES);
                 const uint32_t bytes = tl.swap ? wbytes + uint32_t(KSUB * nbox * TOK_BOX * BK * 2)

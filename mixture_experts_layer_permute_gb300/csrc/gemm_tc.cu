@@ -27,7 +27,7 @@
 // MXFP8 weights (E4M3 codes + one E8M0 scale per 32 along the contraction;
 //   "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): swap-AB tiles
 //   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
-//   7-stage ring of 128-wide k slices (full 128-byte lines; two MMA k-blocks per
+//   6-stage ring of 128-wide k slices (full 128-byte lines; two MMA k-blocks per
 //   hand-off halve the per-byte cost of the single-thread producer and MMA
 //   loops).  Sixteen converter warps (warps 6..13) decode them exactly to
 //   bf16 and store the tile straight into tensor memory with tcgen05.st; the
@@ -40,7 +40,7 @@
 //   and zero codes alike, and one bf16x2 multiply by 2^(scale-7) restores the
 //   value (two multiplies when that factor would leave bf16's range).  A
 //   "converted" mbarrier per stage hands the tile to the MMA issuer.  Tokens
-//   per tile are capped at 32 so that the ring keeps 7 stages of codes.
+//   per tile are capped at 64.
 //
 // Mixed tiles (bf16): one launch serves experts of 64 rows or more with
 // normal 128-row tiles and smaller experts with a swap-AB tile, so a skewed
@@ -77,14 +77,14 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // Per weight type: stage ring layout, TMEM map and CTA shape.
 //   bf16:  smem [A 16 KB][B 32 KB] x 4 stages; TMEM: two 256-column accumulators;
 //          192 threads; up to 256 tokens per swap-AB tile
-//   E4M3:  stages of 128 k (two 64-wide k-blocks): smem [codes 128 rows x 128 B][B tokens 2 x 4 KB]
-//          x 7 stages; TMEM: two 32-column accumulators, then 7 bf16 A tiles of 64 columns (512 in all);
-//          704 threads; up to 32 tokens per tile (an expert with more takes several tiles)
+//   E4M3:  stages of 128 k (two 64-wide k-blocks): smem [codes 128 rows x 128 B][B tokens 2 x 8 KB]
+//          x 6 stages; TMEM: two 64-column accumulators, then 6 bf16 A tiles of 64 columns (512 in all);
+//          704 threads; up to 64 tokens per tile (an expert with more takes several tiles)
 template <bool W8>
 struct Cfg {
     static constexpr int KSUB = W8 ? 2 : 1;                     // 64-wide k-blocks per stage
-    static constexpr int STAGES = W8 ? 7 : 4;
-    static constexpr int TOK_SPAN = W8 ? 32 : 256;              // swap-AB tokens per tile
+    static constexpr int STAGES = W8 ? 6 : 4;
+    static constexpr int TOK_SPAN = W8 ? 64 : 256;              // swap-AB tokens per tile
     static constexpr int B_OFF = W8 ? BM * BK * KSUB : A_BYTES; // tokens (swap) / weights (normal)
     static constexpr int B_SUB = W8 ? TOK_SPAN * BK * 2 : 256 * BK * 2;   // B bytes per 64-wide k-block
     static constexpr int B_BYTES = B_SUB * KSUB;

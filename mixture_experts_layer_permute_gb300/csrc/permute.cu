@@ -238,7 +238,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     const uint4* src = reinterpret_cast<const uint4*>(x + int64_t(r / top_k) * row_bytes);
     uint4* dst = reinterpret_cast<uint4*>(x_out + s * row_bytes);
     const int64_t n = row_bytes / 16;
-    for (int64_t i = lane; i < n; i += 32) dst[i] = src[i];
+    int64_t i = lane;
+    for (; i + 96 < n; i += 128) {   // four vectors in flight per lane
+        const uint4 a = src[i], b = src[i + 32], c = src[i + 64], d = src[i + 96];
+        dst[i] = a;
+        dst[i + 32] = b;
+        dst[i + 64] = c;
+        dst[i + 96] = d;
+    }
+    for (; i < n; i += 32) dst[i] = src[i];
 }
 
 struct Plan {

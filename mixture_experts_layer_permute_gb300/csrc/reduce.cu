@@ -9,6 +9,45 @@ namespace moe {
 
 namespace {
 
+// Raw 16-byte (bf16) or 32-byte (f32) vector of 8 elements.
+template <int DT>
+struct Vec8 {
+    uint4 a, b;
+};
+
+template <int DT>
+MOE_DEVICE Vec8<DT> ld_vec8(const void* base, int64_t elem) {
+    Vec8<DT> v;
+    if constexpr (DT == MOE_F32) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(base) + elem);
+        v.a = p[0];
+        v.b = p[1];
+    } else {
+        v.a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
+        v.b = make_uint4(0, 0, 0, 0);
+    }
+    return v;
+}
+
+template <int DT>
+MOE_DEVICE void unpack8(const Vec8<DT>& v, float (&f)[8]) {
+    if constexpr (DT == MOE_F32) {
+        const uint32_t w[8] = {v.a.x, v.a.y, v.a.z, v.a.w, v.b.x, v.b.y, v.b.z, v.b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[i]);
+    } else {
+        const uint32_t w[4] = {v.a.x, v.a.y, v.a.z, v.a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+}
+
+// Slots are taken 8 at a time: their ids and weights are read first, then all 8 row vectors are
+// requested before any is used, and the products are added in increasing j (the order, and so the
+// result, does not depend on the batching).
 template <int YDT, int ODT>
 __global__ void __launch_bounds__(256) topk_reduce_kernel(const void* __restrict__ y,
                                                           const int32_t* __restrict__ ids,
@@ -20,14 +59,27 @@ __global__ void __launch_bounds__(256) topk_reduce_kernel(const void* __restrict
         const int64_t t = i / vec_per_row;
         const int64_t col = (i - t * vec_per_row) * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < top_k; ++j) {
-            const int e = ids[t * top_k + j];
-            if (e < 0 || e >= E) continue;
-            const float wj = w ? w[t * top_k + j] : 1.0f;
-            float v[8];
-            load8<YDT>(y, (t * top_k + j) * K + col, v);
+        for (int j0 = 0; j0 < top_k; j0 += 8) {
+            int e[8];
+            float wj[8];
+            Vec8<YDT> raw[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj, v[q], acc[q]);
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u;
+                e[u] = j < top_k ? ids[t * top_k + j] : -1;
+                wj[u] = (w && j < top_k) ? w[t * top_k + j] : 1.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (e[u] >= 0 && e[u] < E) raw[u] = ld_vec8<YDT>(y, (t * top_k + j0 + u) * K + col);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (e[u] < 0 || e[u] >= E) continue;
+                float v[8];
+                unpack8<YDT>(raw[u], v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj[u], v[q], acc[q]);
+            }
         }
         store8<ODT>(out, t * K + col, acc);
     }

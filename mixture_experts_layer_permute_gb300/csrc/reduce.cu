@@ -53,11 +53,11 @@ __global__ void __launch_bounds__(256) topk_reduce_kernel(const void* __restrict
                                                           const int32_t* __restrict__ ids,
                                                           const float* __restrict__ w, int64_t T, int top_k, int E,
                                                           int64_t K, void* __restrict__ out) {
-    const int64_t vec_per_row = K / 8;
-    const int64_t n = T * vec_per_row;
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = i / vec_per_row;
-        const int64_t col = (i - t * vec_per_row) * 8;
+    // grid: x over the 8-element column vectors of a row, y over output rows (no index division)
+    const int64_t vec = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (vec >= K / 8) return;
+    const int64_t col = vec * 8;
+    for (int64_t t = blockIdx.y; t < T; t += gridDim.y) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j0 = 0; j0 < top_k; j0 += 8) {
             int e[8];
@@ -90,13 +90,12 @@ __global__ void __launch_bounds__(256) batched_weight_kernel(const void* __restr
                                                              const int32_t* __restrict__ counts,
                                                              const float* __restrict__ w, int E, int max_tokens,
                                                              int64_t K, void* out) {
-    const int64_t vec_per_row = K / 8;
-    const int64_t n = int64_t(E) * max_tokens * vec_per_row;
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t row = i / vec_per_row;
+    const int64_t vec = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (vec >= K / 8) return;
+    const int64_t col = vec * 8;
+    for (int64_t row = blockIdx.y; row < int64_t(E) * max_tokens; row += gridDim.y) {
         const int e = int(row / max_tokens), q = int(row - int64_t(e) * max_tokens);
         if (q >= counts[e]) continue;
-        const int64_t col = (i - row * vec_per_row) * 8;
         const float wr = w ? w[row] : 1.0f;
         float v[8];
         load8<YDT>(y, row * K + col, v);
@@ -106,11 +105,14 @@ __global__ void __launch_bounds__(256) batched_weight_kernel(const void* __restr
     }
 }
 
-unsigned grid_for(int64_t n) {
-    int64_t blocks = (n + 255) / 256;
-    int64_t cap = int64_t(num_sms()) * 8;
-    if (blocks > cap) blocks = cap;
-    return unsigned(blocks < 1 ? 1 : blocks);
+// x blocks cover one row's K/8 vectors; y blocks (rows, strided) fill the GPU to ~8 resident blocks per SM
+dim3 grid_for(int64_t rows, int64_t K) {
+    const int64_t gx = (K / 8 + 255) / 256;
+    int64_t gy = (int64_t(num_sms()) * 8 + gx - 1) / gx;
+    if (gy > rows) gy = rows;
+    if (gy > 65535) gy = 65535;
+    if (gy < 1) gy = 1;
+    return dim3(unsigned(gx), unsigned(gy));
 }
 
 }  // namespace
@@ -118,7 +120,7 @@ unsigned grid_for(int64_t n) {
 cudaError_t launch_topk_reduce(const void* y, int y_dtype, const int32_t* ids, const float* w, int64_t T,
                                int top_k, int E, int64_t K, void* out, int out_dtype, cudaStream_t s) {
     if (T == 0 || K == 0) return cudaSuccess;
-    const unsigned g = grid_for(T * (K / 8));
+    const dim3 g = grid_for(T, K);
 #define MOE_REDUCE(YD, OD) topk_reduce_kernel<YD, OD><<<g, 256, 0, s>>>(y, ids, w, T, top_k, E, K, out)
     if (y_dtype == MOE_BF16 && out_dtype == MOE_BF16) MOE_REDUCE(MOE_BF16, MOE_BF16);
     else if (y_dtype == MOE_BF16 && out_dtype == MOE_F32) MOE_REDUCE(MOE_BF16, MOE_F32);
@@ -131,7 +133,7 @@ cudaError_t launch_topk_reduce(const void* y, int y_dtype, const int32_t* ids, c
 cudaError_t launch_batched_weight(const void* y, int y_dtype, const int32_t* counts, const float* w, int E,
                                   int max_tokens, int64_t K, void* out, int out_dtype, cudaStream_t s) {
     if (E == 0 || max_tokens == 0 || K == 0) return cudaSuccess;
-    const unsigned g = grid_for(int64_t(E) * max_tokens * (K / 8));
+    const dim3 g = grid_for(int64_t(E) * max_tokens, K);
 #define MOE_BW(YD, OD) batched_weight_kernel<YD, OD><<<g, 256, 0, s>>>(y, counts, w, E, max_tokens, K, out)
     if (y_dtype == MOE_BF16 && out_dtype == MOE_BF16) MOE_BW(MOE_BF16, MOE_BF16);
     else if (y_dtype == MOE_BF16 && out_dtype == MOE_F32) MOE_BW(MOE_BF16, MOE_F32);

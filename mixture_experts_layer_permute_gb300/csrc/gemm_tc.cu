@@ -77,7 +77,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // Per weight type: stage ring layout, TMEM map and CTA shape.
 //   bf16:  smem [A 16 KB][B 32 KB] x 4 stages; TMEM: two 256-column accumulators;
 //          192 threads; up to 256 tokens per swap-AB tile
-//   E4M3:  stages of 128 k (two 64-wide k-blocks): smem [codes 128 rows x 128 B][B tokens 2 x 8 KB]
+//   E4M3:  stages of 128 k (two 64-wide k-blocks): smem [codes 128 rows x 128 B, swizzled][B tokens 2 x 8 KB]
 //          x 6 stages; TMEM: two 64-column accumulators, then 6 bf16 A tiles of 64 columns (512 in all);
 //          704 threads; up to 64 tokens per tile (an expert with more takes several tiles)
 template <bool W8>
@@ -435,8 +435,11 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                const uint4* src = reinterpret_cast<const uint4*>(smem + s * STAGE_BYTES + r * (BK * 2) + h * 32);
-                const uint4 v0 = src[0], v1 = src[1];
+                // the code tile lands 128-byte swizzled: 16-byte chunk c of row r sits at chunk c ^ (r % 8), so
+                // the 8 rows of a load phase read 8 different bank groups
+                const uint8_t* row = smem + s * STAGE_BYTES + r * (BK * 2);
+                const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * h) ^ (r & 7)) << 4));
+                const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * h + 1) ^ (r & 7)) << 4));
                 uint32_t o[16];
                 dequant4(v0.x, f1, o[0], o[1]);
                 dequant4(v0.y, f1, o[2], o[3]);
@@ -632,10 +635,11 @@ int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(MOE_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    // bf16 operands land 128-byte swizzled for the MMA; E4M3 codes land as plain rows for the converters
+    // every tile lands 128-byte swizzled: bf16 operands for the MMA, E4M3 code rows (128 bytes) for the
+    // converters' conflict-free reads
     CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank),
                     const_cast<void*>(base), dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(MOE_ERR_ALIGNMENT, std::string("cuTensorMapEncodeTiled failed for ") + what + " (CUresult " +

@@ -29,11 +29,11 @@
 //   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
 //   6-stage ring of 128-wide k slices (full 128-byte lines; two MMA k-blocks per
 //   hand-off halve the per-byte cost of the single-thread producer and MMA
-//   loops).  Sixteen converter warps (warps 6..13) decode them exactly to
+//   loops).  Sixteen converter warps in two groups that take alternate stages (warps 6..13) decode them exactly to
 //   bf16 and store the tile straight into tensor memory with tcgen05.st; the
 //   MMA takes its A operand from TMEM.  Warp w may only reach TMEM lanes
-//   32*(w%4)..+31, so thread (w, lane) owns row 32*(w%4)+lane and quarter
-//   (w-6)/4 of each 128-wide slice: 32 codes and one scale.  Decoding needs no
+//   32*(w%4)..+31, so in its group thread (w, lane) owns row 32*(w%4)+lane and
+//   one half of each 128-wide slice: 64 codes and two scales.  Decoding needs no
 //   conversion instruction: the E4M3
 //   bits placed into bf16 bit positions (sign to bit 15, exponent and
 //   mantissa to bits 10..4) give exactly code * 2^-120 for normal, subnormal
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&ctrl.full[s], 1);
             ptx::mbar_init(&ctrl.empty[s], 1);
-            ptx::mbar_init(&ctrl.conv[s], kConvThreads / 32);   // one arrive per converter warp
+            ptx::mbar_init(&ctrl.conv[s], kConvThreads / 64);   // one arrive per warp of the converting group
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&ctrl.acc_full[b], 1);
@@ -398,64 +398,61 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters
-        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile and scale block
-        // h = (w-6)/4 of each 128-wide slice: codes 32h..32h+31 go to TMEM lane r, columns 16h..16h+15 of
-        // the stage's A tile
-        const int q = warp & 3, h = (warp - 6) >> 2, r = q * 32 + lane;
+        // Two groups of 8 warps convert alternate stages, so two stages are in conversion at once.  In a
+        // group, thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile and half hh of
+        // each 128-wide slice: codes 64hh..64hh+63 (scale blocks 2hh, 2hh+1) go to TMEM lane r, columns
+        // 32hh..32hh+31 of the stage's A tile.
+        const int cw = warp - 6, grp = cw >> 3, hh = (cw >> 2) & 1;
+        const int q = warp & 3, r = q * 32 + lane;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows (4 slices per 16 B)
         uint32_t it = 0;
         for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
             const Tile tl = decode_tile(tab, p, t);
             const uint8_t* srow = p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb;
-            // scales of 4 slices (16 bytes) per register group; the next group is loaded one group ahead
-            uint4 cur = make_uint4(0, 0, 0, 0), nxt = make_uint4(0, 0, 0, 0);
-            if (vec_scales) {
-                cur = __ldg(reinterpret_cast<const uint4*>(srow));
-                if (p.nkb > 4) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 16));
-            }
             bool ok = true;
             for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                uint32_t sc;
+                if (int(it & 1) != grp) continue;   // the other group's stage
+                uint32_t pair;                      // this thread's two scale bytes of the slice
                 if (vec_scales) {
-                    const int j = kb & 3;   // slice j of the group: scale bytes 4j..4j+3, this thread's 4j+h
-                    const uint32_t word = j == 0 ? cur.x : (j == 1 ? cur.y : (j == 2 ? cur.z : cur.w));
-                    sc = (word >> (8 * h)) & 0xFFu;
-                    if (j == 3) {
-                        cur = nxt;
-                        if (kb + 5 < p.nkb) nxt = __ldg(reinterpret_cast<const uint4*>(srow + 4 * (kb + 5)));
-                    }
+                    pair = __ldg(reinterpret_cast<const uint16_t*>(srow + 4 * kb + 2 * hh));
                 } else {
-                    sc = __ldg(srow + 4 * kb + h);
+                    pair = uint32_t(__ldg(srow + 4 * kb + 2 * hh)) | (uint32_t(__ldg(srow + 4 * kb + 2 * hh + 1)) << 8);
                 }
-                // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that factor
-                // leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
-                const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
-                const uint32_t f1 = (e1 << 7) | (e1 << 23);
+                if (kb + 8 < p.nkb) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 4 * (kb + 8)));
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                // the code tile lands 128-byte swizzled: 16-byte chunk c of row r sits at chunk c ^ (r % 8), so
-                // the 8 rows of a load phase read 8 different bank groups
+                // the code tile lands 128-byte swizzled: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
                 const uint8_t* row = smem + s * STAGE_BYTES + r * (BK * 2);
-                const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * h) ^ (r & 7)) << 4));
-                const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * h + 1) ^ (r & 7)) << 4));
-                uint32_t o[16];
-                dequant4(v0.x, f1, o[0], o[1]);
-                dequant4(v0.y, f1, o[2], o[3]);
-                dequant4(v0.z, f1, o[4], o[5]);
-                dequant4(v0.w, f1, o[6], o[7]);
-                dequant4(v1.x, f1, o[8], o[9]);
-                dequant4(v1.y, f1, o[10], o[11]);
-                dequant4(v1.z, f1, o[12], o[13]);
-                dequant4(v1.w, f1, o[14], o[15]);
-                if (sc > 134u) {
-                    const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
+                uint32_t o[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = bf16x2_mul(o[i], f2);
+                for (int b = 0; b < 2; ++b) {
+                    const uint32_t sc = (pair >> (8 * b)) & 0xFFu;
+                    // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that
+                    // factor leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
+                    const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
+                    const uint32_t f1 = (e1 << 7) | (e1 << 23);
+                    const int c0 = 4 * hh + 2 * b;   // logical chunks c0, c0+1: codes 32*(2hh+b) .. +31
+                    const uint4 v0 = *reinterpret_cast<const uint4*>(row + ((c0 ^ (r & 7)) << 4));
+                    const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4));
+                    uint32_t* ob = o + 16 * b;
+                    dequant4(v0.x, f1, ob[0], ob[1]);
+                    dequant4(v0.y, f1, ob[2], ob[3]);
+                    dequant4(v0.z, f1, ob[4], ob[5]);
+                    dequant4(v0.w, f1, ob[6], ob[7]);
+                    dequant4(v1.x, f1, ob[8], ob[9]);
+                    dequant4(v1.y, f1, ob[10], ob[11]);
+                    dequant4(v1.z, f1, ob[12], ob[13]);
+                    dequant4(v1.w, f1, ob[14], ob[15]);
+                    if (sc > 134u) {
+                        const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], f2);
+                    }
                 }
-                ptx::tmem_st_32x32b_x16(
-                    tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + h * 16), o);
+                ptx::tmem_st_32x32b_x32(
+                    tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + hh * 32), o);
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();

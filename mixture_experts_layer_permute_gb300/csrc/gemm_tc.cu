@@ -29,11 +29,11 @@
 //   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
 //   6-stage ring of 128-wide k slices (full 128-byte lines; two MMA k-blocks per
 //   hand-off halve the per-byte cost of the single-thread producer and MMA
-//   loops).  Sixteen converter warps in two groups that take alternate stages (warps 6..13) decode them exactly to
+//   loops).  Sixteen converter warps in four groups that take stages in turn (warps 6..13) decode them exactly to
 //   bf16 and store the tile straight into tensor memory with tcgen05.st; the
 //   MMA takes its A operand from TMEM.  Warp w may only reach TMEM lanes
-//   32*(w%4)..+31, so in its group thread (w, lane) owns row 32*(w%4)+lane and
-//   one half of each 128-wide slice: 64 codes and two scales.  Decoding needs no
+//   32*(w%4)..+31, so in its group thread (w, lane) owns row 32*(w%4)+lane of
+//   the slice: 128 codes and four scales.  Decoding needs no
 //   conversion instruction: the E4M3
 //   bits placed into bf16 bit positions (sign to bit 15, exponent and
 //   mantissa to bits 10..4) give exactly code * 2^-120 for normal, subnormal
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&ctrl.full[s], 1);
             ptx::mbar_init(&ctrl.empty[s], 1);
-            ptx::mbar_init(&ctrl.conv[s], kConvThreads / 64);   // one arrive per warp of the converting group
+            ptx::mbar_init(&ctrl.conv[s], 4);   // one arrive per warp of the converting group
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&ctrl.acc_full[b], 1);
@@ -398,11 +398,10 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters
-        // Two groups of 8 warps convert alternate stages, so two stages are in conversion at once.  In a
-        // group, thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile and half hh of
-        // each 128-wide slice: codes 64hh..64hh+63 (scale blocks 2hh, 2hh+1) go to TMEM lane r, columns
-        // 32hh..32hh+31 of the stage's A tile.
-        const int cw = warp - 6, grp = cw >> 3, hh = (cw >> 2) & 1;
+        // Four groups of 4 warps take stages in turn, so four stages are in conversion at once.  In a group,
+        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile: its 128 codes of the
+        // slice (scale blocks 0..3) go to TMEM lane r, the stage's 64 A-tile columns.
+        const int cw = warp - 6, grp = cw >> 2;
         const int q = warp & 3, r = q * 32 + lane;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows (4 slices per 16 B)
@@ -412,47 +411,51 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             const uint8_t* srow = p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb;
             bool ok = true;
             for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                if (int(it & 1) != grp) continue;   // the other group's stage
-                uint32_t pair;                      // this thread's two scale bytes of the slice
+                if (int(it & 3) != grp) continue;   // another group's stage
+                uint32_t quad;                      // this row's four scale bytes of the slice
                 if (vec_scales) {
-                    pair = __ldg(reinterpret_cast<const uint16_t*>(srow + 4 * kb + 2 * hh));
+                    quad = __ldg(reinterpret_cast<const uint32_t*>(srow + 4 * kb));
                 } else {
-                    pair = uint32_t(__ldg(srow + 4 * kb + 2 * hh)) | (uint32_t(__ldg(srow + 4 * kb + 2 * hh + 1)) << 8);
+                    quad = 0;
+                    for (int b = 0; b < 4; ++b) quad |= uint32_t(__ldg(srow + 4 * kb + b)) << (8 * b);
                 }
-                if (kb + 8 < p.nkb) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 4 * (kb + 8)));
+                if (kb + 16 < p.nkb) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 4 * (kb + 16)));
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
                 // the code tile lands 128-byte swizzled: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
                 const uint8_t* row = smem + s * STAGE_BYTES + r * (BK * 2);
-                uint32_t o[32];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const uint32_t sc = (pair >> (8 * b)) & 0xFFu;
-                    // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that
-                    // factor leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
-                    const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
-                    const uint32_t f1 = (e1 << 7) | (e1 << 23);
-                    const int c0 = 4 * hh + 2 * b;   // logical chunks c0, c0+1: codes 32*(2hh+b) .. +31
-                    const uint4 v0 = *reinterpret_cast<const uint4*>(row + ((c0 ^ (r & 7)) << 4));
-                    const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4));
-                    uint32_t* ob = o + 16 * b;
-                    dequant4(v0.x, f1, ob[0], ob[1]);
-                    dequant4(v0.y, f1, ob[2], ob[3]);
-                    dequant4(v0.z, f1, ob[4], ob[5]);
-                    dequant4(v0.w, f1, ob[6], ob[7]);
-                    dequant4(v1.x, f1, ob[8], ob[9]);
-                    dequant4(v1.y, f1, ob[10], ob[11]);
-                    dequant4(v1.z, f1, ob[12], ob[13]);
-                    dequant4(v1.w, f1, ob[14], ob[15]);
-                    if (sc > 134u) {
-                        const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t o[32];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], f2);
+                    for (int b2 = 0; b2 < 2; ++b2) {
+                        const int b = 2 * half + b2;     // scale block of the slice
+                        const uint32_t sc = (quad >> (8 * b)) & 0xFFu;
+                        // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that
+                        // factor leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
+                        const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
+                        const uint32_t f1 = (e1 << 7) | (e1 << 23);
+                        const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * b) ^ (r & 7)) << 4));
+                        const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * b + 1) ^ (r & 7)) << 4));
+                        uint32_t* ob = o + 16 * b2;
+                        dequant4(v0.x, f1, ob[0], ob[1]);
+                        dequant4(v0.y, f1, ob[2], ob[3]);
+                        dequant4(v0.z, f1, ob[4], ob[5]);
+                        dequant4(v0.w, f1, ob[6], ob[7]);
+                        dequant4(v1.x, f1, ob[8], ob[9]);
+                        dequant4(v1.y, f1, ob[10], ob[11]);
+                        dequant4(v1.z, f1, ob[12], ob[13]);
+                        dequant4(v1.w, f1, ob[14], ob[15]);
+                        if (sc > 134u) {
+                            const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], f2);
+                        }
                     }
+                    ptx::tmem_st_32x32b_x32(
+                        tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + half * 32), o);
                 }
-                ptx::tmem_st_32x32b_x32(
-                    tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + hh * 32), o);
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();

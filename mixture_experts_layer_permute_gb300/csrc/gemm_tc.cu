@@ -26,21 +26,21 @@
 //
 // MXFP8 weights (E4M3 codes + one E8M0 scale per 32 along the contraction;
 //   "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): swap-AB tiles
-//   only.  TMA streams the raw codes (1 byte per weight, each read once) into a
-//   6-stage ring of 128-wide k slices (full 128-byte lines; two MMA k-blocks per
-//   hand-off halve the per-byte cost of the single-thread producer and MMA
-//   loops).  Sixteen converter warps in four groups that take stages in turn (warps 6..13) decode them exactly to
-//   bf16 and store the tile straight into tensor memory with tcgen05.st; the
-//   MMA takes its A operand from TMEM.  Warp w may only reach TMEM lanes
-//   32*(w%4)..+31, so in its group thread (w, lane) owns row 32*(w%4)+lane of
-//   the slice: 128 codes and four scales.  Decoding needs no
-//   conversion instruction: the E4M3
-//   bits placed into bf16 bit positions (sign to bit 15, exponent and
-//   mantissa to bits 10..4) give exactly code * 2^-120 for normal, subnormal
-//   and zero codes alike, and one bf16x2 multiply by 2^(scale-7) restores the
-//   value (two multiplies when that factor would leave bf16's range).  A
-//   "converted" mbarrier per stage hands the tile to the MMA issuer.  Tokens
-//   per tile are capped at 64.
+//   only, 128-wide k slices.  Two rings: TMA streams the raw codes (1 byte per
+//   weight, each read once, full 128-byte lines, 128-byte swizzled) into a
+//   9-stage code ring that is freed as soon as a slice is decoded; four A
+//   slots hold decoded tiles in tensor memory plus the matching token tiles
+//   (loaded by a token-producer warp once the MMA has released the slot).
+//   Sixteen converter warps in four groups take slices in turn (group = slice
+//   index mod 4 = A slot), so four slices are in conversion at once.  Warp w
+//   may only reach TMEM lanes 32*(w%4)..+31, so in its group thread (w, lane)
+//   owns row 32*(w%4)+lane of the slice: 128 codes and four scales.  Decoding
+//   needs no conversion instruction: the E4M3 bits placed into bf16 bit
+//   positions (sign to bit 15, exponent and mantissa to bits 10..4) give
+//   exactly code * 2^-120 for normal, subnormal and zero codes alike, and one
+//   bf16x2 multiply by 2^(scale-7) restores the value (two multiplies when that
+//   factor would leave bf16's range).  The MMA takes its A operand from TMEM.
+//   Tokens per tile are capped at 64.
 //
 // Mixed tiles (bf16): one launch serves experts of 64 rows or more with
 // normal 128-row tiles and smaller experts with a swap-AB tile, so a skewed
@@ -77,35 +77,41 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // Per weight type: stage ring layout, TMEM map and CTA shape.
 //   bf16:  smem [A 16 KB][B 32 KB] x 4 stages; TMEM: two 256-column accumulators;
 //          192 threads; up to 256 tokens per swap-AB tile
-//   E4M3:  stages of 128 k (two 64-wide k-blocks): smem [codes 128 rows x 128 B, swizzled][B tokens 2 x 8 KB]
-//          x 6 stages; TMEM: two 64-column accumulators, then 6 bf16 A tiles of 64 columns (512 in all);
-//          704 threads; up to 64 tokens per tile (an expert with more takes several tiles)
+//   E4M3:  smem: 9 code stages of 128 rows x 128 B, then 4 token slots of 2 x 8 KB;
+//          TMEM: two 64-column accumulators, then 4 bf16 A tiles of 64 columns;
+//          736 threads (+ 16 converter warps, + 1 token warp); up to 64 tokens per tile
 template <bool W8>
 struct Cfg {
     static constexpr int KSUB = W8 ? 2 : 1;                     // 64-wide k-blocks per stage
-    static constexpr int STAGES = W8 ? 6 : 4;
+    static constexpr int STAGES = W8 ? 9 : 4;                   // bf16: operand stages; E4M3: code stages
+    static constexpr int A_SLOTS = 4;                           // E4M3: TMEM A tiles (+ token tiles)
     static constexpr int TOK_SPAN = W8 ? 64 : 256;              // swap-AB tokens per tile
-    static constexpr int B_OFF = W8 ? BM * BK * KSUB : A_BYTES; // tokens (swap) / weights (normal)
-    static constexpr int B_SUB = W8 ? TOK_SPAN * BK * 2 : 256 * BK * 2;   // B bytes per 64-wide k-block
-    static constexpr int B_BYTES = B_SUB * KSUB;
-    static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
-    static constexpr int THREADS = W8 ? 192 + kConvThreads : 192;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+    static constexpr int B_OFF = W8 ? 0 : A_BYTES;              // bf16: B operand offset in a stage
+    static constexpr int B_SUB = TOK_SPAN * BK * 2;             // token bytes per 64-wide k-block (swap)
+    static constexpr int B_BYTES = W8 ? 0 : 256 * BK * 2;
+    static constexpr int STAGE_BYTES = W8 ? BM * BK * KSUB : A_BYTES + B_BYTES;
+    static constexpr int TOK_OFF = STAGES * STAGE_BYTES;        // E4M3: token slots after the code ring
+    static constexpr int TOK_SLOT = B_SUB * KSUB;
+    static constexpr int THREADS = W8 ? 192 + kConvThreads + 32 : 192;   // E4M3: + converters + token warp
+    static constexpr int TOK_WARP = 6 + kConvThreads / 32;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + (W8 ? A_SLOTS * TOK_SLOT : 0) + 1024;
     static constexpr int ACC_STRIDE = W8 ? TOK_SPAN : ACC_COLS; // TMEM columns per accumulator
     static constexpr int A_TMEM = 2 * ACC_STRIDE;               // E4M3: first A tile column
-    static constexpr int A_COLS = KSUB * BK / 2;                // E4M3: TMEM columns per stage
-    static constexpr int TMEM_USED = W8 ? A_TMEM + STAGES * A_COLS : 2 * ACC_STRIDE;
+    static constexpr int A_COLS = KSUB * BK / 2;                // E4M3: TMEM columns per A tile
+    static constexpr int TMEM_USED = W8 ? A_TMEM + A_SLOTS * A_COLS : 2 * ACC_STRIDE;
 };
 static_assert(Cfg<false>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed the TMEM allocation");
 static_assert(Cfg<true>::TMEM_USED <= TMEM_COLS, "E4M3 accumulators and A tiles exceed the TMEM allocation");
 static_assert(Cfg<false>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
 static_assert(Cfg<true>::SMEM + 13 * 1024 <= 227 * 1024, "E4M3 stage ring exceeds shared memory");
 static_assert(Cfg<true>::STAGES <= MAX_STAGES && Cfg<false>::STAGES <= MAX_STAGES, "too many stages");
+static_assert(Cfg<true>::A_SLOTS == 4, "converter groups take A slot (stage index mod 4)");
 
 struct __align__(8) Ctrl {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
-    uint64_t conv[MAX_STAGES];
+    uint64_t conv[MAX_STAGES];   // E4M3: A slot converted and its tokens landed
+    uint64_t a_empty[4];         // E4M3: A slot free (MMA done)
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -255,8 +261,11 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&ctrl.full[s], 1);
-            ptx::mbar_init(&ctrl.empty[s], 1);
-            ptx::mbar_init(&ctrl.conv[s], 4);   // one arrive per warp of the converting group
+            ptx::mbar_init(&ctrl.empty[s], W8 ? 4 : 1);   // E4M3: freed by the 4 warps of the converting group
+        }
+        for (int a = 0; a < Cfg<W8>::A_SLOTS; ++a) {
+            ptx::mbar_init(&ctrl.conv[a], 5);             // 4 converter warps + the token producer
+            ptx::mbar_init(&ctrl.a_empty[a], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&ctrl.acc_full[b], 1);
@@ -307,8 +316,9 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 const uint64_t pol_w = tl.swap ? pol_stream : pol_keep;
                 constexpr int KSUB = Cfg<W8>::KSUB;
                 const uint32_t wbytes = W8 ? uint32_t(BM * BK * KSUB) : uint32_t(A_BYTES);
-                const uint32_t bytes = tl.swap ? wbytes + uint32_t(KSUB * nbox * TOK_BOX * BK * 2)
-                                              : uint32_t(A_BYTES + Cfg<W8>::B_BYTES);
+                const uint32_t bytes = W8 ? wbytes
+                                          : (tl.swap ? wbytes + uint32_t(nbox * TOK_BOX * BK * 2)
+                                                     : uint32_t(A_BYTES + Cfg<W8>::B_BYTES));
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -327,11 +337,12 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                         ptx::tma_load_5d(wdst, mw, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_w);
                     else
                         ptx::tma_load_3d(wdst, mw, &ctrl.full[s], k0, row_w, tl.e, pol_w);
-                    if (tl.swap) {
-                        for (int sub = 0; sub < KSUB; ++sub)
-                            for (int b = 0; b < nbox; ++b)
-                                ptx::tma_load_2d(sb + sub * Cfg<W8>::B_SUB + b * TOK_BOX * BK * 2, mact,
-                                                 &ctrl.full[s], k0 + sub * BK, int32_t(tl.row0 + b * TOK_BOX), pol_a);
+                    if (W8) {
+                        // E4M3 tokens come from the token producer
+                    } else if (tl.swap) {
+                        for (int b = 0; b < nbox; ++b)
+                            ptx::tma_load_2d(sb + b * TOK_BOX * BK * 2, mact, &ctrl.full[s], k0,
+                                             int32_t(tl.row0 + b * TOK_BOX), pol_a);
                     } else {
                         ptx::tma_load_2d(sa, mact, &ctrl.full[s], k0, int32_t(tl.row0), pol_a);
                     }
@@ -363,28 +374,38 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg<W8>::ACC_STRIDE);
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                    if (W8 && !wait_bar(&ctrl.conv[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
-                    const uint32_t sb = sa + Cfg<W8>::B_OFF;
+                    if constexpr (W8) {
+                        // A slot a: decoded weights in TMEM, tokens in the slot's smem tile
+                        const int a = it % Cfg<W8>::A_SLOTS;
+                        const uint32_t ph = (it / Cfg<W8>::A_SLOTS) & 1;
+                        if (!wait_bar(&ctrl.conv[a], ph, ctrl, p.err_word)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        const uint32_t sb = ptx::smem_addr(smem + Cfg<W8>::TOK_OFF + a * Cfg<W8>::TOK_SLOT);
 #pragma unroll
-                    for (int kk = 0; kk < Cfg<W8>::KSUB * BK / UMMA_K; ++kk) {
-                        const int sub = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
-                        const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<W8>::B_SUB + kq * UMMA_K * 2);
-                        if constexpr (W8) {
-                            // A from TMEM: 16 bf16 of a row = 8 columns per k step
+                        for (int kk = 0; kk < Cfg<W8>::KSUB * BK / UMMA_K; ++kk) {
+                            const int sub = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
+                            const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<W8>::B_SUB + kq * UMMA_K * 2);
+                            // 16 bf16 of a row = 8 TMEM columns per k step
                             const uint32_t a_tmem =
-                                tmem_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + kk * 8);
+                                tmem_base + uint32_t(Cfg<W8>::A_TMEM + a * Cfg<W8>::A_COLS + kk * 8);
                             ptx::mma_f16_tmem_a(d_tmem, a_tmem, bd, idesc, (kb | kk) != 0);
-                        } else {
+                        }
+                        ptx::mma_commit(&ctrl.a_empty[a]);
+                    } else {
+                        const int s = it % STAGES;
+                        const uint32_t ph = (it / STAGES) & 1;
+                        if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
+                        const uint32_t sb = sa + Cfg<W8>::B_OFF;
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                             const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
+                            const uint64_t bd = ptx::smem_desc_sw128(sb + kk * UMMA_K * 2);
                             ptx::mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                         }
+                        ptx::mma_commit(&ctrl.empty[s]);
                     }
-                    ptx::mma_commit(&ctrl.empty[s]);
                 }
                 if (!ok) break;
                 ptx::mma_commit(&ctrl.acc_full[buf]);
@@ -397,10 +418,46 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         }
         __syncwarp();
     } else if (W8 && warp >= 6) {
-        // ------------------------------------------------------------ E4M3 converters
-        // Four groups of 4 warps take stages in turn, so four stages are in conversion at once.  In a group,
-        // thread (warp w, lane) owns row r = 32*(w%4) + lane of the 128-row weight tile: its 128 codes of the
-        // slice (scale blocks 0..3) go to TMEM lane r, the stage's 64 A-tile columns.
+        // ------------------------------------------------------------ E4M3 converters and token producer
+        if (warp == Cfg<W8>::TOK_WARP) {
+            // token producer: one lane loads each stage's token rows into A slot (stage % 4) once the MMA
+            // has released that slot
+            if (lane == 0) {
+                const uint64_t pol_keep = ptx::policy_evict_last();
+                uint32_t it = 0;
+                for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
+                    const Tile tl = decode_tile(tab, p, t);
+                    const int nbox = (tl.rows + TOK_BOX - 1) / TOK_BOX;
+                    const uint32_t bytes = uint32_t(Cfg<W8>::KSUB * nbox * TOK_BOX * BK * 2);
+                    bool ok = true;
+                    for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+                        const int a = it % Cfg<W8>::A_SLOTS;
+                        const uint32_t ph = (it / Cfg<W8>::A_SLOTS) & 1;
+                        if (!wait_bar(&ctrl.a_empty[a], ph ^ 1, ctrl, p.err_word)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(&ctrl.conv[a], bytes);
+                        uint8_t* dst = smem + Cfg<W8>::TOK_OFF + a * Cfg<W8>::TOK_SLOT;
+                        const int k0 = kb * BK * Cfg<W8>::KSUB;
+                        for (int sub = 0; sub < Cfg<W8>::KSUB; ++sub)
+                            for (int b = 0; b < nbox; ++b)
+                                ptx::tma_load_2d(dst + sub * Cfg<W8>::B_SUB + b * TOK_BOX * BK * 2, &tm_act,
+                                                 &ctrl.conv[a], k0 + sub * BK, int32_t(tl.row0 + b * TOK_BOX),
+                                                 pol_keep);
+                    }
+                    if (!ok) break;
+                }
+                // token copies in flight land before the CTA can exit (bounded)
+                for (uint32_t j = it > 4u ? it - 4u : 0u; j < it; ++j) {
+                    const uint64_t deadline = ptx::globaltimer() + kWaitNs / 8;
+                    volatile int never = 0;
+                    ptx::mbar_wait_bounded(&ctrl.conv[j % 4], (j / 4) & 1, deadline, &never);
+                }
+            }
+            __syncwarp();
+        } else {
+        // Four groups of 4 warps take stages in turn (group = stage index mod 4 = its A slot), so four
+        // stages are in conversion at once.  In a group, thread (warp w, lane) owns row r = 32*(w%4) + lane
+        // of the 128-row weight tile: its 128 codes of the slice (scale blocks 0..3) go to TMEM lane r, the
+        // slot's 64 A-tile columns.
         const int cw = warp - 6, grp = cw >> 2;
         const int q = warp & 3, r = q * 32 + lane;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
@@ -420,9 +477,11 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                     for (int b = 0; b < 4; ++b) quad |= uint32_t(__ldg(srow + 4 * kb + b)) << (8 * b);
                 }
                 if (kb + 16 < p.nkb) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 4 * (kb + 16)));
-                const int s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1;
+                const int s = it % STAGES, a = grp;
+                const uint32_t ph = (it / STAGES) & 1, pha = (it / Cfg<W8>::A_SLOTS) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
+                if (!wait_bar(&ctrl.a_empty[a], pha ^ 1, ctrl, p.err_word)) { ok = false; break; }
+                ptx::tc_fence_after();   // the MMA that last read this A slot has completed
                 // the code tile lands 128-byte swizzled: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
                 const uint8_t* row = smem + s * STAGE_BYTES + r * (BK * 2);
 #pragma unroll
@@ -454,14 +513,18 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                         }
                     }
                     ptx::tmem_st_32x32b_x32(
-                        tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + s * Cfg<W8>::A_COLS + half * 32), o);
+                        tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + a * Cfg<W8>::A_COLS + half * 32), o);
                 }
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&ctrl.conv[s]);
+                if (lane == 0) {
+                    ptx::mbar_arrive(&ctrl.empty[s]);   // the code stage can be refilled
+                    ptx::mbar_arrive(&ctrl.conv[a]);    // the A slot is ready for the MMA
+                }
             }
             if (!ok) break;
+        }
         }
     } else {
         // ------------------------------------------------------------ epilogue

@@ -68,6 +68,7 @@ def _load():
             "oracle_expert_gate_up": (I32, [P, I32, I64, P, P, P, I32, I32, I32, I64, I64, P, I32]),
             "oracle_expert_down": (I32, [P, I32, I64, P, P, P, I32, I32, I64, I64, P, I32]),
             "oracle_topk_reduce": (I32, [P, I32, P, P, I64, I32, I64, P, I32]),
+            "oracle_batched_topk_reduce": (I32, [P, I32, I64, P, P, I64, I32, I64, P, I32]),
             "oracle_moe_layer": (I32, [P, I32, I64, I64, I64, I32, I32, P, P, P, P, P, P, I32, I32, I32,
                                        P, I32]),
             "oracle_moe_layer_batched": (I32, [P, I32, I32, I64, P, P, I64, I64, P, P, P, P, I32, I32, I32,
@@ -241,6 +242,21 @@ def topk_reduce(y_slots, ids, weights=None, out=F64):
     o = np.empty((T, K), _OUT_NP[out])
     _load().oracle_topk_reduce(py, _dtype_code(y_slots), pi, pw, T, k, K, o.ctypes.data, out)
     return o
+
+
+def batched_topk_reduce(y_rows, route_row, weights=None, out=F64):
+    """Batched-format weight-and-reduce into token order ("Fused MoE Modular Kernel", TopKWeightAndReduce,
+    NaiveBatched): out[t] = sum_j w[t,j] * y_rows[route_row[t,j]] over rows != -1, j increasing.
+    y_rows: (E, max_tokens, K) or (rows, K); route_row: (T, k).  Returns (out, err_bits)."""
+    y_rows, py = _c(y_rows)
+    rr, pr = _c(np.asarray(route_row, np.int32))
+    w, pw = _c(None if weights is None else np.asarray(weights, np.float32))
+    T, k = rr.shape
+    K = y_rows.shape[-1]
+    rows = y_rows.size // K if K else 0
+    o = np.empty((T, K), _OUT_NP[out])
+    err = _load().oracle_batched_topk_reduce(py, _dtype_code(y_rows), rows, pr, pw, T, k, K, o.ctypes.data, out)
+    return o, err
 
 
 def moe_layer(x, ids, weights, w1, w2, w1_scale=None, w2_scale=None, w1_layout=0, quant_h=False, out=F64):

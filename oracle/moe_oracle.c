@@ -430,6 +430,36 @@ ORACLE_EXPORT int oracle_topk_reduce(const void* y_slots, int y_dtype, const int
 }
 
 /*
+ * [MK] TopKWeightAndReduce for the Batched format (NaiveBatched), taken all
+ * the way to token order: the expert outputs sit in rows (e, q) of an
+ * (E, max_tokens, K) buffer, seen here as `rows` rows of K, and route_row maps
+ * each route r = t*k + j to its row (-1: padding or dropped for capacity).
+ *   out[t] = sum over j = 0..k-1 with route_row[t*k+j] != -1 of
+ *            w[t,j] * y_rows[route_row[t*k+j]]
+ * in increasing j, from +0.0.  Rows outside [-1, rows) are skipped and
+ * reported as OR_ERR_ID_RANGE.
+ */
+ORACLE_EXPORT int oracle_batched_topk_reduce(const void* y_rows, int y_dtype, int64_t rows, const int32_t* route_row,
+                                             const float* weights, int64_t T, int k, int64_t K, void* out,
+                                             int out_dtype) {
+    int err = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t n = 0; n < K; ++n) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int64_t row = route_row[t * k + j];
+                if (row == -1) continue;
+                if (row < -1 || row >= rows) { err |= OR_ERR_ID_RANGE; continue; }
+                double w = weights ? (double)weights[t * k + j] : 1.0;
+                acc += w * load_elem(y_rows, y_dtype, row * K + n);
+            }
+            store_elem(out, out_dtype, t * K + n, acc);
+        }
+    }
+    return err;
+}
+
+/*
  * One routed row through the whole expert: gate/up, act*mul, optional MXFP8
  * quantisation of h ([MK] apply(): "Quantisation" between act+mul and W2;
  * h is rounded to binary32, block-32 quantised along I, then decoded), down.

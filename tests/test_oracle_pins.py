@@ -403,6 +403,61 @@ def test_batched_layer_naive_weight(oracle_mod):
         assert np.all(np.isfinite(out[e, :c]))           # garbage rows never read
 
 
+def _batched_gather(xn, row_route, k):
+    """(E, max_tokens, K) rows of x for each batched row (zeros where no route)."""
+    E, maxT = row_route.shape
+    xb = np.zeros((E, maxT, xn.shape[1]), xn.dtype)
+    valid = row_route >= 0
+    xb[valid] = xn[row_route[valid] // k]
+    return xb
+
+
+def test_batched_reduce_path_equals_contiguous_layer(oracle_mod):
+    """Batched permute -> per-(expert, row) FFN without weights -> token-order reduce through route_row equals
+    the contiguous layer, which loops over (token, slot) instead."""
+    w, x, W1, W2, logits = _tiny_inputs(seed=4, T=14, K=64, I=32, E=5, k=3)
+    ids, wts = oracle_mod.topk_route(logits.numpy(), w.top_k)
+    xn = x.numpy()
+    res = oracle_mod.permute_batched(ids, w.E, w.T * w.top_k)      # capacity never reached
+    assert res["err"] == 0
+    xb = _batched_gather(xn, res["row_route"], w.top_k)
+    yb, err = oracle_mod.moe_layer_batched(xb, res["expert_num_tokens"], None, W1.numpy(), W2.numpy())
+    assert err == 0
+    out, err = oracle_mod.batched_topk_reduce(yb, res["route_row"], wts)
+    assert err == 0
+    ref, _ = oracle_mod.moe_layer(xn, ids, wts, W1.numpy(), W2.numpy())
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-15)
+    assert np.abs(ref).max() > 0.1
+
+
+def test_batched_reduce_identity_and_capacity(oracle_mod):
+    """Identity expert, top_k = 1, weight 1: x comes back bit-exactly; routes dropped for capacity add
+    nothing, a token left with no route gives +0.0, rows outside the buffer are reported."""
+    T, K, E, maxT = 29, 16, 4, 6
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(T, K, generator=g).to(torch.bfloat16)
+    xn = wl.to_numpy(x)
+    ids = torch.randint(0, E, (T, 1), generator=g, dtype=torch.int32).numpy()
+    big = oracle_mod.permute_batched(ids, E, T)
+    xb = _batched_gather(xn, big["row_route"], 1)
+    out, err = oracle_mod.batched_topk_reduce(xb, big["route_row"], np.ones((T, 1), np.float32),
+                                              out=oracle_mod.BF16)
+    assert err == 0 and np.array_equal(out, xn)
+    small = oracle_mod.permute_batched(ids, E, maxT)             # some experts overflow
+    assert small["err"] == oracle_mod.ERR_CAPACITY
+    xb = _batched_gather(xn, small["row_route"], 1)
+    out, err = oracle_mod.batched_topk_reduce(xb, small["route_row"], None, out=oracle_mod.F32)
+    dropped = small["route_row"][:, 0] < 0
+    assert dropped.any() and (~dropped).any()
+    kept_ref = xn[~dropped].astype(np.uint32) << 16
+    assert np.array_equal(out[~dropped].view(np.uint32), kept_ref)
+    assert np.all(out[dropped].view(np.uint32) == 0)              # +0.0, not -0.0
+    bad = small["route_row"].copy()
+    bad[0, 0] = E * maxT                                          # one past the buffer
+    _, err = oracle_mod.batched_topk_reduce(xb, bad, None)
+    assert err == oracle_mod.ERR_ID_RANGE
+
+
 def test_affine_routing_golden_and_balance():
     rows = _read_golden("affine_routing.txt")
     ids, wts = wl.affine_routing(wl.mxfp8())

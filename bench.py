@@ -7,7 +7,7 @@ mul, down projection with the route weight, ordered top-k reduce) over one
 batch of synthetic input resident in HBM.  The default workload is the decode
 sweep: the layer at T = 1, 8, 32 and 64 tokens (K=4096, I=1536, E=128,
 top_k=8, bf16), all four passes forming one step.  Other workloads (prefill,
-mxfp8, batched, tiny) can be selected with --workload.
+mxfp8, batched, batched_tokens, tiny) can be selected with --workload.
 
 Rank 0 prints ONE JSON line.  Under torchrun (N > 1) each rank runs an
 independent replica of the workload on its GPU (the layer has no exchange
@@ -47,7 +47,8 @@ def workload_list(name):
         return [wl.decode(T) for T in (1, 8, 32, 64)]
     if name.startswith("decode"):
         return [wl.decode(int(name[len("decode"):]))]
-    return [{"prefill": wl.prefill, "mxfp8": wl.mxfp8, "batched": wl.batched, "tiny": wl.tiny}[name]()]
+    return [{"prefill": wl.prefill, "mxfp8": wl.mxfp8, "batched": wl.batched, "batched_tokens": wl.batched_tokens,
+             "tiny": wl.tiny}[name]()]
 
 
 def describe(name, ws):
@@ -102,13 +103,18 @@ class Instance:
             self.W1 = wl.expert_weights(w, "W1", seed, dev)
             self.W2 = wl.expert_weights(w, "W2", seed, dev)
             self.s1 = self.s2 = None
-        self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
-                                device=dev)
+        if w.layout == "batched_tokens":
+            self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype,
+                                    layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens, device=dev)
+        else:
+            self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
+                                    device=dev)
         self.forward()
         torch.cuda.synchronize()
         ids = self.layer.ids if self.logits is not None else self.ids
-        self.routes = int((ids >= 0).sum().item())
-        self.used_experts = int(torch.unique(ids[ids >= 0]).numel())
+        kept = self.layer.route_row >= 0      # batched: routes beyond the capacity are dropped
+        self.routes = int(kept.sum().item())
+        self.used_experts = int(torch.unique(ids[kept]).numel())
 
     def _mxfp8(self, w, which, seed, dev):
         import torch

@@ -257,6 +257,28 @@ MOE_API int moe_batched_weight_reduce(const void* y, int y_dtype, const int32_t*
                               void* out, int out_dtype, void* stream);
 
 /*
+ * moe_batched_topk_reduce -- TopKWeightAndReduce for the Batched format
+ * carried through to token order ("Fused MoE Modular Kernel",
+ * TopKWeightAndReduce, NaiveBatched; Introduction: the Batched format):
+ *     out[t, n] = sum_{j = 0..top_k-1, route_row[t*top_k+j] != -1} w[t,j] * y[route_row[t*top_k+j], n]
+ * in increasing j, accumulated in fp32 from +0.0 (a token without a kept route
+ * gets +0.0).
+ *   y            (rows, K) F32 or BF16 -- for the batched layout the
+ *                (E, max_tokens, K) expert outputs, rows = E*max_tokens
+ *   route_row    (T*top_k) int32 from moe_permute_align: the row of each
+ *                route, -1 for padding and for routes dropped by capacity;
+ *                other entries outside [0, rows) set MOE_DEVERR_ID_RANGE in
+ *                err_word (may be NULL) and are skipped
+ *   topk_weights (T, top_k) fp32 or NULL (weights already applied)
+ *   out          (T, K) F32 or BF16, must not alias y
+ *   K % 8 == 0; y and out 16-byte aligned.
+ * The result does not depend on the launch: the same inputs give the same bits.
+ */
+MOE_API int moe_batched_topk_reduce(const void* y, int y_dtype, int64_t rows, const int32_t* route_row,
+                                    const float* topk_weights, int64_t T, int top_k, int64_t K,
+                                    void* out, int out_dtype, int32_t* err_word, void* stream);
+
+/*
  * mxfp8_quantize_block32 -- MXFP8 block-32 quantisation along rows
  * ("Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2,
  * _quantize_mxfp8_block32 "After").  For each block of 32 consecutive

@@ -30,7 +30,7 @@ MOE_DEVERR_ID_RANGE, MOE_DEVERR_CAPACITY, MOE_DEVERR_TIMEOUT = 1, 2, 4
 EXPORTED = [
     "moe_last_error", "moe_version", "moe_max_padded_rows", "moe_permute_workspace_size", "moe_topk_route",
     "moe_permute_align", "moe_permute_align_static", "moe_gemm1_swiglu", "moe_gemm2", "moe_unpermute_topk_reduce",
-    "moe_batched_weight_reduce", "mxfp8_quantize_block32",
+    "moe_batched_weight_reduce", "moe_batched_topk_reduce", "mxfp8_quantize_block32",
 ]
 
 
@@ -72,6 +72,7 @@ def load(path: Optional[str] = None):
                                 P]),
             "moe_unpermute_topk_reduce": (I32, [P, I32, P, P, I64, I32, I32, I64, P, I32, P]),
             "moe_batched_weight_reduce": (I32, [P, I32, P, P, I32, I32, I64, P, I32, P]),
+            "moe_batched_topk_reduce": (I32, [P, I32, I64, P, P, I64, I32, I64, P, I32, P, P]),
             "mxfp8_quantize_block32": (I32, [P, I32, I64, I64, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -262,6 +263,25 @@ def moe_batched_weight_reduce(y, expert_num_tokens, row_weights=None, out=None, 
         out = torch.empty((E, max_tokens, K), dtype=_TORCH[out_dtype], device=y.device)
     _check(load().moe_batched_weight_reduce(_ptr(y), dtype_code(y), _ptr(expert_num_tokens), _ptr(row_weights),
                                             E, max_tokens, K, _ptr(out), out_dtype, _stream(stream)))
+    return out
+
+
+def moe_batched_topk_reduce(y, route_row, topk_weights=None, out=None, out_dtype=None, err_word=None,
+                            stream=None):
+    """y: (E, max_tokens, K) or (rows, K); route_row: (T, top_k) or (T*top_k,) with top_k given by
+    topk_weights when it is flat."""
+    K = y.shape[-1]
+    rows = y.numel() // K
+    if route_row.dim() == 2:
+        T, top_k = route_row.shape
+    else:
+        T, top_k = topk_weights.shape
+    if out_dtype is None:
+        out_dtype = dtype_code(y)
+    if out is None:
+        out = torch.empty((T, K), dtype=_TORCH[out_dtype], device=y.device)
+    _check(load().moe_batched_topk_reduce(_ptr(y), dtype_code(y), rows, _ptr(route_row), _ptr(topk_weights), T,
+                                          top_k, K, _ptr(out), out_dtype, _ptr(err_word), _stream(stream)))
     return out
 
 

@@ -306,6 +306,26 @@ int moe_batched_weight_reduce(const void* y, int y_dtype, const int32_t* expert_
                          "moe_batched_weight_reduce");
 }
 
+int moe_batched_topk_reduce(const void* y, int y_dtype, int64_t rows, const int32_t* route_row,
+                            const float* topk_weights, int64_t T, int top_k, int64_t K, void* out, int out_dtype,
+                            int32_t* err_word, void* stream) {
+    g_last_error.clear();
+    MOE_REQUIRE(T >= 0 && rows >= 0 && top_k >= 1 && K > 0, MOE_ERR_INVALID_ARG,
+                "moe_batched_topk_reduce: bad sizes");
+    MOE_REQUIRE(rows <= INT32_MAX, MOE_ERR_INVALID_ARG, "moe_batched_topk_reduce: rows must fit int32");
+    MOE_REQUIRE(is_float_dtype(y_dtype) && is_float_dtype(out_dtype), MOE_ERR_UNSUPPORTED,
+                "moe_batched_topk_reduce: y and out must be F32 or BF16");
+    MOE_REQUIRE(K % 8 == 0, MOE_ERR_ALIGNMENT, "moe_batched_topk_reduce: K must be a multiple of 8");
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(route_row && out && (y || rows == 0), MOE_ERR_INVALID_ARG, "moe_batched_topk_reduce: null pointer");
+    MOE_REQUIRE(y != out, MOE_ERR_INVALID_ARG, "moe_batched_topk_reduce: out must not alias y");
+    MOE_REQUIRE((!y || aligned16(y)) && aligned16(out), MOE_ERR_ALIGNMENT,
+                "moe_batched_topk_reduce: y and out must be 16-byte aligned");
+    return launch_status(launch_rows_topk_reduce(y, y_dtype, rows, route_row, topk_weights, T, top_k, K, out,
+                                                 out_dtype, err_word, as_stream(stream)),
+                         "moe_batched_topk_reduce");
+}
+
 int mxfp8_quantize_block32(const void* x, int x_dtype, int64_t rows, int64_t cols, uint8_t* codes,
                            uint8_t* scales, void* stream) {
     g_last_error.clear();

@@ -30,6 +30,9 @@ cudaError_t launch_gather_rows(const void* x, int esize, int64_t K, const int32_
 
 cudaError_t launch_topk_reduce(const void* y, int y_dtype, const int32_t* ids, const float* w, int64_t T,
                                int top_k, int E, int64_t K, void* out, int out_dtype, cudaStream_t s);
+cudaError_t launch_rows_topk_reduce(const void* y, int y_dtype, int64_t rows, const int32_t* route_row,
+                                    const float* w, int64_t T, int top_k, int64_t K, void* out, int out_dtype,
+                                    int32_t* err_word, cudaStream_t s);
 cudaError_t launch_batched_weight(const void* y, int y_dtype, const int32_t* counts, const float* w, int E,
                                   int max_tokens, int64_t K, void* out, int out_dtype, cudaStream_t s);
 

@@ -48,11 +48,15 @@ MOE_DEVICE void unpack8(const Vec8<DT>& v, float (&f)[8]) {
 // Slots are taken 8 at a time: their ids and weights are read first, then all 8 row vectors are
 // requested before any is used, and the products are added in increasing j (the order, and so the
 // result, does not depend on the batching).
-template <int YDT, int ODT>
+// ROWS = false: slot (t, j) is valid when 0 <= ids[t,j] < lim (= E) and its row is t*top_k + j.
+// ROWS = true:  `ids` is route_row, slot (t, j) reads row ids[t,j] when 0 <= ids[t,j] < lim (= rows);
+//               entries other than -1 outside [0, rows) set MOE_DEVERR_ID_RANGE.
+template <int YDT, int ODT, bool ROWS>
 __global__ void __launch_bounds__(256) topk_reduce_kernel(const void* __restrict__ y,
                                                           const int32_t* __restrict__ ids,
-                                                          const float* __restrict__ w, int64_t T, int top_k, int E,
-                                                          int64_t K, void* __restrict__ out) {
+                                                          const float* __restrict__ w, int64_t T, int top_k,
+                                                          int64_t lim, int64_t K, void* __restrict__ out,
+                                                          int32_t* err_word) {
     // grid: x over the 8-element column vectors of a row, y over output rows (no index division)
     const int64_t vec = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (vec >= K / 8) return;
@@ -69,12 +73,24 @@ __global__ void __launch_bounds__(256) topk_reduce_kernel(const void* __restrict
                 e[u] = j < top_k ? ids[t * top_k + j] : -1;
                 wj[u] = (w && j < top_k) ? w[t * top_k + j] : 1.0f;
             }
+            if constexpr (ROWS) {
+                // one thread per token row reports a bad row index
+                if (vec == 0 && err_word) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (e[u] >= 0 && e[u] < E) raw[u] = ld_vec8<YDT>(y, (t * top_k + j0 + u) * K + col);
+                    for (int u = 0; u < 8; ++u)
+                        if (e[u] < -1 || e[u] >= lim) report(err_word, MOE_DEVERR_ID_RANGE);
+                }
+            }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                if (e[u] < 0 || e[u] >= E) continue;
+                if (e[u] >= 0 && e[u] < lim) {
+                    const int64_t row = ROWS ? int64_t(e[u]) : t * top_k + j0 + u;
+                    raw[u] = ld_vec8<YDT>(y, row * K + col);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (e[u] < 0 || e[u] >= lim) continue;
                 float v[8];
                 unpack8<YDT>(raw[u], v);
 #pragma unroll
@@ -117,17 +133,34 @@ dim3 grid_for(int64_t rows, int64_t K) {
 
 }  // namespace
 
-cudaError_t launch_topk_reduce(const void* y, int y_dtype, const int32_t* ids, const float* w, int64_t T,
-                               int top_k, int E, int64_t K, void* out, int out_dtype, cudaStream_t s) {
+namespace {
+
+template <bool ROWS>
+cudaError_t launch_reduce(const void* y, int y_dtype, const int32_t* ids, const float* w, int64_t T, int top_k,
+                          int64_t lim, int64_t K, void* out, int out_dtype, int32_t* err_word, cudaStream_t s) {
     if (T == 0 || K == 0) return cudaSuccess;
     const dim3 g = grid_for(T, K);
-#define MOE_REDUCE(YD, OD) topk_reduce_kernel<YD, OD><<<g, 256, 0, s>>>(y, ids, w, T, top_k, E, K, out)
+#define MOE_REDUCE(YD, OD) \
+    topk_reduce_kernel<YD, OD, ROWS><<<g, 256, 0, s>>>(y, ids, w, T, top_k, lim, K, out, err_word)
     if (y_dtype == MOE_BF16 && out_dtype == MOE_BF16) MOE_REDUCE(MOE_BF16, MOE_BF16);
     else if (y_dtype == MOE_BF16 && out_dtype == MOE_F32) MOE_REDUCE(MOE_BF16, MOE_F32);
     else if (y_dtype == MOE_F32 && out_dtype == MOE_BF16) MOE_REDUCE(MOE_F32, MOE_BF16);
     else MOE_REDUCE(MOE_F32, MOE_F32);
 #undef MOE_REDUCE
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_topk_reduce(const void* y, int y_dtype, const int32_t* ids, const float* w, int64_t T,
+                               int top_k, int E, int64_t K, void* out, int out_dtype, cudaStream_t s) {
+    return launch_reduce<false>(y, y_dtype, ids, w, T, top_k, E, K, out, out_dtype, nullptr, s);
+}
+
+cudaError_t launch_rows_topk_reduce(const void* y, int y_dtype, int64_t rows, const int32_t* route_row,
+                                    const float* w, int64_t T, int top_k, int64_t K, void* out, int out_dtype,
+                                    int32_t* err_word, cudaStream_t s) {
+    return launch_reduce<true>(y, y_dtype, route_row, w, T, top_k, rows, K, out, out_dtype, err_word, s);
 }
 
 cudaError_t launch_batched_weight(const void* y, int y_dtype, const int32_t* counts, const float* w, int E,

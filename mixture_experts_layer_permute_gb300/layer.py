@@ -7,10 +7,15 @@ intermediates are declared up front and reused), and ``forward`` issues
     moe_topk_route -> moe_permute_align -> moe_gemm1_swiglu -> moe_gemm2
         -> moe_unpermute_topk_reduce          (contiguous layout)
 
-or, for the batched layout,
+or, for the batched layout fed with expert-major rows (T = 0),
 
     moe_gemm1_swiglu -> moe_gemm2 (route weight in the epilogue)
         [-> moe_batched_weight_reduce when the weight is not fused]
+
+or, for the batched layout fed with tokens (T > 0),
+
+    moe_topk_route -> moe_permute_align (batched rows, capacity max_tokens)
+        -> moe_gemm1_swiglu -> moe_gemm2 -> moe_batched_topk_reduce (token order)
 
 with no host synchronisation.  Every step runs in libmoe_layer's kernels.
 The marshalled argument lists of the C calls are kept between calls with the
@@ -56,6 +61,18 @@ class MoELayer:
             self.h = torch.empty((self.rows_cap, I), dtype=act_dtype, device=dev)
             self.y = torch.empty((T * top_k, K), dtype=act_dtype, device=dev)
             self.out = torch.empty((T, K), dtype=act_dtype, device=dev)
+        elif T > 0:   # batched rows, token input and output
+            self.rows_cap = E * max_tokens
+            self.ids = torch.empty((T, top_k), **i32)
+            self.weights = torch.empty((T, top_k), dtype=torch.float32, device=dev)
+            self.row_route = torch.empty(max(self.rows_cap, 1), **i32)
+            self.route_row = torch.empty((T, top_k), **i32)
+            self.workspace = torch.empty(max(B.moe_permute_workspace_size(T, top_k, E), 256), dtype=torch.uint8,
+                                         device=dev)
+            self.x_perm = torch.empty((max(self.rows_cap, 1), K), dtype=act_dtype, device=dev)
+            self.h = torch.empty((E, max_tokens, I), dtype=act_dtype, device=dev)
+            self.y = torch.empty((E, max_tokens, K), dtype=act_dtype, device=dev)
+            self.out = torch.empty((T, K), dtype=act_dtype, device=dev)
         else:
             self.rows_cap = E * max_tokens
             self.h = torch.empty((E, max_tokens, I), dtype=act_dtype, device=dev)
@@ -70,7 +87,7 @@ class MoELayer:
                 raise ValueError("MoELayer.forward takes contiguous device tensors")
         if w1.shape[0] != self.E or w2.shape[0] != self.E:
             raise ValueError("weight expert count does not match the layer")
-        if self.layout == B.MOE_LAYOUT_CONTIGUOUS:
+        if self.layout == B.MOE_LAYOUT_CONTIGUOUS or self.T > 0:
             if tuple(x.shape) != (self.T, self.K) or x.dtype != self.act_dtype:
                 raise ValueError(f"x must be ({self.T}, {self.K}) {self.act_dtype}")
         elif tuple(x.shape) != (self.E, self.max_tokens, self.K):
@@ -83,6 +100,9 @@ class MoELayer:
         wdt = B.dtype_code(w1, e4m3=w1_scale is not None)
         I, K, E, T, k = self.I, self.K, self.E, self.T, self.top_k
         calls = []
+        if self.layout == B.MOE_LAYOUT_BATCHED and T > 0:
+            return self._token_batched_plan(x, w1, w2, logits, topk_ids, topk_weights, w1_scale, w2_scale,
+                                            w1_layout, adt, wdt, stream)
         if self.layout == B.MOE_LAYOUT_BATCHED:
             mt = self.max_tokens
             calls.append((lib.moe_gemm1_swiglu, (x.data_ptr(), adt, self.layout, counts.data_ptr(), None, mt,
@@ -125,6 +145,36 @@ class MoELayer:
                                                       E, K, self.out.data_ptr(), adt, stream), "reduce"))
         return calls
 
+    def _token_batched_plan(self, x, w1, w2, logits, topk_ids, topk_weights, w1_scale, w2_scale, w1_layout, adt,
+                            wdt, stream):
+        lib = self.lib
+        I, K, E, T, k, mt = self.I, self.K, self.E, self.T, self.top_k, self.max_tokens
+        calls = []
+        if logits is not None:
+            calls.append((lib.moe_topk_route, (logits.data_ptr(), T, logits.shape[1], k, 1, self.ids.data_ptr(),
+                                               self.weights.data_ptr(), stream), "route"))
+            ids, weights = self.ids, self.weights
+        else:
+            ids, weights = topk_ids, topk_weights
+        calls.append((lib.moe_permute_align, (ids.data_ptr(), T, k, E, self.layout, 1, mt, x.data_ptr(), adt, K,
+                                              self.x_perm.data_ptr(), self.rows_cap, self.counts.data_ptr(),
+                                              self.offsets.data_ptr(), self.row_route.data_ptr(),
+                                              self.route_row.data_ptr(), self.workspace.data_ptr(),
+                                              self.workspace.numel(), self.err.data_ptr(), stream), "permute"))
+        calls.append((lib.moe_gemm1_swiglu, (self.x_perm.data_ptr(), adt, self.layout, self.counts.data_ptr(), None,
+                                             mt, self.rows_cap, E, K, I, w1.data_ptr(), _p(w1_scale), wdt,
+                                             w1_layout, self.impl, self.h.data_ptr(), adt, self.err.data_ptr(),
+                                             stream), "gemm1"))
+        calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, self.layout, self.counts.data_ptr(), None, mt,
+                                      self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, None, None,
+                                      self.impl, self.y.data_ptr(), adt, self.rows_cap, self.err.data_ptr(),
+                                      stream), "gemm2"))
+        calls.append((lib.moe_batched_topk_reduce, (self.y.data_ptr(), adt, self.rows_cap,
+                                                    self.route_row.data_ptr(), weights.data_ptr(), T, k, K,
+                                                    self.out.data_ptr(), adt, self.err.data_ptr(), stream),
+                      "reduce"))
+        return calls
+
     # ---------------------------------------------------------------- running
     def forward(self, x: torch.Tensor, w1: torch.Tensor, w2: torch.Tensor, logits: Optional[torch.Tensor] = None,
                 topk_ids: Optional[torch.Tensor] = None, topk_weights: Optional[torch.Tensor] = None,
@@ -133,8 +183,10 @@ class MoELayer:
                 stream=None, gemm1_events=None) -> torch.Tensor:
         """Runs the layer on `stream` (default: the current stream) and returns the output buffer.
 
-        Contiguous layout: x (T, K) and either router `logits` (T, E) or `topk_ids`/`topk_weights` (T, top_k).
-        Batched layout: x (E, max_tokens, K), `expert_num_tokens` (E,), optional `row_weights` (E, max_tokens).
+        Contiguous layout, or batched layout with T > 0: x (T, K) and either router `logits` (T, E) or
+        `topk_ids`/`topk_weights` (T, top_k); routes beyond max_tokens per expert are dropped (batched).
+        Batched layout with T = 0: x (E, max_tokens, K), `expert_num_tokens` (E,), optional `row_weights`
+        (E, max_tokens).
         ``gemm1_events`` = (start, end) CUDA events recorded around the gate/up GEMM.
         """
         s = stream if stream is not None else torch.cuda.current_stream()
@@ -158,7 +210,7 @@ class MoELayer:
 
     def launches_per_forward(self) -> int:
         """Kernels one forward launches (for launch accounting)."""
-        if self.layout == B.MOE_LAYOUT_BATCHED:
+        if self.layout == B.MOE_LAYOUT_BATCHED and self.T == 0:
             return 2 if self.weight_in_gemm2 else 3
         n = 3 + 1 + (1 if self.T * self.top_k <= 1024 else 2) + 1   # gemm1 gemm2 reduce, gather, permute, route
         return n if any(name == "route" for _, _, name in (self._plan or [])) else n - 1

@@ -27,6 +27,9 @@ The workloads are the five synthetic configurations of the layer:
 * ``batched``   (E=32, max_tokens=256, K=6144) activations, I=4096,
                 expert_num_tokens uniform in [0, 256], rows beyond the count
                 filled with garbage (NaN or +-1e30), per-row weights U(0, 1).
+* ``batched_tokens``  the batched layout fed with tokens: T=1024, top_k=4,
+                the same E, max_tokens, K and I, x ~ N(0, 1), logits ~ N(0, 1)
+                (about 128 routes per expert, far from the capacity).
 """
 from __future__ import annotations
 
@@ -82,6 +85,11 @@ def mxfp8() -> Workload:
 def batched(garbage: str = "nan") -> Workload:
     return Workload("batched", T=0, K=6144, I=4096, E=32, top_k=1, layout="batched", routing="given",
                     max_tokens=256, garbage=garbage)
+
+
+def batched_tokens() -> Workload:
+    return Workload("batched_tokens", T=1024, K=6144, I=4096, E=32, top_k=4, layout="batched_tokens",
+                    max_tokens=256)
 
 
 def scaled(w: Workload, **changes) -> Workload:

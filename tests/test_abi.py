@@ -35,6 +35,14 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(names) == sorted(m.EXPORTED)
 
 
+def test_every_entry_point_has_a_python_wrapper():
+    for n in m.EXPORTED:
+        if n.startswith("moe_") or n.startswith("mxfp8_"):
+            if n in ("moe_last_error",):
+                continue
+            assert callable(getattr(m, n, None)), n
+
+
 def test_library_is_built_for_sm103a():
     # the build passes exactly one -gencode for sm_103a
     assert build_mod.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -122,6 +130,12 @@ def test_reduce_and_quant_validation(lib):
     assert lib.moe_unpermute_topk_reduce(fake, 1, fake, None, 4, 2, 8, 12, fake, 1, None) == 3   # K % 8
     assert lib.moe_unpermute_topk_reduce(fake, 2, fake, None, 4, 2, 8, 16, fake, 1, None) == 2   # E4M3 y
     assert lib.moe_batched_weight_reduce(fake, 1, fake, None, 0, 4, 16, fake, 1, None) == 1      # E = 0
+    assert lib.moe_batched_topk_reduce(fake, 1, 64, fake, None, 4, 2, 12, ctypes.c_void_p(0x2000), 1, None,
+                                       None) == 3                                                # K % 8
+    assert lib.moe_batched_topk_reduce(fake, 1, 64, fake, None, 4, 2, 16, fake, 1, None, None) == 1  # out == y
+    assert lib.moe_batched_topk_reduce(fake, 1, 64, None, None, 4, 2, 16, ctypes.c_void_p(0x2000), 1, None,
+                                       None) == 1                                                # no route_row
+    assert lib.moe_batched_topk_reduce(None, 1, 0, None, None, 0, 2, 16, None, 1, None, None) == 0   # T = 0
     assert lib.mxfp8_quantize_block32(fake, 1, 4, 33, fake, fake, None) == 3                     # cols % 32
     assert lib.mxfp8_quantize_block32(fake, 2, 4, 32, fake, fake, None) == 2                     # E4M3 input
     assert lib.mxfp8_quantize_block32(None, 1, 0, 32, None, None, None) == 0                     # empty: no-op

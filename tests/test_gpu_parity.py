@@ -199,6 +199,68 @@ def test_batched_weight_reduce(moe):
         assert torch.all(out[e, c:] == 7.0)
 
 
+@pytest.mark.parametrize("ydt,odt,weighted", [(torch.bfloat16, torch.bfloat16, True),
+                                              (torch.float32, torch.float32, True),
+                                              (torch.bfloat16, torch.float32, False)])
+def test_batched_topk_reduce(moe, ydt, odt, weighted):
+    """Token-order reduce of the batched layout through route_row; capacity drops, padding, +0.0."""
+    T, k, E, maxT, K = 300, 6, 16, 100, 1024
+    ids = _ids(T, k, E, seed=9, pad=0.1)
+    ids[7] = -1                                            # a token made only of padding
+    res = oracle.permute_batched(ids.numpy(), E, maxT)      # hot experts overflow: drops
+    assert res["err"] == oracle.ERR_CAPACITY
+    rr = res["route_row"]
+    g = torch.Generator().manual_seed(6)
+    y = torch.randn(E, maxT, K, generator=g).to(ydt)
+    w = torch.rand(T, k, generator=g)
+    odc = moe.MOE_F32 if odt == torch.float32 else moe.MOE_BF16
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = moe.moe_batched_topk_reduce(y.to(DEV), torch.from_numpy(rr).to(DEV), w.to(DEV) if weighted else None,
+                                      out_dtype=odc, err_word=err)
+    ref, rerr = oracle.batched_topk_reduce(wl.to_numpy(y), rr, w.numpy() if weighted else None)
+    assert rerr == 0 and int(err.item()) == 0
+    tol = TOL_F32 if (ydt == torch.float32 and odt == torch.float32) else TOL_BF16
+    assert_close(to_f64(out), ref, tol, "batched topk reduce")
+    o7 = out[7].cpu()
+    assert torch.all(o7 == 0) and not torch.any(torch.signbit(o7.float()))   # +0.0
+    again = moe.moe_batched_topk_reduce(y.to(DEV), torch.from_numpy(rr).to(DEV), w.to(DEV) if weighted else None,
+                                        out_dtype=odc)
+    assert torch.equal(out.view(torch.uint8), again.view(torch.uint8))       # fixed order: same bits
+    # a row index past the buffer is reported and skipped
+    bad = rr.copy()
+    bad[3, 0] = E * maxT
+    moe.moe_batched_topk_reduce(y.to(DEV), torch.from_numpy(bad).to(DEV), None, out_dtype=odc, err_word=err)
+    assert int(err.item()) == moe.MOE_DEVERR_ID_RANGE
+
+
+@pytest.mark.parametrize("impl", ["tcgen05", "swap_ab", "simt"])
+@pytest.mark.parametrize("maxT", [64, 24])
+def test_layer_batched_token_order(moe, impl, maxT):
+    """route -> batched permute (+gather) -> GEMM 1 -> GEMM 2 (no weight) -> token-order reduce equals the
+    contiguous oracle layer with the routes dropped for capacity removed."""
+    T, k, E, K, I = 96, 4, 8, 512, 256
+    w = wl.scaled(wl.tiny(), T=T, K=K, I=I, E=E, top_k=k, x_std=1.0, w_std=0.05)
+    x = wl.activations(w, 3).to(torch.bfloat16)
+    W1 = wl.expert_weights(w, "W1", 3).to(torch.bfloat16)
+    W2 = wl.expert_weights(w, "W2", 3).to(torch.bfloat16)
+    ids, wts = moe.moe_topk_route(wl.router_logits(w, 3).to(DEV), k)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa = moe.moe_permute_align(ids, E, layout=moe.MOE_LAYOUT_BATCHED, max_tokens=maxT, x=x.to(DEV),
+                               err_word=err)
+    h = moe.moe_gemm1_swiglu(pa["x_out"], pa["counts"], pa["offsets"], W1.to(DEV), I,
+                             layout=moe.MOE_LAYOUT_BATCHED, max_tokens=maxT, impl=_impl(moe, impl))
+    yb = moe.moe_gemm2(h.reshape(E * maxT, I), pa["counts"], pa["offsets"], W2.to(DEV), E * maxT,
+                       layout=moe.MOE_LAYOUT_BATCHED, max_tokens=maxT, impl=_impl(moe, impl))
+    out = moe.moe_batched_topk_reduce(yb, pa["route_row"], wts)
+    torch.cuda.synchronize()
+    rr = pa["route_row"].cpu().numpy()
+    ids_kept = np.where(rr >= 0, ids.cpu().numpy(), -1).astype(np.int32)
+    if maxT == 24:
+        assert int(err.item()) == moe.MOE_DEVERR_CAPACITY and (ids_kept < 0).any()
+    ref, _ = oracle.moe_layer(wl.to_numpy(x), ids_kept, wts.cpu().numpy(), wl.to_numpy(W1), wl.to_numpy(W2))
+    assert_close(to_f64(out), ref, TOL_BF16, f"batched token-order layer {impl}")
+
+
 # ----------------------------------------------------------------------------
 # grouped GEMMs
 # ----------------------------------------------------------------------------
@@ -494,3 +556,24 @@ def test_layer_batched_full_size_sampled(moe, garbage):
         if c < w.max_tokens:
             assert torch.all(out[e, c:] == 3.0)             # rows beyond the count untouched
     assert torch.isfinite(out.float()).sum() > 0
+
+
+def test_layer_batched_tokens_full_size_sampled(moe):
+    """Batched layout fed with tokens at full size (T=1024, top_k=4, E=32, max_tokens=256, K=6144, I=4096),
+    as the benchmark runs it: permutation bit-exact, oracle on 2 sampled tokens."""
+    w = wl.batched_tokens()
+    x, logits = wl.activations(w, 0, DEV), wl.router_logits(w, 0, DEV)
+    W1, W2 = wl.expert_weights(w, "W1", 0, DEV), wl.expert_weights(w, "W2", 0, DEV)
+    layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, layout=moe.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens,
+                         device=DEV)
+    out = layer.forward(x, W1, W2, logits=logits)
+    ids, weights = oracle.topk_route(logits.cpu().numpy(), w.top_k)
+    assert np.array_equal(layer.ids.cpu().numpy(), ids)
+    ref_perm = oracle.permute_batched(ids, w.E, w.max_tokens)
+    assert np.array_equal(layer.counts.cpu().numpy(), ref_perm["expert_num_tokens"])
+    assert np.array_equal(layer.route_row.cpu().numpy(), ref_perm["route_row"])
+    assert layer.device_errors() == ref_perm["err"]
+    for t in (0, 1023):
+        cids, (w1h, w2h, _, _) = compact_experts(ids[t:t + 1], W1, W2)
+        ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, weights[t:t + 1], w1h, w2h)
+        assert_close(to_f64(out[t:t + 1]), ref, TOL_BF16, f"batched_tokens token {t}")

@@ -62,6 +62,7 @@ def _load():
             "oracle_e8m0_to_double": (D, [ctypes.c_uint8]),
             "oracle_mxfp8_scale_code": (ctypes.c_uint8, [D]),
             "oracle_mxfp8_quantize": (I32, [P, I32, I64, I64, P, P]),
+            "oracle_mxfp8_dequantize": (I32, [P, P, I64, I64, P]),
             "oracle_topk_route": (I32, [P, I64, I32, I32, I32, P, P]),
             "oracle_permute_contiguous": (I32, [P, I64, I32, I32, I32, P, P, P, P]),
             "oracle_permute_batched": (I32, [P, I64, I32, I32, I32, P, P, P]),
@@ -69,9 +70,9 @@ def _load():
             "oracle_expert_down": (I32, [P, I32, I64, P, P, P, I32, I32, I64, I64, P, I32]),
             "oracle_topk_reduce": (I32, [P, I32, P, P, I64, I32, I64, P, I32]),
             "oracle_batched_topk_reduce": (I32, [P, I32, I64, P, P, I64, I32, I64, P, I32]),
-            "oracle_moe_layer": (I32, [P, I32, I64, I64, I64, I32, I32, P, P, P, P, P, P, I32, I32, I32,
+            "oracle_moe_layer": (I32, [P, I32, I64, I64, I64, I32, I32, P, P, P, P, P, P, I32, I32, I32, I32,
                                        P, I32]),
-            "oracle_moe_layer_batched": (I32, [P, I32, I32, I64, P, P, I64, I64, P, P, P, P, I32, I32, I32,
+            "oracle_moe_layer_batched": (I32, [P, I32, I32, I64, P, P, I64, I64, P, P, P, P, I32, I32, I32, I32,
                                                P, I32]),
         }
         for name, (res, args) in sig.items():
@@ -157,6 +158,27 @@ def mxfp8_quantize(x: np.ndarray):
     if rc != 0:
         raise ValueError("oracle: cols must be a multiple of 32")
     return codes, scales
+
+
+def mxfp8_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Decoded MXFP8 values in fp64: E4M3(code) * 2^(scale - 127), one scale per 32 along the last axis."""
+    codes, pc = _c(np.asarray(codes, np.uint8))
+    scales, ps = _c(np.asarray(scales, np.uint8))
+    cols = codes.shape[-1]
+    rows = codes.size // cols if cols else 0
+    out = np.empty(codes.shape, np.float64)
+    if _load().oracle_mxfp8_dequantize(pc, ps, rows, cols, out.ctypes.data) != 0:
+        raise ValueError("oracle: cols must be a multiple of 32")
+    return out
+
+
+def _quant_h_mode(quant_h) -> int:
+    """quant_h: False (no intermediate quantisation), True or "f32" (h rounded to binary32 first), "bf16"."""
+    if quant_h is False or quant_h is None or quant_h == 0:
+        return 0
+    if quant_h == "bf16":
+        return 2
+    return 1
 
 
 def topk_route(logits: np.ndarray, top_k: int, renormalize: bool = True):
@@ -259,8 +281,10 @@ def batched_topk_reduce(y_rows, route_row, weights=None, out=F64):
     return o, err
 
 
-def moe_layer(x, ids, weights, w1, w2, w1_scale=None, w2_scale=None, w1_layout=0, quant_h=False, out=F64):
-    """The whole contiguous layer; returns (out, err_bits)."""
+def moe_layer(x, ids, weights, w1, w2, w1_scale=None, w2_scale=None, w1_layout=0, quant_h=False, out=F64,
+              quant_x=False):
+    """The whole contiguous layer; returns (out, err_bits).  quant_x: x rows MXFP8-quantised before W1;
+    quant_h: see _quant_h_mode."""
     x, px = _c(x)
     ids, pi = _c(np.asarray(ids, np.int32))
     w, pw = _c(None if weights is None else np.asarray(weights, np.float32))
@@ -273,12 +297,13 @@ def moe_layer(x, ids, weights, w1, w2, w1_scale=None, w2_scale=None, w1_layout=0
     k = ids.shape[1]
     o = np.empty((T, K), _OUT_NP[out])
     err = _load().oracle_moe_layer(px, _dtype_code(x), T, K, two_i // 2, E, k, pi, pw, p1, ps1, p2, ps2,
-                                   _dtype_code(w1, e4m3=True), w1_layout, int(quant_h), o.ctypes.data, out)
+                                   _dtype_code(w1, e4m3=True), w1_layout, int(bool(quant_x)), _quant_h_mode(quant_h),
+                                   o.ctypes.data, out)
     return o, err
 
 
 def moe_layer_batched(xb, expert_num_tokens, weights, w1, w2, w1_scale=None, w2_scale=None, w1_layout=0,
-                      quant_h=False, out=F64, out_init=None):
+                      quant_h=False, out=F64, out_init=None, quant_x=False):
     """The whole batched layer with naive-batched weight application; rows >= count keep out_init."""
     xb, px = _c(xb)
     ent, pe = _c(np.asarray(expert_num_tokens, np.int32))
@@ -294,6 +319,6 @@ def moe_layer_batched(xb, expert_num_tokens, weights, w1, w2, w1_scale=None, w2_
     else:
         o = np.array(out_init, dtype=_OUT_NP[out], copy=True)
     err = _load().oracle_moe_layer_batched(px, _dtype_code(xb), E, maxT, pe, pw, K, two_i // 2, p1, ps1, p2, ps2,
-                                           _dtype_code(w1, e4m3=True), w1_layout, int(quant_h), o.ctypes.data,
-                                           out)
+                                           _dtype_code(w1, e4m3=True), w1_layout, int(bool(quant_x)),
+                                           _quant_h_mode(quant_h), o.ctypes.data, out)
     return o, err

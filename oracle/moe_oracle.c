@@ -41,6 +41,10 @@
  *     dimension (K for W1, I for W2).
  *   - E4M3 encoding: round to nearest even, saturate to +-448, sign of zero
  *     kept.
+ *   - Quantised activations (optional): x rows are MXFP8-quantised along K
+ *     from their stored values; h is rounded to the element type its producer
+ *     stores (binary32 or bfloat16) before its MXFP8 quantisation along I, so
+ *     that a code is decided from the same value on both sides.
  *
  * Parity unpinned: nothing here; see the tests for each pin.
  */
@@ -206,6 +210,19 @@ ORACLE_EXPORT int oracle_mxfp8_quantize(const void* x, int x_dtype, int64_t rows
             }
         }
     }
+    return 0;
+}
+
+/*
+ * Decode MXFP8: out[r, c] = E4M3(codes[r, c]) * 2^(scales[r, c/32] - 127).
+ */
+ORACLE_EXPORT int oracle_mxfp8_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                                          double* out) {
+    if (cols % 32 != 0) return -1;
+    int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            out[r * cols + c] = oracle_e4m3_to_double(codes[r * cols + c]) * oracle_e8m0_to_double(scales[r * nb + c / 32]);
     return 0;
 }
 
@@ -460,25 +477,48 @@ ORACLE_EXPORT int oracle_batched_topk_reduce(const void* y_rows, int y_dtype, in
 }
 
 /*
- * One routed row through the whole expert: gate/up, act*mul, optional MXFP8
- * quantisation of h ([MK] apply(): "Quantisation" between act+mul and W2;
- * h is rounded to binary32, block-32 quantised along I, then decoded), down.
+ * One routed row through the whole expert: optional MXFP8 quantisation of the
+ * activation row ([MK] "prepare": input activation quantisation; block 32
+ * along K, then decoded), gate/up, act*mul, optional MXFP8 quantisation of h
+ * ([MK] apply(): "Quantisation" between act+mul and W2; h is first rounded to
+ * the precision the producer stores it in -- quant_h = 1: binary32,
+ * quant_h = 2: bfloat16 -- then block-32 quantised along I and decoded), down.
  */
 static void expert_ffn_row(const void* xrow, int x_dtype, int e,
                            const void* w1, const uint8_t* w1_scale, const void* w2, const uint8_t* w2_scale,
-                           int w_dtype, int w1_layout, int E, int64_t K, int64_t I, int quant_h,
+                           int w_dtype, int w1_layout, int E, int64_t K, int64_t I, int quant_x, int quant_h,
                            double* h, double* y) {
     int32_t one_expert = e;
-    oracle_expert_gate_up(xrow, x_dtype, 1, &one_expert, w1, w1_scale, w_dtype, w1_layout, E, K, I, h, OR_F64);
+    if (quant_x) {
+        uint8_t* codes = (uint8_t*)malloc((size_t)K);
+        uint8_t* scales = (uint8_t*)malloc((size_t)(K / 32));
+        double* xq = (double*)malloc(sizeof(double) * (size_t)K);
+        oracle_mxfp8_quantize(xrow, x_dtype, 1, K, codes, scales);
+        oracle_mxfp8_dequantize(codes, scales, 1, K, xq);
+        oracle_expert_gate_up(xq, OR_F64, 1, &one_expert, w1, w1_scale, w_dtype, w1_layout, E, K, I, h, OR_F64);
+        free(codes); free(scales); free(xq);
+    } else {
+        oracle_expert_gate_up(xrow, x_dtype, 1, &one_expert, w1, w1_scale, w_dtype, w1_layout, E, K, I, h, OR_F64);
+    }
     if (quant_h) {
-        float* hf = (float*)malloc(sizeof(float) * (size_t)I);
+        void* hs;
+        int hs_dtype;
+        if (quant_h == 2) {
+            uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+            for (int64_t i = 0; i < I; ++i) hb[i] = oracle_double_to_bf16(h[i]);
+            hs = hb;
+            hs_dtype = OR_BF16;
+        } else {
+            float* hf = (float*)malloc(sizeof(float) * (size_t)I);
+            for (int64_t i = 0; i < I; ++i) hf[i] = oracle_round_f32(h[i]);
+            hs = hf;
+            hs_dtype = OR_F32;
+        }
         uint8_t* codes = (uint8_t*)malloc((size_t)I);
         uint8_t* scales = (uint8_t*)malloc((size_t)(I / 32));
-        for (int64_t i = 0; i < I; ++i) hf[i] = oracle_round_f32(h[i]);
-        oracle_mxfp8_quantize(hf, OR_F32, 1, I, codes, scales);
-        for (int64_t i = 0; i < I; ++i)
-            h[i] = oracle_e4m3_to_double(codes[i]) * oracle_e8m0_to_double(scales[i / 32]);
-        free(hf); free(codes); free(scales);
+        oracle_mxfp8_quantize(hs, hs_dtype, 1, I, codes, scales);
+        oracle_mxfp8_dequantize(codes, scales, 1, I, h);
+        free(hs); free(codes); free(scales);
     }
     oracle_expert_down(h, OR_F64, 1, &one_expert, w2, w2_scale, w_dtype, E, K, I, y, OR_F64);
 }
@@ -493,7 +533,7 @@ static void expert_ffn_row(const void* xrow, int x_dtype, int e,
 ORACLE_EXPORT int oracle_moe_layer(const void* x, int x_dtype, int64_t T, int64_t K, int64_t I, int E, int k,
                                    const int32_t* ids, const float* weights,
                                    const void* w1, const uint8_t* w1_scale, const void* w2, const uint8_t* w2_scale,
-                                   int w_dtype, int w1_layout, int quant_h, void* out, int out_dtype) {
+                                   int w_dtype, int w1_layout, int quant_x, int quant_h, void* out, int out_dtype) {
     int err = 0;
     double* h = (double*)malloc(sizeof(double) * (size_t)I);
     double* y = (double*)malloc(sizeof(double) * (size_t)K);
@@ -506,7 +546,8 @@ ORACLE_EXPORT int oracle_moe_layer(const void* x, int x_dtype, int64_t T, int64_
             if (e == -1) continue;
             if (e < -1 || e >= E) { err |= OR_ERR_ID_RANGE; continue; }
             const char* xrow = (const char*)x + (size_t)(t * K) * esz;
-            expert_ffn_row(xrow, x_dtype, e, w1, w1_scale, w2, w2_scale, w_dtype, w1_layout, E, K, I, quant_h, h, y);
+            expert_ffn_row(xrow, x_dtype, e, w1, w1_scale, w2, w2_scale, w_dtype, w1_layout, E, K, I, quant_x, quant_h,
+                           h, y);
             double w = weights ? (double)weights[t * k + j] : 1.0;
             for (int64_t n = 0; n < K; ++n) acc[n] += w * y[n];
         }
@@ -527,8 +568,8 @@ ORACLE_EXPORT int oracle_moe_layer_batched(const void* xb, int x_dtype, int E, i
                                            const int32_t* expert_num_tokens, const float* weights,
                                            int64_t K, int64_t I,
                                            const void* w1, const uint8_t* w1_scale, const void* w2,
-                                           const uint8_t* w2_scale, int w_dtype, int w1_layout, int quant_h,
-                                           void* out, int out_dtype) {
+                                           const uint8_t* w2_scale, int w_dtype, int w1_layout, int quant_x,
+                                           int quant_h, void* out, int out_dtype) {
     double* h = (double*)malloc(sizeof(double) * (size_t)I);
     double* y = (double*)malloc(sizeof(double) * (size_t)K);
     int esz = x_dtype == OR_F32 ? 4 : (x_dtype == OR_BF16 ? 2 : (x_dtype == OR_F64 ? 8 : 1));
@@ -539,7 +580,8 @@ ORACLE_EXPORT int oracle_moe_layer_batched(const void* xb, int x_dtype, int E, i
         for (int64_t r = 0; r < cnt; ++r) {
             int64_t row = (int64_t)e * max_tokens + r;
             const char* xrow = (const char*)xb + (size_t)(row * K) * esz;
-            expert_ffn_row(xrow, x_dtype, e, w1, w1_scale, w2, w2_scale, w_dtype, w1_layout, E, K, I, quant_h, h, y);
+            expert_ffn_row(xrow, x_dtype, e, w1, w1_scale, w2, w2_scale, w_dtype, w1_layout, E, K, I, quant_x, quant_h,
+                           h, y);
             double w = weights ? (double)weights[row] : 1.0;
             for (int64_t n = 0; n < K; ++n) store_elem(out, out_dtype, row * K + n, w * y[n]);
         }

@@ -346,6 +346,59 @@ def test_quantised_intermediate(oracle_mod):
     assert np.allclose(out, ref.numpy(), rtol=1e-9, atol=1e-15)
 
 
+def _py_mx_roundtrip(v):
+    """Block-32 MXFP8 quantise-dequantise of a 1-D tensor: the exact scale rule written out, the element cast
+    done by torch's float8_e4m3fn."""
+    out = torch.empty(v.numel(), dtype=torch.float64)
+    for b in range(v.numel() // 32):
+        blk = v[32 * b:32 * b + 32].double()
+        m = float(blk.abs().max())
+        if m == 0.0:
+            out[32 * b:32 * b + 32] = 0.0
+            continue
+        c = math.frexp(m / 448.0)[1]
+        while m > math.ldexp(448.0, c):
+            c += 1
+        while m <= math.ldexp(448.0, c - 1):
+            c -= 1
+        sc = math.ldexp(1.0, c)
+        out[32 * b:32 * b + 32] = (blk / sc).to(torch.float8_e4m3fn).double() * sc
+    return out
+
+
+def test_mxfp8_dequantize_matches_torch(oracle_mod):
+    g = torch.Generator().manual_seed(21)
+    codes = torch.randint(0, 256, (7, 96), generator=g, dtype=torch.int32)
+    codes[(codes & 0x7F) == 0x7F] = 0x12                 # no NaN codes
+    codes = codes.to(torch.uint8).numpy()
+    scales = torch.randint(100, 160, (7, 3), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    got = oracle_mod.mxfp8_dequantize(codes, scales)
+    assert np.array_equal(got, _torch_dequant(codes, scales).numpy())
+
+
+def test_quantised_activations_and_bf16_intermediate(oracle_mod):
+    """quant_x: each x row MXFP8 round-tripped before W1; quant_h="bf16": h rounded to bf16, then round-tripped
+    before W2 -- against torch fp64 matmuls with the round trips written out (torch float8 casts)."""
+    w, x, W1, W2, logits = _tiny_inputs(seed=8, I=64, dtype=torch.bfloat16)
+    c1, s1 = oracle_mod.mxfp8_quantize(W1.float().numpy())
+    c2, s2 = oracle_mod.mxfp8_quantize(W2.float().numpy())
+    ids, weights = oracle_mod.topk_route(logits.numpy(), w.top_k)
+    out, _ = oracle_mod.moe_layer(wl.to_numpy(x), ids, weights, c1, c2, w1_scale=s1, w2_scale=s2, quant_x=True,
+                                  quant_h="bf16")
+    D1, D2 = _torch_dequant(c1, s1), _torch_dequant(c2, s2)
+    ref = torch.zeros(w.T, w.K, dtype=torch.float64)
+    for t in range(w.T):
+        xq = _py_mx_roundtrip(x[t].double())
+        for j in range(w.top_k):
+            e = int(ids[t, j])
+            h = F.silu(xq @ D1[e, :w.I].T) * (xq @ D1[e, w.I:].T)
+            hq = _py_mx_roundtrip(h.to(torch.bfloat16).double())
+            ref[t] += float(weights[t, j]) * (hq @ D2[e].T)
+    assert np.allclose(out, ref.numpy(), rtol=1e-9, atol=1e-15)
+    plain, _ = oracle_mod.moe_layer(wl.to_numpy(x), ids, weights, c1, c2, w1_scale=s1, w2_scale=s2)
+    assert not np.allclose(out, plain, rtol=1e-3)          # the round trips changed the result
+
+
 def test_padding_slots_contribute_nothing(oracle_mod):
     w, x, W1, W2, logits = _tiny_inputs(seed=7)
     ids, weights = oracle_mod.topk_route(logits.numpy(), w.top_k)

@@ -7,7 +7,7 @@ mul, down projection with the route weight, ordered top-k reduce) over one
 batch of synthetic input resident in HBM.  The default workload is the decode
 sweep: the layer at T = 1, 8, 32 and 64 tokens (K=4096, I=1536, E=128,
 top_k=8, bf16), all four passes forming one step.  Other workloads (prefill,
-mxfp8, batched, batched_tokens, tiny) can be selected with --workload.
+mxfp8, mxfp8_act, batched, batched_tokens, tiny) can be selected with --workload.
 
 Rank 0 prints ONE JSON line.  Under torchrun (N > 1) each rank runs an
 independent replica of the workload on its GPU (the layer has no exchange
@@ -47,15 +47,16 @@ def workload_list(name):
         return [wl.decode(T) for T in (1, 8, 32, 64)]
     if name.startswith("decode"):
         return [wl.decode(int(name[len("decode"):]))]
-    return [{"prefill": wl.prefill, "mxfp8": wl.mxfp8, "batched": wl.batched, "batched_tokens": wl.batched_tokens,
-             "tiny": wl.tiny}[name]()]
+    return [{"prefill": wl.prefill, "mxfp8": wl.mxfp8, "mxfp8_act": wl.mxfp8_act, "batched": wl.batched,
+             "batched_tokens": wl.batched_tokens, "tiny": wl.tiny}[name]()]
 
 
 def describe(name, ws):
     if name == "decode":
         return "decode bf16 sweep T in {1,8,32,64}: K=4096, I=1536, E=128, top_k=8, contiguous, swap-AB tiles"
     w = ws[0]
-    return (f"{w.name}: T={w.T}, K={w.K}, I={w.I}, E={w.E}, top_k={w.top_k}, act={w.act}, weights={w.weight}, "
+    act = f"{w.act} quantised to mxfp8 on the fly" if w.act_quant else w.act
+    return (f"{w.name}: T={w.T}, K={w.K}, I={w.I}, E={w.E}, top_k={w.top_k}, act={act}, weights={w.weight}, "
             f"layout={w.layout}, block_m={w.block_m}, max_tokens={w.max_tokens}")
 
 
@@ -108,7 +109,7 @@ class Instance:
                                     layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens, device=dev)
         else:
             self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
-                                    device=dev)
+                                    act_quant=w.act_quant, device=dev)
         self.forward()
         torch.cuda.synchronize()
         ids = self.layer.ids if self.logits is not None else self.ids
@@ -150,6 +151,8 @@ class Instance:
         wb = 2 * w.I * w.K * (1 if w.weight == "mxfp8" else 2)
         sb = (2 * w.I * w.K // 32) if w.weight == "mxfp8" else 0
         act = 2 if w.act == "bf16" else 4
+        if w.act_quant:   # E4M3 rows + one scale byte per 32 in, bf16 h out
+            return int(self.used_experts * (wb + sb) + self.routes * (w.K * 33 // 32 + w.I * 2))
         return self.used_experts * (wb + sb) + self.routes * (w.K + w.I) * act
 
     def layer_bytes(self):
@@ -294,29 +297,38 @@ class ClockSampler:
 # traffic from the committed ncu summary (valid only for the kernel source it was taken on)
 # ----------------------------------------------------------------------------
 
-def kernel_source_hash():
-    p = os.path.join(ROOT, "mixture_experts_layer_permute_gb300", "csrc", "gemm_tc.cu")
+def kernel_source_hash(name="gemm_tc.cu"):
+    p = os.path.join(ROOT, "mixture_experts_layer_permute_gb300", "csrc", name)
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
 def recorded_traffic(workload):
-    """GEMM 1 DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
-    p = os.path.join(ROOT, "profiles", f"gemm_tc_traffic_{'decode_sweep' if workload == 'decode' else workload}.txt")
-    fields = {}
-    try:
-        with open(p) as f:
-            for line in f:
-                line = line.strip()
-                if line and not line.startswith("#"):
-                    k, _, v = line.partition(" ")
-                    fields[k] = v.split()
-    except OSError:
-        return None
-    if fields.get("gemm_tc_sha", [None])[0] != kernel_source_hash() or fields.get("workload", [None])[0] != workload:
-        return None
-    vals = [int(v) for v in fields.get("gemm1_traffic_bytes", [])]
-    return vals or None
+    """GEMM 1 DRAM bytes per launch from the committed ncu summary, if taken on this kernel source.
+
+    profiles/gemm_{tc,mx}_traffic_<workload>.txt holds `source <file>`, `source_sha <hash>` (or the older
+    `gemm_tc_sha`), `workload` and `gemm1_traffic_bytes` lines."""
+    tag = "decode_sweep" if workload == "decode" else workload
+    for kind in ("tc", "mx"):
+        p = os.path.join(ROOT, "profiles", f"gemm_{kind}_traffic_{tag}.txt")
+        fields = {}
+        try:
+            with open(p) as f:
+                for line in f:
+                    line = line.strip()
+                    if line and not line.startswith("#"):
+                        k, _, v = line.partition(" ")
+                        fields[k] = v.split()
+        except OSError:
+            continue
+        src = fields.get("source", ["gemm_tc.cu"])[0]
+        sha = (fields.get("source_sha") or fields.get("gemm_tc_sha") or [None])[0]
+        if sha != kernel_source_hash(src) or fields.get("workload", [None])[0] != workload:
+            continue
+        vals = [int(v) for v in fields.get("gemm1_traffic_bytes", [])]
+        if vals:
+            return vals
+    return None
 
 
 # ----------------------------------------------------------------------------
@@ -410,7 +422,8 @@ def run_ours(args, rank, world, local_rank):
         achieved = sum(g1_bytes) / (sum(g1_ms) / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4)}
-    roof["kernel"] = "gemm_tc_kernel (moe_gemm1_swiglu)"
+    mx = any(i.w.act_quant for i in insts)
+    roof["kernel"] = ("gemm_mx_kernel" if mx else "gemm_tc_kernel") + " (moe_gemm1_swiglu)"
     roof["peak_source"] = f"MEASURED_PEAKS.json ({peak_kind})" + (", sustained bf16" if prefill else "")
     roof["traffic"] = recorded_traffic(args.workload)
     roof["algorithmic_per_launch"] = [int(b) for b in (g1_flops if prefill else g1_bytes)]
@@ -537,7 +550,7 @@ def oracle_sample(ws, seed, device_inputs=None):
                 W1, W2, S1, S2 = wl.to_numpy(W1t), wl.to_numpy(W2t), None, None
         remap = {e: i for i, e in enumerate(used)}
         cids = np.vectorize(lambda e: remap[int(e)])(ids).astype(np.int32)
-        samples.append(("contig", x, W1, W2, (cids, wts, S1, S2, w.w1_layout), None, int(ids.size)))
+        samples.append(("contig", x, W1, W2, (cids, wts, S1, S2, w.w1_layout, w.act_quant), None, int(ids.size)))
     return samples
 
 
@@ -548,8 +561,9 @@ def run_oracle_samples(samples):
         if kind == "batched":
             oracle.moe_layer_batched(x, [1], None, W1, W2)
         else:
-            cids, wts, S1, S2, w1l = extra
-            oracle.moe_layer(x, cids, wts, W1, W2, w1_scale=S1, w2_scale=S2, w1_layout=w1l)
+            cids, wts, S1, S2, w1l, aq = extra
+            oracle.moe_layer(x, cids, wts, W1, W2, w1_scale=S1, w2_scale=S2, w1_layout=w1l, quant_x=aq,
+                             quant_h="bf16" if aq else False)
         routes += n
     return routes
 

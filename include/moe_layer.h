@@ -187,10 +187,15 @@ MOE_API int moe_permute_align_static(const int32_t* topk_ids, int64_t T, int top
  *     g_i = sum_k a[s,k] W1[e, gate_row(i), k],  u_i likewise with up_row(i),
  *     h[s, i] = silu(g_i) * u_i = g_i / (1 + exp(-g_i)) * u_i,   i < I.
  *
- *   a             rows of activations, element type a_dtype (F32 or BF16)
+ *   a             rows of activations, element type a_dtype (F32, BF16, or E4M3 codes)
  *                   contiguous: (rows_cap, K); expert e owns rows
  *                     [expert_offsets[e], expert_offsets[e] + expert_counts[e])
  *                   batched: (E, max_tokens, K); expert e owns rows [0, expert_counts[e])
+ *   a_scale       E4M3 activations ("Fused MoE Modular Kernel", prepare(): input
+ *                 activation quantisation, from mxfp8_quantize_block32): E8M0 bytes,
+ *                 same rows as `a`, K/32 per row, 4-byte aligned; NULL otherwise.
+ *                 E4M3 activations need E4M3 weights and run on block-scaled tcgen05
+ *                 swap-AB tiles (K % 128 == 0, 2I % 128 == 0) or MOE_IMPL_SIMT.
  *   w1            (E, 2I, K) of w_dtype (F32, BF16 or E4M3); rows per w1_layout
  *   w1_scale      (E, 2I, K/32) E8M0 bytes when w_dtype == MOE_E4M3, else NULL
  *   h             same row indexing as `a`, (rows, I) of h_dtype (F32 or BF16);
@@ -199,7 +204,7 @@ MOE_API int moe_permute_align_static(const int32_t* topk_ids, int64_t T, int top
  *                 weights, K % 64 == 0 and I % 64 == 0 (MOE_ERR_UNSUPPORTED otherwise).
  * Counts and offsets stay on the device: the call needs no host synchronisation.
  */
-MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, int layout,
+MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale, int layout,
                      const int32_t* expert_counts, const int32_t* expert_offsets,
                      int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
                      const void* w1, const uint8_t* w1_scale, int w_dtype, int w1_layout,
@@ -213,8 +218,12 @@ MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, int layout,
  * directly to the source (token, top-k slot) buffer).
  * For every valid row s of expert e:  y_s[n] = w * sum_i h[s,i] W2[e, n, i],  n < K.
  *
- *   h             (rows, I) of h_dtype (BF16, or F32 for the SIMT path), row indexing as
- *                 in moe_gemm1_swiglu
+ *   h             (rows, I) of h_dtype (BF16, F32 for the SIMT path, or E4M3 codes), row
+ *                 indexing as in moe_gemm1_swiglu
+ *   h_scale       E4M3 h ("Fused MoE Modular Kernel", apply(): quantisation between
+ *                 act+mul and W2): E8M0 bytes (rows, I/32), 4-byte aligned; NULL otherwise.
+ *                 As for GEMM 1, E4M3 h needs E4M3 weights (I % 128 == 0, K % 128 == 0
+ *                 on tcgen05 tiles).
  *   w2            (E, K, I) of w_dtype; w2_scale (E, K, I/32) E8M0 for E4M3, else NULL
  *   contiguous:   row s goes to y[row_route[s]] (rows with row_route -1 are skipped);
  *                 y is (y_rows, K) with y_rows = T*top_k; route_weights, if not NULL,
@@ -223,7 +232,7 @@ MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, int layout,
  *                 NULL, is (E*max_tokens) indexed by row; row_route may be NULL.
  *   y             y_dtype F32 or BF16.
  */
-MOE_API int moe_gemm2(const void* h, int h_dtype, int layout,
+MOE_API int moe_gemm2(const void* h, int h_dtype, const uint8_t* h_scale, int layout,
               const int32_t* expert_counts, const int32_t* expert_offsets,
               int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
               const void* w2, const uint8_t* w2_scale, int w_dtype,

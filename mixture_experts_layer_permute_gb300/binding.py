@@ -66,10 +66,10 @@ def load(path: Optional[str] = None):
                                         P, P]),
             "moe_permute_align_static": (I32, [P, I64, I32, I32, I32, I32, I32, P, I32, I64, P, I64, P, P, P, P,
                                                P, P]),
-            "moe_gemm1_swiglu": (I32, [P, I32, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, I32, I32, P, I32,
-                                       P, P]),
-            "moe_gemm2": (I32, [P, I32, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, P, P, I32, P, I32, I64, P,
-                                P]),
+            "moe_gemm1_swiglu": (I32, [P, I32, P, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, I32, I32, P,
+                                       I32, P, P]),
+            "moe_gemm2": (I32, [P, I32, P, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, P, P, I32, P, I32, I64,
+                                P, P]),
             "moe_unpermute_topk_reduce": (I32, [P, I32, P, P, I64, I32, I32, I64, P, I32, P]),
             "moe_batched_weight_reduce": (I32, [P, I32, P, P, I32, I32, I64, P, I32, P]),
             "moe_batched_topk_reduce": (I32, [P, I32, I64, P, P, I64, I32, I64, P, I32, P, P]),
@@ -210,17 +210,20 @@ def moe_permute_align_static(topk_ids, E, layout=MOE_LAYOUT_CONTIGUOUS, block_m=
 
 def moe_gemm1_swiglu(a, expert_counts, expert_offsets, w1, I, layout=MOE_LAYOUT_CONTIGUOUS, max_tokens=0,
                      w1_scale=None, w1_layout=MOE_W1_GATE_UP, impl=MOE_IMPL_AUTO, h=None, h_dtype=None,
-                     err_word=None, stream=None):
+                     err_word=None, stream=None, a_scale=None):
+    """a_scale: E8M0 scales when `a` holds E4M3 codes (uint8) of MXFP8 activations."""
     E = w1.shape[0]
     K = w1.shape[-1]
     rows_cap = a.shape[0] if layout == MOE_LAYOUT_CONTIGUOUS else E * max_tokens
+    a_dt = dtype_code(a, e4m3=a_scale is not None)
     if h_dtype is None:
-        h_dtype = dtype_code(a)
+        h_dtype = MOE_BF16 if a_dt == MOE_E4M3 else a_dt
     if h is None:
         shape = (rows_cap, I) if layout == MOE_LAYOUT_CONTIGUOUS else (E, max_tokens, I)
         h = torch.empty(shape, dtype=_TORCH[h_dtype], device=a.device)
     _check(load().moe_gemm1_swiglu(
-        _ptr(a), dtype_code(a), layout, _ptr(expert_counts), _ptr(expert_offsets), max_tokens, rows_cap, E, K, I,
+        _ptr(a), a_dt, _ptr(a_scale), layout, _ptr(expert_counts), _ptr(expert_offsets), max_tokens, rows_cap, E, K,
+        I,
         _ptr(w1), _ptr(w1_scale), dtype_code(w1, e4m3=w1_scale is not None), w1_layout, impl, _ptr(h), h_dtype,
         _ptr(err_word), _stream(stream)))
     return h
@@ -228,16 +231,19 @@ def moe_gemm1_swiglu(a, expert_counts, expert_offsets, w1, I, layout=MOE_LAYOUT_
 
 def moe_gemm2(h, expert_counts, expert_offsets, w2, y_rows, layout=MOE_LAYOUT_CONTIGUOUS, max_tokens=0,
               w2_scale=None, row_route=None, route_weights=None, impl=MOE_IMPL_AUTO, y=None, y_dtype=None,
-              err_word=None, stream=None):
+              err_word=None, stream=None, h_scale=None):
+    """h_scale: E8M0 scales when `h` holds E4M3 codes (uint8) of an MXFP8 intermediate."""
     E, K, I = w2.shape
     rows_cap = h.shape[0] if layout == MOE_LAYOUT_CONTIGUOUS else E * max_tokens
+    h_dt = dtype_code(h, e4m3=h_scale is not None)
     if y_dtype is None:
-        y_dtype = dtype_code(h)
+        y_dtype = MOE_BF16 if h_dt == MOE_E4M3 else h_dt
     if y is None:
         shape = (y_rows, K) if layout == MOE_LAYOUT_CONTIGUOUS else (E, max_tokens, K)
         y = torch.empty(shape, dtype=_TORCH[y_dtype], device=h.device)
     _check(load().moe_gemm2(
-        _ptr(h), dtype_code(h), layout, _ptr(expert_counts), _ptr(expert_offsets), max_tokens, rows_cap, E, K, I,
+        _ptr(h), h_dt, _ptr(h_scale), layout, _ptr(expert_counts), _ptr(expert_offsets), max_tokens, rows_cap, E,
+        K, I,
         _ptr(w2), _ptr(w2_scale), dtype_code(w2, e4m3=w2_scale is not None), _ptr(row_route), _ptr(route_weights),
         impl, _ptr(y), y_dtype, y_rows, _ptr(err_word), _stream(stream)))
     return y

@@ -152,8 +152,14 @@ int validate_gemm(const GemmArgs& g, const char* name) {
     MOE_REQUIRE(g.a && g.w && g.counts && g.out, MOE_ERR_INVALID_ARG, n + ": null pointer");
     MOE_REQUIRE(aligned16(g.a) && aligned16(g.w) && aligned16(g.out), MOE_ERR_ALIGNMENT,
                 n + ": activation, weight and output pointers must be 16-byte aligned");
-    MOE_REQUIRE(is_float_dtype(g.a_dtype) && is_float_dtype(g.out_dtype), MOE_ERR_UNSUPPORTED,
-                n + ": activations and outputs must be F32 or BF16");
+    MOE_REQUIRE((is_float_dtype(g.a_dtype) || g.a_dtype == MOE_E4M3) && is_float_dtype(g.out_dtype),
+                MOE_ERR_UNSUPPORTED, n + ": activations must be F32, BF16 or E4M3; outputs F32 or BF16");
+    if (g.a_dtype == MOE_E4M3) {
+        MOE_REQUIRE(g.a_scale, MOE_ERR_INVALID_ARG, n + ": E4M3 activations need scales");
+        MOE_REQUIRE((reinterpret_cast<uintptr_t>(g.a_scale) & 3u) == 0, MOE_ERR_ALIGNMENT,
+                    n + ": activation scales must be 4-byte aligned");
+        MOE_REQUIRE(g.w_dtype == MOE_E4M3, MOE_ERR_UNSUPPORTED, n + ": E4M3 activations need E4M3 weights");
+    }
     MOE_REQUIRE(g.w_dtype == MOE_F32 || g.w_dtype == MOE_BF16 || g.w_dtype == MOE_E4M3, MOE_ERR_UNSUPPORTED,
                 n + ": unknown weight dtype");
     MOE_REQUIRE(g.w_dtype != MOE_E4M3 || g.w_scale, MOE_ERR_INVALID_ARG, n + ": E4M3 weights need scales");
@@ -169,7 +175,25 @@ int validate_gemm(const GemmArgs& g, const char* name) {
     return MOE_OK;
 }
 
+// E4M3 activations (with E4M3 weights): block-scaled tcgen05 swap-AB tiles, or the CUDA-core kernel.
+int run_gemm_mx(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
+    if (impl == MOE_IMPL_SIMT) return launch_status(launch_gemm_simt(g, s), name);
+    MOE_REQUIRE(impl == MOE_IMPL_AUTO || impl == MOE_IMPL_TCGEN05_SWAP_AB, MOE_ERR_UNSUPPORTED,
+                std::string(name) + ": E4M3 activations run on swap-AB tcgen05 tiles (or SIMT)");
+    if (device_cc() < 100) {
+        if (impl == MOE_IMPL_AUTO) return launch_status(launch_gemm_simt(g, s), name);
+        return fail(MOE_ERR_UNSUPPORTED, std::string(name) + ": tcgen05 needs an sm_100+ device");
+    }
+    int rc = launch_gemm_mx(g, s);
+    if (rc != MOE_OK && impl == MOE_IMPL_AUTO && rc == MOE_ERR_UNSUPPORTED) {
+        g_last_error.clear();
+        return launch_status(launch_gemm_simt(g, s), name);
+    }
+    return rc;
+}
+
 int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
+    if (g.a_dtype == MOE_E4M3) return run_gemm_mx(g, impl, s, name);
     const bool tc_ok = g.a_dtype == MOE_BF16 && (g.w_dtype == MOE_BF16 || g.w_dtype == MOE_E4M3) &&
                        g.out_dtype == MOE_BF16 && device_cc() >= 100;
     int chosen = impl;
@@ -204,7 +228,7 @@ int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
 
 }  // namespace
 
-int moe_gemm1_swiglu(const void* a, int a_dtype, int layout, const int32_t* expert_counts,
+int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale, int layout, const int32_t* expert_counts,
                      const int32_t* expert_offsets, int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
                      const void* w1, const uint8_t* w1_scale, int w_dtype, int w1_layout, int impl, void* h,
                      int h_dtype, int32_t* err_word, void* stream) {
@@ -213,6 +237,7 @@ int moe_gemm1_swiglu(const void* a, int a_dtype, int layout, const int32_t* expe
     g.gemm = 1;
     g.a = a;
     g.a_dtype = a_dtype;
+    g.a_scale = a_scale;
     g.layout = layout;
     g.counts = expert_counts;
     g.offsets = layout == MOE_LAYOUT_CONTIGUOUS ? expert_offsets : nullptr;
@@ -237,15 +262,17 @@ int moe_gemm1_swiglu(const void* a, int a_dtype, int layout, const int32_t* expe
     return run_gemm(g, impl, as_stream(stream), "moe_gemm1_swiglu");
 }
 
-int moe_gemm2(const void* hh, int h_dtype, int layout, const int32_t* expert_counts, const int32_t* expert_offsets,
-              int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I, const void* w2,
-              const uint8_t* w2_scale, int w_dtype, const int32_t* row_route, const float* route_weights, int impl,
-              void* y, int y_dtype, int64_t y_rows, int32_t* err_word, void* stream) {
+int moe_gemm2(const void* hh, int h_dtype, const uint8_t* h_scale, int layout, const int32_t* expert_counts,
+              const int32_t* expert_offsets, int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
+              const void* w2, const uint8_t* w2_scale, int w_dtype, const int32_t* row_route,
+              const float* route_weights, int impl, void* y, int y_dtype, int64_t y_rows, int32_t* err_word,
+              void* stream) {
     g_last_error.clear();
     GemmArgs g{};
     g.gemm = 2;
     g.a = hh;
     g.a_dtype = h_dtype;
+    g.a_scale = h_scale;
     g.layout = layout;
     g.counts = expert_counts;
     g.offsets = layout == MOE_LAYOUT_CONTIGUOUS ? expert_offsets : nullptr;

@@ -1,6 +1,7 @@
 // CUDA-core grouped GEMMs (fp32 FMA).  This is the path for fp32 layers --
 // tensor-core tf32 would not hold a 1e-5 relative tolerance -- and for shapes
-// the tcgen05 tiles do not cover.  A CTA computes a 64 x 64 tile of
+// the tcgen05 tiles do not cover.  Activations are F32, BF16 or MXFP8 (E4M3
+// codes + E8M0 scales, with MXFP8 weights); weights F32, BF16 or MXFP8.  A CTA computes a 64 x 64 tile of
 // C = A[rows of one expert] * B^T[64 weight rows] in 16-wide k steps staged
 // through shared memory; each of the 256 threads owns a 4 x 4 block of C.
 //   GEMM 1: the 64 weight rows are the gate rows and the up rows of 32 units,
@@ -80,7 +81,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * 256, r = idx / BK, kk = idx % BK;
             float v = 0.f;
-            if (r < valid) v = load_as_float<ADT>(g.a, (row0 + r) * kdim + k0 + kk);
+            if (r < valid) {
+                if constexpr (ADT == MOE_E4M3) v = load_weight<MOE_E4M3>(g.a, g.a_scale, row0 + r, k0 + kk, kdim);
+                else v = load_as_float<ADT>(g.a, (row0 + r) * kdim + k0 + kk);
+            }
             As[kk][r] = v;
         }
         // B: 64 weight rows x 16 k
@@ -170,6 +174,7 @@ cudaError_t launch2(const GemmArgs& g, dim3 grid, cudaStream_t s) {
 template <int GEMM>
 cudaError_t launch1(const GemmArgs& g, dim3 grid, cudaStream_t s) {
     if (g.a_dtype == MOE_F32) return launch2<GEMM, MOE_F32>(g, grid, s);
+    if (g.a_dtype == MOE_E4M3) return launch3<GEMM, MOE_E4M3, MOE_E4M3>(g, grid, s);   // MXFP8 x MXFP8
     return launch2<GEMM, MOE_BF16>(g, grid, s);
 }
 

@@ -43,6 +43,7 @@ struct GemmArgs {
     int gemm;               // 1: gate/up + SiLU-and-mul, 2: down projection
     const void* a;          // activations (gemm 1) or h (gemm 2)
     int a_dtype;
+    const uint8_t* a_scale; // E4M3 activations: E8M0 scales (rows, kdim/32)
     int layout;
     const int32_t* counts;
     const int32_t* offsets; // contiguous layout; NULL for batched
@@ -67,5 +68,7 @@ cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t s);
 enum { TC_NORMAL = 0, TC_SWAP = 1, TC_MIXED = 2 };
 // Returns MOE_OK or a status (with message) when the tcgen05 path cannot run.
 int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s);
+// Block-scaled MXFP8 (E4M3 activations and weights) on swap-AB tcgen05 tiles.
+int launch_gemm_mx(const GemmArgs& g, cudaStream_t s);
 
 }  // namespace moe

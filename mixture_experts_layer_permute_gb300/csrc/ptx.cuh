@@ -149,6 +149,19 @@ MOE_DEVICE void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc
         : "memory");
 }
 
+// D[tmem] (+)= (A * 2^(SFA-127)) * (B * 2^(SFB-127))^T, kind::mxf8f6f4 with one E8M0 scale per 32 along K
+// (scale_vec::1X): A and B E4M3 in shared memory (descriptors), K = 32 per instruction.  The scale factors
+// sit in TMEM at sfa_tmem / sfb_tmem; the byte of each 32-bit column used by this instruction is the
+// scale-factor id carried in idesc (bits 29-30 for A, 4-5 for B).
+MOE_DEVICE void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa_tmem,
+                         uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once all tcgen05.mma issued by this thread have completed.
 MOE_DEVICE void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -180,6 +193,13 @@ MOE_DEVICE void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 MOE_DEVICE void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 4 consecutive 32-bit columns: thread i writes columns [col, col+4) of lane (base + i).
+MOE_DEVICE void tmem_st_32x32b_x4(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
+}
 
 // 32 lanes x 8 consecutive 32-bit columns: thread i writes columns [col, col+8) of lane (base + i).
 MOE_DEVICE void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
@@ -237,6 +257,18 @@ MOE_DEVICE constexpr uint32_t idesc_bf16(int M, int N) {
            | (uint32_t(N >> 3) << 17)      // N / 8
            | (uint32_t(M >> 4) << 24);     // M / 16
 }
+
+// Instruction descriptor, kind::mxf8f6f4 with E4M3 A and B, both K-major, E8M0 (UE8M0) scale factors, FP32 D;
+// the scale-factor ids (bits 4-5 for B, 29-30 for A) are or-ed in per instruction.
+MOE_DEVICE constexpr uint32_t idesc_mxf8(int M, int N) {
+    return (0u << 7)                       // A format: E4M3
+           | (0u << 10)                    // B format: E4M3
+           | (uint32_t(N >> 3) << 17)      // N / 8
+           | (1u << 23)                    // scale factor type: UE8M0
+           | (uint32_t(M >> 4) << 24);     // M / 16
+}
+
+MOE_DEVICE constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) { return (a_id << 29) | (b_id << 4); }
 
 }  // namespace ptx
 }  // namespace moe

@@ -7,6 +7,12 @@ intermediates are declared up front and reused), and ``forward`` issues
     moe_topk_route -> moe_permute_align -> moe_gemm1_swiglu -> moe_gemm2
         -> moe_unpermute_topk_reduce          (contiguous layout)
 
+with, for MXFP8 weights and ``act_quant=True``, the activations quantised on
+the fly so that both GEMMs run block-scaled MXFP8 x MXFP8:
+
+    ... moe_permute_align -> mxfp8_quantize_block32 (x rows) -> moe_gemm1_swiglu
+        -> mxfp8_quantize_block32 (h) -> moe_gemm2 -> moe_unpermute_topk_reduce
+
 or, for the batched layout fed with expert-major rows (T = 0),
 
     moe_gemm1_swiglu -> moe_gemm2 (route weight in the epilogue)
@@ -38,8 +44,13 @@ def _p(t):
 class MoELayer:
     def __init__(self, T: int, K: int, I: int, E: int, top_k: int, act_dtype=torch.bfloat16, block_m: int = 1,
                  layout: int = B.MOE_LAYOUT_CONTIGUOUS, max_tokens: int = 0, impl: int = B.MOE_IMPL_AUTO,
-                 weight_in_gemm2: bool = True, device="cuda"):
+                 weight_in_gemm2: bool = True, device="cuda", act_quant: bool = False):
         self.T, self.K, self.I, self.E, self.top_k = T, K, I, E, top_k
+        if act_quant and layout != B.MOE_LAYOUT_CONTIGUOUS:
+            raise ValueError("act_quant (MXFP8 activations) is implemented for the contiguous layout")
+        if act_quant and (K % 32 or I % 32):
+            raise ValueError("act_quant needs K and I multiples of 32")
+        self.act_quant = act_quant
         self.block_m, self.layout, self.max_tokens, self.impl = block_m, layout, max_tokens, impl
         self.weight_in_gemm2 = weight_in_gemm2
         self.act_dtype = act_dtype
@@ -61,6 +72,12 @@ class MoELayer:
             self.h = torch.empty((self.rows_cap, I), dtype=act_dtype, device=dev)
             self.y = torch.empty((T * top_k, K), dtype=act_dtype, device=dev)
             self.out = torch.empty((T, K), dtype=act_dtype, device=dev)
+            if act_quant:
+                u8 = dict(dtype=torch.uint8, device=dev)
+                self.x_codes = torch.empty((self.rows_cap, K), **u8)
+                self.x_scales = torch.empty((self.rows_cap, K // 32), **u8)
+                self.h_codes = torch.empty((self.rows_cap, I), **u8)
+                self.h_scales = torch.empty((self.rows_cap, I // 32), **u8)
         elif T > 0:   # batched rows, token input and output
             self.rows_cap = E * max_tokens
             self.ids = torch.empty((T, top_k), **i32)
@@ -105,12 +122,12 @@ class MoELayer:
                                             w1_layout, adt, wdt, stream)
         if self.layout == B.MOE_LAYOUT_BATCHED:
             mt = self.max_tokens
-            calls.append((lib.moe_gemm1_swiglu, (x.data_ptr(), adt, self.layout, counts.data_ptr(), None, mt,
+            calls.append((lib.moe_gemm1_swiglu, (x.data_ptr(), adt, None, self.layout, counts.data_ptr(), None, mt,
                                                  self.rows_cap, E, K, I, w1.data_ptr(), _p(w1_scale), wdt,
                                                  w1_layout, self.impl, self.h.data_ptr(), adt, self.err.data_ptr(),
                                                  stream), "gemm1"))
             rw = row_weights if self.weight_in_gemm2 else None
-            calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, self.layout, counts.data_ptr(), None, mt,
+            calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, None, self.layout, counts.data_ptr(), None, mt,
                                           self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, None, _p(rw),
                                           self.impl, self.out.data_ptr(), adt, self.rows_cap, self.err.data_ptr(),
                                           stream), "gemm2"))
@@ -131,12 +148,28 @@ class MoELayer:
                                               self.row_route.data_ptr(), self.route_row.data_ptr(),
                                               self.workspace.data_ptr(), self.workspace.numel(),
                                               self.err.data_ptr(), stream), "permute"))
-        calls.append((lib.moe_gemm1_swiglu, (self.x_perm.data_ptr(), adt, self.layout, self.counts.data_ptr(),
+        if self.act_quant:
+            if wdt != B.MOE_E4M3:
+                raise ValueError("act_quant needs MXFP8 (E4M3 + scales) weights")
+            calls.append((lib.mxfp8_quantize_block32, (self.x_perm.data_ptr(), adt, self.rows_cap, K,
+                                                       self.x_codes.data_ptr(), self.x_scales.data_ptr(), stream),
+                          "quant_x"))
+            a1, a1dt, a1s = self.x_codes.data_ptr(), B.MOE_E4M3, self.x_scales.data_ptr()
+        else:
+            a1, a1dt, a1s = self.x_perm.data_ptr(), adt, None
+        calls.append((lib.moe_gemm1_swiglu, (a1, a1dt, a1s, self.layout, self.counts.data_ptr(),
                                              self.offsets.data_ptr(), 0, self.rows_cap, E, K, I, w1.data_ptr(),
                                              _p(w1_scale), wdt, w1_layout, self.impl, self.h.data_ptr(), adt,
                                              self.err.data_ptr(), stream), "gemm1"))
+        if self.act_quant:
+            calls.append((lib.mxfp8_quantize_block32, (self.h.data_ptr(), adt, self.rows_cap, I,
+                                                       self.h_codes.data_ptr(), self.h_scales.data_ptr(), stream),
+                          "quant_h"))
+            a2, a2dt, a2s = self.h_codes.data_ptr(), B.MOE_E4M3, self.h_scales.data_ptr()
+        else:
+            a2, a2dt, a2s = self.h.data_ptr(), adt, None
         rw = weights if self.weight_in_gemm2 else None
-        calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, self.layout, self.counts.data_ptr(),
+        calls.append((lib.moe_gemm2, (a2, a2dt, a2s, self.layout, self.counts.data_ptr(),
                                       self.offsets.data_ptr(), 0, self.rows_cap, E, K, I, w2.data_ptr(),
                                       _p(w2_scale), wdt, self.row_route.data_ptr(), _p(rw), self.impl,
                                       self.y.data_ptr(), adt, T * k, self.err.data_ptr(), stream), "gemm2"))
@@ -161,11 +194,11 @@ class MoELayer:
                                               self.offsets.data_ptr(), self.row_route.data_ptr(),
                                               self.route_row.data_ptr(), self.workspace.data_ptr(),
                                               self.workspace.numel(), self.err.data_ptr(), stream), "permute"))
-        calls.append((lib.moe_gemm1_swiglu, (self.x_perm.data_ptr(), adt, self.layout, self.counts.data_ptr(), None,
+        calls.append((lib.moe_gemm1_swiglu, (self.x_perm.data_ptr(), adt, None, self.layout, self.counts.data_ptr(), None,
                                              mt, self.rows_cap, E, K, I, w1.data_ptr(), _p(w1_scale), wdt,
                                              w1_layout, self.impl, self.h.data_ptr(), adt, self.err.data_ptr(),
                                              stream), "gemm1"))
-        calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, self.layout, self.counts.data_ptr(), None, mt,
+        calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, None, self.layout, self.counts.data_ptr(), None, mt,
                                       self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, None, None,
                                       self.impl, self.y.data_ptr(), adt, self.rows_cap, self.err.data_ptr(),
                                       stream), "gemm2"))
@@ -213,6 +246,8 @@ class MoELayer:
         if self.layout == B.MOE_LAYOUT_BATCHED and self.T == 0:
             return 2 if self.weight_in_gemm2 else 3
         n = 3 + 1 + (1 if self.T * self.top_k <= 1024 else 2) + 1   # gemm1 gemm2 reduce, gather, permute, route
+        if self.act_quant:
+            n += 2                                                    # quantise x rows and h
         return n if any(name == "route" for _, _, name in (self._plan or [])) else n - 1
 
     def device_errors(self, reset: bool = True) -> int:

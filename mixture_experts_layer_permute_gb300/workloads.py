@@ -24,6 +24,8 @@ The workloads are the five synthetic configurations of the layer:
                 gate/up interleave-16 layout, topk_ids[t, j] = ((8t + j) 73 + 19)
                 mod 512 and weights 1/8 (the balanced routing pattern of the
                 "Cake MegaMoE" PR analysis, section 1 "After").
+* ``mxfp8_act`` the mxfp8 workload with x rows and h quantised to MXFP8 on the
+                fly (E4M3 codes, one E8M0 scale per 32).
 * ``batched``   (E=32, max_tokens=256, K=6144) activations, I=4096,
                 expert_num_tokens uniform in [0, 256], rows beyond the count
                 filled with garbage (NaN or +-1e30), per-row weights U(0, 1).
@@ -59,6 +61,7 @@ class Workload:
     x_std: float = 1.0
     w_std: float = 0.02
     garbage: str = "nan"         # batched: fill of rows beyond the count
+    act_quant: bool = False      # activations (x rows, h) quantised to MXFP8 on the fly
 
     @property
     def routes(self) -> int:
@@ -80,6 +83,11 @@ def prefill() -> Workload:
 def mxfp8() -> Workload:
     return Workload("mxfp8_weights", T=512, K=7168, I=2048, E=512, top_k=8, weight="mxfp8", routing="affine",
                     w1_layout=1)
+
+
+def mxfp8_act() -> Workload:
+    """The mxfp8 workload with its activations quantised on the fly (block-scaled MXFP8 x MXFP8 GEMMs)."""
+    return dataclasses.replace(mxfp8(), name="mxfp8_act_quant", act_quant=True)
 
 
 def batched(garbage: str = "nan") -> Workload:

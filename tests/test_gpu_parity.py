@@ -382,6 +382,72 @@ def test_gemm2_e4m3(moe, impl, shape):
     assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 e4m3 {impl}")
 
 
+MX_SHAPES = E4M3_SHAPES + [(700, 2, 6, 256, 128)]   # + skewed: full, long and short token segments
+
+
+def _mx_rows(moe, a):
+    """MXFP8 rows (codes, scales) of bf16 rows `a` on the GPU, checked bit-exact against the oracle."""
+    codes, scales = moe.mxfp8_quantize_block32(a.to(DEV))
+    rc, rs = oracle.mxfp8_quantize(wl.to_numpy(a.cpu()))
+    assert np.array_equal(codes.cpu().numpy(), rc) and np.array_equal(scales.cpu().numpy(), rs)
+    return codes, scales, rc, rs
+
+
+@pytest.mark.parametrize("impl", ["swap_ab", "auto", "simt"])
+@pytest.mark.parametrize("shape", MX_SHAPES)
+@pytest.mark.parametrize("w1_layout", [0, 1])
+def test_gemm1_swiglu_mxf8(moe, impl, shape, w1_layout):
+    """MXFP8 activations x MXFP8 weights (block-scaled tcgen05 MMA) against the oracle on the decoded values."""
+    T, k, E, K, I = shape
+    w, x, ids, _ = _routed(T, k, E, K, seed=T + 5 * E)
+    W1 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8", w_std=0.05), "W1", 9)
+    c1, s1, rc1, rs1 = _e4m3_weights(moe, W1)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    xc, xs, _, _ = _mx_rows(moe, res["x_out"])
+    h = moe.moe_gemm1_swiglu(xc, res["counts"], res["offsets"], c1, I, w1_scale=s1, a_scale=xs,
+                             w1_layout=w1_layout, impl=_impl(moe, impl))
+    xr = wl.to_numpy(x)[np.arange(T * k) // k]
+    xq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(xr))          # the rows the GPU multiplied
+    href = oracle.expert_gate_up(xq, ids.reshape(-1), rc1, w1_scale=rs1, w1_layout=w1_layout)
+    rr = res["route_row"].cpu().numpy().reshape(-1)
+    assert_close(to_f64(h.cpu()[torch.from_numpy(rr).long()]), href, TOL_BF16, f"gemm1 mxf8 {impl}")
+
+
+@pytest.mark.parametrize("impl", ["swap_ab", "simt"])
+@pytest.mark.parametrize("shape", MX_SHAPES)
+def test_gemm2_mxf8(moe, impl, shape):
+    T, k, E, K, I = shape
+    w, _, ids, weights = _routed(T, k, E, K, seed=T + 6 * E)
+    W2 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8", w_std=0.05), "W2", 10)
+    c2, s2, rc2, rs2 = _e4m3_weights(moe, W2)
+    R = T * k
+    hsrc = wl._normal((R, I), 1.0, 11, "h", 0, "cpu", torch.bfloat16)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1)
+    hperm = torch.zeros((res["rows_cap"], I), dtype=torch.bfloat16, device=DEV)
+    hperm[res["route_row"].view(-1).long()] = hsrc.to(DEV)
+    hc, hs, _, _ = _mx_rows(moe, hperm)
+    wt = torch.from_numpy(weights).to(DEV).reshape(-1)
+    y = moe.moe_gemm2(hc, res["counts"], res["offsets"], c2, R, w2_scale=s2, h_scale=hs, row_route=res["row_route"],
+                      route_weights=wt, impl=_impl(moe, impl))
+    hq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(wl.to_numpy(hsrc)))
+    yref = oracle.expert_down(hq, ids.reshape(-1), rc2, w2_scale=rs2)
+    yref = yref * weights.reshape(-1, 1).astype(np.float64)
+    assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 mxf8 {impl}")
+
+
+def test_mxf8_refuses_normal_tiles(moe):
+    T, k, E, K, I = 64, 2, 4, 256, 128
+    w, x, ids, _ = _routed(T, k, E, K, seed=12)
+    W1 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8"), "W1", 7)
+    c1, s1 = moe.mxfp8_quantize_block32(W1.to(DEV))
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    xc, xs = moe.mxfp8_quantize_block32(res["x_out"])
+    for impl in (moe.MOE_IMPL_TCGEN05, moe.MOE_IMPL_TCGEN05_MIXED):
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_gemm1_swiglu(xc, res["counts"], res["offsets"], c1, I, w1_scale=s1, a_scale=xs, impl=impl)
+        assert ei.value.status == 2
+
+
 def test_e4m3_normal_tiles_unsupported_but_auto_works(moe):
     T, k, E, K, I = 64, 2, 4, 256, 128
     w, x, ids, _ = _routed(T, k, E, K, seed=11)
@@ -533,6 +599,44 @@ def test_layer_mxfp8_full_size_sampled(moe):
         ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, w_t[t:t + 1].numpy(), w1h, w2h, w1_scale=s1h,
                                   w2_scale=s2h, w1_layout=1)
         assert_close(to_f64(out[t:t + 1]), ref, TOL_BF16, f"mxfp8 token {t}")
+
+
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+def test_layer_mxf8_activations_small(moe, impl):
+    """Whole layer with MXFP8 weights and activations quantised on the fly (x rows and h), against the oracle
+    with the same quantisation points (x from its stored bf16 values, h rounded to bf16 first)."""
+    T, k, E, K, I = 80, 4, 8, 512, 256
+    w = wl.scaled(wl.decode(T), T=T, K=K, I=I, E=E, top_k=k, weight="mxfp8", w_std=0.05)
+    x, logits = wl.activations(w, 2), wl.router_logits(w, 2)
+    c1, s1, rc1, rs1 = _e4m3_weights(moe, wl.expert_weights(w, "W1", 2))
+    c2, s2, rc2, rs2 = _e4m3_weights(moe, wl.expert_weights(w, "W2", 2))
+    layer = moe.MoELayer(T, K, I, E, k, act_quant=True, impl=_impl(moe, impl), device=DEV)
+    out = layer.forward(x.to(DEV), c1, c2, logits=logits.to(DEV), w1_scale=s1, w2_scale=s2)
+    assert layer.device_errors() == 0
+    ids, wts = oracle.topk_route(logits.numpy(), k)
+    ref, _ = oracle.moe_layer(wl.to_numpy(x), ids, wts, rc1, rc2, w1_scale=rs1, w2_scale=rs2, quant_x=True,
+                              quant_h="bf16")
+    assert_close(to_f64(out), ref, TOL_BF16, f"layer mxf8 activations {impl}")
+
+
+def test_layer_mxfp8_act_quant_full_size_sampled(moe):
+    """MXFP8 workload (E=512, K=7168, I=2048, interleave-16 W1, affine routing) with activations quantised on the
+    fly, as the benchmark's mxfp8_act workload runs it; oracle on 2 tokens."""
+    w = wl.mxfp8()
+    x = wl.activations(w, 0, DEV)
+    ids_t, w_t = wl.affine_routing(w)
+    c1, s1 = _mxfp8_weights(moe, w, "W1", 0)
+    c2, s2 = _mxfp8_weights(moe, w, "W2", 0)
+    layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_quant=True, device=DEV)
+    out = layer.forward(x, c1, c2, topk_ids=ids_t.to(DEV), topk_weights=w_t.to(DEV), w1_scale=s1, w2_scale=s2,
+                        w1_layout=moe.MOE_W1_INTERLEAVE16)
+    assert layer.device_errors() == 0
+    ids = ids_t.numpy()
+    for t in (0, 511):
+        cids, (w1h, w2h, s1h, s2h) = compact_experts(ids[t:t + 1], c1, c2, s1, s2)
+        ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, w_t[t:t + 1].numpy(), w1h, w2h, w1_scale=s1h,
+                                  w2_scale=s2h, w1_layout=1, quant_x=True, quant_h="bf16")
+        assert_close(to_f64(out[t:t + 1]), ref, TOL_BF16, f"mxfp8 act-quant token {t}")
 
 
 @pytest.mark.parametrize("garbage", ["nan", "big"])

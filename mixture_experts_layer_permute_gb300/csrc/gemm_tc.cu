@@ -74,38 +74,48 @@ constexpr int MAX_STAGES = 12;
 constexpr int kConvThreads = 512;           // E4M3 converter warps 6..21
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// Per weight type: stage ring layout, TMEM map and CTA shape.
-//   bf16:  smem [A 16 KB][B 32 KB] x 4 stages; TMEM: two 256-column accumulators;
-//          192 threads; up to 256 tokens per swap-AB tile
-//   E4M3:  smem: 9 code stages of 128 rows x 128 B, then 4 token slots of 2 x 8 KB;
-//          TMEM: two 64-column accumulators, then 4 bf16 A tiles of 64 columns;
-//          736 threads (+ 16 converter warps, + 1 token warp); up to 64 tokens per tile
-template <bool W8>
+// Per variant: stage ring layout, TMEM map and CTA shape.
+//   V_BF16:   smem [A 16 KB][B 32 KB] x 4 stages; TMEM: two 256-column accumulators;
+//             192 threads; normal tiles, mixed launches, swap-AB tiles of up to 256 tokens
+//   V_SWAP64: bf16 swap-AB tiles of up to 64 tokens: smem [A 16 KB][B 8 KB] x 8 stages (twice the
+//             weight bytes in flight of V_BF16); TMEM: two 64-column accumulators; 192 threads
+//   V_E4M3:   smem: 9 code stages of 128 rows x 128 B, then 4 token slots of 2 x 8 KB;
+//             TMEM: two 64-column accumulators, then 4 bf16 A tiles of 64 columns;
+//             736 threads (+ 16 converter warps, + 1 token warp); up to 64 tokens per tile
+enum { V_BF16 = 0, V_E4M3 = 1, V_SWAP64 = 2 };
+
+template <int V>
 struct Cfg {
+    static constexpr bool W8 = V == V_E4M3;
+    static constexpr bool NARROW = V == V_SWAP64;
     static constexpr int KSUB = W8 ? 2 : 1;                     // 64-wide k-blocks per stage
-    static constexpr int STAGES = W8 ? 9 : 4;                   // bf16: operand stages; E4M3: code stages
+    static constexpr int STAGES = W8 ? 9 : (NARROW ? 8 : 4);    // bf16: operand stages; E4M3: code stages
     static constexpr int A_SLOTS = 4;                           // E4M3: TMEM A tiles (+ token tiles)
-    static constexpr int TOK_SPAN = W8 ? 64 : 256;              // swap-AB tokens per tile
+    static constexpr int TOK_SPAN = (W8 || NARROW) ? 64 : 256;  // swap-AB tokens per tile
     static constexpr int B_OFF = W8 ? 0 : A_BYTES;              // bf16: B operand offset in a stage
     static constexpr int B_SUB = TOK_SPAN * BK * 2;             // token bytes per 64-wide k-block (swap)
-    static constexpr int B_BYTES = W8 ? 0 : 256 * BK * 2;
+    static constexpr int B_BYTES = W8 ? 0 : (NARROW ? B_SUB : 256 * BK * 2);
     static constexpr int STAGE_BYTES = W8 ? BM * BK * KSUB : A_BYTES + B_BYTES;
     static constexpr int TOK_OFF = STAGES * STAGE_BYTES;        // E4M3: token slots after the code ring
     static constexpr int TOK_SLOT = B_SUB * KSUB;
     static constexpr int THREADS = W8 ? 192 + kConvThreads + 32 : 192;   // E4M3: + converters + token warp
     static constexpr int TOK_WARP = 6 + kConvThreads / 32;
     static constexpr int SMEM = STAGES * STAGE_BYTES + (W8 ? A_SLOTS * TOK_SLOT : 0) + 1024;
-    static constexpr int ACC_STRIDE = W8 ? TOK_SPAN : ACC_COLS; // TMEM columns per accumulator
+    static constexpr int ACC_STRIDE = (W8 || NARROW) ? TOK_SPAN : ACC_COLS; // TMEM columns per accumulator
     static constexpr int A_TMEM = 2 * ACC_STRIDE;               // E4M3: first A tile column
     static constexpr int A_COLS = KSUB * BK / 2;                // E4M3: TMEM columns per A tile
     static constexpr int TMEM_USED = W8 ? A_TMEM + A_SLOTS * A_COLS : 2 * ACC_STRIDE;
 };
-static_assert(Cfg<false>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed the TMEM allocation");
-static_assert(Cfg<true>::TMEM_USED <= TMEM_COLS, "E4M3 accumulators and A tiles exceed the TMEM allocation");
-static_assert(Cfg<false>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
-static_assert(Cfg<true>::SMEM + 13 * 1024 <= 227 * 1024, "E4M3 stage ring exceeds shared memory");
-static_assert(Cfg<true>::STAGES <= MAX_STAGES && Cfg<false>::STAGES <= MAX_STAGES, "too many stages");
-static_assert(Cfg<true>::A_SLOTS == 4, "converter groups take A slot (stage index mod 4)");
+static_assert(Cfg<V_BF16>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed the TMEM allocation");
+static_assert(Cfg<V_SWAP64>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed the TMEM allocation");
+static_assert(Cfg<V_E4M3>::TMEM_USED <= TMEM_COLS, "E4M3 accumulators and A tiles exceed the TMEM allocation");
+static_assert(Cfg<V_BF16>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
+static_assert(Cfg<V_SWAP64>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
+static_assert(Cfg<V_E4M3>::SMEM + 13 * 1024 <= 227 * 1024, "E4M3 stage ring exceeds shared memory");
+static_assert(Cfg<V_E4M3>::STAGES <= MAX_STAGES && Cfg<V_BF16>::STAGES <= MAX_STAGES &&
+                  Cfg<V_SWAP64>::STAGES <= MAX_STAGES,
+              "too many stages");
+static_assert(Cfg<V_E4M3>::A_SLOTS == 4, "converter groups take A slot (stage index mod 4)");
 
 struct __align__(8) Ctrl {
     uint64_t full[MAX_STAGES];
@@ -239,15 +249,19 @@ MOE_DEVICE uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     return r;
 }
 
-template <bool W8>
-__global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
+template <int V>
+__global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_act_s, const __grid_constant__ CUtensorMap tm_w_s,
                    const TcParams p) {
     // tm_act/tm_w: boxes of normal tiles (or of every tile when all tiles are of one kind);
     // tm_act_s/tm_w_s: boxes of the swap-AB tiles of a mixed launch
-    constexpr int STAGES = Cfg<W8>::STAGES;
-    constexpr int STAGE_BYTES = Cfg<W8>::STAGE_BYTES;
+    constexpr bool W8 = Cfg<V>::W8;
+    constexpr int STAGES = Cfg<V>::STAGES;
+    constexpr int STAGE_BYTES = Cfg<V>::STAGE_BYTES;
+    if constexpr (Cfg<V>::NARROW) {
+        if (!p.swap || p.mixed) return;   // the narrow ring holds swap-AB tiles only (the host never asks more)
+    }
     extern __shared__ uint8_t smem_raw[];
     __shared__ ExpertTable tab;
     __shared__ Ctrl ctrl;
@@ -263,7 +277,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             ptx::mbar_init(&ctrl.full[s], 1);
             ptx::mbar_init(&ctrl.empty[s], W8 ? 4 : 1);   // E4M3: freed by the 4 warps of the converting group
         }
-        for (int a = 0; a < Cfg<W8>::A_SLOTS; ++a) {
+        for (int a = 0; a < Cfg<V>::A_SLOTS; ++a) {
             ptx::mbar_init(&ctrl.conv[a], 5);             // 4 converter warps + the token producer
             ptx::mbar_init(&ctrl.a_empty[a], 1);
         }
@@ -314,17 +328,17 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 const CUtensorMap* mact = (p.mixed && tl.swap) ? &tm_act_s : &tm_act;
                 const CUtensorMap* mw = (p.mixed && tl.swap) ? &tm_w_s : &tm_w;
                 const uint64_t pol_w = tl.swap ? pol_stream : pol_keep;
-                constexpr int KSUB = Cfg<W8>::KSUB;
+                constexpr int KSUB = Cfg<V>::KSUB;
                 const uint32_t wbytes = W8 ? uint32_t(BM * BK * KSUB) : uint32_t(A_BYTES);
                 const uint32_t bytes = W8 ? wbytes
                                           : (tl.swap ? wbytes + uint32_t(nbox * TOK_BOX * BK * 2)
-                                                     : uint32_t(A_BYTES + Cfg<W8>::B_BYTES));
+                                                     : uint32_t(A_BYTES + Cfg<V>::B_BYTES));
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!wait_bar(&ctrl.empty[s], ph ^ 1, ctrl, p.err_word)) break;
                     uint8_t* sa = smem + s * STAGE_BYTES;
-                    uint8_t* sb = sa + Cfg<W8>::B_OFF;
+                    uint8_t* sb = sa + Cfg<V>::B_OFF;
                     ptx::mbar_arrive_expect_tx(&ctrl.full[s], bytes);
                     if (p.skip_first_copy && blockIdx.x == 0 && it == 0) continue;   // bytes that never arrive
                     const int k0 = kb * BK * KSUB;
@@ -371,23 +385,23 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 int n_mma = 256;
                 if (tl.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
                 const uint32_t idesc = ptx::idesc_bf16(BM, n_mma);
-                const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg<W8>::ACC_STRIDE);
+                const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg<V>::ACC_STRIDE);
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     if constexpr (W8) {
                         // A slot a: decoded weights in TMEM, tokens in the slot's smem tile
-                        const int a = it % Cfg<W8>::A_SLOTS;
-                        const uint32_t ph = (it / Cfg<W8>::A_SLOTS) & 1;
+                        const int a = it % Cfg<V>::A_SLOTS;
+                        const uint32_t ph = (it / Cfg<V>::A_SLOTS) & 1;
                         if (!wait_bar(&ctrl.conv[a], ph, ctrl, p.err_word)) { ok = false; break; }
                         ptx::tc_fence_after();
-                        const uint32_t sb = ptx::smem_addr(smem + Cfg<W8>::TOK_OFF + a * Cfg<W8>::TOK_SLOT);
+                        const uint32_t sb = ptx::smem_addr(smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT);
 #pragma unroll
-                        for (int kk = 0; kk < Cfg<W8>::KSUB * BK / UMMA_K; ++kk) {
+                        for (int kk = 0; kk < Cfg<V>::KSUB * BK / UMMA_K; ++kk) {
                             const int sub = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
-                            const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<W8>::B_SUB + kq * UMMA_K * 2);
+                            const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<V>::B_SUB + kq * UMMA_K * 2);
                             // 16 bf16 of a row = 8 TMEM columns per k step
                             const uint32_t a_tmem =
-                                tmem_base + uint32_t(Cfg<W8>::A_TMEM + a * Cfg<W8>::A_COLS + kk * 8);
+                                tmem_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS + kk * 8);
                             ptx::mma_f16_tmem_a(d_tmem, a_tmem, bd, idesc, (kb | kk) != 0);
                         }
                         ptx::mma_commit(&ctrl.a_empty[a]);
@@ -397,7 +411,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                         if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
                         ptx::tc_fence_after();
                         const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
-                        const uint32_t sb = sa + Cfg<W8>::B_OFF;
+                        const uint32_t sb = sa + Cfg<V>::B_OFF;
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                             const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
@@ -419,7 +433,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
         __syncwarp();
     } else if (W8 && warp >= 6) {
         // ------------------------------------------------------------ E4M3 converters and token producer
-        if (warp == Cfg<W8>::TOK_WARP) {
+        if (warp == Cfg<V>::TOK_WARP) {
             // token producer: one lane loads each stage's token rows into A slot (stage % 4) once the MMA
             // has released that slot
             if (lane == 0) {
@@ -428,18 +442,18 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
                     const Tile tl = decode_tile(tab, p, t);
                     const int nbox = (tl.rows + TOK_BOX - 1) / TOK_BOX;
-                    const uint32_t bytes = uint32_t(Cfg<W8>::KSUB * nbox * TOK_BOX * BK * 2);
+                    const uint32_t bytes = uint32_t(Cfg<V>::KSUB * nbox * TOK_BOX * BK * 2);
                     bool ok = true;
                     for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                        const int a = it % Cfg<W8>::A_SLOTS;
-                        const uint32_t ph = (it / Cfg<W8>::A_SLOTS) & 1;
+                        const int a = it % Cfg<V>::A_SLOTS;
+                        const uint32_t ph = (it / Cfg<V>::A_SLOTS) & 1;
                         if (!wait_bar(&ctrl.a_empty[a], ph ^ 1, ctrl, p.err_word)) { ok = false; break; }
                         ptx::mbar_arrive_expect_tx(&ctrl.conv[a], bytes);
-                        uint8_t* dst = smem + Cfg<W8>::TOK_OFF + a * Cfg<W8>::TOK_SLOT;
-                        const int k0 = kb * BK * Cfg<W8>::KSUB;
-                        for (int sub = 0; sub < Cfg<W8>::KSUB; ++sub)
+                        uint8_t* dst = smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT;
+                        const int k0 = kb * BK * Cfg<V>::KSUB;
+                        for (int sub = 0; sub < Cfg<V>::KSUB; ++sub)
                             for (int b = 0; b < nbox; ++b)
-                                ptx::tma_load_2d(dst + sub * Cfg<W8>::B_SUB + b * TOK_BOX * BK * 2, &tm_act,
+                                ptx::tma_load_2d(dst + sub * Cfg<V>::B_SUB + b * TOK_BOX * BK * 2, &tm_act,
                                                  &ctrl.conv[a], k0 + sub * BK, int32_t(tl.row0 + b * TOK_BOX),
                                                  pol_keep);
                     }
@@ -478,7 +492,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                 }
                 if (kb + 16 < p.nkb) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 4 * (kb + 16)));
                 const int s = it % STAGES, a = grp;
-                const uint32_t ph = (it / STAGES) & 1, pha = (it / Cfg<W8>::A_SLOTS) & 1;
+                const uint32_t ph = (it / STAGES) & 1, pha = (it / Cfg<V>::A_SLOTS) & 1;
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
                 if (!wait_bar(&ctrl.a_empty[a], pha ^ 1, ctrl, p.err_word)) { ok = false; break; }
                 ptx::tc_fence_after();   // the MMA that last read this A slot has completed
@@ -513,7 +527,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
                         }
                     }
                     ptx::tmem_st_32x32b_x32(
-                        tmem_base + lane_base + uint32_t(Cfg<W8>::A_TMEM + a * Cfg<W8>::A_COLS + half * 32), o);
+                        tmem_base + lane_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS + half * 32), o);
                 }
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
@@ -537,7 +551,7 @@ __global__ void __launch_bounds__(Cfg<W8>::THREADS, 1)
             const uint32_t aph = (tc >> 1) & 1;
             if (!wait_bar(&ctrl.acc_full[buf], aph, ctrl, p.err_word)) break;
             ptx::tc_fence_after();
-            const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * Cfg<W8>::ACC_STRIDE);
+            const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * Cfg<V>::ACC_STRIDE);
             if (!tl.swap) {
                 const int r = q * 32 + lane;                  // tile row of this thread
                 const bool valid = r < tl.rows;
@@ -755,7 +769,7 @@ bool timeout_test_hook() {
     return on;
 }
 
-template <bool W8>
+template <int V>
 int set_smem_attr() {
     static std::mutex mu;
     static bool done[64] = {};
@@ -763,7 +777,7 @@ int set_smem_attr() {
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && !done[dev]) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<W8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<W8>::SMEM) !=
+        if (cudaFuncSetAttribute(gemm_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<V>::SMEM) !=
             cudaSuccess)
             return fail(MOE_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem) failed");
         done[dev] = true;
@@ -784,7 +798,7 @@ int build_maps(const GemmArgs& g, bool swap, bool w8, int64_t kdim, int64_t wrow
         if (rc) return rc;
     }
     const int64_t es = w8 ? 1 : 2;
-    const cuuint32_t kbox = cuuint32_t(w8 ? BK * Cfg<true>::KSUB : BK);
+    const cuuint32_t kbox = cuuint32_t(w8 ? BK * Cfg<V_E4M3>::KSUB : BK);
     if (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) {
         // view W1[e] (2I, K) as (K, 16, 2, I/16): row = half*I + 16*blk + q
         cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
@@ -809,7 +823,7 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     if (g.gemm == 1 && g.out_dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 GEMM 1 writes bf16 h");
     const int64_t kdim = g.gemm == 1 ? g.K : g.I;
     if (kdim % BK != 0) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: contraction length must be a multiple of 64");
-    if (w8 && kdim % (BK * Cfg<true>::KSUB) != 0)
+    if (w8 && kdim % (BK * Cfg<V_E4M3>::KSUB) != 0)
         return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: E4M3 weights need a contraction length multiple of 128");
     const int64_t wrows = g.gemm == 1 ? 2 * g.I : g.K;   // weight rows per expert
     const int wtile = swap ? 128 : 256;
@@ -857,7 +871,7 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     p.E = g.E;
     p.max_tokens = g.max_tokens;
     p.rows_cap = g.rows_cap;
-    p.nkb = int(kdim / (BK * (w8 ? Cfg<true>::KSUB : 1)));   // stages per tile
+    p.nkb = int(kdim / (BK * (w8 ? Cfg<V_E4M3>::KSUB : 1)));   // stages per tile
     p.nt = int(wrows / wtile);
     p.mixed = mixed ? 1 : 0;
     p.nt_n = int(wrows / 256);
@@ -873,13 +887,16 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     p.out_dtype = g.out_dtype;
     p.out_rows = g.out_rows;
     p.err_word = g.err_word;
-    p.span = swap ? (w8 ? Cfg<true>::TOK_SPAN : Cfg<false>::TOK_SPAN) : BM;
+    // bf16 swap-AB launches use the narrow 8-stage ring (64-token spans)
+    const int variant = w8 ? V_E4M3 : (swap ? V_SWAP64 : V_BF16);
+    p.span = swap ? (variant == V_E4M3 ? Cfg<V_E4M3>::TOK_SPAN : Cfg<V_SWAP64>::TOK_SPAN) : BM;
     p.w_scale = g.w_scale;
     p.wrows = wrows;
     p.nsb = kdim / 32;
     p.skip_first_copy = timeout_test_hook() ? 1 : 0;
 
-    int rc = w8 ? set_smem_attr<true>() : set_smem_attr<false>();
+    int rc = variant == V_E4M3 ? set_smem_attr<V_E4M3>()
+                               : (variant == V_SWAP64 ? set_smem_attr<V_SWAP64>() : set_smem_attr<V_BF16>());
     if (rc) return rc;
     // upper bound on the tiles, then one CTA per SM at most
     const int span = p.span;
@@ -889,12 +906,15 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     const int64_t tiles = segs * p.nt + (mixed ? int64_t(g.E) * p.nt_s : 0);
     if (tiles == 0) return MOE_OK;
     const int grid = int(std::min<int64_t>(tiles, num_sms()));
-    if (w8)
-        gemm_tc_kernel<true><<<grid, Cfg<true>::THREADS, Cfg<true>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
-                                                                                 maps.w_s, p);
+    if (variant == V_E4M3)
+        gemm_tc_kernel<V_E4M3><<<grid, Cfg<V_E4M3>::THREADS, Cfg<V_E4M3>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
+                                                                                     maps.w_s, p);
+    else if (variant == V_SWAP64)
+        gemm_tc_kernel<V_SWAP64><<<grid, Cfg<V_SWAP64>::THREADS, Cfg<V_SWAP64>::SMEM, s>>>(
+            maps.act, maps.w, maps.act_s, maps.w_s, p);
     else
-        gemm_tc_kernel<false><<<grid, Cfg<false>::THREADS, Cfg<false>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
-                                                                                   maps.w_s, p);
+        gemm_tc_kernel<V_BF16><<<grid, Cfg<V_BF16>::THREADS, Cfg<V_BF16>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
+                                                                                     maps.w_s, p);
     return check_launch("gemm_tc_kernel");
 }
 

@@ -151,8 +151,8 @@ class Instance:
         wb = 2 * w.I * w.K * (1 if w.weight == "mxfp8" else 2)
         sb = (2 * w.I * w.K // 32) if w.weight == "mxfp8" else 0
         act = 2 if w.act == "bf16" else 4
-        if w.act_quant:   # E4M3 rows + one scale byte per 32 in, bf16 h out
-            return int(self.used_experts * (wb + sb) + self.routes * (w.K * 33 // 32 + w.I * 2))
+        if w.act_quant:   # MXFP8 rows in, MXFP8 h out (E4M3 codes + one scale byte per 32)
+            return int(self.used_experts * (wb + sb) + self.routes * (w.K + w.I) * 33 // 32)
         return self.used_experts * (wb + sb) + self.routes * (w.K + w.I) * act
 
     def layer_bytes(self):

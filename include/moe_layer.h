@@ -198,8 +198,14 @@ MOE_API int moe_permute_align_static(const int32_t* topk_ids, int64_t T, int top
  *                 swap-AB tiles (K % 128 == 0, 2I % 128 == 0) or MOE_IMPL_SIMT.
  *   w1            (E, 2I, K) of w_dtype (F32, BF16 or E4M3); rows per w1_layout
  *   w1_scale      (E, 2I, K/32) E8M0 bytes when w_dtype == MOE_E4M3, else NULL
- *   h             same row indexing as `a`, (rows, I) of h_dtype (F32 or BF16);
+ *   h             same row indexing as `a`, (rows, I) of h_dtype (F32, BF16, or E4M3 codes);
  *                 only valid rows are written.
+ *   h_scale       h_dtype == MOE_E4M3 ("Fused MoE Modular Kernel", apply(): quantisation
+ *                 between act+mul and W2, done in this call's epilogue): E8M0 scales of h,
+ *                 (rows, I/32), written with h; the codes equal those of
+ *                 mxfp8_quantize_block32 applied to the BF16 h this call would otherwise
+ *                 write.  NULL for F32/BF16 h.  Block-scaled tcgen05 tiles (E4M3 activations)
+ *                 or MOE_IMPL_SIMT.
  *   impl          MOE_IMPL_*; the tcgen05 paths need BF16 activations, BF16 or E4M3
  *                 weights, K % 64 == 0 and I % 64 == 0 (MOE_ERR_UNSUPPORTED otherwise).
  * Counts and offsets stay on the device: the call needs no host synchronisation.
@@ -208,7 +214,7 @@ MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale,
                      const int32_t* expert_counts, const int32_t* expert_offsets,
                      int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
                      const void* w1, const uint8_t* w1_scale, int w_dtype, int w1_layout,
-                     int impl, void* h, int h_dtype, int32_t* err_word, void* stream);
+                     int impl, void* h, int h_dtype, uint8_t* h_scale, int32_t* err_word, void* stream);
 
 /*
  * moe_gemm2 -- grouped GEMM with W2 ("Fused MoE Modular Kernel", apply():

@@ -67,7 +67,7 @@ def load(path: Optional[str] = None):
             "moe_permute_align_static": (I32, [P, I64, I32, I32, I32, I32, I32, P, I32, I64, P, I64, P, P, P, P,
                                                P, P]),
             "moe_gemm1_swiglu": (I32, [P, I32, P, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, I32, I32, P,
-                                       I32, P, P]),
+                                       I32, P, P, P]),
             "moe_gemm2": (I32, [P, I32, P, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, P, P, I32, P, I32, I64,
                                 P, P]),
             "moe_unpermute_topk_reduce": (I32, [P, I32, P, P, I64, I32, I32, I64, P, I32, P]),
@@ -210,23 +210,26 @@ def moe_permute_align_static(topk_ids, E, layout=MOE_LAYOUT_CONTIGUOUS, block_m=
 
 def moe_gemm1_swiglu(a, expert_counts, expert_offsets, w1, I, layout=MOE_LAYOUT_CONTIGUOUS, max_tokens=0,
                      w1_scale=None, w1_layout=MOE_W1_GATE_UP, impl=MOE_IMPL_AUTO, h=None, h_dtype=None,
-                     err_word=None, stream=None, a_scale=None):
-    """a_scale: E8M0 scales when `a` holds E4M3 codes (uint8) of MXFP8 activations."""
+                     err_word=None, stream=None, a_scale=None, h_scale=None):
+    """a_scale: E8M0 scales when `a` holds E4M3 codes (uint8) of MXFP8 activations.
+    h_dtype=MOE_E4M3: h is written as MXFP8 (E4M3 codes + E8M0 scales); returns (h, h_scale) then."""
     E = w1.shape[0]
     K = w1.shape[-1]
     rows_cap = a.shape[0] if layout == MOE_LAYOUT_CONTIGUOUS else E * max_tokens
     a_dt = dtype_code(a, e4m3=a_scale is not None)
     if h_dtype is None:
         h_dtype = MOE_BF16 if a_dt == MOE_E4M3 else a_dt
+    shape = (rows_cap, I) if layout == MOE_LAYOUT_CONTIGUOUS else (E, max_tokens, I)
     if h is None:
-        shape = (rows_cap, I) if layout == MOE_LAYOUT_CONTIGUOUS else (E, max_tokens, I)
-        h = torch.empty(shape, dtype=_TORCH[h_dtype], device=a.device)
+        h = torch.empty(shape, dtype=torch.uint8 if h_dtype == MOE_E4M3 else _TORCH[h_dtype], device=a.device)
+    if h_dtype == MOE_E4M3 and h_scale is None:
+        h_scale = torch.empty(shape[:-1] + (I // 32,), dtype=torch.uint8, device=a.device)
     _check(load().moe_gemm1_swiglu(
         _ptr(a), a_dt, _ptr(a_scale), layout, _ptr(expert_counts), _ptr(expert_offsets), max_tokens, rows_cap, E, K,
         I,
         _ptr(w1), _ptr(w1_scale), dtype_code(w1, e4m3=w1_scale is not None), w1_layout, impl, _ptr(h), h_dtype,
-        _ptr(err_word), _stream(stream)))
-    return h
+        _ptr(h_scale), _ptr(err_word), _stream(stream)))
+    return (h, h_scale) if h_dtype == MOE_E4M3 else h
 
 
 def moe_gemm2(h, expert_counts, expert_offsets, w2, y_rows, layout=MOE_LAYOUT_CONTIGUOUS, max_tokens=0,

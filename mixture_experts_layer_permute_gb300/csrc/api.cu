@@ -152,8 +152,13 @@ int validate_gemm(const GemmArgs& g, const char* name) {
     MOE_REQUIRE(g.a && g.w && g.counts && g.out, MOE_ERR_INVALID_ARG, n + ": null pointer");
     MOE_REQUIRE(aligned16(g.a) && aligned16(g.w) && aligned16(g.out), MOE_ERR_ALIGNMENT,
                 n + ": activation, weight and output pointers must be 16-byte aligned");
-    MOE_REQUIRE((is_float_dtype(g.a_dtype) || g.a_dtype == MOE_E4M3) && is_float_dtype(g.out_dtype),
-                MOE_ERR_UNSUPPORTED, n + ": activations must be F32, BF16 or E4M3; outputs F32 or BF16");
+    MOE_REQUIRE((is_float_dtype(g.a_dtype) || g.a_dtype == MOE_E4M3) &&
+                    (is_float_dtype(g.out_dtype) || (g.gemm == 1 && g.out_dtype == MOE_E4M3)),
+                MOE_ERR_UNSUPPORTED, n + ": activations must be F32, BF16 or E4M3; outputs F32 or BF16 (or E4M3 h)");
+    if (g.out_dtype == MOE_E4M3) {
+        MOE_REQUIRE(g.out_scale, MOE_ERR_INVALID_ARG, n + ": E4M3 h needs an h_scale output");
+        MOE_REQUIRE(g.I % 32 == 0, MOE_ERR_ALIGNMENT, n + ": E4M3 h needs I % 32 == 0");
+    }
     if (g.a_dtype == MOE_E4M3) {
         MOE_REQUIRE(g.a_scale, MOE_ERR_INVALID_ARG, n + ": E4M3 activations need scales");
         MOE_REQUIRE((reinterpret_cast<uintptr_t>(g.a_scale) & 3u) == 0, MOE_ERR_ALIGNMENT,
@@ -231,10 +236,11 @@ int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
 int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale, int layout, const int32_t* expert_counts,
                      const int32_t* expert_offsets, int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
                      const void* w1, const uint8_t* w1_scale, int w_dtype, int w1_layout, int impl, void* h,
-                     int h_dtype, int32_t* err_word, void* stream) {
+                     int h_dtype, uint8_t* h_scale, int32_t* err_word, void* stream) {
     g_last_error.clear();
     GemmArgs g{};
     g.gemm = 1;
+    g.out_scale = h_scale;
     g.a = a;
     g.a_dtype = a_dtype;
     g.a_scale = a_scale;

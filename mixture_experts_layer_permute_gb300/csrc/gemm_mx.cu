@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mx_codec.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -73,6 +74,8 @@ struct __align__(8) Ctrl {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t xq[2];             // fused h quantisation: block maxima of a warp pair exchanged (2 warps)
+    float xmax[2][2][2][16];    // [warp pair][chunk parity][warp of the pair][token of the chunk]
     uint32_t tmem_base;
     volatile int abort;
 };
@@ -99,6 +102,7 @@ struct MxParams {
     const uint8_t* w_scale;   // (E, wrows, kdim/32)
     int64_t wrows;
     int64_t nsb;              // scale bytes per row (kdim / 32)
+    uint8_t* h_scale;         // GEMM 1 with E4M3 h: E8M0 scales (rows_cap, I/32); NULL: bf16 h
 };
 
 MOE_DEVICE bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl& c, int32_t* err_word) {
@@ -161,6 +165,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             ptx::mbar_init(&ctrl.acc_empty[b], 4);
         }
         ptx::mbar_init(&ctrl.drain, 1);
+        ptx::mbar_init(&ctrl.xq[0], 2);
+        ptx::mbar_init(&ctrl.xq[1], 2);
         ctrl.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -300,6 +306,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         uint32_t tc = 0;
+        uint32_t xc = 0;                              // fused h quantisation: chunks exchanged so far
         for (int32_t t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const Tile tl = decode_tile(tab, p, t);
             const int buf = tc & 1;
@@ -310,7 +317,60 @@ __global__ void __launch_bounds__(THREADS, 1)
             // TMEM lane = weight row of the tile, column = token
             const int n_tok = tl.rows;
             const int n_chunks = (n_tok + 15) / 16;
-            if (p.gemm == 1) {
+            if (p.gemm == 1 && p.h_scale) {
+                // MXFP8 h ("Fused MoE Modular Kernel", apply(): quantisation between act+mul and W2, here in
+                // the epilogue): h is rounded to bf16 as the bf16 output would be, a block of 32 units along I
+                // is held by two warps (16 units each: q = 2j, 2j + 1), which exchange their block maxima
+                // through shared memory, then each lane writes its unit's code and lane 0 of the even warp the
+                // scale -- the same codes mxfp8_quantize_block32 makes from the bf16 h.
+                const int64_t unit = int64_t(tl.nb) * 64 + q * 16 + (lane & 15);
+                const int pair = q >> 1, half = q & 1;
+                uint8_t* hc = static_cast<uint8_t*>(p.out);
+                bool ok = true;
+#pragma unroll 1
+                for (int cb = 0; cb < n_chunks; ++cb, ++xc) {
+                    uint32_t v[16];
+                    ptx::tmem_ld_32x32b_x16(tacc + cb * 16, v);
+                    ptx::tmem_ld_wait();
+                    float hv[16], mx[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float mine = __uint_as_float(v[i]);
+                        const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+                        const float g = lane < 16 ? mine : other;
+                        const float u = lane < 16 ? other : mine;
+                        hv[i] = bf16_bits_to_float(float_to_bf16_bits(silu_mul(g, u)));
+                        float m = fabsf(hv[i]);
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                        mx[i] = m;   // max over this warp's 16 units (both lane halves hold the same)
+                    }
+                    const int par = xc & 1;
+                    float* mine_buf = ctrl.xmax[pair][par][half];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (lane == i) mine_buf[i] = mx[i];
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&ctrl.xq[pair]);
+                    if (!wait_bar(&ctrl.xq[pair], xc & 1, ctrl, p.err_word)) { ok = false; break; }
+                    const float* other_buf = ctrl.xmax[pair][par][half ^ 1];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int n = cb * 16 + i;
+                        const float bm = fmaxf(mx[i], other_buf[i]);
+                        const int code = mx_scale_code(bm);
+                        const uint8_t c = uint8_t(mx_cvt_e4m3x2(hv[i] * mx_inv_scale(code), 0.f) & 0xFFu);
+                        if (n < n_tok) {
+                            if (lane < 16) hc[(tl.row0 + n) * p.I + unit] = c;
+                            if (half == 0 && lane == 0)
+                                p.h_scale[(tl.row0 + n) * (p.I / 32) + int64_t(tl.nb) * 2 + pair] = uint8_t(code);
+                        }
+                    }
+                }
+                if (!ok) break;
+            } else if (p.gemm == 1) {
                 // lanes 0..15: gate of unit u, lanes 16..31: up of unit u, u = 64*nb + 16*q + (lane & 15)
                 const int64_t unit = int64_t(tl.nb) * 64 + q * 16 + (lane & 15);
                 uint16_t* h = static_cast<uint16_t*>(p.out);
@@ -478,7 +538,10 @@ int launch_gemm_mx(const GemmArgs& g, cudaStream_t s) {
     if (g.a_dtype != MOE_E4M3 || g.w_dtype != MOE_E4M3)
         return fail(MOE_ERR_UNSUPPORTED, "block-scaled MXFP8 path: E4M3 activations and weights only");
     if (!g.a_scale || !g.w_scale) return fail(MOE_ERR_INVALID_ARG, "block-scaled MXFP8 path: scales missing");
-    if (g.gemm == 1 && g.out_dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "MXFP8 GEMM 1 writes bf16 h");
+    if (g.gemm == 1 && g.out_dtype != MOE_BF16 && g.out_dtype != MOE_E4M3)
+        return fail(MOE_ERR_UNSUPPORTED, "MXFP8 GEMM 1 writes bf16 or MXFP8 h");
+    if (g.gemm == 1 && g.out_dtype == MOE_E4M3 && !g.out_scale)
+        return fail(MOE_ERR_INVALID_ARG, "MXFP8 h needs its scale output");
     const int64_t kdim = g.gemm == 1 ? g.K : g.I;
     if (kdim % KS != 0)
         return fail(MOE_ERR_UNSUPPORTED, "block-scaled MXFP8 path: contraction length must be a multiple of 128");
@@ -535,6 +598,7 @@ int launch_gemm_mx(const GemmArgs& g, cudaStream_t s) {
     p.w_scale = g.w_scale;
     p.wrows = wrows;
     p.nsb = kdim / 32;
+    p.h_scale = (g.gemm == 1 && g.out_dtype == MOE_E4M3) ? g.out_scale : nullptr;
 
     int rc = set_smem_attr();
     if (rc) return rc;

@@ -12,6 +12,7 @@
 // no host copy of the counts.
 #include "common.cuh"
 #include "internal.h"
+#include "mx_codec.cuh"
 
 namespace moe {
 
@@ -125,11 +126,39 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) Cs[ty * 4 + i][tx * 4 + j] = acc[i][j];
         __syncthreads();
-        for (int idx = tid; idx < BM * (BN / 2); idx += 256) {
-            const int r = idx / (BN / 2), u = idx % (BN / 2);
-            const int64_t unit = n0 + u;
-            if (r < valid && unit < g.I)
-                store_from_float<ODT>(g.out, (row0 + r) * ncols_out + unit, silu_mul(Cs[r][u], Cs[r][u + 32]));
+        if constexpr (ODT == MOE_E4M3) {
+            // MXFP8 h: the tile's 32 units (n0 % 32 == 0, I % 32 == 0) are one scale block of each row; one
+            // thread per row rounds h to bf16, finds the block maximum and writes 32 codes and the scale
+            const int r = tid;
+            if (r < BM && r < valid && n0 + 32 <= g.I) {
+                float hv[32];
+                float m = 0.f;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    hv[u] = bf16_bits_to_float(float_to_bf16_bits(silu_mul(Cs[r][u], Cs[r][u + 32])));
+                    m = fmaxf(m, fabsf(hv[u]));
+                }
+                const int code = mx_scale_code(m);
+                const float inv = mx_inv_scale(code);
+                uint32_t packed[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t lo = mx_cvt_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv);
+                    const uint32_t hi = mx_cvt_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv);
+                    packed[i] = lo | (hi << 16);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.out) + (row0 + r) * g.I + n0);
+                dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                g.out_scale[(row0 + r) * (g.I / 32) + n0 / 32] = uint8_t(code);
+            }
+        } else {
+            for (int idx = tid; idx < BM * (BN / 2); idx += 256) {
+                const int r = idx / (BN / 2), u = idx % (BN / 2);
+                const int64_t unit = n0 + u;
+                if (r < valid && unit < g.I)
+                    store_from_float<ODT>(g.out, (row0 + r) * ncols_out + unit, silu_mul(Cs[r][u], Cs[r][u + 32]));
+            }
         }
     } else {
 #pragma unroll
@@ -159,6 +188,12 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
 
 template <int GEMM, int ADT, int WDT>
 cudaError_t launch3(const GemmArgs& g, dim3 grid, cudaStream_t s) {
+    if constexpr (GEMM == 1) {
+        if (g.out_dtype == MOE_E4M3) {
+            gemm_simt_kernel<GEMM, ADT, WDT, MOE_E4M3><<<grid, 256, 0, s>>>(g);
+            return cudaGetLastError();
+        }
+    }
     if (g.out_dtype == MOE_F32) gemm_simt_kernel<GEMM, ADT, WDT, MOE_F32><<<grid, 256, 0, s>>>(g);
     else gemm_simt_kernel<GEMM, ADT, WDT, MOE_BF16><<<grid, 256, 0, s>>>(g);
     return cudaGetLastError();

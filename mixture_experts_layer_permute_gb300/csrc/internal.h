@@ -59,6 +59,7 @@ struct GemmArgs {
     const float* route_w;       // gemm 2, optional
     void* out;
     int out_dtype;
+    uint8_t* out_scale;     // GEMM 1 with E4M3 h: E8M0 scales of h (rows, I/32)
     int64_t out_rows;
     int32_t* err_word;
 };

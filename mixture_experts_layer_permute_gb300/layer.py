@@ -10,8 +10,8 @@ intermediates are declared up front and reused), and ``forward`` issues
 with, for MXFP8 weights and ``act_quant=True``, the activations quantised on
 the fly so that both GEMMs run block-scaled MXFP8 x MXFP8:
 
-    ... moe_permute_align -> mxfp8_quantize_block32 (x rows) -> moe_gemm1_swiglu
-        -> mxfp8_quantize_block32 (h) -> moe_gemm2 -> moe_unpermute_topk_reduce
+    ... moe_permute_align -> mxfp8_quantize_block32 (x rows) -> moe_gemm1_swiglu (h written as MXFP8
+        by its epilogue) -> moe_gemm2 -> moe_unpermute_topk_reduce
 
 or, for the batched layout fed with expert-major rows (T = 0),
 
@@ -124,8 +124,8 @@ class MoELayer:
             mt = self.max_tokens
             calls.append((lib.moe_gemm1_swiglu, (x.data_ptr(), adt, None, self.layout, counts.data_ptr(), None, mt,
                                                  self.rows_cap, E, K, I, w1.data_ptr(), _p(w1_scale), wdt,
-                                                 w1_layout, self.impl, self.h.data_ptr(), adt, self.err.data_ptr(),
-                                                 stream), "gemm1"))
+                                                 w1_layout, self.impl, self.h.data_ptr(), adt, None,
+                                                 self.err.data_ptr(), stream), "gemm1"))
             rw = row_weights if self.weight_in_gemm2 else None
             calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, None, self.layout, counts.data_ptr(), None, mt,
                                           self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, None, _p(rw),
@@ -157,17 +157,15 @@ class MoELayer:
             a1, a1dt, a1s = self.x_codes.data_ptr(), B.MOE_E4M3, self.x_scales.data_ptr()
         else:
             a1, a1dt, a1s = self.x_perm.data_ptr(), adt, None
+        if self.act_quant:   # GEMM 1's epilogue writes h as MXFP8 (codes + scales)
+            hout, hdt, hs = self.h_codes.data_ptr(), B.MOE_E4M3, self.h_scales.data_ptr()
+        else:
+            hout, hdt, hs = self.h.data_ptr(), adt, None
         calls.append((lib.moe_gemm1_swiglu, (a1, a1dt, a1s, self.layout, self.counts.data_ptr(),
                                              self.offsets.data_ptr(), 0, self.rows_cap, E, K, I, w1.data_ptr(),
-                                             _p(w1_scale), wdt, w1_layout, self.impl, self.h.data_ptr(), adt,
+                                             _p(w1_scale), wdt, w1_layout, self.impl, hout, hdt, hs,
                                              self.err.data_ptr(), stream), "gemm1"))
-        if self.act_quant:
-            calls.append((lib.mxfp8_quantize_block32, (self.h.data_ptr(), adt, self.rows_cap, I,
-                                                       self.h_codes.data_ptr(), self.h_scales.data_ptr(), stream),
-                          "quant_h"))
-            a2, a2dt, a2s = self.h_codes.data_ptr(), B.MOE_E4M3, self.h_scales.data_ptr()
-        else:
-            a2, a2dt, a2s = self.h.data_ptr(), adt, None
+        a2, a2dt, a2s = hout, hdt, hs
         rw = weights if self.weight_in_gemm2 else None
         calls.append((lib.moe_gemm2, (a2, a2dt, a2s, self.layout, self.counts.data_ptr(),
                                       self.offsets.data_ptr(), 0, self.rows_cap, E, K, I, w2.data_ptr(),
@@ -196,8 +194,8 @@ class MoELayer:
                                               self.workspace.numel(), self.err.data_ptr(), stream), "permute"))
         calls.append((lib.moe_gemm1_swiglu, (self.x_perm.data_ptr(), adt, None, self.layout, self.counts.data_ptr(), None,
                                              mt, self.rows_cap, E, K, I, w1.data_ptr(), _p(w1_scale), wdt,
-                                             w1_layout, self.impl, self.h.data_ptr(), adt, self.err.data_ptr(),
-                                             stream), "gemm1"))
+                                             w1_layout, self.impl, self.h.data_ptr(), adt, None,
+                                             self.err.data_ptr(), stream), "gemm1"))
         calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, None, self.layout, self.counts.data_ptr(), None, mt,
                                       self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, None, None,
                                       self.impl, self.y.data_ptr(), adt, self.rows_cap, self.err.data_ptr(),
@@ -247,7 +245,7 @@ class MoELayer:
             return 2 if self.weight_in_gemm2 else 3
         n = 3 + 1 + (1 if self.T * self.top_k <= 1024 else 2) + 1   # gemm1 gemm2 reduce, gather, permute, route
         if self.act_quant:
-            n += 2                                                    # quantise x rows and h
+            n += 1                                                    # quantise x rows (h: in GEMM 1)
         return n if any(name == "route" for _, _, name in (self._plan or [])) else n - 1
 
     def device_errors(self, reset: bool = True) -> int:

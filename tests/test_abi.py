@@ -106,14 +106,14 @@ def test_permute_validation(lib):
 def test_gemm_validation(lib):
     fake = ctypes.c_void_p(0x1000)
     # K not a multiple of 32
-    rc = lib.moe_gemm1_swiglu(fake, 1, None, 0, fake, fake, 0, 64, 4, 100, 64, fake, None, 1, 0, 0, fake, 1, None, None)
+    rc = lib.moe_gemm1_swiglu(fake, 1, None, 0, fake, fake, 0, 64, 4, 100, 64, fake, None, 1, 0, 0, fake, 1, None, None, None)
     assert rc == 3 and "multiples of 32" in lib_error()
     # E4M3 weights without scales
-    rc = lib.moe_gemm1_swiglu(fake, 1, None, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 2, 0, 0, fake, 1, None, None)
+    rc = lib.moe_gemm1_swiglu(fake, 1, None, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 2, 0, 0, fake, 1, None, None, None)
     assert rc == 1
     # misaligned activations
     rc = lib.moe_gemm1_swiglu(ctypes.c_void_p(0x1002), 1, None, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, 0, 0,
-                              fake, 1, None, None)
+                              fake, 1, None, None, None)
     assert rc == 3
     # contiguous gemm2 needs row_route
     rc = lib.moe_gemm2(fake, 1, None, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, None, None, 0, fake, 1, 10, None,
@@ -124,18 +124,22 @@ def test_gemm_validation(lib):
                        None)
     assert rc == 1
     # E4M3 activations: scales required, E4M3 weights required, normal tiles refused
-    rc = lib.moe_gemm1_swiglu(fake, 2, None, 0, fake, fake, 0, 64, 4, 128, 64, fake, fake, 2, 0, 0, fake, 1, None,
+    rc = lib.moe_gemm1_swiglu(fake, 2, None, 0, fake, fake, 0, 64, 4, 128, 64, fake, fake, 2, 0, 0, fake, 1, None, None,
                               None)
     assert rc == 1 and "scales" in lib_error()
-    rc = lib.moe_gemm1_swiglu(fake, 2, fake, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, 0, 0, fake, 1, None,
+    rc = lib.moe_gemm1_swiglu(fake, 2, fake, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, 0, 0, fake, 1, None, None,
                               None)
     assert rc == 2 and "E4M3 weights" in lib_error()
     rc = lib.moe_gemm1_swiglu(fake, 2, ctypes.c_void_p(0x1001), 0, fake, fake, 0, 64, 4, 128, 64, fake, fake, 2, 0,
-                              0, fake, 1, None, None)
+                              0, fake, 1, None, None, None)
     assert rc == 3
     rc = lib.moe_gemm2(fake, 2, fake, 0, fake, fake, 0, 64, 4, 128, 128, fake, fake, 2, fake, None, 1, fake, 1, 10,
                        None, None)
     assert rc == 2 and "swap-AB" in lib_error()
+    # E4M3 h needs its scale output
+    rc = lib.moe_gemm1_swiglu(fake, 2, fake, 0, fake, fake, 0, 64, 4, 128, 64, fake, fake, 2, 0, 0, fake, 2, None,
+                              None, None)
+    assert rc == 1 and "h_scale" in lib_error()
 
 
 def test_reduce_and_quant_validation(lib):

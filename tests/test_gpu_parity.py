@@ -435,6 +435,27 @@ def test_gemm2_mxf8(moe, impl, shape):
     assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 mxf8 {impl}")
 
 
+@pytest.mark.parametrize("impl", ["swap_ab", "simt"])
+@pytest.mark.parametrize("shape", MX_SHAPES)
+@pytest.mark.parametrize("w1_layout", [0, 1])
+def test_gemm1_mxf8_fused_h_quant(moe, impl, shape, w1_layout):
+    """h written as MXFP8 by GEMM 1's epilogue equals, bit for bit, mxfp8_quantize_block32 of the bf16 h the
+    same GEMM writes otherwise (codes and scales of every valid row)."""
+    T, k, E, K, I = shape
+    w, x, ids, _ = _routed(T, k, E, K, seed=T + 7 * E)
+    W1 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8", w_std=0.05), "W1", 13)
+    c1, s1, _, _ = _e4m3_weights(moe, W1)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    xc, xs = moe.mxfp8_quantize_block32(res["x_out"])
+    kw = dict(w1_scale=s1, a_scale=xs, w1_layout=w1_layout, impl=_impl(moe, impl))
+    h = moe.moe_gemm1_swiglu(xc, res["counts"], res["offsets"], c1, I, **kw)
+    rc, rs = moe.mxfp8_quantize_block32(h)
+    hc, hs = moe.moe_gemm1_swiglu(xc, res["counts"], res["offsets"], c1, I, h_dtype=moe.MOE_E4M3, **kw)
+    rows = res["route_row"].view(-1).long()
+    assert torch.equal(hc[rows], rc[rows]) and torch.equal(hs[rows], rs[rows])
+    assert int((hs[rows] > 0).sum()) > 0
+
+
 def test_mxf8_refuses_normal_tiles(moe):
     T, k, E, K, I = 64, 2, 4, 256, 128
     w, x, ids, _ = _routed(T, k, E, K, seed=12)

@@ -243,6 +243,44 @@ MOE_DEVICE void dequant4(uint32_t w, uint32_t f1, uint32_t& lo, uint32_t& hi) {
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(f1));
 }
 
+// Normal-tile GEMM 1 epilogue, one 32-column chunk c of a row: columns [gate16, up16] of units
+// 128*nb + 16*c .. +15 -> 16 bf16 values of h.
+MOE_DEVICE void store_h_chunk(const TcParams& p, const uint32_t (&v)[32], bool valid, int64_t row, int nb, int c) {
+    if (!valid) return;
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float h0 = silu_mul(__uint_as_float(v[2 * i]), __uint_as_float(v[16 + 2 * i]));
+        const float h1 = silu_mul(__uint_as_float(v[2 * i + 1]), __uint_as_float(v[16 + 2 * i + 1]));
+        o[i] = pack_bf16x2(h0, h1);
+    }
+    const int64_t unit = int64_t(nb) * 128 + c * 16;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.I + unit);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Normal-tile GEMM 2 epilogue, one 32-column chunk c of a row: weight times the 32 outputs, written to the
+// route's row of y.
+MOE_DEVICE void store_y_chunk(const TcParams& p, const uint32_t (&v)[32], int64_t dst_row, float wt, int nb, int c) {
+    if (dst_row < 0) return;
+    const int64_t col = int64_t(nb) * 256 + c * 32;
+    if (p.out_dtype == MOE_BF16) {
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(wt * __uint_as_float(v[2 * i]), wt * __uint_as_float(v[2 * i + 1]));
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + dst_row * p.K + col);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + dst_row * p.K + col);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(wt * __uint_as_float(v[4 * i]), wt * __uint_as_float(v[4 * i + 1]),
+                                 wt * __uint_as_float(v[4 * i + 2]), wt * __uint_as_float(v[4 * i + 3]));
+    }
+}
+
 MOE_DEVICE uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -553,71 +591,40 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             ptx::tc_fence_after();
             const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * Cfg<V>::ACC_STRIDE);
             if (!tl.swap) {
+              if constexpr (V == V_BF16) {   // the other variants run swap-AB tiles only
                 const int r = q * 32 + lane;                  // tile row of this thread
                 const bool valid = r < tl.rows;
                 const int64_t row = tl.row0 + r;
-                if (p.gemm == 1) {
-                    uint16_t* h = static_cast<uint16_t*>(p.out);
-#pragma unroll 1
-                    for (int c = 0; c < ACC_COLS / 32; ++c) {
-                        uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(tacc + c * 32, v);
-                        ptx::tmem_ld_wait();
-                        if (valid) {
-                            uint32_t o[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float h0 = silu_mul(__uint_as_float(v[2 * i]), __uint_as_float(v[16 + 2 * i]));
-                                const float h1 =
-                                    silu_mul(__uint_as_float(v[2 * i + 1]), __uint_as_float(v[16 + 2 * i + 1]));
-                                o[i] = pack_bf16x2(h0, h1);
-                            }
-                            const int64_t unit = int64_t(tl.nb) * 128 + c * 16;
-                            uint4* dst = reinterpret_cast<uint4*>(h + row * p.I + unit);
-                            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                int64_t dst_row = -1;                         // GEMM 2: destination row, weight
+                float wt = 1.f;
+                if (p.gemm == 2 && valid) {
+                    if (p.layout == MOE_LAYOUT_CONTIGUOUS) {
+                        const int32_t route = p.row_route[row];
+                        if (route >= 0 && route < p.out_rows) {
+                            dst_row = route;
+                            if (p.route_w) wt = p.route_w[route];
                         }
-                    }
-                } else {
-                    int64_t dst_row = -1;
-                    float wt = 1.f;
-                    if (valid) {
-                        if (p.layout == MOE_LAYOUT_CONTIGUOUS) {
-                            const int32_t route = p.row_route[row];
-                            if (route >= 0 && route < p.out_rows) {
-                                dst_row = route;
-                                if (p.route_w) wt = p.route_w[route];
-                            }
-                        } else {
-                            dst_row = row;
-                            if (p.route_w) wt = p.route_w[row];
-                        }
-                    }
-#pragma unroll 1
-                    for (int c = 0; c < ACC_COLS / 32; ++c) {
-                        uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(tacc + c * 32, v);
-                        ptx::tmem_ld_wait();
-                        if (dst_row >= 0) {
-                            const int64_t col = int64_t(tl.nb) * 256 + c * 32;
-                            if (p.out_dtype == MOE_BF16) {
-                                uint32_t o[16];
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    o[i] = pack_bf16x2(wt * __uint_as_float(v[2 * i]), wt * __uint_as_float(v[2 * i + 1]));
-                                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + dst_row * p.K + col);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                            } else {
-                                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + dst_row * p.K + col);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    dst[i] = make_float4(wt * __uint_as_float(v[4 * i]), wt * __uint_as_float(v[4 * i + 1]),
-                                                         wt * __uint_as_float(v[4 * i + 2]), wt * __uint_as_float(v[4 * i + 3]));
-                            }
-                        }
+                    } else {
+                        dst_row = row;
+                        if (p.route_w) wt = p.route_w[row];
                     }
                 }
+                // 8 chunks of 32 columns; chunk c + 1 is read from TMEM while chunk c is converted and stored
+                uint32_t va[32], vb[32];
+                ptx::tmem_ld_32x32b_x32(tacc, va);
+                ptx::tmem_ld_wait_regs(va);
+#pragma unroll 1
+                for (int c = 0; c < ACC_COLS / 32; c += 2) {
+                    ptx::tmem_ld_32x32b_x32(tacc + (c + 1) * 32, vb);
+                    if (p.gemm == 1) store_h_chunk(p, va, valid, row, tl.nb, c);
+                    else store_y_chunk(p, va, dst_row, wt, tl.nb, c);
+                    ptx::tmem_ld_wait_regs(vb);
+                    if (c + 2 < ACC_COLS / 32) ptx::tmem_ld_32x32b_x32(tacc + (c + 2) * 32, va);
+                    if (p.gemm == 1) store_h_chunk(p, vb, valid, row, tl.nb, c + 1);
+                    else store_y_chunk(p, vb, dst_row, wt, tl.nb, c + 1);
+                    if (c + 2 < ACC_COLS / 32) ptx::tmem_ld_wait_regs(va);
+                }
+              }
             } else {
                 // swap-AB: TMEM lane = weight row of the tile, column = token
                 const int n_tok = tl.rows;

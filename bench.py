@@ -73,7 +73,7 @@ def read_peaks():
 class Instance:
     """Device inputs and the layer object of one workload."""
 
-    def __init__(self, w, seed, device):
+    def __init__(self, w, seed, device, fused=True):
         import torch
         import mixture_experts_layer_permute_gb300 as m
         from mixture_experts_layer_permute_gb300 import workloads as wl
@@ -109,7 +109,7 @@ class Instance:
                                     layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens, device=dev)
         else:
             self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
-                                    act_quant=w.act_quant, device=dev)
+                                    act_quant=w.act_quant, fused_experts=fused, device=dev)
         self.forward()
         torch.cuda.synchronize()
         ids = self.layer.ids if self.logits is not None else self.ids
@@ -167,6 +167,13 @@ class Instance:
 
     def layer_flops(self):
         return 6.0 * self.w.K * self.w.I * self.routes
+
+    def gemm2_bytes(self):
+        w = self.w
+        return self.used_experts * w.K * w.I * 2 + self.routes * (w.I + w.K) * 2
+
+    def fused(self):
+        return any(name == "gemm1" and fn is self.layer.lib.moe_experts_fused for fn, _, name in (self.layer._plan or []))
 
     def gemm1_flops(self):
         return 4.0 * self.w.K * self.w.I * self.routes
@@ -303,7 +310,7 @@ def kernel_source_hash(name="gemm_tc.cu"):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, fused=False):
     """GEMM 1 DRAM bytes per launch from the committed ncu summary, if taken on this kernel source.
 
     profiles/gemm_{tc,mx}_traffic_<workload>.txt holds `source <file>`, `source_sha <hash>` (or the older
@@ -325,6 +332,8 @@ def recorded_traffic(workload):
         sha = (fields.get("source_sha") or fields.get("gemm_tc_sha") or [None])[0]
         if sha != kernel_source_hash(src) or fields.get("workload", [None])[0] != workload:
             continue
+        if fields.get("experts", ["split"])[0] != ("fused" if fused else "split"):
+            continue
         vals = [int(v) for v in fields.get("gemm1_traffic_bytes", [])]
         if vals:
             return vals
@@ -345,7 +354,7 @@ def run_ours(args, rank, world, local_rank):
     if args.experts:
         from mixture_experts_layer_permute_gb300 import workloads as wl
         ws = [wl.scaled(w, E=args.experts) for w in ws]
-    insts = [Instance(w, args.seed, dev) for w in ws]
+    insts = [Instance(w, args.seed, dev, fused=not args.split_experts) for w in ws]
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
@@ -410,7 +419,7 @@ def run_ours(args, rank, world, local_rank):
     # GEMM 1 roofline (HBM bound for decode/mxfp8/batched, tensor bound for prefill)
     hbm, tf_burst, tf_sust, peak_kind = read_peaks()
     g1_ms = [sum(a.elapsed_time(b) for a, b in e) / args.steps for e in ev]
-    g1_bytes = [i.gemm1_bytes() for i in insts]
+    g1_bytes = [i.gemm1_bytes() + (i.gemm2_bytes() if i.fused() else 0) for i in insts]
     g1_flops = [i.gemm1_flops() for i in insts]
     prefill = args.workload == "prefill"
     if prefill:
@@ -423,9 +432,11 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4)}
     mx = any(i.w.act_quant for i in insts)
-    roof["kernel"] = ("gemm_mx_kernel" if mx else "gemm_tc_kernel") + " (moe_gemm1_swiglu)"
+    fused = any(i.fused() for i in insts)
+    roof["kernel"] = ("gemm_mx_kernel" if mx else "gemm_tc_kernel") + (
+        " (moe_experts_fused: GEMM 1 + GEMM 2 in one launch)" if fused else " (moe_gemm1_swiglu)")
     roof["peak_source"] = f"MEASURED_PEAKS.json ({peak_kind})" + (", sustained bf16" if prefill else "")
-    roof["traffic"] = recorded_traffic(args.workload)
+    roof["traffic"] = recorded_traffic(args.workload, fused)
     roof["algorithmic_per_launch"] = [int(b) for b in (g1_flops if prefill else g1_bytes)]
     roof["launch_ms"] = [round(x, 4) for x in g1_ms]
 
@@ -627,6 +638,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="issue the timed steps from Python, not as a CUDA graph")
+    ap.add_argument("--split-experts", action="store_true",
+                    help="run GEMM 1 and GEMM 2 as two launches even where the plan uses swap-AB tiles (by default "
+                         "they are one launch, moe_experts_fused)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: fewer experts than the workload (a small case for ncu)")
     args = ap.parse_args()

@@ -246,6 +246,36 @@ MOE_API int moe_gemm2(const void* h, int h_dtype, const uint8_t* h_scale, int la
               int impl, void* y, int y_dtype, int64_t y_rows, int32_t* err_word, void* stream);
 
 /*
+ * moe_experts_fused -- moe_gemm1_swiglu followed by moe_gemm2 in ONE launch
+ * (the "model kernel" of the two-kernel run in the "Cake MegaMoE EP16"
+ * FlashInfer PR 5148 analysis, section 4: the experts' GEMMs, then a separate
+ * ordered Top-K reduce).  For the decode regime (few tokens per expert):
+ * bf16 activations and weights, swap-AB tcgen05 tiles, contiguous layout.
+ * GEMM 1 tiles run first; the GEMM 2 tiles of a token segment start once the
+ * GEMM 1 tiles of that segment have written their h, so GEMM 2's weights
+ * stream while GEMM 1's last tiles finish and no second launch is paid.
+ * Results equal moe_gemm1_swiglu + moe_gemm2 with MOE_IMPL_TCGEN05_SWAP_AB.
+ *
+ *   a, counts, offsets, rows_cap, E, K, I, w1, w1_layout   as moe_gemm1_swiglu
+ *   w2, row_route, route_weights, y, y_dtype, y_rows        as moe_gemm2 (contiguous)
+ *   a_dtype, w_dtype   MOE_BF16
+ *   h          caller-owned (rows_cap, I) BF16 buffer for the intermediate; must not
+ *              alias a or y; holds h on return
+ *   workspace  >= moe_experts_fused_workspace_size(rows_cap, E) bytes, 256-byte
+ *              aligned; cleared by the call (an asynchronous memset on `stream`)
+ *   K % 128 == 0, I % 64 == 0; an sm_100+ device.
+ * The launch is cooperative (every CTA resident); a wait that runs out sets
+ * MOE_DEVERR_TIMEOUT after 2 s instead of hanging.
+ */
+MOE_API size_t moe_experts_fused_workspace_size(int64_t rows_cap, int E);
+MOE_API int moe_experts_fused(const void* a, int a_dtype, const int32_t* expert_counts,
+                              const int32_t* expert_offsets, int64_t rows_cap, int E, int64_t K, int64_t I,
+                              const void* w1, int w1_layout, const void* w2, int w_dtype,
+                              const int32_t* row_route, const float* route_weights, void* h, void* y,
+                              int y_dtype, int64_t y_rows, void* workspace, size_t workspace_bytes,
+                              int32_t* err_word, void* stream);
+
+/*
  * moe_unpermute_topk_reduce -- ordered TopK weight-and-reduce
  * ("Fused MoE Modular Kernel", TopKWeightAndReduce, Contiguous; "Cake
  * MegaMoE EP16" analysis, section 4: a separate ordered Top-K reduce kernel).

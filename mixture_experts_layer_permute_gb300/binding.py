@@ -31,6 +31,7 @@ EXPORTED = [
     "moe_last_error", "moe_version", "moe_max_padded_rows", "moe_permute_workspace_size", "moe_topk_route",
     "moe_permute_align", "moe_permute_align_static", "moe_gemm1_swiglu", "moe_gemm2", "moe_unpermute_topk_reduce",
     "moe_batched_weight_reduce", "moe_batched_topk_reduce", "mxfp8_quantize_block32",
+    "moe_experts_fused_workspace_size", "moe_experts_fused",
 ]
 
 
@@ -61,6 +62,9 @@ def load(path: Optional[str] = None):
             "moe_version": (I32, []),
             "moe_max_padded_rows": (I64, [I64, I32, I32, I32]),
             "moe_permute_workspace_size": (SZ, [I64, I32, I32]),
+            "moe_experts_fused_workspace_size": (SZ, [I64, I32]),
+            "moe_experts_fused": (I32, [P, I32, P, P, I64, I32, I64, I64, P, I32, P, I32, P, P, P, P, I32, I64, P,
+                                        SZ, P, P]),
             "moe_topk_route": (I32, [P, I64, I32, I32, I32, P, P, P]),
             "moe_permute_align": (I32, [P, I64, I32, I32, I32, I32, I32, P, I32, I64, P, I64, P, P, P, P, P, SZ,
                                         P, P]),
@@ -250,6 +254,32 @@ def moe_gemm2(h, expert_counts, expert_offsets, w2, y_rows, layout=MOE_LAYOUT_CO
         _ptr(w2), _ptr(w2_scale), dtype_code(w2, e4m3=w2_scale is not None), _ptr(row_route), _ptr(route_weights),
         impl, _ptr(y), y_dtype, y_rows, _ptr(err_word), _stream(stream)))
     return y
+
+
+def moe_experts_fused_workspace_size(rows_cap: int, E: int) -> int:
+    return load().moe_experts_fused_workspace_size(rows_cap, E)
+
+
+def moe_experts_fused(a, expert_counts, expert_offsets, w1, w2, I, row_route, y_rows, route_weights=None,
+                      w1_layout=MOE_W1_GATE_UP, h=None, y=None, y_dtype=None, workspace=None, err_word=None,
+                      stream=None):
+    """GEMM 1 + GEMM 2 in one launch (bf16, contiguous layout, swap-AB tiles).  Returns (h, y)."""
+    E, K, _ = w2.shape
+    rows_cap = a.shape[0]
+    if y_dtype is None:
+        y_dtype = dtype_code(a)
+    if h is None:
+        h = torch.empty((rows_cap, I), dtype=torch.bfloat16, device=a.device)
+    if y is None:
+        y = torch.empty((y_rows, K), dtype=_TORCH[y_dtype], device=a.device)
+    if workspace is None:
+        workspace = torch.empty(max(moe_experts_fused_workspace_size(rows_cap, E), 256), dtype=torch.uint8,
+                                device=a.device)
+    _check(load().moe_experts_fused(
+        _ptr(a), dtype_code(a), _ptr(expert_counts), _ptr(expert_offsets), rows_cap, E, K, I, _ptr(w1), w1_layout,
+        _ptr(w2), dtype_code(w2), _ptr(row_route), _ptr(route_weights), _ptr(h), _ptr(y), y_dtype, y_rows,
+        _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream)))
+    return h, y
 
 
 def moe_unpermute_topk_reduce(y, topk_ids, E, topk_weights=None, out=None, out_dtype=None, stream=None):

@@ -304,6 +304,59 @@ int moe_gemm2(const void* hh, int h_dtype, const uint8_t* h_scale, int layout, c
     return run_gemm(g, impl, as_stream(stream), "moe_gemm2");
 }
 
+size_t moe_experts_fused_workspace_size(int64_t rows_cap, int E) {
+    if (rows_cap < 0 || E < 1) return 0;
+    return experts_fused_workspace_bytes(rows_cap, E);
+}
+
+int moe_experts_fused(const void* a, int a_dtype, const int32_t* expert_counts, const int32_t* expert_offsets,
+                      int64_t rows_cap, int E, int64_t K, int64_t I, const void* w1, int w1_layout, const void* w2,
+                      int w_dtype, const int32_t* row_route, const float* route_weights, void* h, void* y,
+                      int y_dtype, int64_t y_rows, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                      void* stream) {
+    g_last_error.clear();
+    GemmArgs g1{};
+    g1.gemm = 1;
+    g1.a = a;
+    g1.a_dtype = a_dtype;
+    g1.layout = MOE_LAYOUT_CONTIGUOUS;
+    g1.counts = expert_counts;
+    g1.offsets = expert_offsets;
+    g1.rows_cap = rows_cap;
+    g1.E = E;
+    g1.K = K;
+    g1.I = I;
+    g1.w = w1;
+    g1.w_dtype = w_dtype;
+    g1.w1_layout = w1_layout;
+    g1.out = h;
+    g1.out_dtype = MOE_BF16;
+    g1.err_word = err_word;
+    int rc = validate_gemm(g1, "moe_experts_fused");
+    if (rc) return rc;
+    GemmArgs g2 = g1;
+    g2.gemm = 2;
+    g2.a = h;
+    g2.w = w2;
+    g2.w1_layout = 0;
+    g2.row_route = row_route;
+    g2.route_w = route_weights;
+    g2.out = y;
+    g2.out_dtype = y_dtype;
+    g2.out_rows = y_rows;
+    rc = validate_gemm(g2, "moe_experts_fused");
+    if (rc) return rc;
+    MOE_REQUIRE(w1_layout == MOE_W1_GATE_UP || w1_layout == MOE_W1_INTERLEAVE16, MOE_ERR_INVALID_ARG,
+                "moe_experts_fused: unknown w1_layout");
+    MOE_REQUIRE(row_route, MOE_ERR_INVALID_ARG, "moe_experts_fused: row_route is required");
+    MOE_REQUIRE(y_rows >= 0, MOE_ERR_INVALID_ARG, "moe_experts_fused: y_rows < 0");
+    MOE_REQUIRE(h != a && h != y, MOE_ERR_INVALID_ARG, "moe_experts_fused: h must not alias a or y");
+    MOE_REQUIRE(workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, MOE_ERR_ALIGNMENT,
+                "moe_experts_fused: workspace must be 256-byte aligned");
+    MOE_REQUIRE(device_cc() >= 100, MOE_ERR_UNSUPPORTED, "moe_experts_fused: tcgen05 needs an sm_100+ device");
+    return launch_experts_fused(g1, g2, static_cast<int32_t*>(workspace), workspace_bytes, as_stream(stream));
+}
+
 int moe_unpermute_topk_reduce(const void* y, int y_dtype, const int32_t* topk_ids, const float* topk_weights,
                               int64_t T, int top_k, int E, int64_t K, void* out, int out_dtype, void* stream) {
     g_last_error.clear();

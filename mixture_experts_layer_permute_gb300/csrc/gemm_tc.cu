@@ -155,6 +155,13 @@ struct TcParams {
     int64_t wrows;       // weight rows per expert
     int64_t nsb;         // scale bytes per weight row (kdim / 32)
     int skip_first_copy; // test hook: CTA 0 never issues its first weight copy (see timeout_test_hook)
+    // fused experts (GEMM 1 tiles, then GEMM 2 tiles, in one launch; bf16 swap-AB tiles, contiguous layout):
+    // tm_act/tm_w map x rows and W1, tm_act_s/tm_w_s map h and W2; out is h, out2 is y
+    int fused;
+    int nkb2, nt2;       // GEMM 2: k-blocks per tile, weight blocks per expert
+    void* out2;
+    int out2_dtype;
+    int32_t* seg_done;   // per token segment: GEMM 1 epilogue warps done (zero at launch)
 };
 
 MOE_DEVICE bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl& c, int32_t* err_word) {
@@ -168,8 +175,30 @@ MOE_DEVICE bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl& c, int32_t* err_w
     return false;
 }
 
+// Fused launches: waits until *ctr >= need (GEMM 1 epilogue warps of a token segment have published h), read
+// with acquire semantics at GPU scope; bounded like every other wait.
+MOE_DEVICE bool wait_counter(const int32_t* ctr, int32_t need, Ctrl& c, int32_t* err_word) {
+    const uint64_t deadline = ptx::globaltimer() + kWaitNs;
+    uint32_t n = 0;
+    while (true) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= need) return true;
+        if ((++n & 255u) == 0) {
+            if (c.abort) return false;
+            if (ptx::globaltimer() > deadline) {
+                c.abort = 1;
+                report(err_word, MOE_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // Tile -> (expert, rows, n-tile / weight block, tokens) decoding, shared by all roles.
 struct Tile {
+    int gemm;         // 1 or 2 (fused launches hold both)
+    int32_t seg;      // fused: global token-segment index
     int swap;         // this tile puts weights on the MMA M side
     int e;
     int64_t row0;     // first activation row of the tile
@@ -185,6 +214,29 @@ MOE_DEVICE int32_t mixed_tail(int32_t c) { return c >= 64 ? 0 : c; }
 
 MOE_DEVICE Tile decode_tile(const ExpertTable& tab, const TcParams& p, int32_t t) {
     Tile tl;
+    tl.gemm = p.gemm;
+    tl.seg = 0;
+    if (p.fused) {
+        // the table counts token segments; GEMM 1 tiles (segment, W1 block) come first, then GEMM 2 tiles
+        const int32_t t1 = tab.total * p.nt;
+        int32_t tt = t, nt = p.nt;
+        if (t >= t1) {
+            tl.gemm = 2;
+            tt = t - t1;
+            nt = p.nt2;
+        } else {
+            tl.gemm = 1;
+        }
+        const int32_t g = tt / nt;
+        tl.seg = g;
+        tl.nb = tt - g * nt;
+        tl.e = find_expert(tab, p.E, g);
+        const int32_t seg = g - tiles_before(tab, tl.e);
+        tl.swap = 1;
+        tl.row0 = int64_t(tab.start[tl.e]) + int64_t(seg) * p.span;
+        tl.rows = min(p.span, tab.count[tl.e] - seg * p.span);
+        return tl;
+    }
     tl.e = find_expert(tab, p.E, t);
     const int32_t local = t - tiles_before(tab, tl.e);
     if (p.mixed) {
@@ -339,7 +391,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
         ptx::tmem_alloc(&ctrl.tmem_base, TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    const int span = p.span, ntl = p.nt, mixed = p.mixed, ntn = p.nt_n, nts = p.nt_s;
+    const int span = p.span, ntl = p.fused ? 1 : p.nt, mixed = p.mixed, ntn = p.nt_n, nts = p.nt_s;
     build_expert_table(tab, p.E, p.counts, p.offsets, p.max_tokens, p.rows_cap,
                        [span, ntl, mixed, ntn, nts](int32_t c) {
                            if (mixed) return mixed_normal_tiles(c) * ntn + (mixed_tail(c) > 0 ? nts : 0);
@@ -349,7 +401,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = ctrl.tmem_base;
-    const int32_t total = tab.total;
+    const int32_t total = p.fused ? tab.total * (p.nt + p.nt2) : tab.total;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -363,15 +415,23 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
                 const Tile tl = decode_tile(tab, p, t);
                 const int nbox = tl.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
-                const CUtensorMap* mact = (p.mixed && tl.swap) ? &tm_act_s : &tm_act;
-                const CUtensorMap* mw = (p.mixed && tl.swap) ? &tm_w_s : &tm_w;
+                const bool second = (p.mixed && tl.swap) || (tl.gemm == 2 && p.fused);   // maps of the second kind
+                const CUtensorMap* mact = second ? &tm_act_s : &tm_act;
+                const CUtensorMap* mw = second ? &tm_w_s : &tm_w;
+                const int nkb = tl.gemm == 2 && p.fused ? p.nkb2 : p.nkb;
+                const int w_mode = tl.gemm == 2 && p.fused ? 0 : p.w_mode;
+                if (p.fused && tl.gemm == 2) {
+                    // this segment's h is complete once all 4 epilogue warps of its nt GEMM 1 tiles published
+                    if (!wait_counter(&p.seg_done[tl.seg], 4 * p.nt, ctrl, p.err_word)) break;
+                    asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> TMA reads
+                }
                 const uint64_t pol_w = tl.swap ? pol_stream : pol_keep;
                 constexpr int KSUB = Cfg<V>::KSUB;
                 const uint32_t wbytes = W8 ? uint32_t(BM * BK * KSUB) : uint32_t(A_BYTES);
                 const uint32_t bytes = W8 ? wbytes
                                           : (tl.swap ? wbytes + uint32_t(nbox * TOK_BOX * BK * 2)
                                                      : uint32_t(A_BYTES + Cfg<V>::B_BYTES));
-                for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!wait_bar(&ctrl.empty[s], ph ^ 1, ctrl, p.err_word)) break;
@@ -385,7 +445,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                     uint8_t* wdst = W8 ? sa : (tl.swap ? sa : sb);
                     const int wrows = tl.swap ? 128 : 256;
                     const int row_w = tl.nb * wrows;          // first weight row (interleaved order)
-                    if (p.w_mode == 1)
+                    if (w_mode == 1)
                         ptx::tma_load_5d(wdst, mw, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_w);
                     else
                         ptx::tma_load_3d(wdst, mw, &ctrl.full[s], k0, row_w, tl.e, pol_w);
@@ -424,8 +484,9 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                 if (tl.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
                 const uint32_t idesc = ptx::idesc_bf16(BM, n_mma);
                 const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg<V>::ACC_STRIDE);
+                const int nkb = tl.gemm == 2 && p.fused ? p.nkb2 : p.nkb;
                 bool ok = true;
-                for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
                     if constexpr (W8) {
                         // A slot a: decoded weights in TMEM, tokens in the slot's smem tile
                         const int a = it % Cfg<V>::A_SLOTS;
@@ -629,7 +690,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                 // swap-AB: TMEM lane = weight row of the tile, column = token
                 const int n_tok = tl.rows;
                 const int n_chunks = (n_tok + 15) / 16;
-                if (p.gemm == 1) {
+                if (tl.gemm == 1) {
                     // lanes 0..15: gate of unit u, lanes 16..31: up of unit u, u = 64*nb + 16*q + (lane & 15)
                     const int64_t unit = int64_t(tl.nb) * 64 + q * 16 + (lane & 15);
                     uint16_t* h = static_cast<uint16_t*>(p.out);
@@ -650,7 +711,17 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                                 h[(tl.row0 + n) * p.I + unit] = float_to_bf16_bits(silu_mul(g, u));
                         }
                     }
+                    if (p.fused) {
+                        // publish this warp's part of the segment's h for the GEMM 2 tiles (release at GPU scope)
+                        __syncwarp();
+                        if (lane == 0) {
+                            __threadfence();
+                            atomicAdd(&p.seg_done[tl.seg], 1);
+                        }
+                    }
                 } else {
+                    void* yout = p.fused ? p.out2 : p.out;
+                    const int ydt = p.fused ? p.out2_dtype : p.out_dtype;
                     const int64_t col = int64_t(tl.nb) * 128 + q * 32 + lane;   // output hidden index
 #pragma unroll 1
                     for (int cb = 0; cb < n_chunks; ++cb) {
@@ -674,10 +745,10 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                                 if (p.route_w) wt = p.route_w[row];
                             }
                             const float val = wt * __uint_as_float(v[i]);
-                            if (p.out_dtype == MOE_BF16)
-                                static_cast<uint16_t*>(p.out)[dst_row * p.K + col] = float_to_bf16_bits(val);
+                            if (ydt == MOE_BF16)
+                                static_cast<uint16_t*>(yout)[dst_row * p.K + col] = float_to_bf16_bits(val);
                             else
-                                static_cast<float*>(p.out)[dst_row * p.K + col] = val;
+                                static_cast<float*>(yout)[dst_row * p.K + col] = val;
                         }
                     }
                 }
@@ -820,6 +891,38 @@ int build_maps(const GemmArgs& g, bool swap, bool w8, int64_t kdim, int64_t wrow
     return make_map(w, g.w, 3, dims, str, box, g.gemm == 1 ? "W1" : "W2", w8);
 }
 
+// Tensor maps of one launch (normal or swap-AB tiles, and for mixed launches both), encoded once per shape.
+int cached_maps(const GemmArgs& g, int mode, bool w8, int64_t kdim, int64_t wrows, int w_mode, MapSet* out) {
+    const bool swap = mode == TC_SWAP, mixed = mode == TC_MIXED;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    const MapKey key{dev_id, g.a, g.w, kdim, g.rows_cap, wrows, g.I, g.K, g.E, g.gemm,
+                     mode | (w8 ? 4 : 0), w_mode};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return MOE_OK;
+        }
+    }
+    MapSet maps;
+    int rc = build_maps(g, swap, w8, kdim, wrows, &maps.act, &maps.w);
+    if (rc) return rc;
+    if (mixed) {
+        rc = build_maps(g, true, w8, kdim, wrows, &maps.act_s, &maps.w_s);
+        if (rc) return rc;
+    } else {
+        maps.act_s = maps.act;
+        maps.w_s = maps.w;
+    }
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (g_maps.size() >= 256) g_maps.clear();
+    g_maps[key] = maps;
+    *out = maps;
+    return MOE_OK;
+}
+
 int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     const bool swap = mode == TC_SWAP, mixed = mode == TC_MIXED;
     const bool w8 = g.w_dtype == MOE_E4M3;
@@ -842,36 +945,11 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     if (g.rows_cap == 0) return MOE_OK;   // no rows, nothing to do
 
     const int w_mode = (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0;
-    int dev_id = 0;
-    cudaGetDevice(&dev_id);
-    const MapKey key{dev_id, g.a, g.w, kdim, g.rows_cap, wrows, g.I, g.K, g.E, g.gemm,
-                     mode | (w8 ? 4 : 0), w_mode};
     MapSet maps;
-    bool cached = false;
-    {
-        std::lock_guard<std::mutex> lock(g_map_mu);
-        auto it = g_maps.find(key);
-        if (it != g_maps.end()) {
-            maps = it->second;
-            cached = true;
-        }
-    }
-    if (!cached) {
-        int rc = build_maps(g, swap, w8, kdim, wrows, &maps.act, &maps.w);
-        if (rc) return rc;
-        if (mixed) {
-            rc = build_maps(g, true, w8, kdim, wrows, &maps.act_s, &maps.w_s);
-            if (rc) return rc;
-        } else {
-            maps.act_s = maps.act;
-            maps.w_s = maps.w;
-        }
-        std::lock_guard<std::mutex> lock(g_map_mu);
-        if (g_maps.size() >= 256) g_maps.clear();
-        g_maps[key] = maps;
-    }
+    int rc0 = cached_maps(g, mode, w8, kdim, wrows, w_mode, &maps);
+    if (rc0) return rc0;
 
-    TcParams p;
+    TcParams p{};
     p.gemm = g.gemm;
     p.swap = swap ? 1 : 0;
     p.layout = g.layout;
@@ -923,6 +1001,82 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
         gemm_tc_kernel<V_BF16><<<grid, Cfg<V_BF16>::THREADS, Cfg<V_BF16>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
                                                                                      maps.w_s, p);
     return check_launch("gemm_tc_kernel");
+}
+
+size_t experts_fused_workspace_bytes(int64_t rows_cap, int E) {
+    const int64_t segs = (rows_cap + Cfg<V_SWAP64>::TOK_SPAN - 1) / Cfg<V_SWAP64>::TOK_SPAN + E;
+    return size_t((segs * 4 + 255) / 256 * 256);
+}
+
+// GEMM 1 and GEMM 2 of the bf16 swap-AB regime in one cooperative launch (all CTAs resident, so a GEMM 2 tile
+// may wait for the GEMM 1 tiles of its token segment, which other resident CTAs reach first in tile order).
+int launch_experts_fused(const GemmArgs& g1, const GemmArgs& g2, int32_t* seg_done, size_t ws_bytes,
+                         cudaStream_t s) {
+    if (g1.a_dtype != MOE_BF16 || g1.w_dtype != MOE_BF16 || g2.w_dtype != MOE_BF16 || g1.out_dtype != MOE_BF16)
+        return fail(MOE_ERR_UNSUPPORTED, "fused experts: bf16 activations, weights and h only");
+    if (g1.layout != MOE_LAYOUT_CONTIGUOUS) return fail(MOE_ERR_UNSUPPORTED, "fused experts: contiguous layout only");
+    if (g1.K % 128 != 0 || g1.I % 64 != 0)
+        return fail(MOE_ERR_UNSUPPORTED, "fused experts: K % 128 == 0 and I % 64 == 0 needed");
+    if (g1.rows_cap >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "fused experts: too many rows");
+    if (ws_bytes < experts_fused_workspace_bytes(g1.rows_cap, g1.E))
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "fused experts: workspace smaller than moe_experts_fused_workspace_size()");
+    if (g1.rows_cap == 0) return MOE_OK;
+    const int w_mode = g1.w1_layout == MOE_W1_GATE_UP ? 1 : 0;
+    MapSet m1, m2;
+    int rc = cached_maps(g1, TC_SWAP, false, g1.K, 2 * g1.I, w_mode, &m1);
+    if (rc) return rc;
+    rc = cached_maps(g2, TC_SWAP, false, g1.I, g1.K, 0, &m2);
+    if (rc) return rc;
+
+    TcParams p{};
+    p.gemm = 1;
+    p.swap = 1;
+    p.layout = MOE_LAYOUT_CONTIGUOUS;
+    p.E = g1.E;
+    p.rows_cap = g1.rows_cap;
+    p.nkb = int(g1.K / BK);
+    p.nt = int(2 * g1.I / 128);
+    p.w_mode = w_mode;
+    p.I = g1.I;
+    p.K = g1.K;
+    p.counts = g1.counts;
+    p.offsets = g1.offsets;
+    p.row_route = g2.row_route;
+    p.route_w = g2.route_w;
+    p.out = g1.out;
+    p.out_dtype = MOE_BF16;
+    p.out_rows = g2.out_rows;
+    p.err_word = g1.err_word;
+    p.span = Cfg<V_SWAP64>::TOK_SPAN;
+    p.wrows = 2 * g1.I;
+    p.fused = 1;
+    p.nkb2 = int(g1.I / BK);
+    p.nt2 = int(g1.K / 128);
+    p.out2 = g2.out;
+    p.out2_dtype = g2.out_dtype;
+    p.seg_done = seg_done;
+    p.skip_first_copy = timeout_test_hook() ? 1 : 0;
+
+    rc = set_smem_attr<V_SWAP64>();
+    if (rc) return rc;
+    const int64_t segs = (g1.rows_cap + p.span - 1) / p.span + g1.E;
+    if (cudaMemsetAsync(seg_done, 0, size_t(segs) * 4, s) != cudaSuccess)
+        return fail(MOE_ERR_LAUNCH, "fused experts: clearing the segment counters failed");
+    const int64_t tiles = segs * (p.nt + p.nt2);
+    const int grid = int(std::min<int64_t>(tiles, num_sms()));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(Cfg<V_SWAP64>::THREADS);
+    cfg.dynamicSmemBytes = Cfg<V_SWAP64>::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<V_SWAP64>, m1.act, m1.w, m2.act, m2.w, p) != cudaSuccess)
+        return check_launch("gemm_tc_kernel (fused experts)");
+    return check_launch("gemm_tc_kernel (fused experts)");
 }
 
 }  // namespace moe

@@ -69,6 +69,11 @@ cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t s);
 enum { TC_NORMAL = 0, TC_SWAP = 1, TC_MIXED = 2 };
 // Returns MOE_OK or a status (with message) when the tcgen05 path cannot run.
 int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s);
+// GEMM 1 then GEMM 2 (bf16, swap-AB tiles, contiguous layout) in one cooperative launch; seg_done is the
+// caller's workspace (per token segment counters, cleared by the call).
+size_t experts_fused_workspace_bytes(int64_t rows_cap, int E);
+int launch_experts_fused(const GemmArgs& g1, const GemmArgs& g2, int32_t* seg_done, size_t ws_bytes,
+                         cudaStream_t s);
 // Block-scaled MXFP8 (E4M3 activations and weights) on swap-AB tcgen05 tiles.
 int launch_gemm_mx(const GemmArgs& g, cudaStream_t s);
 

@@ -44,13 +44,18 @@ def _p(t):
 class MoELayer:
     def __init__(self, T: int, K: int, I: int, E: int, top_k: int, act_dtype=torch.bfloat16, block_m: int = 1,
                  layout: int = B.MOE_LAYOUT_CONTIGUOUS, max_tokens: int = 0, impl: int = B.MOE_IMPL_AUTO,
-                 weight_in_gemm2: bool = True, device="cuda", act_quant: bool = False):
+                 weight_in_gemm2: bool = True, device="cuda", act_quant: bool = False,
+                 fused_experts: bool = True):
         self.T, self.K, self.I, self.E, self.top_k = T, K, I, E, top_k
         if act_quant and layout != B.MOE_LAYOUT_CONTIGUOUS:
             raise ValueError("act_quant (MXFP8 activations) is implemented for the contiguous layout")
         if act_quant and (K % 32 or I % 32):
             raise ValueError("act_quant needs K and I multiples of 32")
         self.act_quant = act_quant
+        # GEMM 1 + GEMM 2 in one launch (moe_experts_fused) where the contiguous bf16 plan runs swap-AB tiles
+        self.fused_experts = (fused_experts and layout == B.MOE_LAYOUT_CONTIGUOUS and not act_quant
+                              and impl in (B.MOE_IMPL_AUTO, B.MOE_IMPL_TCGEN05_SWAP_AB) and K % 128 == 0
+                              and I % 64 == 0)
         self.block_m, self.layout, self.max_tokens, self.impl = block_m, layout, max_tokens, impl
         self.weight_in_gemm2 = weight_in_gemm2
         self.act_dtype = act_dtype
@@ -72,6 +77,9 @@ class MoELayer:
             self.h = torch.empty((self.rows_cap, I), dtype=act_dtype, device=dev)
             self.y = torch.empty((T * top_k, K), dtype=act_dtype, device=dev)
             self.out = torch.empty((T, K), dtype=act_dtype, device=dev)
+            if self.fused_experts:
+                self.fused_ws = torch.empty(max(B.moe_experts_fused_workspace_size(self.rows_cap, E), 256),
+                                            dtype=torch.uint8, device=dev)
             if act_quant:
                 u8 = dict(dtype=torch.uint8, device=dev)
                 self.x_codes = torch.empty((self.rows_cap, K), **u8)
@@ -157,6 +165,18 @@ class MoELayer:
             a1, a1dt, a1s = self.x_codes.data_ptr(), B.MOE_E4M3, self.x_scales.data_ptr()
         else:
             a1, a1dt, a1s = self.x_perm.data_ptr(), adt, None
+        swap_regime = self.impl == B.MOE_IMPL_TCGEN05_SWAP_AB or self.rows_cap // max(E, 1) < 64
+        if (self.fused_experts and swap_regime and adt == B.MOE_BF16 and wdt == B.MOE_BF16
+                and self.weight_in_gemm2):
+            calls.append((lib.moe_experts_fused, (self.x_perm.data_ptr(), adt, self.counts.data_ptr(),
+                                                  self.offsets.data_ptr(), self.rows_cap, E, K, I, w1.data_ptr(),
+                                                  w1_layout, w2.data_ptr(), wdt, self.row_route.data_ptr(),
+                                                  weights.data_ptr(), self.h.data_ptr(), self.y.data_ptr(), adt,
+                                                  T * k, self.fused_ws.data_ptr(), self.fused_ws.numel(),
+                                                  self.err.data_ptr(), stream), "gemm1"))
+            calls.append((lib.moe_unpermute_topk_reduce, (self.y.data_ptr(), adt, ids.data_ptr(), None, T, k, E,
+                                                          K, self.out.data_ptr(), adt, stream), "reduce"))
+            return calls
         if self.act_quant:   # GEMM 1's epilogue writes h as MXFP8 (codes + scales)
             hout, hdt, hs = self.h_codes.data_ptr(), B.MOE_E4M3, self.h_scales.data_ptr()
         else:
@@ -244,6 +264,8 @@ class MoELayer:
         if self.layout == B.MOE_LAYOUT_BATCHED and self.T == 0:
             return 2 if self.weight_in_gemm2 else 3
         n = 3 + 1 + (1 if self.T * self.top_k <= 1024 else 2) + 1   # gemm1 gemm2 reduce, gather, permute, route
+        if any(name == "gemm1" and fn is self.lib.moe_experts_fused for fn, _, name in (self._plan or [])):
+            n -= 1                                                    # GEMM 1 + GEMM 2 in one launch
         if self.act_quant:
             n += 1                                                    # quantise x rows (h: in GEMM 1)
         return n if any(name == "route" for _, _, name in (self._plan or [])) else n - 1

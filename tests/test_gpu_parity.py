@@ -702,3 +702,58 @@ def test_layer_batched_tokens_full_size_sampled(moe):
         cids, (w1h, w2h, _, _) = compact_experts(ids[t:t + 1], W1, W2)
         ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, weights[t:t + 1], w1h, w2h)
         assert_close(to_f64(out[t:t + 1]), ref, TOL_BF16, f"batched_tokens token {t}")
+
+
+# ----------------------------------------------------------------------------
+# GEMM 1 + GEMM 2 in one launch
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape", [(5, 8, 64, 512, 128, 0), (96, 4, 8, 512, 256, 1), (700, 2, 6, 256, 128, 0),
+                                   (1, 8, 128, 1024, 192, 1)])
+def test_experts_fused_matches_two_launches(moe, shape):
+    """moe_experts_fused equals moe_gemm1_swiglu + moe_gemm2 on swap-AB tiles bit for bit (same tiles, same
+    accumulation order) and the oracle within tolerance; run twice (the workspace is cleared by each call)."""
+    T, k, E, K, I, w1_layout = shape
+    w, x, ids, weights = _routed(T, k, E, K, seed=T + 9 * E)
+    ws = wl.scaled(w, I=I, w_std=0.05)
+    W1 = wl.expert_weights(ws, "W1", 14).to(torch.bfloat16)
+    W2 = wl.expert_weights(ws, "W2", 14).to(torch.bfloat16)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    R = T * k
+    wt = torch.from_numpy(weights).to(DEV).reshape(-1)
+    swap = moe.MOE_IMPL_TCGEN05_SWAP_AB
+    h2 = moe.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1.to(DEV), I, w1_layout=w1_layout,
+                              impl=swap)
+    y2 = moe.moe_gemm2(h2, res["counts"], res["offsets"], W2.to(DEV), R, row_route=res["row_route"],
+                       route_weights=wt, impl=swap)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for _ in range(2):
+        h1, y1 = moe.moe_experts_fused(res["x_out"], res["counts"], res["offsets"], W1.to(DEV), W2.to(DEV), I,
+                                       res["row_route"], R, route_weights=wt, w1_layout=w1_layout, err_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    ref, _ = oracle.moe_layer(wl.to_numpy(x), ids, weights, wl.to_numpy(W1), wl.to_numpy(W2), w1_layout=w1_layout)
+    # y holds w * FFN per (token, slot); summing the slots reproduces the layer
+    out = moe.moe_unpermute_topk_reduce(y1, torch.from_numpy(ids).to(DEV), E)
+    assert_close(to_f64(out), ref, TOL_BF16, "fused experts")
+
+
+def test_layer_decode_fused_experts_full_size(moe):
+    """Decode configuration at full size with GEMM 1 + GEMM 2 in one launch: equals the two-launch layer bit for
+    bit, sampled tokens against the oracle."""
+    w = wl.decode(32)
+    x, logits = wl.activations(w, 0, DEV), wl.router_logits(w, 0, DEV)
+    W1, W2 = wl.expert_weights(w, "W1", 0, DEV), wl.expert_weights(w, "W2", 0, DEV)
+    a = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, fused_experts=False, device=DEV)
+    b = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, fused_experts=True, device=DEV)
+    out_a = a.forward(x, W1, W2, logits=logits).clone()
+    out_b = b.forward(x, W1, W2, logits=logits)
+    assert b.launches_per_forward() == a.launches_per_forward() - 1
+    assert b.device_errors() == 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    ids, weights = oracle.topk_route(logits.cpu().numpy(), w.top_k)
+    for t in (0, 31):
+        cids, (w1h, w2h, _, _) = compact_experts(ids[t:t + 1], W1, W2)
+        ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, weights[t:t + 1], w1h, w2h)
+        assert_close(to_f64(out_b[t:t + 1]), ref, TOL_BF16, f"fused decode token {t}")

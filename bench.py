@@ -340,6 +340,19 @@ def recorded_traffic(workload, fused=False):
     return None
 
 
+def aggregate_over_ranks(ms_total, routes, world, device):
+    """Whole-job figures of N replicas: the slowest rank's time (max) and every rank's routes (sum)."""
+    if world <= 1:
+        return float(ms_total), float(routes)
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(ms_total)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    rr = torch.tensor([float(routes)], dtype=torch.float64, device=device)
+    dist.all_reduce(rr, op=dist.ReduceOp.SUM)
+    return float(tt.item()), float(rr.item())
+
+
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
@@ -405,15 +418,7 @@ def run_ours(args, rank, world, local_rank):
     clocks = clk.summary()
 
     routes_per_step = sum(i.routes for i in insts)
-    t_max = ms_total
-    total_routes = routes_per_step * args.steps
-    if world > 1:
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
-        rr = torch.tensor([total_routes], dtype=torch.float64, device=dev)
-        dist.all_reduce(rr, op=dist.ReduceOp.SUM)
-        total_routes = float(rr.item())
+    t_max, total_routes = aggregate_over_ranks(ms_total, routes_per_step * args.steps, world, dev)
     value = total_routes / (t_max / 1e3)
 
     # GEMM 1 roofline (HBM bound for decode/mxfp8/batched, tensor bound for prefill)

@@ -149,7 +149,9 @@ int validate_gemm(const GemmArgs& g, const char* name) {
     MOE_REQUIRE(g.K % 32 == 0 && g.I % 32 == 0, MOE_ERR_ALIGNMENT, n + ": K and I must be multiples of 32");
     MOE_REQUIRE(g.layout == MOE_LAYOUT_CONTIGUOUS || g.layout == MOE_LAYOUT_BATCHED, MOE_ERR_INVALID_ARG,
                 n + ": unknown layout");
-    MOE_REQUIRE(g.a && g.w && g.counts && g.out, MOE_ERR_INVALID_ARG, n + ": null pointer");
+    // no rows (an empty batch): the activation and output buffers may be empty (NULL)
+    const int64_t rows = g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens;
+    MOE_REQUIRE(g.w && g.counts && ((g.a && g.out) || rows == 0), MOE_ERR_INVALID_ARG, n + ": null pointer");
     MOE_REQUIRE(aligned16(g.a) && aligned16(g.w) && aligned16(g.out), MOE_ERR_ALIGNMENT,
                 n + ": activation, weight and output pointers must be 16-byte aligned");
     MOE_REQUIRE((is_float_dtype(g.a_dtype) || g.a_dtype == MOE_E4M3) &&
@@ -198,6 +200,7 @@ int run_gemm_mx(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
 }
 
 int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
+    if ((g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens) == 0) return MOE_OK;
     if (g.a_dtype == MOE_E4M3) return run_gemm_mx(g, impl, s, name);
     const bool tc_ok = g.a_dtype == MOE_BF16 && (g.w_dtype == MOE_BF16 || g.w_dtype == MOE_E4M3) &&
                        g.out_dtype == MOE_BF16 && device_cc() >= 100;
@@ -350,7 +353,8 @@ int moe_experts_fused(const void* a, int a_dtype, const int32_t* expert_counts, 
                 "moe_experts_fused: unknown w1_layout");
     MOE_REQUIRE(row_route, MOE_ERR_INVALID_ARG, "moe_experts_fused: row_route is required");
     MOE_REQUIRE(y_rows >= 0, MOE_ERR_INVALID_ARG, "moe_experts_fused: y_rows < 0");
-    MOE_REQUIRE(h != a && h != y, MOE_ERR_INVALID_ARG, "moe_experts_fused: h must not alias a or y");
+    MOE_REQUIRE(rows_cap == 0 || (h != a && h != y), MOE_ERR_INVALID_ARG,
+                "moe_experts_fused: h must not alias a or y");
     MOE_REQUIRE(workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, MOE_ERR_ALIGNMENT,
                 "moe_experts_fused: workspace must be 256-byte aligned");
     MOE_REQUIRE(device_cc() >= 100, MOE_ERR_UNSUPPORTED, "moe_experts_fused: tcgen05 needs an sm_100+ device");

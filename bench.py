@@ -472,28 +472,77 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_e2e(args, insts, dev):
-    """Same metric through the public API with host buffers: H2D of x and logits, layer, D2H of the output."""
+    """Same metric through the public API with host buffers: every step copies its inputs (x and router logits
+    of every pass, packed in one pinned staging buffer: one H2D copy) to the device, runs the layer and reads each
+    pass's output back to pinned host memory."""
     import torch
-    host = []
+    # staging: the inputs of all passes back to back (256-byte aligned views), on the host (pinned) and device
+    parts = []
     for inst in insts:
-        hx = inst.x.cpu().pin_memory() if inst.w.layout != "batched" else inst.xb.cpu().pin_memory()
-        hl = inst.logits.cpu().pin_memory() if getattr(inst, "logits", None) is not None else None
-        out = inst.layer.out
-        ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        dx = torch.empty_like(inst.x if inst.w.layout != "batched" else inst.xb)
-        dl = torch.empty_like(inst.logits) if hl is not None else None
-        host.append((hx, hl, ho, dx, dl))
+        src_x = inst.x if inst.w.layout != "batched" else inst.xb
+        lg = getattr(inst, "logits", None)
+        parts.append((src_x, lg))
+    off, offs = 0, []
+    for src_x, lg in parts:
+        ox = off
+        off += (src_x.numel() * src_x.element_size() + 255) // 256 * 256
+        ol = None
+        if lg is not None:
+            ol = off
+            off += (lg.numel() * lg.element_size() + 255) // 256 * 256
+        offs.append((ox, ol))
+    hstage = torch.empty(off, dtype=torch.uint8, pin_memory=True)
+    dstage = torch.empty(off, dtype=torch.uint8, device=dev)
+
+    def view(buf, o, like):
+        n = like.numel() * like.element_size()
+        return buf[o:o + n].view(like.dtype).view(like.shape)
+
+    host = []
+    for inst, (src_x, lg), (ox, ol) in zip(insts, parts, offs):
+        view(hstage, ox, src_x).copy_(src_x.cpu())
+        if lg is not None:
+            view(hstage, ol, lg).copy_(lg.cpu())
+        dx = view(dstage, ox, src_x)
+        dl = view(dstage, ol, lg) if lg is not None else None
+        ho = torch.empty(inst.layer.out.shape, dtype=inst.layer.out.dtype, pin_memory=True)
+        host.append((ho, dx, dl))
+
+    def kwargs_of(inst, dl):
+        if inst.w.layout == "batched":
+            return dict(expert_num_tokens=inst.counts, row_weights=inst.rw)
+        if dl is not None:
+            return dict(logits=dl, w1_scale=inst.s1, w2_scale=inst.s2, w1_layout=inst.w.w1_layout)
+        return dict(topk_ids=inst.ids, topk_weights=inst.tw, w1_scale=inst.s1, w2_scale=inst.s2,
+                    w1_layout=inst.w.w1_layout)
+
+    def h2d():
+        dstage.copy_(hstage, non_blocking=True)
+
+    def d2h_of(inst, ho):
+        return lambda: ho.copy_(inst.layer.out, non_blocking=True)
+
+    # one CUDA graph per pass (MoELayer.capture); the first also holds the step's H2D copy
+    graphs = None
+    if not args.eager:
+        try:
+            graphs = []
+            for n, (inst, (ho, dx, dl)) in enumerate(zip(insts, host)):
+                graphs.append(inst.layer.capture(dx, inst.W1, inst.W2, before=h2d if n == 0 else None,
+                                                 after=d2h_of(inst, ho), **kwargs_of(inst, dl)))
+        except RuntimeError as exc:
+            print(f"bench: e2e graph capture failed ({exc}); e2e runs eagerly", file=sys.stderr)
+            graphs = None
 
     def step():
-        for inst, (hx, hl, ho, dx, dl) in zip(insts, host):
-            dx.copy_(hx, non_blocking=True)
-            if hl is not None:
-                dl.copy_(hl, non_blocking=True)
-            if inst.w.layout == "batched":
-                out = inst.layer.forward(dx, inst.W1, inst.W2, expert_num_tokens=inst.counts, row_weights=inst.rw)
-            else:
-                out = inst.forward(x=dx, logits=dl)
-            ho.copy_(out, non_blocking=True)
+        if graphs is not None:
+            for g in graphs:
+                g.replay()
+            return
+        h2d()
+        for inst, (ho, dx, dl) in zip(insts, host):
+            inst.layer.forward(dx, inst.W1, inst.W2, **kwargs_of(inst, dl))
+            d2h_of(inst, ho)()
 
     for _ in range(max(1, args.warmup)):
         step()
@@ -504,10 +553,9 @@ def run_e2e(args, insts, dev):
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     routes = sum(i.routes for i in insts) * args.steps
-    h2d = sum(h[0].numel() * h[0].element_size() + (h[1].numel() * h[1].element_size() if h[1] is not None else 0)
-              for h in host)
-    d2h = sum(h[2].numel() * h[2].element_size() for h in host)
-    return {"value": round(routes / dt, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    d2h = sum(h[0].numel() * h[0].element_size() for h in host)
+    return {"value": round(routes / dt, 1), "unit": UNIT, "h2d_bytes_per_step": int(hstage.numel()),
+            "d2h_bytes_per_step": d2h}
 
 
 # ----------------------------------------------------------------------------

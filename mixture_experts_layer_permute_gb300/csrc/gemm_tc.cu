@@ -273,14 +273,6 @@ MOE_DEVICE int64_t tile_weight_row(const TcParams& p, int nb, int r) {
     return int64_t(nb) * 128 + r;
 }
 
-// bf16x2 factors that turn code * 2^-120 into code * 2^(scale-127): f1 = 2^(scale-7) when that is a
-// bf16 normal (scale <= 134), else f1 = 2^(scale-127) and f2 = 2^120.
-MOE_DEVICE void e8m0_factors(uint32_t code, uint32_t& f1, uint32_t& f2) {
-    const uint32_t e1 = code <= 134u ? code + 120u : code;   // bf16 exponent field of f1
-    f1 = (e1 << 7) | (e1 << 23);
-    f2 = code <= 134u ? 0u : ((247u << 7) | (247u << 23));
-}
-
 // 4 E4M3 codes (one 32-bit word) -> 2 bf16x2 words (codes 0,1 and 2,3) times f1.
 // prmt copies each code into the low byte of a 16-bit half and its sign into the high byte;
 // shifting by 4 moves exponent+mantissa to bits 10..4 and the sign bits to 15..12 (and 19..16,

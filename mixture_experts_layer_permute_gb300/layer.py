@@ -26,7 +26,8 @@ or, for the batched layout fed with tokens (T > 0),
 with no host synchronisation.  Every step runs in libmoe_layer's kernels.
 The marshalled argument lists of the C calls are kept between calls with the
 same tensors and stream, so a decode step spends a few microseconds per call
-on the host; the calls also capture into a CUDA graph (``capture``).
+on the host; ``capture`` records one forward into a CUDA graph whose replay
+re-runs the layer on the same tensors (new inputs are copied into them).
 """
 from __future__ import annotations
 
@@ -258,6 +259,27 @@ class MoELayer:
             if gemm1_events is not None and name == "gemm1":
                 gemm1_events[1].record(s)
         return self.out
+
+    def capture(self, x: torch.Tensor, w1: torch.Tensor, w2: torch.Tensor, before=None, after=None,
+                **kwargs) -> torch.cuda.CUDAGraph:
+        """Records one forward on (x, w1, w2, **kwargs) into a CUDA graph and returns it.
+
+        ``graph.replay()`` then runs route/permute/GEMMs/reduce on the same tensors; write new inputs into
+        them (or let ``before`` do it) and read ``self.out`` after the replay.  ``before`` and ``after`` are
+        optional callables recorded around the forward, e.g. the copies of a step's inputs from pinned host
+        buffers and of its output back.  One eager forward runs first (it builds the call plan and sets up the
+        library on the device).
+        """
+        self.forward(x, w1, w2, **kwargs)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            if before is not None:
+                before()
+            self.forward(x, w1, w2, **kwargs)
+            if after is not None:
+                after()
+        return graph
 
     def launches_per_forward(self) -> int:
         """Kernels one forward launches (for launch accounting)."""

@@ -757,3 +757,30 @@ def test_layer_decode_fused_experts_full_size(moe):
         cids, (w1h, w2h, _, _) = compact_experts(ids[t:t + 1], W1, W2)
         ref, _ = oracle.moe_layer(wl.to_numpy(x[t:t + 1]), cids, weights[t:t + 1], w1h, w2h)
         assert_close(to_f64(out_b[t:t + 1]), ref, TOL_BF16, f"fused decode token {t}")
+
+
+def test_layer_capture_replays_with_new_inputs(moe):
+    """MoELayer.capture: the graph re-runs the whole layer on the same tensors; inputs copied in from pinned host
+    buffers by the recorded `before` and the output read back by `after` come out as an eager forward's."""
+    w = wl.scaled(wl.decode(16), T=16, K=512, I=256, E=16, top_k=4)
+    W1, W2 = wl.expert_weights(w, "W1", 1, DEV), wl.expert_weights(w, "W2", 1, DEV)
+    hx = torch.empty((w.T, w.K), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.T, w.E), dtype=torch.float32).pin_memory()
+    dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=DEV)
+    dl = torch.empty((w.T, w.E), dtype=torch.float32, device=DEV)
+    layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, device=DEV)
+    ho = torch.empty((w.T, w.K), dtype=torch.bfloat16).pin_memory()
+    hx.copy_(wl.activations(w, 1))
+    hl.copy_(wl.router_logits(w, 1))
+    g = layer.capture(dx, W1, W2, logits=dl,
+                      before=lambda: (dx.copy_(hx, non_blocking=True), dl.copy_(hl, non_blocking=True)),
+                      after=lambda: ho.copy_(layer.out, non_blocking=True))
+    eager = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, device=DEV)
+    for seed in (2, 3):                          # new inputs between replays
+        hx.copy_(wl.activations(w, seed))
+        hl.copy_(wl.router_logits(w, seed))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = eager.forward(hx.to(DEV), W1, W2, logits=hl.to(DEV))
+        torch.cuda.synchronize()
+        assert torch.equal(ho.view(torch.int16), ref.cpu().view(torch.int16))

@@ -54,7 +54,9 @@ class MoELayer:
             raise ValueError("act_quant needs K and I multiples of 32")
         self.act_quant = act_quant
         # GEMM 1 + GEMM 2 in one launch (moe_experts_fused) where the contiguous bf16 plan runs swap-AB tiles
-        self.fused_experts = (fused_experts and layout == B.MOE_LAYOUT_CONTIGUOUS and not act_quant
+        dev0 = torch.device(device)
+        tc_device = dev0.type == "cuda" and torch.cuda.get_device_capability(dev0)[0] >= 10
+        self.fused_experts = (fused_experts and tc_device and layout == B.MOE_LAYOUT_CONTIGUOUS and not act_quant
                               and impl in (B.MOE_IMPL_AUTO, B.MOE_IMPL_TCGEN05_SWAP_AB) and K % 128 == 0
                               and I % 64 == 0)
         self.block_m, self.layout, self.max_tokens, self.impl = block_m, layout, max_tokens, impl

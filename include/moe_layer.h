@@ -158,6 +158,28 @@ MOE_API int moe_permute_align(const int32_t* topk_ids, int64_t T, int top_k, int
                       void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream);
 
 /*
+ * moe_route_permute_align -- moe_topk_route followed by moe_permute_align on
+ * the ids it writes ("Fused MoE Modular Kernel", apply(): select_experts, then
+ * Permute): same arguments, same results bit for bit, same errors.  For
+ * decode-sized batches (T <= 128 and T*top_k <= 1024) the routing, the
+ * placement and the gather of x run as one launch, in place of the three
+ * launches of the separate calls; larger batches take the separate launches.
+ *
+ *   logits, renormalize, topk_ids, topk_weights   as for moe_topk_route
+ *                                                  (topk_ids is written and
+ *                                                  then read by the placement)
+ *   every other argument                           as for moe_permute_align
+ * Limits: those of both calls (1 <= top_k <= min(E, 32), E <= 1024).
+ */
+MOE_API int moe_route_permute_align(const float* logits, int64_t T, int E, int top_k, int renormalize,
+                      int32_t* topk_ids, float* topk_weights,
+                      int layout, int block_m, int max_tokens,
+                      const void* x, int x_dtype, int64_t K, void* x_out, int64_t rows_cap,
+                      int32_t* expert_counts, int32_t* expert_offsets,
+                      int32_t* row_route, int32_t* route_row,
+                      void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream);
+
+/*
  * moe_permute_align_static -- moe_permute_align for callers that cannot
  * allocate device memory.  The sources describe no such variant; it exists for
  * callers with no allocator to hand: plugins inside a host framework that owns

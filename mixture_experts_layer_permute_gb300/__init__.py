@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     MOE_LAYOUT_CONTIGUOUS, MOE_W1_GATE_UP, MOE_W1_INTERLEAVE16, MoEError, load, moe_batched_topk_reduce, moe_batched_weight_reduce, moe_experts_fused,
     moe_experts_fused_workspace_size,
     moe_gemm1_swiglu, moe_gemm2, moe_max_padded_rows, moe_permute_align, moe_permute_align_static, moe_permute_workspace_size,
+    moe_route_permute_align,
     moe_topk_route, moe_unpermute_topk_reduce, moe_version, mxfp8_quantize_block32)
 
 

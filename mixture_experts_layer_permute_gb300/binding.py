@@ -29,7 +29,7 @@ MOE_DEVERR_ID_RANGE, MOE_DEVERR_CAPACITY, MOE_DEVERR_TIMEOUT = 1, 2, 4
 
 EXPORTED = [
     "moe_last_error", "moe_version", "moe_max_padded_rows", "moe_permute_workspace_size", "moe_topk_route",
-    "moe_permute_align", "moe_permute_align_static", "moe_gemm1_swiglu", "moe_gemm2", "moe_unpermute_topk_reduce",
+    "moe_permute_align", "moe_permute_align_static", "moe_route_permute_align", "moe_gemm1_swiglu", "moe_gemm2", "moe_unpermute_topk_reduce",
     "moe_batched_weight_reduce", "moe_batched_topk_reduce", "mxfp8_quantize_block32",
     "moe_experts_fused_workspace_size", "moe_experts_fused",
 ]
@@ -68,6 +68,8 @@ def load(path: Optional[str] = None):
             "moe_topk_route": (I32, [P, I64, I32, I32, I32, P, P, P]),
             "moe_permute_align": (I32, [P, I64, I32, I32, I32, I32, I32, P, I32, I64, P, I64, P, P, P, P, P, SZ,
                                         P, P]),
+            "moe_route_permute_align": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, I32, P, I32, I64, P, I64, P,
+                                              P, P, P, P, SZ, P, P]),
             "moe_permute_align_static": (I32, [P, I64, I32, I32, I32, I32, I32, P, I32, I64, P, I64, P, P, P, P,
                                                P, P]),
             "moe_gemm1_swiglu": (I32, [P, I32, P, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, I32, I32, P,
@@ -178,6 +180,46 @@ def moe_permute_align(topk_ids, E, layout=MOE_LAYOUT_CONTIGUOUS, block_m=1, max_
         workspace.numel(), _ptr(err_word), _stream(stream)))
     return dict(counts=expert_counts, offsets=expert_offsets, row_route=row_route, route_row=route_row,
                 x_out=x_out, rows_cap=rows_cap)
+
+
+def moe_route_permute_align(logits, top_k, E=None, renormalize=True, layout=MOE_LAYOUT_CONTIGUOUS, block_m=1,
+                            max_tokens=0, x=None, x_out=None, rows_cap=None, topk_ids=None, topk_weights=None,
+                            expert_counts=None, expert_offsets=None, row_route=None, route_row=None, workspace=None,
+                            err_word=None, stream=None):
+    """moe_topk_route then moe_permute_align in one call (one launch for decode-sized batches).
+    Returns dict(topk_ids, topk_weights, counts, offsets, row_route, route_row, x_out)."""
+    T, E_logits = logits.shape
+    E = E_logits if E is None else E
+    dev = logits.device
+    if rows_cap is None:
+        rows_cap = (moe_max_padded_rows(T, top_k, E, block_m) if layout == MOE_LAYOUT_CONTIGUOUS
+                    else E * max_tokens)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, top_k), dtype=torch.float32, device=dev)
+    if expert_counts is None:
+        expert_counts = torch.empty(E, dtype=torch.int32, device=dev)
+    if expert_offsets is None:
+        expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if row_route is None:
+        row_route = torch.empty(max(rows_cap, 1), dtype=torch.int32, device=dev)
+    if route_row is None:
+        route_row = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(moe_permute_workspace_size(T, top_k, E), dtype=torch.uint8, device=dev)
+    K, x_dtype = 0, MOE_BF16
+    if x is not None:
+        K = x.shape[-1]
+        x_dtype = dtype_code(x)
+        if x_out is None:
+            x_out = torch.empty((rows_cap, K), dtype=x.dtype, device=dev)
+    _check(load().moe_route_permute_align(
+        _ptr(logits), T, E, top_k, int(bool(renormalize)), _ptr(topk_ids), _ptr(topk_weights), layout, block_m,
+        max_tokens, _ptr(x), x_dtype, K, _ptr(x_out), rows_cap, _ptr(expert_counts), _ptr(expert_offsets),
+        _ptr(row_route), _ptr(route_row), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream)))
+    return dict(topk_ids=topk_ids, topk_weights=topk_weights, counts=expert_counts, offsets=expert_offsets,
+                row_route=row_route, route_row=route_row, x_out=x_out, rows_cap=rows_cap)
 
 
 def moe_permute_align_static(topk_ids, E, layout=MOE_LAYOUT_CONTIGUOUS, block_m=1, max_tokens=0, x=None,

@@ -93,51 +93,106 @@ int moe_topk_route(const float* logits, int64_t T, int E, int top_k, int renorma
                          "moe_topk_route");
 }
 
+namespace {
+
+// Argument checks of moe_permute_align (the routing ids are checked by the caller).
+int validate_permute(const char* name, int64_t T, int top_k, int E, int layout, int block_m, int max_tokens,
+                     const void* x, int x_dtype, int64_t K, const void* x_out, int64_t rows_cap,
+                     const int32_t* expert_counts, const int32_t* expert_offsets, const int32_t* row_route,
+                     const int32_t* route_row, const void* workspace, size_t workspace_bytes) {
+    const std::string n(name);
+    MOE_REQUIRE(T >= 0 && top_k >= 1 && top_k <= 1024, MOE_ERR_INVALID_ARG, n + ": bad T or top_k");
+    MOE_REQUIRE(E >= 1 && E <= 1024, MOE_ERR_INVALID_ARG, n + ": E must be in [1, 1024]");
+    MOE_REQUIRE(layout == MOE_LAYOUT_CONTIGUOUS || layout == MOE_LAYOUT_BATCHED, MOE_ERR_INVALID_ARG,
+                n + ": unknown layout");
+    MOE_REQUIRE(T * top_k < (int64_t(1) << 31), MOE_ERR_INVALID_ARG, n + ": more than 2^31 routes");
+    if (layout == MOE_LAYOUT_CONTIGUOUS) {
+        MOE_REQUIRE(block_m >= 1 && block_m <= 4096, MOE_ERR_INVALID_ARG, n + ": block_m in [1, 4096]");
+        MOE_REQUIRE(rows_cap >= moe_max_padded_rows(T, top_k, E, block_m), MOE_ERR_INVALID_ARG,
+                    n + ": rows_cap < T*top_k + E*(block_m-1)");
+    } else {
+        MOE_REQUIRE(max_tokens >= 0, MOE_ERR_INVALID_ARG, n + ": max_tokens < 0");
+        MOE_REQUIRE(rows_cap == int64_t(E) * max_tokens, MOE_ERR_INVALID_ARG,
+                    n + ": batched rows_cap must equal E*max_tokens");
+    }
+    MOE_REQUIRE(rows_cap < (int64_t(1) << 31), MOE_ERR_INVALID_ARG, n + ": rows_cap >= 2^31");
+    MOE_REQUIRE(expert_counts && expert_offsets && (row_route || rows_cap == 0) && (route_row || T == 0),
+                MOE_ERR_INVALID_ARG, n + ": null output pointer");
+    const size_t need = permute_workspace_bytes(T, top_k, E);
+    MOE_REQUIRE(workspace_bytes >= need, MOE_ERR_WORKSPACE_TOO_SMALL,
+                n + ": workspace smaller than moe_permute_workspace_size()");
+    MOE_REQUIRE(workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, MOE_ERR_ALIGNMENT,
+                n + ": workspace must be 256-byte aligned");
+    if (x) {
+        MOE_REQUIRE(is_float_dtype(x_dtype), MOE_ERR_UNSUPPORTED, n + ": x must be F32 or BF16");
+        MOE_REQUIRE(K > 0 && (K * esize(x_dtype)) % 16 == 0, MOE_ERR_ALIGNMENT,
+                    n + ": K * element size must be a multiple of 16 bytes");
+        MOE_REQUIRE(x_out || rows_cap == 0, MOE_ERR_INVALID_ARG, n + ": x given without x_out");
+        MOE_REQUIRE(aligned16(x) && aligned16(x_out), MOE_ERR_ALIGNMENT,
+                    n + ": x and x_out must be 16-byte aligned");
+    }
+    return MOE_OK;
+}
+
+// The permute launches (and the gather when x is given) of validated arguments.
+int run_permute(const char* name, const int32_t* topk_ids, int64_t T, int top_k, int E, int layout, int block_m,
+                int max_tokens, const void* x, int x_dtype, int64_t K, void* x_out, int64_t rows_cap,
+                int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_route, int32_t* route_row,
+                void* workspace, int32_t* err_word, cudaStream_t s) {
+    int rc = launch_status(launch_permute(topk_ids, T, top_k, E, layout, block_m, max_tokens, expert_counts,
+                                          expert_offsets, row_route, route_row, workspace, err_word, s),
+                           name);
+    if (rc || !x) return rc;
+    return launch_status(launch_gather_rows(x, esize(x_dtype), K, row_route, top_k,
+                                            layout == MOE_LAYOUT_CONTIGUOUS ? expert_offsets : nullptr, E,
+                                            rows_cap, x_out, s),
+                         name);
+}
+
+}  // namespace
+
 int moe_permute_align(const int32_t* topk_ids, int64_t T, int top_k, int E, int layout, int block_m,
                       int max_tokens, const void* x, int x_dtype, int64_t K, void* x_out, int64_t rows_cap,
                       int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_route, int32_t* route_row,
                       void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream) {
     g_last_error.clear();
-    MOE_REQUIRE(T >= 0 && top_k >= 1 && top_k <= 1024, MOE_ERR_INVALID_ARG, "moe_permute_align: bad T or top_k");
-    MOE_REQUIRE(E >= 1 && E <= 1024, MOE_ERR_INVALID_ARG, "moe_permute_align: E must be in [1, 1024]");
-    MOE_REQUIRE(layout == MOE_LAYOUT_CONTIGUOUS || layout == MOE_LAYOUT_BATCHED, MOE_ERR_INVALID_ARG,
-                "moe_permute_align: unknown layout");
-    MOE_REQUIRE(T * top_k < (int64_t(1) << 31), MOE_ERR_INVALID_ARG, "moe_permute_align: more than 2^31 routes");
-    if (layout == MOE_LAYOUT_CONTIGUOUS) {
-        MOE_REQUIRE(block_m >= 1 && block_m <= 4096, MOE_ERR_INVALID_ARG, "moe_permute_align: block_m in [1, 4096]");
-        MOE_REQUIRE(rows_cap >= moe_max_padded_rows(T, top_k, E, block_m), MOE_ERR_INVALID_ARG,
-                    "moe_permute_align: rows_cap < T*top_k + E*(block_m-1)");
-    } else {
-        MOE_REQUIRE(max_tokens >= 0, MOE_ERR_INVALID_ARG, "moe_permute_align: max_tokens < 0");
-        MOE_REQUIRE(rows_cap == int64_t(E) * max_tokens, MOE_ERR_INVALID_ARG,
-                    "moe_permute_align: batched rows_cap must equal E*max_tokens");
-    }
-    MOE_REQUIRE(rows_cap < (int64_t(1) << 31), MOE_ERR_INVALID_ARG, "moe_permute_align: rows_cap >= 2^31");
+    int rc = validate_permute("moe_permute_align", T, top_k, E, layout, block_m, max_tokens, x, x_dtype, K, x_out,
+                              rows_cap, expert_counts, expert_offsets, row_route, route_row, workspace,
+                              workspace_bytes);
+    if (rc) return rc;
     MOE_REQUIRE(topk_ids || T == 0, MOE_ERR_INVALID_ARG, "moe_permute_align: null topk_ids");
-    MOE_REQUIRE(expert_counts && expert_offsets && (row_route || rows_cap == 0) && (route_row || T == 0),
-                MOE_ERR_INVALID_ARG, "moe_permute_align: null output pointer");
-    const size_t need = permute_workspace_bytes(T, top_k, E);
-    MOE_REQUIRE(workspace_bytes >= need, MOE_ERR_WORKSPACE_TOO_SMALL,
-                "moe_permute_align: workspace smaller than moe_permute_workspace_size()");
-    MOE_REQUIRE(workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, MOE_ERR_ALIGNMENT,
-                "moe_permute_align: workspace must be 256-byte aligned");
-    if (x) {
-        MOE_REQUIRE(is_float_dtype(x_dtype), MOE_ERR_UNSUPPORTED, "moe_permute_align: x must be F32 or BF16");
-        MOE_REQUIRE(K > 0 && (K * esize(x_dtype)) % 16 == 0, MOE_ERR_ALIGNMENT,
-                    "moe_permute_align: K * element size must be a multiple of 16 bytes");
-        MOE_REQUIRE(x_out || rows_cap == 0, MOE_ERR_INVALID_ARG, "moe_permute_align: x given without x_out");
-        MOE_REQUIRE(aligned16(x) && aligned16(x_out), MOE_ERR_ALIGNMENT,
-                    "moe_permute_align: x and x_out must be 16-byte aligned");
-    }
+    return run_permute("moe_permute_align", topk_ids, T, top_k, E, layout, block_m, max_tokens, x, x_dtype, K,
+                       x_out, rows_cap, expert_counts, expert_offsets, row_route, route_row, workspace, err_word,
+                       as_stream(stream));
+}
+
+int moe_route_permute_align(const float* logits, int64_t T, int E, int top_k, int renormalize, int32_t* topk_ids,
+                            float* topk_weights, int layout, int block_m, int max_tokens, const void* x,
+                            int x_dtype, int64_t K, void* x_out, int64_t rows_cap, int32_t* expert_counts,
+                            int32_t* expert_offsets, int32_t* row_route, int32_t* route_row, void* workspace,
+                            size_t workspace_bytes, int32_t* err_word, void* stream) {
+    g_last_error.clear();
+    const char* name = "moe_route_permute_align";
+    MOE_REQUIRE(top_k >= 1 && top_k <= std::min(E, 32), MOE_ERR_INVALID_ARG,
+                "moe_route_permute_align: top_k must be in [1, min(E, 32)]");
+    int rc = validate_permute(name, T, top_k, E, layout, block_m, max_tokens, x, x_dtype, K, x_out, rows_cap,
+                              expert_counts, expert_offsets, row_route, route_row, workspace, workspace_bytes);
+    if (rc) return rc;
+    MOE_REQUIRE((logits && topk_ids && topk_weights) || T == 0, MOE_ERR_INVALID_ARG,
+                "moe_route_permute_align: null logits, topk_ids or topk_weights");
     cudaStream_t s = as_stream(stream);
-    int rc = launch_status(launch_permute(topk_ids, T, top_k, E, layout, block_m, max_tokens, expert_counts,
-                                          expert_offsets, row_route, route_row, workspace, err_word, s),
-                           "moe_permute_align");
-    if (rc || !x) return rc;
-    return launch_status(launch_gather_rows(x, esize(x_dtype), K, row_route, top_k,
-                                            layout == MOE_LAYOUT_CONTIGUOUS ? expert_offsets : nullptr, E,
-                                            rows_cap, x_out, s),
-                         "moe_permute_align (gather)");
+    const int64_t row_bytes = x ? K * esize(x_dtype) : 0;
+    if (route_permute_fusable(T, top_k, row_bytes))
+        return launch_status(launch_route_permute(logits, T, E, top_k, renormalize, topk_ids, topk_weights, layout,
+                                                  block_m, max_tokens, expert_counts, expert_offsets, row_route,
+                                                  route_row, x, row_bytes, x ? x_out : nullptr, err_word, s),
+                             name);
+    if (T > 0) {
+        rc = launch_status(launch_topk_route(logits, T, E, top_k, renormalize, topk_ids, topk_weights, s), name);
+        if (rc) return rc;
+    }
+    return run_permute(name, topk_ids, T, top_k, E, layout, block_m, max_tokens, x, x_dtype, K, x_out, rows_cap,
+                       expert_counts, expert_offsets, row_route, route_row, workspace, err_word, s);
 }
 
 namespace {

@@ -28,6 +28,13 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int top_k, int E, int 
 cudaError_t launch_gather_rows(const void* x, int esize, int64_t K, const int32_t* row_route, int top_k,
                                const int32_t* offsets, int E, int64_t rows_cap, void* x_out, cudaStream_t s);
 
+// route + permute (+ gather when x_out is set) in one launch; only for the sizes route_permute_fusable accepts
+bool route_permute_fusable(int64_t T, int top_k, int64_t row_bytes);
+cudaError_t launch_route_permute(const float* logits, int64_t T, int E, int top_k, int renorm, int32_t* ids,
+                                 float* weights, int layout, int block_m, int max_tokens, int32_t* counts,
+                                 int32_t* offsets, int32_t* row_route, int32_t* route_row, const void* x,
+                                 int64_t row_bytes, void* x_out, int32_t* err_word, cudaStream_t s);
+
 cudaError_t launch_topk_reduce(const void* y, int y_dtype, const int32_t* ids, const float* w, int64_t T,
                                int top_k, int E, int64_t K, void* out, int out_dtype, cudaStream_t s);
 cudaError_t launch_rows_topk_reduce(const void* y, int y_dtype, int64_t rows, const int32_t* route_row,

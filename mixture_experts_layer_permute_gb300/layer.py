@@ -4,7 +4,7 @@
 workspace_shapes() idea of the "Fused MoE Modular Kernel" design doc: the
 intermediates are declared up front and reused), and ``forward`` issues
 
-    moe_topk_route -> moe_permute_align -> moe_gemm1_swiglu -> moe_gemm2
+    moe_route_permute_align (moe_topk_route + moe_permute_align) -> moe_gemm1_swiglu -> moe_gemm2
         -> moe_unpermute_topk_reduce          (contiguous layout)
 
 with, for MXFP8 weights and ``act_quant=True``, the activations quantised on
@@ -20,10 +20,12 @@ or, for the batched layout fed with expert-major rows (T = 0),
 
 or, for the batched layout fed with tokens (T > 0),
 
-    moe_topk_route -> moe_permute_align (batched rows, capacity max_tokens)
+    moe_route_permute_align (batched rows, capacity max_tokens)
         -> moe_gemm1_swiglu -> moe_gemm2 -> moe_batched_topk_reduce (token order)
 
-with no host synchronisation.  Every step runs in libmoe_layer's kernels.
+Given ``topk_ids``/``topk_weights`` instead of router logits, moe_permute_align
+takes the place of moe_route_permute_align.  There is no host synchronisation,
+and every step runs in libmoe_layer's kernels.
 The marshalled argument lists of the C calls are kept between calls with the
 same tensors and stream, so a decode step spends a few microseconds per call
 on the host; ``capture`` records one forward into a CUDA graph whose replay
@@ -115,6 +117,8 @@ class MoELayer:
                 raise ValueError("MoELayer.forward takes contiguous device tensors")
         if w1.shape[0] != self.E or w2.shape[0] != self.E:
             raise ValueError("weight expert count does not match the layer")
+        if logits is not None and tuple(logits.shape) != (self.T, self.E):
+            raise ValueError(f"logits must be ({self.T}, {self.E})")
         if self.layout == B.MOE_LAYOUT_CONTIGUOUS or self.T > 0:
             if tuple(x.shape) != (self.T, self.K) or x.dtype != self.act_dtype:
                 raise ValueError(f"x must be ({self.T}, {self.K}) {self.act_dtype}")
@@ -147,18 +151,17 @@ class MoELayer:
                                                               _p(row_weights), E, mt, K, self.out.data_ptr(), adt,
                                                               stream), "reduce"))
             return calls
-        if logits is not None:
-            calls.append((lib.moe_topk_route, (logits.data_ptr(), T, logits.shape[1], k, 1, self.ids.data_ptr(),
-                                               self.weights.data_ptr(), stream), "route"))
+        perm_args = (self.layout, self.block_m, 0, x.data_ptr(), adt, K, self.x_perm.data_ptr(), self.rows_cap,
+                     self.counts.data_ptr(), self.offsets.data_ptr(), self.row_route.data_ptr(),
+                     self.route_row.data_ptr(), self.workspace.data_ptr(), self.workspace.numel(),
+                     self.err.data_ptr(), stream)
+        if logits is not None:   # routing, placement and gather (one launch for decode-sized batches)
+            calls.append((lib.moe_route_permute_align, (logits.data_ptr(), T, E, k, 1, self.ids.data_ptr(),
+                                                        self.weights.data_ptr()) + perm_args, "route_permute"))
             ids, weights = self.ids, self.weights
         else:
             ids, weights = topk_ids, topk_weights
-        calls.append((lib.moe_permute_align, (ids.data_ptr(), T, k, E, self.layout, self.block_m, 0, x.data_ptr(),
-                                              adt, K, self.x_perm.data_ptr(), self.rows_cap,
-                                              self.counts.data_ptr(), self.offsets.data_ptr(),
-                                              self.row_route.data_ptr(), self.route_row.data_ptr(),
-                                              self.workspace.data_ptr(), self.workspace.numel(),
-                                              self.err.data_ptr(), stream), "permute"))
+            calls.append((lib.moe_permute_align, (ids.data_ptr(), T, k, E) + perm_args, "permute"))
         if self.act_quant:
             if wdt != B.MOE_E4M3:
                 raise ValueError("act_quant needs MXFP8 (E4M3 + scales) weights")
@@ -204,17 +207,17 @@ class MoELayer:
         lib = self.lib
         I, K, E, T, k, mt = self.I, self.K, self.E, self.T, self.top_k, self.max_tokens
         calls = []
+        perm_args = (self.layout, 1, mt, x.data_ptr(), adt, K, self.x_perm.data_ptr(), self.rows_cap,
+                     self.counts.data_ptr(), self.offsets.data_ptr(), self.row_route.data_ptr(),
+                     self.route_row.data_ptr(), self.workspace.data_ptr(), self.workspace.numel(),
+                     self.err.data_ptr(), stream)
         if logits is not None:
-            calls.append((lib.moe_topk_route, (logits.data_ptr(), T, logits.shape[1], k, 1, self.ids.data_ptr(),
-                                               self.weights.data_ptr(), stream), "route"))
+            calls.append((lib.moe_route_permute_align, (logits.data_ptr(), T, E, k, 1, self.ids.data_ptr(),
+                                                        self.weights.data_ptr()) + perm_args, "route_permute"))
             ids, weights = self.ids, self.weights
         else:
             ids, weights = topk_ids, topk_weights
-        calls.append((lib.moe_permute_align, (ids.data_ptr(), T, k, E, self.layout, 1, mt, x.data_ptr(), adt, K,
-                                              self.x_perm.data_ptr(), self.rows_cap, self.counts.data_ptr(),
-                                              self.offsets.data_ptr(), self.row_route.data_ptr(),
-                                              self.route_row.data_ptr(), self.workspace.data_ptr(),
-                                              self.workspace.numel(), self.err.data_ptr(), stream), "permute"))
+            calls.append((lib.moe_permute_align, (ids.data_ptr(), T, k, E) + perm_args, "permute"))
         calls.append((lib.moe_gemm1_swiglu, (self.x_perm.data_ptr(), adt, None, self.layout, self.counts.data_ptr(), None,
                                              mt, self.rows_cap, E, K, I, w1.data_ptr(), _p(w1_scale), wdt,
                                              w1_layout, self.impl, self.h.data_ptr(), adt, None,
@@ -287,12 +290,18 @@ class MoELayer:
         """Kernels one forward launches (for launch accounting)."""
         if self.layout == B.MOE_LAYOUT_BATCHED and self.T == 0:
             return 2 if self.weight_in_gemm2 else 3
-        n = 3 + 1 + (1 if self.T * self.top_k <= 1024 else 2) + 1   # gemm1 gemm2 reduce, gather, permute, route
+        R = self.T * self.top_k
+        routed = any(name == "route_permute" for _, _, name in (self._plan or []))
+        if routed and 1 <= self.T <= 128 and R <= 1024:
+            front = 1                                                 # route + permute + gather in one launch
+        else:
+            front = (1 if routed else 0) + (1 if R <= 1024 else 2) + 1   # route, permute, gather
+        n = front + 3                                                 # gemm1 gemm2 reduce
         if any(name == "gemm1" and fn is self.lib.moe_experts_fused for fn, _, name in (self._plan or [])):
             n -= 1                                                    # GEMM 1 + GEMM 2 in one launch
         if self.act_quant:
             n += 1                                                    # quantise x rows (h: in GEMM 1)
-        return n if any(name == "route" for _, _, name in (self._plan or [])) else n - 1
+        return n
 
     def device_errors(self, reset: bool = True) -> int:
         """Device error bits (MOE_DEVERR_*) accumulated since the last reset (synchronises)."""

@@ -103,6 +103,24 @@ def test_permute_validation(lib):
     assert rc == 3
 
 
+def test_route_permute_validation(lib):
+    fake = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
+
+    def call(T=4, E=8, k=2, layout=0, bm=1, mt=0, x=None, K=0, x_out=None, rows_cap=8, ws=fake, ws_bytes=1 << 20,
+             logits=fake):
+        return lib.moe_route_permute_align(logits, T, E, k, 1, fake, fake, layout, bm, mt, x, 1, K, x_out,
+                                           rows_cap, fake, fake, fake, fake, ws, ws_bytes, None, None)
+    assert call(k=9) == 1 and lib_error().startswith("moe_route_permute_align")      # top_k > E
+    assert call(k=33, E=64) == 1                                                      # top_k > 32
+    assert call(E=2000) == 1                                                          # E > 1024
+    assert call(bm=16) == 1 and "rows_cap" in lib_error()                             # rows_cap too small
+    assert call(ws_bytes=0) == 4                                                      # workspace too small
+    assert call(ws=ctypes.c_void_p(0x1004)) == 3                                      # misaligned workspace
+    assert call(layout=1, mt=16, rows_cap=100) == 1                                   # batched rows_cap
+    assert call(x=fake, K=12, x_out=fake) == 3                                        # 24-byte rows
+    assert call(logits=None) == 1 and "null" in lib_error()                           # no logits
+
+
 def test_gemm_validation(lib):
     fake = ctypes.c_void_p(0x1000)
     # K not a multiple of 32

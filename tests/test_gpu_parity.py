@@ -43,6 +43,30 @@ def test_route_bit_exact(moe, T, E, k, renorm):
     np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("E", [64, 1024])
+def test_route_signed_zeros_and_infinities(moe, E):
+    """-0 and +0 compare equal, so among zero logits the lower index wins whatever the signs; -inf logits are
+    chosen last and get weight 0."""
+    T, k = 8, 5
+    g = torch.Generator().manual_seed(E)
+    logits = -torch.rand((T, E), generator=g) - 1.0          # every other logit <= -1
+    for t in range(T):
+        pos = torch.randperm(E, generator=g)[:3]
+        logits[t, torch.randperm(E, generator=g)[: E // 2]] = float("-inf")
+        logits[t, pos] = torch.tensor([-0.0 if (n + t) % 2 == 0 else 0.0 for n in range(3)])
+    if E == 1024:
+        logits[:, 3:] = float("-inf")                          # three finite logits: two -inf ones are chosen
+        logits[:, :3] = torch.tensor([-0.0, -1.5, 0.0])
+    for renorm in (True, False):
+        ids, wts = moe.moe_topk_route(logits.to(DEV), k, renormalize=renorm)
+        rids, rw = oracle.topk_route(logits.numpy(), k, renormalize=renorm)
+        assert np.array_equal(ids.cpu().numpy(), rids)
+        np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+        res = moe.moe_route_permute_align(logits.to(DEV), k, renormalize=renorm)
+        assert torch.equal(res["topk_ids"], ids)
+        assert torch.equal(res["topk_weights"].view(torch.int32), wts.view(torch.int32))
+
+
 def test_route_zipf_prefill(moe):
     w = wl.prefill()
     logits = wl.router_logits(w, 0)
@@ -133,6 +157,88 @@ def test_permute_batched_bit_exact(moe, T, k, E, cap):
         for q in range(ref["expert_num_tokens"][e]):
             r = ref["row_route"][e, q]
             assert torch.equal(xo[e, q], x[r // k])
+
+
+# ----------------------------------------------------------------------------
+# routing + placement + gather in one call
+# ----------------------------------------------------------------------------
+
+# T, E, k, renormalize, layout, block_m, max_tokens, x dtype (None: no gather), K
+ROUTE_PERMUTE_CASES = [
+    (1, 128, 8, True, "contiguous", 1, 0, torch.bfloat16, 4096),     # decode T = 1 at full K: one launch
+    (64, 128, 8, True, "contiguous", 1, 0, torch.bfloat16, 4096),    # decode T = 64
+    (128, 128, 8, True, "contiguous", 16, 0, torch.bfloat16, 256),   # 1024 routes, padded rows: still one launch
+    (129, 128, 8, True, "contiguous", 1, 0, torch.bfloat16, 256),    # one token more: the separate launches
+    (33, 40, 5, False, "contiguous", 4, 0, torch.float32, 96),       # exact ties, plain softmax, fp32 rows
+    (7, 1024, 32, True, "contiguous", 1, 0, torch.bfloat16, 64),     # 32 logits per lane
+    (20, 32, 1, True, "contiguous", 128, 0, torch.bfloat16, 8),      # top_k = 1, 16-byte rows, wide padding
+    (5, 3, 3, True, "contiguous", 1, 0, None, 0),                    # top_k = E, no gather
+    (100, 16, 4, True, "batched", 1, 12, torch.bfloat16, 64),        # capacity drops routes (one launch)
+    (2000, 64, 4, True, "batched", 1, 200, torch.bfloat16, 32),      # batched, separate launches
+]
+
+
+@pytest.mark.parametrize("T,E,k,renorm,layout,bm,cap,xdt,K", ROUTE_PERMUTE_CASES)
+def test_route_permute_bit_exact(moe, T, E, k, renorm, layout, bm, cap, xdt, K):
+    """moe_route_permute_align against the oracle's routing and placement, and bit-identical to
+    moe_topk_route followed by moe_permute_align."""
+    w = wl.scaled(wl.decode(T), E=E, top_k=k)
+    logits = wl.router_logits(w, seed=T + E)
+    if E == 40:
+        logits = torch.round(logits * 2) / 2          # exact ties: lower index must win
+    x = wl._normal((T, K), 1.0, 5, "x", 0, "cpu", xdt) if xdt is not None else None
+    lay = moe.MOE_LAYOUT_CONTIGUOUS if layout == "contiguous" else moe.MOE_LAYOUT_BATCHED
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    xd = x.to(DEV) if x is not None else None
+    res = moe.moe_route_permute_align(logits.to(DEV), k, renormalize=renorm, layout=lay, block_m=bm,
+                                      max_tokens=cap, x=xd, err_word=err)
+    rids, rw = oracle.topk_route(logits.numpy(), k, renormalize=renorm)
+    assert np.array_equal(res["topk_ids"].cpu().numpy(), rids)
+    np.testing.assert_allclose(res["topk_weights"].cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+
+    # the separate calls give the same bits
+    ids2, w2 = moe.moe_topk_route(logits.to(DEV), k, renormalize=renorm)
+    err2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sep = moe.moe_permute_align(ids2, E, lay, bm, cap, x=xd, err_word=err2)
+    assert torch.equal(res["topk_ids"], ids2)
+    assert torch.equal(res["topk_weights"].view(torch.int32), w2.view(torch.int32))
+    for key in ("counts", "offsets", "route_row"):
+        assert torch.equal(res[key], sep[key]), key
+    assert int(err.item()) == int(err2.item())
+
+    if lay == moe.MOE_LAYOUT_CONTIGUOUS:
+        ref = oracle.permute_contiguous(rids, E, bm)
+        rows = int(ref["offsets"][E])
+        assert np.array_equal(res["counts"].cpu().numpy(), ref["counts"])
+        assert np.array_equal(res["offsets"].cpu().numpy(), ref["offsets"])
+        assert np.array_equal(res["row_route"][:rows].cpu().numpy(), ref["sorted_route"])
+        route_of_row = ref["sorted_route"]
+    else:
+        ref = oracle.permute_batched(rids, E, cap)
+        rows = E * cap
+        assert np.array_equal(res["counts"].cpu().numpy(), ref["expert_num_tokens"])
+        assert np.array_equal(res["offsets"].cpu().numpy(), np.arange(E + 1) * cap)
+        assert np.array_equal(res["row_route"][:rows].cpu().numpy(), ref["row_route"].reshape(-1))
+        route_of_row = ref["row_route"].reshape(-1)
+    assert np.array_equal(res["route_row"].cpu().numpy(), ref["route_row"])
+    assert int(err.item()) == ref["err"]
+    assert torch.equal(res["row_route"][:rows], sep["row_route"][:rows])
+    if x is not None:
+        # every routed row is its token's row, bit for bit
+        valid = route_of_row >= 0
+        src = torch.from_numpy(route_of_row[valid] // k).long()
+        xo = res["x_out"][:rows].cpu()[torch.from_numpy(valid)]
+        bits = torch.int16 if xdt == torch.bfloat16 else torch.int32
+        assert torch.equal(xo.view(bits), x[src].view(bits))
+
+
+def test_route_permute_empty(moe):
+    """T = 0: no routes, every count and offset is zero."""
+    logits = torch.empty((0, 16), dtype=torch.float32, device=DEV)
+    res = moe.moe_route_permute_align(logits, 2, x=torch.empty((0, 64), dtype=torch.bfloat16, device=DEV))
+    torch.cuda.synchronize()
+    assert res["topk_ids"].shape == (0, 2)
+    assert not torch.any(res["counts"]) and not torch.any(res["offsets"])
 
 
 # ----------------------------------------------------------------------------

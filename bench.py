@@ -489,8 +489,8 @@ def run_ours(args, rank, world, local_rank):
 
 def run_e2e(args, insts, dev):
     """Same metric through the public API with host buffers: every step copies its inputs (x and router logits
-    of every pass, packed in one pinned staging buffer: one H2D copy) to the device, runs the layer and reads each
-    pass's output back to pinned host memory."""
+    of every pass, packed in one pinned staging buffer: one H2D copy) to the device, runs the layer (MoELayer.forward
+    per pass) and reads each pass's output back to pinned host memory."""
     import torch
     # staging: the inputs of all passes back to back (256-byte aligned views), on the host (pinned) and device
     parts = []
@@ -538,27 +538,37 @@ def run_e2e(args, insts, dev):
     def d2h_of(inst, ho):
         return lambda: ho.copy_(inst.layer.out, non_blocking=True)
 
-    # one CUDA graph per pass (MoELayer.capture); the first also holds the step's H2D copy
-    graphs = None
-    if not args.eager:
-        try:
-            graphs = []
-            for n, (inst, (ho, dx, dl)) in enumerate(zip(insts, host)):
-                graphs.append(inst.layer.capture(dx, inst.W1, inst.W2, before=h2d if n == 0 else None,
-                                                 after=d2h_of(inst, ho), **kwargs_of(inst, dl)))
-        except RuntimeError as exc:
-            print(f"bench: e2e graph capture failed ({exc}); e2e runs eagerly", file=sys.stderr)
-            graphs = None
+    # one CUDA graph per step: the step's H2D copy, then the passes; each pass's output is read back on a side
+    # stream while the next pass computes, and the side stream rejoins before the step ends
+    side = torch.cuda.Stream(device=dev)
 
-    def step():
-        if graphs is not None:
-            for g in graphs:
-                g.replay()
-            return
+    def body():
+        cur = torch.cuda.current_stream()
         h2d()
         for inst, (ho, dx, dl) in zip(insts, host):
             inst.layer.forward(dx, inst.W1, inst.W2, **kwargs_of(inst, dl))
-            d2h_of(inst, ho)()
+            side.wait_stream(cur)
+            with torch.cuda.stream(side):
+                d2h_of(inst, ho)()
+        cur.wait_stream(side)
+
+    graph = None
+    if not args.eager:
+        try:
+            body()                    # eager once: builds each layer's call plan for these tensors
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                body()
+        except RuntimeError as exc:
+            print(f"bench: e2e graph capture failed ({exc}); e2e runs eagerly", file=sys.stderr)
+            graph = None
+
+    def step():
+        if graph is not None:
+            graph.replay()
+        else:
+            body()
 
     for _ in range(max(1, args.warmup)):
         step()

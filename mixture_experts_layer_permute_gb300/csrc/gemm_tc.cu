@@ -42,6 +42,11 @@
 //   factor would leave bf16's range).  The MMA takes its A operand from TMEM.
 //   Tokens per tile are capped at 64.
 //
+// Wide tiles (bf16, batched layout): 256 token rows x 256 weight rows as two
+// 128-row MMA halves that share each B stage, so an expert of up to 256 rows
+// streams each weight tile once; the two halves fill TMEM, so there is one
+// accumulator and 8 epilogue warps (warp w: half (w-2)/4, lane quarter w%4).
+//
 // Mixed tiles (bf16): one launch serves experts of 64 rows or more with
 // normal 128-row tiles and smaller experts with a swap-AB tile, so a skewed
 // routing does not pay a mostly empty 128-row tile per small expert.
@@ -82,32 +87,43 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 //   V_E4M3:   smem: 9 code stages of 128 rows x 128 B, then 4 token slots of 2 x 8 KB;
 //             TMEM: two 64-column accumulators, then 4 bf16 A tiles of 64 columns;
 //             736 threads (+ 16 converter warps, + 1 token warp); up to 64 tokens per tile
-enum { V_BF16 = 0, V_E4M3 = 1, V_SWAP64 = 2 };
+//   V_WIDE:   batched-layout normal tiles of 256 token rows (two 128-row MMA halves sharing each B stage):
+//             smem [A rows 0..127 16 KB][A rows 128..255 16 KB][B 32 KB] x 3 stages; TMEM: one accumulator of
+//             two 256-column halves (the whole 512 columns, so no second buffer); 320 threads (8 epilogue
+//             warps, one per TMEM lane quarter and half).  Each stage carries twice the MMA work of a V_BF16
+//             stage for 4/3 of its bytes.
+enum { V_BF16 = 0, V_E4M3 = 1, V_SWAP64 = 2, V_WIDE = 3 };
 
 template <int V>
 struct Cfg {
     static constexpr bool W8 = V == V_E4M3;
     static constexpr bool NARROW = V == V_SWAP64;
+    static constexpr bool WIDE = V == V_WIDE;
     static constexpr int KSUB = W8 ? 2 : 1;                     // 64-wide k-blocks per stage
-    static constexpr int STAGES = W8 ? 9 : (NARROW ? 8 : 4);    // bf16: operand stages; E4M3: code stages
+    static constexpr int STAGES = W8 ? 9 : (NARROW ? 8 : (WIDE ? 3 : 4));   // bf16: operand stages; E4M3: code stages
+    static constexpr int A_PARTS = WIDE ? 2 : 1;                // 128-row A tiles per stage
     static constexpr int A_SLOTS = 4;                           // E4M3: TMEM A tiles (+ token tiles)
     static constexpr int TOK_SPAN = (W8 || NARROW) ? 64 : 256;  // swap-AB tokens per tile
-    static constexpr int B_OFF = W8 ? 0 : A_BYTES;              // bf16: B operand offset in a stage
+    static constexpr int B_OFF = W8 ? 0 : A_PARTS * A_BYTES;    // bf16: B operand offset in a stage
     static constexpr int B_SUB = TOK_SPAN * BK * 2;             // token bytes per 64-wide k-block (swap)
     static constexpr int B_BYTES = W8 ? 0 : (NARROW ? B_SUB : 256 * BK * 2);
-    static constexpr int STAGE_BYTES = W8 ? BM * BK * KSUB : A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = W8 ? BM * BK * KSUB : A_PARTS * A_BYTES + B_BYTES;
     static constexpr int TOK_OFF = STAGES * STAGE_BYTES;        // E4M3: token slots after the code ring
     static constexpr int TOK_SLOT = B_SUB * KSUB;
-    static constexpr int THREADS = W8 ? 192 + kConvThreads + 32 : 192;   // E4M3: + converters + token warp
+    static constexpr int EPI_WARPS = WIDE ? 8 : 4;
+    static constexpr int THREADS = W8 ? 192 + kConvThreads + 32 : 64 + 32 * EPI_WARPS;   // E4M3: + converters + token warp
     static constexpr int TOK_WARP = 6 + kConvThreads / 32;
     static constexpr int SMEM = STAGES * STAGE_BYTES + (W8 ? A_SLOTS * TOK_SLOT : 0) + 1024;
-    static constexpr int ACC_STRIDE = (W8 || NARROW) ? TOK_SPAN : ACC_COLS; // TMEM columns per accumulator
+    static constexpr int ACC_STRIDE = (W8 || NARROW) ? TOK_SPAN : ACC_COLS; // TMEM columns per accumulator (half)
+    static constexpr int NBUF = WIDE ? 1 : 2;                   // accumulators (the wide one fills TMEM)
     static constexpr int A_TMEM = 2 * ACC_STRIDE;               // E4M3: first A tile column
     static constexpr int A_COLS = KSUB * BK / 2;                // E4M3: TMEM columns per A tile
-    static constexpr int TMEM_USED = W8 ? A_TMEM + A_SLOTS * A_COLS : 2 * ACC_STRIDE;
+    static constexpr int TMEM_USED = W8 ? A_TMEM + A_SLOTS * A_COLS : (WIDE ? 2 * ACC_COLS : 2 * ACC_STRIDE);
 };
 static_assert(Cfg<V_BF16>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed the TMEM allocation");
 static_assert(Cfg<V_SWAP64>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed the TMEM allocation");
+static_assert(Cfg<V_WIDE>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed the TMEM allocation");
+static_assert(Cfg<V_WIDE>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
 static_assert(Cfg<V_E4M3>::TMEM_USED <= TMEM_COLS, "E4M3 accumulators and A tiles exceed the TMEM allocation");
 static_assert(Cfg<V_BF16>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
 static_assert(Cfg<V_SWAP64>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
@@ -344,6 +360,9 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
     if constexpr (Cfg<V>::NARROW) {
         if (!p.swap || p.mixed) return;   // the narrow ring holds swap-AB tiles only (the host never asks more)
     }
+    if constexpr (Cfg<V>::WIDE) {
+        if (p.swap || p.mixed || p.fused) return;   // normal tiles only (the host never asks more)
+    }
     extern __shared__ uint8_t smem_raw[];
     __shared__ ExpertTable tab;
     __shared__ Ctrl ctrl;
@@ -365,7 +384,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&ctrl.acc_full[b], 1);
-            ptx::mbar_init(&ctrl.acc_empty[b], 4);
+            ptx::mbar_init(&ctrl.acc_empty[b], Cfg<V>::EPI_WARPS);
         }
         ptx::mbar_init(&ctrl.drain, 1);
         ctrl.abort = 0;
@@ -420,9 +439,10 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                 const uint64_t pol_w = tl.swap ? pol_stream : pol_keep;
                 constexpr int KSUB = Cfg<V>::KSUB;
                 const uint32_t wbytes = W8 ? uint32_t(BM * BK * KSUB) : uint32_t(A_BYTES);
+                const int aparts = (Cfg<V>::WIDE && tl.rows > BM) ? 2 : 1;   // wide tiles: second row half used
                 const uint32_t bytes = W8 ? wbytes
                                           : (tl.swap ? wbytes + uint32_t(nbox * TOK_BOX * BK * 2)
-                                                     : uint32_t(A_BYTES + Cfg<V>::B_BYTES));
+                                                     : uint32_t(aparts * A_BYTES + Cfg<V>::B_BYTES));
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -449,6 +469,8 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                                              int32_t(tl.row0 + b * TOK_BOX), pol_a);
                     } else {
                         ptx::tma_load_2d(sa, mact, &ctrl.full[s], k0, int32_t(tl.row0), pol_a);
+                        if (aparts == 2)
+                            ptx::tma_load_2d(sa + A_BYTES, mact, &ctrl.full[s], k0, int32_t(tl.row0 + BM), pol_a);
                     }
                 }
             }
@@ -468,10 +490,11 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             uint32_t it = 0, tc = 0;
             for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x, ++tc) {
                 const Tile tl = decode_tile(tab, p, t);
-                const int buf = tc & 1;
-                const uint32_t aph = (tc >> 1) & 1;
+                const int buf = Cfg<V>::NBUF == 2 ? int(tc & 1) : 0;
+                const uint32_t aph = Cfg<V>::NBUF == 2 ? (tc >> 1) & 1 : tc & 1;
                 if (!wait_bar(&ctrl.acc_empty[buf], aph ^ 1, ctrl, p.err_word)) break;
                 ptx::tc_fence_after();
+                const bool half2 = Cfg<V>::WIDE && tl.rows > BM;   // wide tiles: MMAs for rows 128..255
                 int n_mma = 256;
                 if (tl.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
                 const uint32_t idesc = ptx::idesc_bf16(BM, n_mma);
@@ -508,6 +531,10 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                             const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
                             const uint64_t bd = ptx::smem_desc_sw128(sb + kk * UMMA_K * 2);
                             ptx::mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                            if (half2) {
+                                const uint64_t ad2 = ptx::smem_desc_sw128(sa + A_BYTES + kk * UMMA_K * 2);
+                                ptx::mma_f16(d_tmem + ACC_COLS, ad2, bd, idesc, (kb | kk) != 0);
+                            }
                         }
                         ptx::mma_commit(&ctrl.empty[s]);
                     }
@@ -634,18 +661,20 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const int half = Cfg<V>::WIDE ? (warp - 2) >> 2 : 0;   // wide tiles: row half of this warp
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         uint32_t tc = 0;
         for (int32_t t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const Tile tl = decode_tile(tab, p, t);
-            const int buf = tc & 1;
-            const uint32_t aph = (tc >> 1) & 1;
+            const int buf = Cfg<V>::NBUF == 2 ? int(tc & 1) : 0;
+            const uint32_t aph = Cfg<V>::NBUF == 2 ? (tc >> 1) & 1 : tc & 1;
             if (!wait_bar(&ctrl.acc_full[buf], aph, ctrl, p.err_word)) break;
             ptx::tc_fence_after();
-            const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * Cfg<V>::ACC_STRIDE);
+            const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * Cfg<V>::ACC_STRIDE + half * ACC_COLS);
             if (!tl.swap) {
-              if constexpr (V == V_BF16) {   // the other variants run swap-AB tiles only
-                const int r = q * 32 + lane;                  // tile row of this thread
+              if constexpr (V == V_BF16 || V == V_WIDE) {   // the other variants run swap-AB tiles only
+               if (half * BM < tl.rows) {                     // (a wide tile may have no second half)
+                const int r = half * BM + q * 32 + lane;      // tile row of this thread
                 const bool valid = r < tl.rows;
                 const int64_t row = tl.row0 + r;
                 int64_t dst_row = -1;                         // GEMM 2: destination row, weight
@@ -677,6 +706,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                     else store_y_chunk(p, vb, dst_row, wt, tl.nb, c + 1);
                     if (c + 2 < ACC_COLS / 32) ptx::tmem_ld_wait_regs(va);
                 }
+               }
               }
             } else {
                 // swap-AB: TMEM lane = weight row of the tile, column = token
@@ -964,16 +994,24 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     p.out_dtype = g.out_dtype;
     p.out_rows = g.out_rows;
     p.err_word = g.err_word;
-    // bf16 swap-AB launches use the narrow 8-stage ring (64-token spans)
-    const int variant = w8 ? V_E4M3 : (swap ? V_SWAP64 : V_BF16);
-    p.span = swap ? (variant == V_E4M3 ? Cfg<V_E4M3>::TOK_SPAN : Cfg<V_SWAP64>::TOK_SPAN) : BM;
+    // bf16 swap-AB launches use the narrow 8-stage ring (64-token spans).  Normal tiles of the batched layout
+    // are 256 rows, so one tile covers an expert of up to max_tokens = 256 and streams each weight tile once;
+    // the contiguous layout keeps 128-row tiles, whose second accumulator hides the epilogue (measured on the
+    // skewed prefill: 256-row tiles took GEMM 1 from 0.629 to 0.665 ms)
+    const int variant = w8 ? V_E4M3
+                           : (swap ? V_SWAP64
+                                   : ((mixed || g.layout == MOE_LAYOUT_CONTIGUOUS) ? V_BF16 : V_WIDE));
+    p.span = swap ? (variant == V_E4M3 ? Cfg<V_E4M3>::TOK_SPAN : Cfg<V_SWAP64>::TOK_SPAN)
+                  : (variant == V_WIDE ? 2 * BM : BM);
     p.w_scale = g.w_scale;
     p.wrows = wrows;
     p.nsb = kdim / 32;
     p.skip_first_copy = timeout_test_hook() ? 1 : 0;
 
-    int rc = variant == V_E4M3 ? set_smem_attr<V_E4M3>()
-                               : (variant == V_SWAP64 ? set_smem_attr<V_SWAP64>() : set_smem_attr<V_BF16>());
+    int rc = variant == V_E4M3     ? set_smem_attr<V_E4M3>()
+             : variant == V_SWAP64 ? set_smem_attr<V_SWAP64>()
+             : variant == V_WIDE   ? set_smem_attr<V_WIDE>()
+                                   : set_smem_attr<V_BF16>();
     if (rc) return rc;
     // upper bound on the tiles, then one CTA per SM at most
     const int span = p.span;
@@ -989,6 +1027,9 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     else if (variant == V_SWAP64)
         gemm_tc_kernel<V_SWAP64><<<grid, Cfg<V_SWAP64>::THREADS, Cfg<V_SWAP64>::SMEM, s>>>(
             maps.act, maps.w, maps.act_s, maps.w_s, p);
+    else if (variant == V_WIDE)
+        gemm_tc_kernel<V_WIDE><<<grid, Cfg<V_WIDE>::THREADS, Cfg<V_WIDE>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
+                                                                                     maps.w_s, p);
     else
         gemm_tc_kernel<V_BF16><<<grid, Cfg<V_BF16>::THREADS, Cfg<V_BF16>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
                                                                                      maps.w_s, p);

@@ -432,6 +432,38 @@ def test_gemm2(moe, impl, shape, weighted):
     assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 {impl}")
 
 
+@pytest.mark.parametrize("impl", ["tcgen05", "auto"])
+@pytest.mark.parametrize("maxT", [300, 256, 140])
+@pytest.mark.parametrize("w1_layout", [0, 1])
+def test_gemms_batched_layout(moe, impl, maxT, w1_layout):
+    """Batched (E, max_tokens, K) rows with counts above 128 and 256: normal tiles of 256 rows, the second
+    half full, ragged or empty, both W1 layouts, GEMM 2 with the per-row weight."""
+    E, K, I = 5, 256, 256
+    w = wl.scaled(wl.tiny(), T=1, K=K, I=I, E=E, top_k=1, x_std=1.0, w_std=0.05)
+    g = torch.Generator().manual_seed(maxT + w1_layout)
+    counts = torch.tensor([maxT, maxT - 1, 129, 128, 7][:E], dtype=torch.int32).clamp(max=maxT)
+    x = wl._normal((E, maxT, K), 1.0, 11, "x", 0, "cpu", torch.bfloat16)
+    rw = torch.rand((E, maxT), generator=g)
+    W1 = wl.expert_weights(w, "W1", 4).to(torch.bfloat16)
+    W2 = wl.expert_weights(w, "W2", 4).to(torch.bfloat16)
+    offs = torch.arange(E + 1, dtype=torch.int32) * maxT
+    h = moe.moe_gemm1_swiglu(x.to(DEV).reshape(E * maxT, K), counts.to(DEV), offs.to(DEV), W1.to(DEV), I,
+                             layout=moe.MOE_LAYOUT_BATCHED, max_tokens=maxT, w1_layout=w1_layout,
+                             impl=_impl(moe, impl))
+    y = moe.moe_gemm2(h, counts.to(DEV), offs.to(DEV), W2.to(DEV), E * maxT, layout=moe.MOE_LAYOUT_BATCHED,
+                      max_tokens=maxT, route_weights=rw.to(DEV).reshape(-1), impl=_impl(moe, impl))
+    torch.cuda.synchronize()
+    hc, yc = h.cpu().reshape(E, maxT, I), y.cpu().reshape(E, maxT, K)
+    for e in range(E):
+        c = int(counts[e])
+        ids = np.full(c, e, dtype=np.int32)
+        href = oracle.expert_gate_up(wl.to_numpy(x[e, :c]), ids, wl.to_numpy(W1), w1_layout=w1_layout)
+        assert_close(to_f64(hc[e, :c]), href, TOL_BF16, f"batched gemm1 expert {e}")
+        yref = oracle.expert_down(wl.to_numpy(hc[e, :c]), ids, wl.to_numpy(W2))
+        yref = yref * rw[e, :c].numpy().astype(np.float64)[:, None]
+        assert_close(to_f64(yc[e, :c]), yref, TOL_BF16, f"batched gemm2 expert {e}")
+
+
 E4M3_SHAPES = [  # T, k, E, K, I
     (96, 4, 8, 512, 256),            # ~48 tokens per expert
     (300, 1, 2, 256, 128),           # ~150 tokens per expert: three 64-token segments

@@ -672,6 +672,34 @@ def test_layer_bf16_small(moe, impl, bm):
     assert layer.device_errors() == 0
 
 
+@pytest.mark.parametrize("T,layout", [(128, "contiguous"), (129, "contiguous"), (100, "batched"),
+                                      (129, "batched")])
+def test_layer_routing_launch_boundary(moe, T, layout):
+    """Router logits in, on both sides of the one-launch routing limit (T <= 128, 1024 routes): the layer matches
+    the oracle and issues the launches launches_per_forward() counts (1 or 4 before the GEMMs)."""
+    k, E = 8, 32
+    w = wl.scaled(wl.decode(64), T=T, K=256, I=128, E=E, top_k=k)
+    x, logits = wl.activations(w, 12), wl.router_logits(w, 12)
+    W1, W2 = wl.expert_weights(w, "W1", 12), wl.expert_weights(w, "W2", 12)
+    lay = moe.MOE_LAYOUT_CONTIGUOUS if layout == "contiguous" else moe.MOE_LAYOUT_BATCHED
+    mt = 48 if layout == "batched" else 0                    # batched: some routes dropped for capacity
+    layer = moe.MoELayer(T, w.K, w.I, E, k, layout=lay, max_tokens=mt, device=DEV)
+    out = layer.forward(x.to(DEV), W1.to(DEV), W2.to(DEV), logits=logits.to(DEV))
+    torch.cuda.synchronize()
+    ids, weights = oracle.topk_route(logits.numpy(), k)
+    assert np.array_equal(layer.ids.cpu().numpy(), ids)
+    if layout == "batched":
+        kept = layer.route_row.cpu().numpy() >= 0
+        ids = np.where(kept, ids, -1).astype(np.int32)
+    ref, _ = oracle.moe_layer(wl.to_numpy(x), ids, weights, wl.to_numpy(W1), wl.to_numpy(W2))
+    assert_close(to_f64(out.cpu()), ref, TOL_BF16, f"layer T={T} {layout}")
+    names = [name for _, _, name in layer._plan]
+    assert names[0] == "route_permute"
+    front = 1 if T <= 128 else 1 + 2 + 1                     # route, permute (two launches above 1024 routes), gather
+    gemms = 1 if any(fn is layer.lib.moe_experts_fused for fn, _, _ in layer._plan) else 2
+    assert layer.launches_per_forward() == front + gemms + 1
+
+
 def test_layer_padding_tokens(moe):
     """Tokens whose slots are all padding (id -1, weight 0) come out as +0.0."""
     w = wl.scaled(wl.decode(64), T=24, K=256, I=128, E=8, top_k=2)

@@ -358,6 +358,7 @@ def aggregate_over_ranks(ms_total, routes, world, device):
 # ----------------------------------------------------------------------------
 
 def run_ours(args, rank, world, local_rank):
+    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -423,6 +424,30 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
     ms_total = start.elapsed_time(end)
     clocks = clk.summary()
+    # spread and noise floor: the timed graph replayed four more times, and the K steps issued eagerly once
+    # (outside the timed region; `value` is the first replay alone)
+    reps = [ms_total / args.steps]
+    for _ in range(4 if graph is not None else 0):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        reps.append(a.elapsed_time(b) / args.steps)
+    eager_ms = reps[0]
+    if graph is not None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for s in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = a.elapsed_time(b) / args.steps
+    timing_stats = {"ms_per_step_replays": [round(x, 4) for x in reps],
+                    "median": round(statistics.median(reps), 4),
+                    "p10": round(float(np.percentile(reps, 10)), 4), "p90": round(float(np.percentile(reps, 90)), 4),
+                    "eager_ms_per_step": round(eager_ms, 4)}
+
     # the same K steps again, with the GEMM events
     if graph_ev is not None:
         graph_ev.replay()
@@ -482,7 +507,7 @@ def run_ours(args, rank, world, local_rank):
                        "l2": "inputs larger than L2 (touched expert weights exceed 129 MB every pass)",
                        "routes_per_step": routes_per_step},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-            "sweep": sweep,
+            "timing_stats": timing_stats, "sweep": sweep,
         }
         print(json.dumps(line), flush=True)
 

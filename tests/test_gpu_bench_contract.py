@@ -38,6 +38,9 @@ def test_bench_line_has_every_key():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    ts = d["timing_stats"]
+    assert len(ts["ms_per_step_replays"]) == 5 and ts["ms_per_step_replays"][0] == d["ms_per_step"]
+    assert ts["p10"] <= ts["median"] <= ts["p90"] and ts["eager_ms_per_step"] > 0
 
 
 def test_reference_arm_line():

@@ -127,6 +127,7 @@ int validate_permute(const char* name, int64_t T, int top_k, int E, int layout, 
         MOE_REQUIRE(is_float_dtype(x_dtype), MOE_ERR_UNSUPPORTED, n + ": x must be F32 or BF16");
         MOE_REQUIRE(K > 0 && (K * esize(x_dtype)) % 16 == 0, MOE_ERR_ALIGNMENT,
                     n + ": K * element size must be a multiple of 16 bytes");
+        MOE_REQUIRE(K * esize(x_dtype) < (int64_t(1) << 31), MOE_ERR_INVALID_ARG, n + ": rows of 2^31 bytes or more");
         MOE_REQUIRE(x_out || rows_cap == 0, MOE_ERR_INVALID_ARG, n + ": x given without x_out");
         MOE_REQUIRE(aligned16(x) && aligned16(x_out), MOE_ERR_ALIGNMENT,
                     n + ": x and x_out must be 16-byte aligned");
@@ -438,6 +439,8 @@ int moe_batched_weight_reduce(const void* y, int y_dtype, const int32_t* expert_
                               void* stream) {
     g_last_error.clear();
     MOE_REQUIRE(E >= 1 && max_tokens >= 0 && K > 0, MOE_ERR_INVALID_ARG, "moe_batched_weight_reduce: bad sizes");
+    MOE_REQUIRE(int64_t(E) * max_tokens < (int64_t(1) << 31), MOE_ERR_INVALID_ARG,
+                "moe_batched_weight_reduce: E * max_tokens must be below 2^31");
     MOE_REQUIRE(is_float_dtype(y_dtype) && is_float_dtype(out_dtype), MOE_ERR_UNSUPPORTED,
                 "moe_batched_weight_reduce: y and out must be F32 or BF16");
     MOE_REQUIRE(K % 8 == 0, MOE_ERR_ALIGNMENT, "moe_batched_weight_reduce: K must be a multiple of 8");

@@ -109,8 +109,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     if (r < 0) return;
     const uint4* src = reinterpret_cast<const uint4*>(x + int64_t(r / top_k) * row_bytes);
     uint4* dst = reinterpret_cast<uint4*>(x_out + s * row_bytes);
-    const int64_t n = row_bytes / 16;
-    int64_t i = lane;
+    const int n = int(row_bytes / 16);   // vectors per row (the host keeps a row under 2^31 bytes)
+    int i = lane;
+#pragma unroll 1
     for (; i + 96 < n; i += 128) {   // four vectors in flight per lane
         const uint4 a = src[i], b = src[i + 32], c = src[i + 64], d = src[i + 96];
         dst[i] = a;
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
         dst[i + 64] = c;
         dst[i + 96] = d;
     }
+#pragma unroll 1
     for (; i < n; i += 32) dst[i] = src[i];
 }
 

@@ -109,15 +109,16 @@ __global__ void __launch_bounds__(256) batched_weight_kernel(const void* __restr
     const int64_t vec = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (vec >= K / 8) return;
     const int64_t col = vec * 8;
-    for (int64_t row = blockIdx.y; row < int64_t(E) * max_tokens; row += gridDim.y) {
-        const int e = int(row / max_tokens), q = int(row - int64_t(e) * max_tokens);
+    const int rows = E * max_tokens;   // the host keeps E * max_tokens below 2^31
+    for (int row = blockIdx.y; row < rows; row += gridDim.y) {
+        const int e = row / max_tokens, q = row - e * max_tokens;
         if (q >= counts[e]) continue;
         const float wr = w ? w[row] : 1.0f;
         float v[8];
-        load8<YDT>(y, row * K + col, v);
+        load8<YDT>(y, int64_t(row) * K + col, v);
 #pragma unroll
         for (int c = 0; c < 8; ++c) v[c] = wr * v[c];
-        store8<ODT>(out, row * K + col, v);
+        store8<ODT>(out, int64_t(row) * K + col, v);
     }
 }
 

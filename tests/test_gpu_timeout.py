@@ -6,7 +6,8 @@ sets).  The bounded wait gives up after ~2 s: the kernel must report
 MOE_DEVERR_TIMEOUT in err_word, free its tensor memory and return, leaving the CUDA
 context usable -- the same process then runs routing and checks it against the oracle.
 In the fused experts launch the GEMM 2 tiles that wait on CTA 0's unfinished GEMM 1
-tile give up the same way (their wait on the segment counter is bounded too).
+tile give up the same way (their wait on the segment counter is bounded too).  The
+batched case runs the 256-row normal tiles (one accumulator, 8 epilogue warps).
 """
 import os
 import subprocess
@@ -30,10 +31,16 @@ x, logits = wl.activations(w, 0).cuda(), wl.router_logits(w, 0)
 W1 = wl.expert_weights(w, "W1", 0).cuda()
 W2 = wl.expert_weights(w, "W2", 0).cuda()
 ids, _ = m.moe_topk_route(logits.cuda(), 2)
-res = m.moe_permute_align(ids, 4, m.MOE_LAYOUT_CONTIGUOUS, 1, x=x)
+if "{impl}" == "BATCHED":   # batched rows: 256-row normal tiles
+    res = m.moe_permute_align(ids, 4, m.MOE_LAYOUT_BATCHED, 1, 64, x=x)
+else:
+    res = m.moe_permute_align(ids, 4, m.MOE_LAYOUT_CONTIGUOUS, 1, x=x)
 err = torch.zeros(1, dtype=torch.int32, device="cuda")
 t0 = time.time()
-if "{impl}" == "FUSED":
+if "{impl}" == "BATCHED":
+    m.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1, 128, layout=m.MOE_LAYOUT_BATCHED,
+                       max_tokens=64, impl=m.MOE_IMPL_TCGEN05, err_word=err)
+elif "{impl}" == "FUSED":
     m.moe_experts_fused(res["x_out"], res["counts"], res["offsets"], W1, W2, 128, res["row_route"], 128,
                         err_word=err)
 else:
@@ -48,7 +55,7 @@ print("ROUTE_OK", bool(np.array_equal(ids2.cpu().numpy(), rids)))
 """
 
 
-@pytest.mark.parametrize("impl", ["TCGEN05", "TCGEN05_SWAP_AB", "FUSED"])
+@pytest.mark.parametrize("impl", ["TCGEN05", "TCGEN05_SWAP_AB", "FUSED", "BATCHED"])
 def test_gemm_wait_runs_out_and_reports(moe, impl):
     env = dict(os.environ, MOE_TEST_SKIP_FIRST_COPY="1")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT, impl=impl)], env=env, capture_output=True,

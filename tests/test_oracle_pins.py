@@ -131,6 +131,27 @@ def test_route_brute_force_selection_with_ties(oracle_mod):
         assert len(set(ids[t])) == 4
 
 
+def test_route_signed_zeros_and_minus_infinity(oracle_mod):
+    """-0 and +0 are equal logits (the lower index wins between them); -inf logits rank last, tie among
+    themselves by index, and get weight 0 (exp(-inf) = 0) with or without renormalisation."""
+    g = torch.Generator().manual_seed(3)
+    logits = (-torch.rand(16, 12, generator=g) - 1.0).numpy().astype(np.float32)
+    logits[:, 7:] = -np.inf
+    for t in range(16):
+        zeros = torch.randperm(7, generator=g)[:3].numpy()
+        logits[t, zeros] = [-0.0, 0.0, -0.0] if t % 2 else [0.0, -0.0, 0.0]
+    for renorm in (True, False):
+        ids, w = oracle_mod.topk_route(logits, 9, renormalize=renorm)
+        for t in range(16):
+            order = sorted(range(12), key=lambda e: (-float(logits[t, e]), e))   # Python: -0.0 == 0.0
+            assert list(ids[t]) == order[:9]
+            assert np.all(w[t, 7:] == 0) and np.all(w[t, :7] > 0)
+            fin = logits[t, :7].astype(np.float64)
+            p = np.exp(fin - fin.max())
+            denom = p[ids[t, :7]].sum() if renorm else p.sum()
+            assert np.allclose(w[t, :7], p[ids[t, :7]] / denom, rtol=2e-7, atol=0)
+
+
 def test_route_weights_renormalised_softmax(oracle_mod):
     g = torch.Generator().manual_seed(1)
     logits = torch.randn(32, 128, generator=g).numpy()

@@ -10,6 +10,11 @@
  * following the decomposition of the vLLM design doc "Fused MoE Modular
  * Kernel", section "apply()": Permute, Matmul with W1, Act + Mul,
  * Quantisation, Matmul with W2, Unpermute, TopK weight application + reduce.
+ * Two calls stand for pairs of those steps where one launch serves better:
+ * moe_route_permute_align (routing + placement + row gather; one launch for
+ * decode-sized batches) and moe_experts_fused (both GEMMs in one launch, the
+ * decode regime).  moe_batched_topk_reduce combines batched rows into token
+ * order.
  *
  * Conventions shared by every call
  * --------------------------------

@@ -73,7 +73,7 @@ def read_peaks():
 class Instance:
     """Device inputs and the layer object of one workload."""
 
-    def __init__(self, w, seed, device, fused=True):
+    def __init__(self, w, seed, device, fused=True, tiled=True):
         import torch
         import mixture_experts_layer_permute_gb300 as m
         from mixture_experts_layer_permute_gb300 import workloads as wl
@@ -88,6 +88,7 @@ class Instance:
             self.layer = m.MoELayer(0, w.K, w.I, w.E, 1, layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens,
                                     device=dev)
             self.s1 = self.s2 = None
+            self.W1r, self.W2r, self.w1_layout = self.W1, self.W2, w.w1_layout
             self.routes = int(self.counts.sum().item())
             self.used_experts = int((self.counts > 0).sum().item())
             return
@@ -110,8 +111,17 @@ class Instance:
         else:
             self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
                                     act_quant=w.act_quant, fused_experts=fused, device=dev)
+        # weights as the kernels stream them: row-major, or (fused decode plan, bf16) re-laid out once into the
+        # tile-contiguous layout by moe_tile_weights -- weight preparation, outside every timed region
+        self.W1r, self.W2r, self.w1_layout = self.W1, self.W2, w.w1_layout
         self.forward()
         torch.cuda.synchronize()
+        if tiled and w.weight == "bf16" and w.layout == "contiguous" and self.fused():
+            self.W1r = m.moe_tile_weights(self.W1, 1, w.w1_layout)
+            self.W2r = m.moe_tile_weights(self.W2, 2)
+            self.w1_layout = m.MOE_W_TILED
+            self.forward()
+            torch.cuda.synchronize()
         ids = self.layer.ids if self.logits is not None else self.ids
         kept = self.layer.route_row >= 0      # batched: routes beyond the capacity are dropped
         self.routes = int(kept.sum().item())
@@ -130,16 +140,16 @@ class Instance:
 
     def forward(self, x=None, logits=None, gemm1_events=None):
         L = self.layer
-        w1_layout = self.w.w1_layout
+        w1_layout = self.w1_layout
         if self.w.layout == "batched":
-            return L.forward(self.xb, self.W1, self.W2, expert_num_tokens=self.counts, row_weights=self.rw,
+            return L.forward(self.xb, self.W1r, self.W2r, expert_num_tokens=self.counts, row_weights=self.rw,
                              gemm1_events=gemm1_events)
         x = self.x if x is None else x
         if self.logits is not None:
             lg = self.logits if logits is None else logits
-            return L.forward(x, self.W1, self.W2, logits=lg, w1_scale=self.s1, w2_scale=self.s2,
+            return L.forward(x, self.W1r, self.W2r, logits=lg, w1_scale=self.s1, w2_scale=self.s2,
                              w1_layout=w1_layout, gemm1_events=gemm1_events)
-        return L.forward(x, self.W1, self.W2, topk_ids=self.ids, topk_weights=self.tw, w1_scale=self.s1,
+        return L.forward(x, self.W1r, self.W2r, topk_ids=self.ids, topk_weights=self.tw, w1_scale=self.s1,
                          w2_scale=self.s2, w1_layout=w1_layout, gemm1_events=gemm1_events)
 
     def launches(self):
@@ -310,7 +320,7 @@ def kernel_source_hash(name="gemm_tc.cu"):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(workload, fused=False):
+def recorded_traffic(workload, fused=False, tiled=False):
     """GEMM 1 DRAM bytes per launch from the committed ncu summary, if taken on this kernel source.
 
     profiles/gemm_{tc,mx}_traffic_<workload>.txt holds `source <file>`, `source_sha <hash>` (or the older
@@ -333,6 +343,8 @@ def recorded_traffic(workload, fused=False):
         if sha != kernel_source_hash(src) or fields.get("workload", [None])[0] != workload:
             continue
         if fields.get("experts", ["split"])[0] != ("fused" if fused else "split"):
+            continue
+        if fields.get("weights", ["stored"])[0] != ("tiled" if tiled else "stored"):
             continue
         vals = [int(v) for v in fields.get("gemm1_traffic_bytes", [])]
         if vals:
@@ -368,7 +380,8 @@ def run_ours(args, rank, world, local_rank):
     if args.experts:
         from mixture_experts_layer_permute_gb300 import workloads as wl
         ws = [wl.scaled(w, E=args.experts) for w in ws]
-    insts = [Instance(w, args.seed, dev, fused=not args.split_experts) for w in ws]
+    insts = [Instance(w, args.seed, dev, fused=not args.split_experts, tiled=not args.row_major_weights)
+             for w in ws]
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
@@ -480,7 +493,7 @@ def run_ours(args, rank, world, local_rank):
     roof["kernel"] = ("gemm_mx_kernel" if mx else "gemm_tc_kernel") + (
         " (moe_experts_fused: GEMM 1 + GEMM 2 in one launch)" if fused else " (moe_gemm1_swiglu)")
     roof["peak_source"] = f"MEASURED_PEAKS.json ({peak_kind})" + (", sustained bf16" if prefill else "")
-    roof["traffic"] = recorded_traffic(args.workload, fused)
+    roof["traffic"] = recorded_traffic(args.workload, fused, any(i.w1_layout == i.m.MOE_W_TILED for i in insts))
     roof["algorithmic_per_launch"] = [int(b) for b in (g1_flops if prefill else g1_bytes)]
     roof["launch_ms"] = [round(x, 4) for x in g1_ms]
     roof["timing"] = ("CUDA events around each GEMM launch, in a replay of the same K steps right after the "
@@ -504,6 +517,8 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": insts[0].w.act, "data": "synthetic",
             "config": {"workload": describe(args.workload, ws), "parallelism": f"replicas x{world}",
                        "launch": mode,
+                       "weights": ("tile-contiguous (moe_tile_weights, prepared once, untimed)"
+                                   if any(i.w1_layout == i.m.MOE_W_TILED for i in insts) else "as stored"),
                        "l2": "inputs larger than L2 (touched expert weights exceed 129 MB every pass)",
                        "routes_per_step": routes_per_step},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
@@ -553,9 +568,9 @@ def run_e2e(args, insts, dev):
         if inst.w.layout == "batched":
             return dict(expert_num_tokens=inst.counts, row_weights=inst.rw)
         if dl is not None:
-            return dict(logits=dl, w1_scale=inst.s1, w2_scale=inst.s2, w1_layout=inst.w.w1_layout)
+            return dict(logits=dl, w1_scale=inst.s1, w2_scale=inst.s2, w1_layout=inst.w1_layout)
         return dict(topk_ids=inst.ids, topk_weights=inst.tw, w1_scale=inst.s1, w2_scale=inst.s2,
-                    w1_layout=inst.w.w1_layout)
+                    w1_layout=inst.w1_layout)
 
     def h2d():
         dstage.copy_(hstage, non_blocking=True)
@@ -571,7 +586,7 @@ def run_e2e(args, insts, dev):
         cur = torch.cuda.current_stream()
         h2d()
         for inst, (ho, dx, dl) in zip(insts, host):
-            inst.layer.forward(dx, inst.W1, inst.W2, **kwargs_of(inst, dl))
+            inst.layer.forward(dx, inst.W1r, inst.W2r, **kwargs_of(inst, dl))
             side.wait_stream(cur)
             with torch.cuda.stream(side):
                 d2h_of(inst, ho)()
@@ -745,6 +760,9 @@ def main():
     ap.add_argument("--split-experts", action="store_true",
                     help="run GEMM 1 and GEMM 2 as two launches even where the plan uses swap-AB tiles (by default "
                          "they are one launch, moe_experts_fused)")
+    ap.add_argument("--row-major-weights", action="store_true",
+                    help="stream the weights as stored (E, rows, cols); by default the fused decode plan reads them "
+                         "re-laid out once by moe_tile_weights")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: fewer experts than the workload (a small case for ncu)")
     args = ap.parse_args()

@@ -83,6 +83,8 @@ extern "C" {
 #define MOE_W1_INTERLEAVE16 1         /* rows in groups of 32: 16 gate rows then the 16 matching up rows
                                          ("Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2,
                                          _interleave_gate_up_16 "After") */
+#define MOE_W_TILED 2                 /* moe_experts_fused only: W1 AND W2 in the tile-contiguous layout
+                                         written by moe_tile_weights */
 
 /* ---- GEMM implementations ---- */
 #define MOE_IMPL_AUTO 0               /* swap-AB tiles when routes/expert are few, else normal tiles;
@@ -291,11 +293,35 @@ MOE_API int moe_gemm2(const void* h, int h_dtype, const uint8_t* h_scale, int la
  *              alias a or y; holds h on return
  *   workspace  >= moe_experts_fused_workspace_size(rows_cap, E) bytes, 256-byte
  *              aligned; cleared by the call (an asynchronous memset on `stream`)
+ *   w1_layout  MOE_W1_GATE_UP or MOE_W1_INTERLEAVE16 (W2 row-major), or MOE_W_TILED:
+ *              w1 and w2 both as written by moe_tile_weights (same results, bit for bit)
  *   K % 128 == 0, I % 64 == 0; an sm_100+ device.
  * The launch is cooperative (every CTA resident); a wait that runs out sets
  * MOE_DEVERR_TIMEOUT after 2 s instead of hanging.
  */
 MOE_API size_t moe_experts_fused_workspace_size(int64_t rows_cap, int E);
+
+/*
+ * moe_tile_weights -- offline re-layout of bf16 expert weights into the
+ * tile-contiguous layout that moe_experts_fused streams with MOE_W_TILED (a
+ * weight-preparation step, like the gate/up interleave of the "Cake MegaMoE
+ * EP16" FlashInfer PR 5148 analysis, section 2, or the MXFP8 quantisation):
+ * every 128-row x 64-column block that one pipeline stage loads is stored as
+ * one contiguous 16 KB run, so each stage reads whole DRAM pages instead of
+ * 128 pieces of 128 bytes one weight row apart.
+ *     out[e][b][c][r][j] = w[e][row(b, r)][64*c + j]
+ *     (b < rows/128 row blocks, c < cols/64 column blocks, r < 128, j < 64)
+ *   which = 1: w is W1 (E, 2I, K) in layout w1_layout; rows = 2I, cols = K; each
+ *              block holds 64 gate/up units as [16 gate rows, the 16 matching
+ *              up rows] x 4: row(b, r) = unit u = 64b + 16(r/32) + r%16, its gate
+ *              row (r%32 < 16) or up row (r%32 >= 16) -- for MOE_W1_GATE_UP
+ *              rows u and I + u, for MOE_W1_INTERLEAVE16 row 128b + r.
+ *   which = 2: w is W2 (E, K, I); rows = K, cols = I; row(b, r) = 128b + r.
+ *   w_dtype    MOE_BF16.  rows % 128 == 0 and cols % 64 == 0.
+ *   w, out     device, 16-byte aligned, E*rows*cols elements each, not overlapping.
+ */
+MOE_API int moe_tile_weights(const void* w, int w_dtype, int which, int w1_layout, int E, int64_t rows,
+                             int64_t cols, void* out, void* stream);
 MOE_API int moe_experts_fused(const void* a, int a_dtype, const int32_t* expert_counts,
                               const int32_t* expert_offsets, int64_t rows_cap, int E, int64_t K, int64_t I,
                               const void* w1, int w1_layout, const void* w2, int w_dtype,

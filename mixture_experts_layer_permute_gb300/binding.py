@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe_layer.so")
 MOE_OK = 0
 MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_LAYOUT_CONTIGUOUS, MOE_LAYOUT_BATCHED = 0, 1
-MOE_W1_GATE_UP, MOE_W1_INTERLEAVE16 = 0, 1
+MOE_W1_GATE_UP, MOE_W1_INTERLEAVE16, MOE_W_TILED = 0, 1, 2
 MOE_IMPL_AUTO, MOE_IMPL_TCGEN05, MOE_IMPL_TCGEN05_SWAP_AB, MOE_IMPL_SIMT, MOE_IMPL_TCGEN05_MIXED = 0, 1, 2, 3, 4
 MOE_DEVERR_ID_RANGE, MOE_DEVERR_CAPACITY, MOE_DEVERR_TIMEOUT = 1, 2, 4
 
@@ -31,7 +31,7 @@ EXPORTED = [
     "moe_last_error", "moe_version", "moe_max_padded_rows", "moe_permute_workspace_size", "moe_topk_route",
     "moe_permute_align", "moe_permute_align_static", "moe_route_permute_align", "moe_gemm1_swiglu", "moe_gemm2", "moe_unpermute_topk_reduce",
     "moe_batched_weight_reduce", "moe_batched_topk_reduce", "mxfp8_quantize_block32",
-    "moe_experts_fused_workspace_size", "moe_experts_fused",
+    "moe_experts_fused_workspace_size", "moe_experts_fused", "moe_tile_weights",
 ]
 
 
@@ -66,6 +66,7 @@ def load(path: Optional[str] = None):
             "moe_experts_fused": (I32, [P, I32, P, P, I64, I32, I64, I64, P, I32, P, I32, P, P, P, P, I32, I64, P,
                                         SZ, P, P]),
             "moe_topk_route": (I32, [P, I64, I32, I32, I32, P, P, P]),
+            "moe_tile_weights": (I32, [P, I32, I32, I32, I32, I64, I64, P, P]),
             "moe_permute_align": (I32, [P, I64, I32, I32, I32, I32, I32, P, I32, I64, P, I64, P, P, P, P, P, SZ,
                                         P, P]),
             "moe_route_permute_align": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, I32, P, I32, I64, P, I64, P,
@@ -180,6 +181,18 @@ def moe_permute_align(topk_ids, E, layout=MOE_LAYOUT_CONTIGUOUS, block_m=1, max_
         workspace.numel(), _ptr(err_word), _stream(stream)))
     return dict(counts=expert_counts, offsets=expert_offsets, row_route=row_route, route_row=route_row,
                 x_out=x_out, rows_cap=rows_cap)
+
+
+def moe_tile_weights(w, which, w1_layout=MOE_W1_GATE_UP, out=None, stream=None):
+    """Offline re-layout of bf16 W1 (which=1, (E, 2I, K) in w1_layout) or W2 (which=2, (E, K, I)) into the
+    tile-contiguous layout moe_experts_fused reads with w1_layout=MOE_W_TILED.  Returns a tensor of w's shape
+    holding the tiled bytes."""
+    E, rows, cols = w.shape
+    if out is None:
+        out = torch.empty_like(w)
+    _check(load().moe_tile_weights(_ptr(w), dtype_code(w), which, w1_layout, E, rows, cols, _ptr(out),
+                                   _stream(stream)))
+    return out
 
 
 def moe_route_permute_align(logits, top_k, E=None, renormalize=True, layout=MOE_LAYOUT_CONTIGUOUS, block_m=1,

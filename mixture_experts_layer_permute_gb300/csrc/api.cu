@@ -397,7 +397,7 @@ int moe_experts_fused(const void* a, int a_dtype, const int32_t* expert_counts, 
     g2.gemm = 2;
     g2.a = h;
     g2.w = w2;
-    g2.w1_layout = 0;
+    g2.w1_layout = w1_layout == MOE_W_TILED ? MOE_W_TILED : 0;   // tiled: W2 tiled as well
     g2.row_route = row_route;
     g2.route_w = route_weights;
     g2.out = y;
@@ -405,8 +405,8 @@ int moe_experts_fused(const void* a, int a_dtype, const int32_t* expert_counts, 
     g2.out_rows = y_rows;
     rc = validate_gemm(g2, "moe_experts_fused");
     if (rc) return rc;
-    MOE_REQUIRE(w1_layout == MOE_W1_GATE_UP || w1_layout == MOE_W1_INTERLEAVE16, MOE_ERR_INVALID_ARG,
-                "moe_experts_fused: unknown w1_layout");
+    MOE_REQUIRE(w1_layout == MOE_W1_GATE_UP || w1_layout == MOE_W1_INTERLEAVE16 || w1_layout == MOE_W_TILED,
+                MOE_ERR_INVALID_ARG, "moe_experts_fused: unknown w1_layout");
     MOE_REQUIRE(row_route, MOE_ERR_INVALID_ARG, "moe_experts_fused: row_route is required");
     MOE_REQUIRE(y_rows >= 0, MOE_ERR_INVALID_ARG, "moe_experts_fused: y_rows < 0");
     MOE_REQUIRE(rows_cap == 0 || (h != a && h != y), MOE_ERR_INVALID_ARG,
@@ -415,6 +415,26 @@ int moe_experts_fused(const void* a, int a_dtype, const int32_t* expert_counts, 
                 "moe_experts_fused: workspace must be 256-byte aligned");
     MOE_REQUIRE(device_cc() >= 100, MOE_ERR_UNSUPPORTED, "moe_experts_fused: tcgen05 needs an sm_100+ device");
     return launch_experts_fused(g1, g2, static_cast<int32_t*>(workspace), workspace_bytes, as_stream(stream));
+}
+
+int moe_tile_weights(const void* w, int w_dtype, int which, int w1_layout, int E, int64_t rows, int64_t cols,
+                     void* out, void* stream) {
+    g_last_error.clear();
+    MOE_REQUIRE(w_dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_tile_weights: bf16 weights only");
+    MOE_REQUIRE(which == 1 || which == 2, MOE_ERR_INVALID_ARG, "moe_tile_weights: which must be 1 (W1) or 2 (W2)");
+    MOE_REQUIRE(which == 2 || w1_layout == MOE_W1_GATE_UP || w1_layout == MOE_W1_INTERLEAVE16, MOE_ERR_INVALID_ARG,
+                "moe_tile_weights: unknown w1_layout");
+    MOE_REQUIRE(E >= 1 && rows > 0 && cols > 0, MOE_ERR_INVALID_ARG, "moe_tile_weights: bad sizes");
+    MOE_REQUIRE(rows % 128 == 0 && cols % 64 == 0, MOE_ERR_ALIGNMENT,
+                "moe_tile_weights: rows % 128 and cols % 64 must be 0");
+    MOE_REQUIRE(w && out, MOE_ERR_INVALID_ARG, "moe_tile_weights: null pointer");
+    MOE_REQUIRE(aligned16(w) && aligned16(out), MOE_ERR_ALIGNMENT, "moe_tile_weights: w and out must be 16-byte aligned");
+    const int64_t bytes = int64_t(E) * rows * cols * 2;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(w), b = reinterpret_cast<uintptr_t>(out);
+    MOE_REQUIRE(a + uintptr_t(bytes) <= b || b + uintptr_t(bytes) <= a, MOE_ERR_INVALID_ARG,
+                "moe_tile_weights: w and out overlap");
+    return launch_status(launch_tile_weights(w, which, w1_layout, E, rows, cols, out, as_stream(stream)),
+                         "moe_tile_weights");
 }
 
 int moe_unpermute_topk_reduce(const void* y, int y_dtype, const int32_t* topk_ids, const float* topk_weights,

@@ -154,7 +154,8 @@ struct TcParams {
     int64_t rows_cap;
     int nkb;             // k-blocks per tile
     int nt;              // normal: n-tiles per m-tile; swap: weight blocks per expert
-    int w_mode;          // weights map: 0 = 3-D (k, rows, E), 1 = 5-D gate/up interleaving view
+    int w_mode;          // weights map: 0 = 3-D (k, rows, E), 1 = 5-D gate/up interleaving view,
+                         // 2 = 4-D tile-contiguous (64, 128, k-blocks, E x 128-row blocks; swap-AB tiles)
     int64_t I, K;
     const int32_t* counts;
     const int32_t* offsets;
@@ -175,6 +176,7 @@ struct TcParams {
     // tm_act/tm_w map x rows and W1, tm_act_s/tm_w_s map h and W2; out is h, out2 is y
     int fused;
     int nkb2, nt2;       // GEMM 2: k-blocks per tile, weight blocks per expert
+    int w_mode2;         // GEMM 2: weights map (0 or 2)
     void* out2;
     int out2_dtype;
     int32_t* seg_done;   // per token segment: GEMM 1 epilogue warps done (zero at launch)
@@ -430,7 +432,8 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                 const CUtensorMap* mact = second ? &tm_act_s : &tm_act;
                 const CUtensorMap* mw = second ? &tm_w_s : &tm_w;
                 const int nkb = tl.gemm == 2 && p.fused ? p.nkb2 : p.nkb;
-                const int w_mode = tl.gemm == 2 && p.fused ? 0 : p.w_mode;
+                const int w_mode = tl.gemm == 2 && p.fused ? p.w_mode2 : p.w_mode;
+                const int wblocks = tl.gemm == 2 && p.fused ? p.nt2 : p.nt;   // 128-row weight blocks per expert
                 if (p.fused && tl.gemm == 2) {
                     // this segment's h is complete once all 4 epilogue warps of its nt GEMM 1 tiles published
                     if (!wait_counter(&p.seg_done[tl.seg], 4 * p.nt, ctrl, p.err_word)) break;
@@ -459,6 +462,8 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                     const int row_w = tl.nb * wrows;          // first weight row (interleaved order)
                     if (w_mode == 1)
                         ptx::tma_load_5d(wdst, mw, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_w);
+                    else if (w_mode == 2)   // one contiguous 16 KB block per k-block
+                        ptx::tma_load_4d(wdst, mw, &ctrl.full[s], 0, 0, kb, tl.e * wblocks + tl.nb, pol_w);
                     else
                         ptx::tma_load_3d(wdst, mw, &ctrl.full[s], k0, row_w, tl.e, pol_w);
                     if (W8) {
@@ -899,6 +904,13 @@ int build_maps(const GemmArgs& g, bool swap, bool w8, int64_t kdim, int64_t wrow
     }
     const int64_t es = w8 ? 1 : 2;
     const cuuint32_t kbox = cuuint32_t(w8 ? BK * Cfg<V_E4M3>::KSUB : BK);
+    if (g.w1_layout == MOE_W_TILED) {
+        // tile-contiguous weights (moe_tile_weights): [E x 128-row blocks][k-blocks][128 rows][64 columns]
+        cuuint64_t dims[4] = {cuuint64_t(BK), 128, cuuint64_t(kdim / BK), cuuint64_t(g.E * (wrows / 128))};
+        cuuint64_t str[3] = {cuuint64_t(BK * 2), cuuint64_t(128 * BK * 2), cuuint64_t(kdim / BK * 128 * BK * 2)};
+        cuuint32_t box[4] = {BK, 128, 1, 1};
+        return make_map(w, g.w, 4, dims, str, box, g.gemm == 1 ? "W1 (tiled)" : "W2 (tiled)");
+    }
     if (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) {
         // view W1[e] (2I, K) as (K, 16, 2, I/16): row = half*I + 16*blk + q
         cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
@@ -1054,11 +1066,12 @@ int launch_experts_fused(const GemmArgs& g1, const GemmArgs& g2, int32_t* seg_do
     if (ws_bytes < experts_fused_workspace_bytes(g1.rows_cap, g1.E))
         return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "fused experts: workspace smaller than moe_experts_fused_workspace_size()");
     if (g1.rows_cap == 0) return MOE_OK;
-    const int w_mode = g1.w1_layout == MOE_W1_GATE_UP ? 1 : 0;
+    const bool tiled = g1.w1_layout == MOE_W_TILED;
+    const int w_mode = tiled ? 2 : (g1.w1_layout == MOE_W1_GATE_UP ? 1 : 0);
     MapSet m1, m2;
     int rc = cached_maps(g1, TC_SWAP, false, g1.K, 2 * g1.I, w_mode, &m1);
     if (rc) return rc;
-    rc = cached_maps(g2, TC_SWAP, false, g1.I, g1.K, 0, &m2);
+    rc = cached_maps(g2, TC_SWAP, false, g1.I, g1.K, tiled ? 2 : 0, &m2);
     if (rc) return rc;
 
     TcParams p{};
@@ -1085,6 +1098,7 @@ int launch_experts_fused(const GemmArgs& g1, const GemmArgs& g2, int32_t* seg_do
     p.fused = 1;
     p.nkb2 = int(g1.I / BK);
     p.nt2 = int(g1.K / 128);
+    p.w_mode2 = tiled ? 2 : 0;
     p.out2 = g2.out;
     p.out2_dtype = g2.out_dtype;
     p.seg_done = seg_done;

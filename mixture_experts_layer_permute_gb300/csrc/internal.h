@@ -28,6 +28,10 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int top_k, int E, int 
 cudaError_t launch_gather_rows(const void* x, int esize, int64_t K, const int32_t* row_route, int top_k,
                                const int32_t* offsets, int E, int64_t rows_cap, void* x_out, cudaStream_t s);
 
+// tile-contiguous weight layout (moe_tile_weights)
+cudaError_t launch_tile_weights(const void* w, int which, int w1_layout, int E, int64_t rows, int64_t cols,
+                                void* out, cudaStream_t s);
+
 // route + permute (+ gather when x_out is set) in one launch; only for the sizes route_permute_fusable accepts
 bool route_permute_fusable(int64_t T, int top_k, int64_t row_bytes);
 cudaError_t launch_route_permute(const float* logits, int64_t T, int E, int top_k, int renorm, int32_t* ids,

@@ -183,6 +183,8 @@ class MoELayer:
             calls.append((lib.moe_unpermute_topk_reduce, (self.y.data_ptr(), adt, ids.data_ptr(), None, T, k, E,
                                                           K, self.out.data_ptr(), adt, stream), "reduce"))
             return calls
+        if w1_layout == B.MOE_W_TILED:
+            raise ValueError("MOE_W_TILED weights run on the fused decode plan only (bf16, swap-AB regime)")
         if self.act_quant:   # GEMM 1's epilogue writes h as MXFP8 (codes + scales)
             hout, hdt, hs = self.h_codes.data_ptr(), B.MOE_E4M3, self.h_scales.data_ptr()
         else:

@@ -121,6 +121,18 @@ def test_route_permute_validation(lib):
     assert call(logits=None) == 1 and "null" in lib_error()                           # no logits
 
 
+def test_tile_weights_validation(lib):
+    fake, other = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x40000000)
+    assert lib.moe_tile_weights(fake, 0, 1, 0, 2, 256, 128, other, None) == 2      # fp32 weights
+    assert lib.moe_tile_weights(fake, 1, 3, 0, 2, 256, 128, other, None) == 1      # which
+    assert lib.moe_tile_weights(fake, 1, 1, 7, 2, 256, 128, other, None) == 1      # w1_layout
+    assert lib.moe_tile_weights(fake, 1, 2, 0, 2, 200, 128, other, None) == 3      # rows % 128
+    assert lib.moe_tile_weights(fake, 1, 2, 0, 2, 256, 96, other, None) == 3       # cols % 64
+    assert lib.moe_tile_weights(fake, 1, 2, 0, 2, 256, 128, ctypes.c_void_p(0x100100), None) == 1   # overlap
+    assert lib.moe_tile_weights(None, 1, 2, 0, 2, 256, 128, other, None) == 1      # null
+    assert lib.moe_tile_weights(ctypes.c_void_p(0x100008), 1, 2, 0, 2, 256, 128, other, None) == 3  # alignment
+
+
 def test_gemm_validation(lib):
     fake = ctypes.c_void_p(0x1000)
     # K not a multiple of 32

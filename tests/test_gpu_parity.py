@@ -905,6 +905,76 @@ def test_experts_fused_matches_two_launches(moe, shape):
     assert_close(to_f64(out), ref, TOL_BF16, "fused experts")
 
 
+def _tiled_reference(w, which, w1_layout):
+    """Test plumbing: the tile-contiguous layout built with numpy indexing from its definition."""
+    E, rows, cols = w.shape
+    if which == 1 and w1_layout == 0:
+        I = rows // 2
+        order = []
+        for b in range(rows // 128):
+            for r in range(128):
+                unit = 64 * b + 16 * (r // 32) + r % 16
+                order.append(I + unit if (r // 16) % 2 else unit)
+        w = w[:, order, :]
+    t = w.reshape(E, rows // 128, 128, cols // 64, 64).permute(0, 1, 3, 2, 4)
+    return t.contiguous().reshape(E, rows, cols)
+
+
+@pytest.mark.parametrize("which,w1_layout,shape", [(1, 0, (3, 256, 192)), (1, 1, (3, 256, 192)),
+                                                   (2, 0, (2, 384, 128)), (1, 0, (1, 3072, 4096))])
+def test_tile_weights_layout(moe, which, w1_layout, shape):
+    """moe_tile_weights writes exactly the documented layout (bit for bit)."""
+    w = wl._normal(shape, 1.0, 21, "w", 0, "cpu", torch.bfloat16)
+    t = moe.moe_tile_weights(w.to(DEV), which, w1_layout)
+    torch.cuda.synchronize()
+    ref = _tiled_reference(w, which, w1_layout)
+    assert torch.equal(t.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("shape", [(5, 8, 64, 512, 128, 0), (96, 4, 8, 512, 256, 1), (700, 2, 6, 256, 128, 0)])
+def test_experts_fused_tiled_weights(moe, shape):
+    """moe_experts_fused on tile-contiguous W1 and W2 (MOE_W_TILED) gives the same h and y, bit for bit, as on
+    the row-major weights (same tiles, same accumulation order)."""
+    T, k, E, K, I, w1_layout = shape
+    w, x, ids, weights = _routed(T, k, E, K, seed=T + 11 * E)
+    ws = wl.scaled(w, I=I, w_std=0.05)
+    W1 = wl.expert_weights(ws, "W1", 15).to(torch.bfloat16).to(DEV)
+    W2 = wl.expert_weights(ws, "W2", 15).to(torch.bfloat16).to(DEV)
+    W1t, W2t = moe.moe_tile_weights(W1, 1, w1_layout), moe.moe_tile_weights(W2, 2)
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    R = T * k
+    wt = torch.from_numpy(weights).to(DEV).reshape(-1)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    h1, y1 = moe.moe_experts_fused(res["x_out"], res["counts"], res["offsets"], W1, W2, I, res["row_route"], R,
+                                   route_weights=wt, w1_layout=w1_layout, err_word=err)
+    h2, y2 = moe.moe_experts_fused(res["x_out"], res["counts"], res["offsets"], W1t, W2t, I, res["row_route"], R,
+                                   route_weights=wt, w1_layout=moe.MOE_W_TILED, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rr = res["route_row"].view(-1).long()
+    assert torch.equal(h1[rr].view(torch.int16), h2[rr].view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_layer_decode_tiled_weights_full_size(moe):
+    """The decode layer at full size on tile-contiguous weights equals the layer on row-major weights bit for
+    bit; a plan that is not the fused decode plan refuses tiled weights."""
+    w = wl.decode(64)
+    x, logits = wl.activations(w, 1, DEV), wl.router_logits(w, 1, DEV)
+    W1, W2 = wl.expert_weights(w, "W1", 1, DEV), wl.expert_weights(w, "W2", 1, DEV)
+    W1t, W2t = moe.moe_tile_weights(W1, 1), moe.moe_tile_weights(W2, 2)
+    layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, device=DEV)
+    out_a = layer.forward(x, W1, W2, logits=logits).clone()
+    out_b = layer.forward(x, W1t, W2t, logits=logits, w1_layout=moe.MOE_W_TILED)
+    torch.cuda.synchronize()
+    assert layer.device_errors() == 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    big = moe.MoELayer(4096, w.K, w.I, w.E, w.top_k, block_m=128, device=DEV)     # normal tiles
+    with pytest.raises(ValueError):
+        big.forward(wl._normal((4096, w.K), 1.0, 3, "x", 0, DEV, torch.bfloat16), W1t, W2t,
+                    logits=wl._normal((4096, w.E), 1.0, 3, "l", 0, DEV, torch.float32), w1_layout=moe.MOE_W_TILED)
+
+
 def test_layer_decode_fused_experts_full_size(moe):
     """Decode configuration at full size with GEMM 1 + GEMM 2 in one launch: equals the two-launch layer bit for
     bit, sampled tokens against the oracle."""

@@ -1,0 +1,38 @@
+"""bench.py's host-side bookkeeping without a GPU: the committed ncu traffic summaries are reported only for the
+kernel source, plan and weight layout they were captured on."""
+import os
+import shutil
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_decode_traffic_record_matches_its_plan_only():
+    rec = bench.recorded_traffic("decode", fused=True, tiled=True)
+    assert rec is not None and len(rec) == 4 and all(v > 0 for v in rec)
+    # the capture covers the fused launch on tile-contiguous weights: other plans get no traffic figure
+    assert bench.recorded_traffic("decode", fused=True, tiled=False) is None
+    assert bench.recorded_traffic("decode", fused=False, tiled=True) is None
+    assert bench.recorded_traffic("prefill", fused=False, tiled=False) is None
+
+
+def test_traffic_record_dropped_when_the_kernel_source_changes(tmp_path, monkeypatch):
+    # a copy of the repository layout whose gemm_tc.cu differs by one byte
+    src = os.path.join(ROOT, "mixture_experts_layer_permute_gb300", "csrc", "gemm_tc.cu")
+    csrc = tmp_path / "mixture_experts_layer_permute_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    with open(src, "rb") as f:
+        (csrc / "gemm_tc.cu").write_bytes(f.read() + b"\n")
+    shutil.copytree(os.path.join(ROOT, "profiles"), tmp_path / "profiles")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("decode", fused=True, tiled=True) is None
+
+
+def test_describe_names_the_workload():
+    ws = bench.workload_list("decode")
+    assert [w.T for w in ws] == [1, 8, 32, 64]
+    assert "decode" in bench.describe("decode", ws)
+    assert "prefill" in bench.describe("prefill", bench.workload_list("prefill"))

@@ -246,6 +246,8 @@ class MoELayer:
         `topk_ids`/`topk_weights` (T, top_k); routes beyond max_tokens per expert are dropped (batched).
         Batched layout with T = 0: x (E, max_tokens, K), `expert_num_tokens` (E,), optional `row_weights`
         (E, max_tokens).
+        ``w1_layout``: MOE_W1_GATE_UP or MOE_W1_INTERLEAVE16 for row-major W1, or MOE_W_TILED when W1 and W2 come
+        from moe_tile_weights (the fused decode plan only; other plans raise ValueError).
         ``gemm1_events`` = (start, end) CUDA events recorded around the gate/up GEMM.
         """
         s = stream if stream is not None else torch.cuda.current_stream()

@@ -25,7 +25,12 @@
  * - Matrices are row-major and dense (the last index is contiguous).
  * - Element types: MOE_F32 (binary32), MOE_BF16 (bfloat16), MOE_E4M3
  *   (OCP E4M3FN codes, one byte each, always paired with one E8M0 scale byte
- *   per 32 consecutive elements along the contraction dimension).
+ *   per 32 consecutive elements along the contraction dimension).  The E4M3
+ *   NaN codes 0x7F and 0xFF, and the E8M0 NaN scale 0xFF, are outside the
+ *   contract: mxfp8_quantize_block32 never writes them (it saturates, and its
+ *   largest scale is 254), and a GEMM given them returns unspecified values
+ *   without an error bit (the bf16-activation path decodes 0x7F/0xFF as the
+ *   finite value 480 * scale, where the format defines NaN).
  * - Expert ids are int32; -1 marks a padding slot that every step skips
  *   (transformers PR 49606 analysis "DeepGEMM Mega MoE as an EP
  *   implementation", section 2: padded slots carry expert id -1, weight 0).
@@ -39,6 +44,12 @@
  *   MOE_DEVERR_TIMEOUT when a pipeline wait inside a GEMM gave up (the
  *   kernel then returns early and its outputs are unspecified).
  * - Sizes are int64 where they can exceed 2^31 elements.
+ * - Test hook: when the environment variable MOE_TEST_SKIP_FIRST_COPY is "1"
+ *   at the first tcgen05 GEMM launch of the process, CTA 0 of every tcgen05
+ *   GEMM leaves its first stage's copy out, so that stage never fills and
+ *   the kernel reports MOE_DEVERR_TIMEOUT after 2 s (its outputs are then
+ *   unspecified).  It exists to test the bounded waits without a fault;
+ *   never set it in production.
  */
 #ifndef MOE_LAYER_H
 #define MOE_LAYER_H
@@ -105,12 +116,15 @@ MOE_API const char* moe_last_error(void);
 MOE_API int moe_version(void);
 
 /* Upper bound on the rows of the contiguous layout:
- * T*top_k + E*(block_m - 1) = max over routings of sum_e ceil(count_e/block_m)*block_m. */
+ * T*top_k + E*(block_m - 1) = max over routings of sum_e ceil(count_e/block_m)*block_m.
+ * -1 for arguments the permute calls reject (T < 0, top_k or E outside [1, 1024], block_m outside
+ * [1, 4096], or T*top_k >= 2^31, which is tested without forming the product). */
 MOE_API int64_t moe_max_padded_rows(int64_t T, int top_k, int E, int block_m);
 
 /* Bytes of scratch moe_permute_align needs for T tokens, top_k slots, E experts
  * (the two workspaces declared up front in "Fused MoE Modular Kernel",
- * workspace_shapes()). */
+ * workspace_shapes()).  0 for arguments the permute calls reject (as for
+ * moe_max_padded_rows). */
 MOE_API size_t moe_permute_workspace_size(int64_t T, int top_k, int E);
 
 /*
@@ -199,8 +213,13 @@ MOE_API int moe_route_permute_align(const float* logits, int64_t T, int E, int t
  * exits.  This call allocates nothing.
  *   - Routings needing more than 2 MiB of scratch (moe_permute_workspace_size
  *     > 2 MiB, about 450k routes) return MOE_ERR_WORKSPACE_TOO_SMALL.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - The first call in each CUDA context of a device looks up the array's
+ *     device address (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.  The address is kept for that context only, so after
+ *     cudaDeviceReset (or a re-created primary context) the next call looks
+ *     it up again -- again outside any capture.
+ *   - T, top_k and E are checked before any size is formed: T*top_k < 2^31,
+ *     top_k and E in [1, 1024]; otherwise MOE_ERR_INVALID_ARG, nothing read.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and must be serialised by the caller.
  */

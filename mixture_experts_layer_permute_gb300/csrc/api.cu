@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 #include <string>
 
@@ -18,6 +19,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int esize(int dt) { return dt == MOE_F32 ? 4 : (dt == MOE_BF16 ? 2 : 1); }
 bool is_float_dtype(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// T >= 0 and 1 <= top_k <= 1024 with T*top_k < 2^31, tested without forming the product (a huge T would
+// overflow it).
+bool routes_in_range(int64_t T, int top_k) {
+    return T >= 0 && top_k >= 1 && top_k <= 1024 && T <= int64_t(INT32_MAX) / top_k;
+}
 
 int launch_status(cudaError_t e, const char* what) {
     if (e == cudaSuccess) return MOE_OK;
@@ -70,12 +77,12 @@ const char* moe_last_error(void) { return g_last_error.c_str(); }
 int moe_version(void) { return (1 << 16) | 0; }
 
 int64_t moe_max_padded_rows(int64_t T, int top_k, int E, int block_m) {
-    if (T < 0 || top_k < 1 || E < 1 || block_m < 1) return -1;
+    if (!routes_in_range(T, top_k) || E < 1 || E > 1024 || block_m < 1 || block_m > 4096) return -1;
     return T * top_k + int64_t(E) * (block_m - 1);
 }
 
 size_t moe_permute_workspace_size(int64_t T, int top_k, int E) {
-    if (T < 0 || top_k < 1 || E < 1) return 0;
+    if (!routes_in_range(T, top_k) || E < 1 || E > 1024) return 0;
     return permute_workspace_bytes(T, top_k, E);
 }
 
@@ -102,10 +109,10 @@ int validate_permute(const char* name, int64_t T, int top_k, int E, int layout, 
                      const int32_t* route_row, const void* workspace, size_t workspace_bytes) {
     const std::string n(name);
     MOE_REQUIRE(T >= 0 && top_k >= 1 && top_k <= 1024, MOE_ERR_INVALID_ARG, n + ": bad T or top_k");
+    MOE_REQUIRE(routes_in_range(T, top_k), MOE_ERR_INVALID_ARG, n + ": T*top_k must stay below 2^31");
     MOE_REQUIRE(E >= 1 && E <= 1024, MOE_ERR_INVALID_ARG, n + ": E must be in [1, 1024]");
     MOE_REQUIRE(layout == MOE_LAYOUT_CONTIGUOUS || layout == MOE_LAYOUT_BATCHED, MOE_ERR_INVALID_ARG,
                 n + ": unknown layout");
-    MOE_REQUIRE(T * top_k < (int64_t(1) << 31), MOE_ERR_INVALID_ARG, n + ": more than 2^31 routes");
     if (layout == MOE_LAYOUT_CONTIGUOUS) {
         MOE_REQUIRE(block_m >= 1 && block_m <= 4096, MOE_ERR_INVALID_ARG, n + ": block_m in [1, 4096]");
         MOE_REQUIRE(rows_cap >= moe_max_padded_rows(T, top_k, E, block_m), MOE_ERR_INVALID_ARG,
@@ -440,8 +447,8 @@ int moe_tile_weights(const void* w, int w_dtype, int which, int w1_layout, int E
 int moe_unpermute_topk_reduce(const void* y, int y_dtype, const int32_t* topk_ids, const float* topk_weights,
                               int64_t T, int top_k, int E, int64_t K, void* out, int out_dtype, void* stream) {
     g_last_error.clear();
-    MOE_REQUIRE(T >= 0 && top_k >= 1 && E >= 1 && K > 0, MOE_ERR_INVALID_ARG,
-                "moe_unpermute_topk_reduce: bad sizes");
+    MOE_REQUIRE(routes_in_range(T, top_k) && E >= 1 && K > 0, MOE_ERR_INVALID_ARG,
+                "moe_unpermute_topk_reduce: bad sizes (T*top_k must stay below 2^31)");
     MOE_REQUIRE(is_float_dtype(y_dtype) && is_float_dtype(out_dtype), MOE_ERR_UNSUPPORTED,
                 "moe_unpermute_topk_reduce: y and out must be F32 or BF16");
     MOE_REQUIRE(K % 8 == 0, MOE_ERR_ALIGNMENT, "moe_unpermute_topk_reduce: K must be a multiple of 8");
@@ -478,8 +485,8 @@ int moe_batched_topk_reduce(const void* y, int y_dtype, int64_t rows, const int3
                             const float* topk_weights, int64_t T, int top_k, int64_t K, void* out, int out_dtype,
                             int32_t* err_word, void* stream) {
     g_last_error.clear();
-    MOE_REQUIRE(T >= 0 && rows >= 0 && top_k >= 1 && K > 0, MOE_ERR_INVALID_ARG,
-                "moe_batched_topk_reduce: bad sizes");
+    MOE_REQUIRE(routes_in_range(T, top_k) && rows >= 0 && K > 0, MOE_ERR_INVALID_ARG,
+                "moe_batched_topk_reduce: bad sizes (T*top_k must stay below 2^31)");
     MOE_REQUIRE(rows <= INT32_MAX, MOE_ERR_INVALID_ARG, "moe_batched_topk_reduce: rows must fit int32");
     MOE_REQUIRE(is_float_dtype(y_dtype) && is_float_dtype(out_dtype), MOE_ERR_UNSUPPORTED,
                 "moe_batched_topk_reduce: y and out must be F32 or BF16");

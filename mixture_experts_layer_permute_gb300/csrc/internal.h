@@ -85,6 +85,9 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s);
 size_t experts_fused_workspace_bytes(int64_t rows_cap, int E);
 int launch_experts_fused(const GemmArgs& g1, const GemmArgs& g2, int32_t* seg_done, size_t ws_bytes,
                          cudaStream_t s);
+// Test hook of the bounded waits (MOE_TEST_SKIP_FIRST_COPY=1 at the first launch): CTA 0 of each tcgen05 GEMM
+// announces its first stage's bytes but never issues the copy.
+bool timeout_test_hook();
 // Block-scaled MXFP8 (E4M3 activations and weights) on swap-AB tcgen05 tiles.
 int launch_gemm_mx(const GemmArgs& g, cudaStream_t s);
 

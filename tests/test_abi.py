@@ -186,3 +186,41 @@ def test_reduce_and_quant_validation(lib):
     assert lib.mxfp8_quantize_block32(fake, 1, 4, 33, fake, fake, None) == 3                     # cols % 32
     assert lib.mxfp8_quantize_block32(fake, 2, 4, 32, fake, fake, None) == 2                     # E4M3 input
     assert lib.mxfp8_quantize_block32(None, 1, 0, 32, None, None, None) == 0                     # empty: no-op
+
+
+def test_route_counts_that_overflow_are_rejected(lib):
+    # T*top_k would overflow int64 (or reach 2^31): every entry point rejects it before forming the product
+    fake = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
+    huge = 2 ** 61
+    assert m.moe_max_padded_rows(huge, 8, 128, 1) == -1
+    assert m.moe_max_padded_rows(2 ** 28, 8, 128, 1) == -1          # exactly 2^31 routes
+    assert m.moe_max_padded_rows(2 ** 28 - 1, 8, 128, 1) == (2 ** 28 - 1) * 8
+    assert m.moe_max_padded_rows(4, 2000, 8, 1) == -1               # top_k > 1024
+    assert m.moe_permute_workspace_size(huge, 8, 128) == 0
+    assert m.moe_permute_workspace_size(4, 8, 2000) == 0
+    rc = lib.moe_permute_align(fake, huge, 8, 128, 0, 1, 0, None, 1, 0, None, 8, fake, fake, fake, fake, fake,
+                               1 << 20, None, None)
+    assert rc == 1 and "2^31" in lib_error()
+    rc = lib.moe_permute_align_static(fake, huge, 8, 128, 0, 1, 0, None, 1, 0, None, 8, fake, fake, fake, fake,
+                                      None, None)
+    assert rc == 1 and "2^31" in lib_error()
+    assert lib.moe_unpermute_topk_reduce(fake, 1, fake, None, huge, 8, 128, 16, fake, 1, None) == 1
+    assert lib.moe_batched_topk_reduce(fake, 1, 64, fake, None, huge, 8, 16, ctypes.c_void_p(0x2000), 1, None,
+                                       None) == 1
+
+
+def test_permute_static_validation(lib):
+    # the entry point without a workspace: its own early checks run on the host, with nothing launched and no
+    # pointer read (the pointers below are never dereferenced)
+    fake = ctypes.c_void_p(0x1000)
+
+    def call(T=4, k=2, E=8, layout=0, bm=1, mt=0, rows_cap=8):
+        return lib.moe_permute_align_static(fake, T, k, E, layout, bm, mt, None, 1, 0, None, rows_cap, fake, fake,
+                                            fake, fake, None, None)
+    for bad in (dict(T=-1), dict(k=0), dict(k=1025), dict(E=0), dict(E=1025)):
+        assert call(**bad) == 1, bad
+        assert lib_error().startswith("moe_permute_align_static")
+    # a routing whose scratch exceeds the built-in array: refused with the limit in the message
+    rc = call(T=70000, k=8, E=128, rows_cap=70000 * 8)
+    assert rc == 4
+    assert "2097152" in lib_error() and "moe_permute_align" in lib_error()

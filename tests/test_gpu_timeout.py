@@ -7,7 +7,10 @@ MOE_DEVERR_TIMEOUT in err_word, free its tensor memory and return, leaving the C
 context usable -- the same process then runs routing and checks it against the oracle.
 In the fused experts launch the GEMM 2 tiles that wait on CTA 0's unfinished GEMM 1
 tile give up the same way (their wait on the segment counter is bounded too).  The
-batched case runs the 256-row normal tiles (one accumulator, 8 epilogue warps).
+batched case runs the 256-row normal tiles (one accumulator, 8 epilogue warps); the
+E4M3 case the MXFP8-weight tiles whose converter warps wait on the code ring; the MX
+case the block-scaled MXFP8 kernel (gemm_mx_kernel), whose MMA waits on the ring
+while its scale writers run ahead.
 """
 import os
 import subprocess
@@ -37,9 +40,18 @@ else:
     res = m.moe_permute_align(ids, 4, m.MOE_LAYOUT_CONTIGUOUS, 1, x=x)
 err = torch.zeros(1, dtype=torch.int32, device="cuda")
 t0 = time.time()
+if "{impl}" in ("E4M3", "MX"):   # MXFP8 weights: E4M3 codes + E8M0 scales
+    W1c, W1s = m.mxfp8_quantize_block32(W1)
 if "{impl}" == "BATCHED":
     m.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1, 128, layout=m.MOE_LAYOUT_BATCHED,
                        max_tokens=64, impl=m.MOE_IMPL_TCGEN05, err_word=err)
+elif "{impl}" == "E4M3":        # bf16 activations x MXFP8 weights: converter warps decode into TMEM
+    m.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1c, 128, w1_scale=W1s,
+                       impl=m.MOE_IMPL_TCGEN05_SWAP_AB, err_word=err)
+elif "{impl}" == "MX":          # MXFP8 activations x MXFP8 weights: block-scaled MMA (gemm_mx_kernel)
+    xc, xs = m.mxfp8_quantize_block32(res["x_out"])
+    m.moe_gemm1_swiglu(xc, res["counts"], res["offsets"], W1c, 128, w1_scale=W1s, a_scale=xs,
+                       impl=m.MOE_IMPL_TCGEN05_SWAP_AB, err_word=err)
 elif "{impl}" == "FUSED":
     m.moe_experts_fused(res["x_out"], res["counts"], res["offsets"], W1, W2, 128, res["row_route"], 128,
                         err_word=err)
@@ -55,7 +67,7 @@ print("ROUTE_OK", bool(np.array_equal(ids2.cpu().numpy(), rids)))
 """
 
 
-@pytest.mark.parametrize("impl", ["TCGEN05", "TCGEN05_SWAP_AB", "FUSED", "BATCHED"])
+@pytest.mark.parametrize("impl", ["TCGEN05", "TCGEN05_SWAP_AB", "FUSED", "BATCHED", "E4M3", "MX"])
 def test_gemm_wait_runs_out_and_reports(moe, impl):
     env = dict(os.environ, MOE_TEST_SKIP_FIRST_COPY="1")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT, impl=impl)], env=env, capture_output=True,

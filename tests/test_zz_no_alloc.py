@@ -54,3 +54,25 @@ def test_static_scratch_batched_and_limit(moe):
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_permute_align_static(big, 128, moe.MOE_LAYOUT_CONTIGUOUS, 1)
     assert ei.value.status == 4 and "2097152" in str(ei.value)
+
+
+def test_static_small_routing_with_bad_ids_sets_the_same_error_bits(moe):
+    # at most 1024 routes take the one-CTA placement, which never touches the scratch; ids outside [-1, E) must
+    # be skipped and flagged exactly as moe_permute_align does
+    T, k, E = 100, 8, 32
+    ids = _ids(T, k, E, 4)
+    ids[3, 1], ids[50, 7], ids[99, 0] = E, -7, 1000
+    ids = ids.to(DEV)
+    x = torch.randn(T, 128, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16).to(DEV)
+    errs = []
+    outs = []
+    for fn in (moe.moe_permute_align, moe.moe_permute_align_static):
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        outs.append(fn(ids, E, moe.MOE_LAYOUT_CONTIGUOUS, 4, x=x, err_word=err))
+        errs.append(err)
+    torch.cuda.synchronize()
+    ref, got = outs
+    rows = int(ref["offsets"][E].item())
+    _same(got, ref, rows)
+    assert int(errs[0].item()) == int(errs[1].item()) == moe.MOE_DEVERR_ID_RANGE
+    assert int((ref["route_row"] >= 0).sum().item()) == int(((ids >= 0) & (ids < E)).sum().item())

@@ -9,13 +9,20 @@ sweep: the layer at T = 1, 8, 32 and 64 tokens (K=4096, I=1536, E=128,
 top_k=8, bf16), all four passes forming one step.  Other workloads (prefill,
 mxfp8, mxfp8_act, batched, batched_tokens, tiny) can be selected with --workload.
 
-Rank 0 prints ONE JSON line.  Under torchrun (N > 1) each rank runs an
-independent replica of the workload on its GPU (the layer has no exchange
-step), a barrier brackets the timed region and the max time over ranks is
-used; value = routed tokens of all ranks / that time.
+Rank 0 prints ONE JSON line.  After the headline workload, every other
+configuration is timed in the same process on the same GPU (`configs`: value,
+ms_per_step, the roofline of its dominant kernel, the whole-layer roofline
+fraction and the clocks of its own timed region; --configs picks a subset,
+--no-configs none).  `sweep` gives each pass of the headline workload its GEMM 1
+and whole-layer time.
 
---impl reference times the CPU oracle (the plain fp64 C reference) on a
-bounded sample of the same workload on the host cores.
+--gpus N runs N independent replicas, one per GPU (the layer has no exchange
+step): under torchrun each rank is one replica; without a launcher bench.py
+starts N local ranks itself.  A barrier brackets the timed region, the max time
+over ranks is used, and value = routed tokens of all ranks / that time.
+
+--impl reference times the CPU oracle (the plain fp64 C reference) on a bounded
+sample of the same workload on all host cores.
 """
 from __future__ import annotations
 
@@ -73,7 +80,7 @@ def read_peaks():
 class Instance:
     """Device inputs and the layer object of one workload."""
 
-    def __init__(self, w, seed, device, fused=True, tiled=True):
+    def __init__(self, w, seed, device, fused=True, tiled=True, weights=None):
         import torch
         import mixture_experts_layer_permute_gb300 as m
         from mixture_experts_layer_permute_gb300 import workloads as wl
@@ -98,7 +105,9 @@ class Instance:
             self.logits = None
         else:
             self.logits = wl.router_logits(w, seed, dev)
-        if w.weight == "mxfp8":
+        if w.weight == "mxfp8" and weights is not None:   # the same draw, quantised once by another instance
+            self.W1, self.s1, self.W2, self.s2 = weights
+        elif w.weight == "mxfp8":
             self.W1, self.s1 = self._mxfp8(w, "W1", seed, dev)
             self.W2, self.s2 = self._mxfp8(w, "W2", seed, dev)
         else:
@@ -369,10 +378,179 @@ def aggregate_over_ranks(ms_total, routes, world, device):
 # our arm
 # ----------------------------------------------------------------------------
 
-def run_ours(args, rank, world, local_rank):
+def measure(insts, args, stream, world=1, flush=None):
+    """Times K steps of the passes in `insts` (one step = one forward of each, in order).
+
+    Graph mode (default): the K steps are captured in one CUDA graph with no event node inside and one replay
+    is timed with events on the stream around it (barriers on both sides for N > 1), while the SM clocks are
+    sampled; four more replays and one eager run of the same steps give the spread.  A second graph of the same
+    K steps with CUDA events around every GEMM 1 launch (or fused experts launch) gives the launch durations
+    behind the roofline, and for more than one pass a graph of K steps of each pass alone gives that pass's
+    whole-layer time.  `flush` (a device buffer larger than L2): for inputs that fit in L2, the buffer is
+    rewritten before every step and the timed quantity is the sum of CUDA events around each forward.
+    """
     import numpy as np
     import torch
     import torch.distributed as dist
+    K = args.steps
+    ext = not args.eager
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True, external=ext), torch.cuda.Event(enable_timing=True, external=ext)
+    gev = [[ev() for _ in range(K)] for _ in insts]      # GEMM 1 (or fused experts) launches
+    lev = [[ev() for _ in range(K)] for _ in insts]      # whole forwards (flush mode)
+
+    def step(s=None, gemm=False):
+        for n, inst in enumerate(insts):
+            inst.forward(gemm1_events=gev[n][s] if gemm else None)
+
+    def step_flush(s):
+        flush.fill_(s & 127)
+        for n, inst in enumerate(insts):
+            lev[n][s][0].record(stream)
+            inst.forward()
+            lev[n][s][1].record(stream)
+
+    timed = step_flush if flush is not None else (lambda s: step(s))
+    for s in range(args.warmup):
+        timed(s % K)
+    torch.cuda.synchronize()
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for s in range(K):
+                fn(s)
+        g.replay()                    # untimed: uploads the graph
+        torch.cuda.synchronize()
+        return g
+
+    mode = "eager" if args.eager else "cuda_graph"
+    g_main = g_gemm = None
+    g_pass = []
+    if not args.eager:
+        try:
+            g_main = graph_of(timed)
+            g_gemm = graph_of(lambda s: step(s, gemm=True))
+            if len(insts) > 1 and flush is None:
+                g_pass = [graph_of(lambda s, i=inst: i.forward()) for inst in insts]
+        except Exception as exc:      # capture unavailable: time the same launches eagerly
+            print(f"bench: graph capture failed ({exc}); timing eagerly", file=sys.stderr)
+            g_main = g_gemm = None
+            g_pass = []
+            mode = "eager (capture failed)"
+            gev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+                   for _ in insts]
+            lev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+                   for _ in insts]
+
+    def run_main():
+        if g_main is not None:
+            g_main.replay()
+        else:
+            for s in range(K):
+                timed(s)
+
+    def once():
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run_main()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if flush is not None:
+            return sum(x.elapsed_time(y) for e in lev for x, y in e)
+        return a.elapsed_time(b)
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms_total = once()
+        if world > 1:
+            dist.barrier()
+    reps = [ms_total / K] + [once() / K for _ in range(4 if g_main is not None else 0)]
+    eager_ms = reps[0]
+    if g_main is not None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for s in range(K):
+            timed(s)
+        b.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = (sum(x.elapsed_time(y) for e in lev for x, y in e) if flush is not None
+                    else a.elapsed_time(b)) / K
+    stats = {"ms_per_step_replays": [round(x, 4) for x in reps], "median": round(statistics.median(reps), 4),
+             "p10": round(float(np.percentile(reps, 10)), 4), "p90": round(float(np.percentile(reps, 90)), 4),
+             "eager_ms_per_step": round(eager_ms, 4)}
+    # the GEMM launch durations, from the same K steps again with their events
+    if g_gemm is not None:
+        g_gemm.replay()
+    else:
+        for s in range(K):
+            step(s, gemm=True)
+    torch.cuda.synchronize()
+    g1_ms = [sum(a.elapsed_time(b) for a, b in e) / K for e in gev]
+    # whole-layer time of each pass
+    if flush is not None:
+        layer_ms = [sum(a.elapsed_time(b) for a, b in e) / K for e in lev]
+    elif g_pass:
+        layer_ms = []
+        for g in g_pass:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            layer_ms.append(a.elapsed_time(b) / K)
+    else:
+        layer_ms = [ms_total / K]
+    return {"ms_total": ms_total, "clocks": clk.summary(), "timing_stats": stats, "g1_ms": g1_ms,
+            "layer_ms": layer_ms, "mode": mode}
+
+
+def gemm_roofline(insts, g1_ms, peaks, tensor_bound):
+    """Roofline of the dominant kernel (GEMM 1, or GEMM 1 + GEMM 2 where one launch runs both): algorithmic
+    bytes (HBM bound) or flops (tensor bound) per launch over its average launch duration."""
+    hbm, tf_burst, _tf_sust, peak_kind = peaks
+    g1_bytes = [i.gemm1_bytes() + (i.gemm2_bytes() if i.fused() else 0) for i in insts]
+    g1_flops = [i.gemm1_flops() for i in insts]
+    if tensor_bound:
+        achieved = sum(g1_flops) / (sum(g1_ms) / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": round(achieved / tf_burst, 4)}
+    else:
+        achieved = sum(g1_bytes) / (sum(g1_ms) / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4)}
+    mx = any(i.w.act_quant for i in insts)
+    fused = any(i.fused() for i in insts)
+    roof["kernel"] = ("gemm_mx_kernel" if mx else "gemm_tc_kernel") + (
+        " (moe_experts_fused: GEMM 1 + GEMM 2 in one launch)" if fused else " (moe_gemm1_swiglu)")
+    roof["peak_source"] = (f"MEASURED_PEAKS.json ({peak_kind}), " +
+                           ("bf16_tflops (burst: the GEMM runs inside a timed replay of milliseconds)"
+                            if tensor_bound else "hbm_gbs"))
+    roof["algorithmic_per_launch"] = [int(b) for b in (g1_flops if tensor_bound else g1_bytes)]
+    roof["launch_ms"] = [round(x, 4) for x in g1_ms]
+    roof["timing"] = "CUDA events around each GEMM launch, in a replay of the same K steps right after the timed one"
+    return roof
+
+
+def layer_sweep(insts, m, peaks):
+    """Per pass: routes, touched experts, algorithmic bytes and flops, GEMM 1 and whole-layer time, and the
+    layer's roofline time max(flops / tensor peak, bytes / HBM peak)."""
+    hbm, tf_burst = peaks[0], peaks[1]
+    out = []
+    for n, inst in enumerate(insts):
+        t_roof = max(inst.layer_flops() / (tf_burst * 1e12), inst.layer_bytes() / (hbm * 1e9)) * 1e3
+        out.append({"workload": inst.w.name, "routes": inst.routes, "experts_touched": inst.used_experts,
+                    "layer_bytes": inst.layer_bytes(), "layer_flops": inst.layer_flops(),
+                    "gemm1_ms": round(m["g1_ms"][n], 4), "layer_ms": round(m["layer_ms"][n], 4),
+                    "roofline_ms": round(t_roof, 4), "layer_frac": round(t_roof / m["layer_ms"][n], 4)})
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
 
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
@@ -383,130 +561,22 @@ def run_ours(args, rank, world, local_rank):
     insts = [Instance(w, args.seed, dev, fused=not args.split_experts, tiled=not args.row_major_weights)
              for w in ws]
     stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        for n, inst in enumerate(insts):
-            inst.forward(gemm1_events=None if ev is None else ev[n])
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
-    # The K timed steps run as one captured CUDA graph (the launch sequence of a
-    # decode server); --eager issues them from Python instead.  The GEMM launch
-    # durations for the roofline come from CUDA events around every GEMM 1
-    # launch in a second replay of the same K steps: an event node between two
-    # launches adds several microseconds to a pass, so the timed graph has none.
-    mode = "eager" if args.eager else "cuda_graph"
-    ev = [[(torch.cuda.Event(enable_timing=True, external=not args.eager),
-            torch.cuda.Event(enable_timing=True, external=not args.eager))
-           for _ in range(args.steps)] for _ in insts]
-    graph = graph_ev = None
-    if not args.eager:
-        try:
-            graph, graph_ev = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                for s in range(args.steps):
-                    step()
-            with torch.cuda.graph(graph_ev):
-                for s in range(args.steps):
-                    step([e[s] for e in ev])
-            graph.replay()            # untimed: uploads the graphs
-            graph_ev.replay()
-            torch.cuda.synchronize()
-        except Exception as exc:      # capture unavailable: time the same launches eagerly
-            print(f"bench: graph capture failed ({exc}); timing eagerly", file=sys.stderr)
-            graph = graph_ev = None
-            mode = "eager (capture failed)"
-            ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)] for _ in insts]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
-        start.record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            for s in range(args.steps):
-                step()
-        end.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-    ms_total = start.elapsed_time(end)
-    clocks = clk.summary()
-    # spread and noise floor: the timed graph replayed four more times, and the K steps issued eagerly once
-    # (outside the timed region; `value` is the first replay alone)
-    reps = [ms_total / args.steps]
-    for _ in range(4 if graph is not None else 0):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        graph.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        reps.append(a.elapsed_time(b) / args.steps)
-    eager_ms = reps[0]
-    if graph is not None:
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for s in range(args.steps):
-            step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        eager_ms = a.elapsed_time(b) / args.steps
-    timing_stats = {"ms_per_step_replays": [round(x, 4) for x in reps],
-                    "median": round(statistics.median(reps), 4),
-                    "p10": round(float(np.percentile(reps, 10)), 4), "p90": round(float(np.percentile(reps, 90)), 4),
-                    "eager_ms_per_step": round(eager_ms, 4)}
-
-    # the same K steps again, with the GEMM events
-    if graph_ev is not None:
-        graph_ev.replay()
-    else:
-        for s in range(args.steps):
-            step([e[s] for e in ev])
-    torch.cuda.synchronize()
-
+    peaks = read_peaks()
+    flush = l2_flush_buffer(insts, dev)
+    m = measure(insts, args, stream, world, flush)
     routes_per_step = sum(i.routes for i in insts)
-    t_max, total_routes = aggregate_over_ranks(ms_total, routes_per_step * args.steps, world, dev)
+    t_max, total_routes = aggregate_over_ranks(m["ms_total"], routes_per_step * args.steps, world, dev)
     value = total_routes / (t_max / 1e3)
-
-    # GEMM 1 roofline (HBM bound for decode/mxfp8/batched, tensor bound for prefill)
-    hbm, tf_burst, tf_sust, peak_kind = read_peaks()
-    g1_ms = [sum(a.elapsed_time(b) for a, b in e) / args.steps for e in ev]
-    g1_bytes = [i.gemm1_bytes() + (i.gemm2_bytes() if i.fused() else 0) for i in insts]
-    g1_flops = [i.gemm1_flops() for i in insts]
     prefill = args.workload == "prefill"
-    if prefill:
-        achieved = sum(g1_flops) / (sum(g1_ms) / 1e3) / 1e12
-        peak = tf_sust or tf_burst
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4)}
-    else:
-        achieved = sum(g1_bytes) / (sum(g1_ms) / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4)}
-    mx = any(i.w.act_quant for i in insts)
-    fused = any(i.fused() for i in insts)
-    roof["kernel"] = ("gemm_mx_kernel" if mx else "gemm_tc_kernel") + (
-        " (moe_experts_fused: GEMM 1 + GEMM 2 in one launch)" if fused else " (moe_gemm1_swiglu)")
-    roof["peak_source"] = f"MEASURED_PEAKS.json ({peak_kind})" + (", sustained bf16" if prefill else "")
-    roof["traffic"] = recorded_traffic(args.workload, fused, any(i.w1_layout == i.m.MOE_W_TILED for i in insts))
-    roof["algorithmic_per_launch"] = [int(b) for b in (g1_flops if prefill else g1_bytes)]
-    roof["launch_ms"] = [round(x, 4) for x in g1_ms]
-    roof["timing"] = ("CUDA events around each GEMM launch, in a replay of the same K steps right after the "
-                      "timed one")
+    roof = gemm_roofline(insts, m["g1_ms"], peaks, tensor_bound=prefill)
+    roof["traffic"] = recorded_traffic(args.workload, any(i.fused() for i in insts),
+                                       any(i.w1_layout == i.m.MOE_W_TILED for i in insts))
+    sweep = layer_sweep(insts, m, peaks)
+    del flush
 
-    # whole-layer roofline per pass: max(flops / tensor peak, bytes / HBM peak)
-    sweep = []
-    for n, inst in enumerate(insts):
-        t_roof = max(inst.layer_flops() / (tf_burst * 1e12), inst.layer_bytes() / (hbm * 1e9)) * 1e3
-        sweep.append({"workload": inst.w.name, "routes": inst.routes, "experts_touched": inst.used_experts,
-                      "layer_bytes": inst.layer_bytes(), "layer_flops": inst.layer_flops(),
-                      "gemm1_ms": round(g1_ms[n], 4), "roofline_ms": round(t_roof, 4)})
-
+    configs = None
+    if world == 1 and rank == 0 and not args.no_configs:
+        configs = run_configs(args, dev, stream, peaks, skip=args.workload)
     e2e = None if args.no_e2e else run_e2e(args, insts, dev)
     launches = sum(i.launches() for i in insts) * args.steps
     cpu = cpu_baseline(args, insts) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
@@ -516,15 +586,72 @@ def run_ours(args, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": insts[0].w.act, "data": "synthetic",
             "config": {"workload": describe(args.workload, ws), "parallelism": f"replicas x{world}",
-                       "launch": mode,
+                       "launch": m["mode"],
                        "weights": ("tile-contiguous (moe_tile_weights, prepared once, untimed)"
                                    if any(i.w1_layout == i.m.MOE_W_TILED for i in insts) else "as stored"),
-                       "l2": "inputs larger than L2 (touched expert weights exceed 129 MB every pass)",
+                       "l2": l2_note(insts),
                        "routes_per_step": routes_per_step},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-            "timing_stats": timing_stats, "sweep": sweep,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": m["clocks"],
+            "timing_stats": m["timing_stats"], "sweep": sweep, "configs": configs,
         }
         print(json.dumps(line), flush=True)
+
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def l2_flush_buffer(insts, dev):
+    """A 512 MiB device buffer rewritten between steps when one step's touched bytes fit in L2 (else None)."""
+    import torch
+    if sum(i.layer_bytes() for i in insts) > 2 * L2_BYTES:
+        return None
+    return torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+
+
+def l2_note(insts):
+    if sum(i.layer_bytes() for i in insts) > 2 * L2_BYTES:
+        return "inputs larger than L2 (the touched expert weights of every step exceed 129 MB)"
+    return "L2 flushed between steps (512 MiB write, outside the timed forwards)"
+
+
+# the other configurations, timed in the same process after the headline workload
+CONFIG_WORKLOADS = ("tiny", "prefill", "mxfp8", "mxfp8_act", "batched", "batched_tokens")
+
+
+def run_configs(args, dev, stream, peaks, skip=None):
+    """Every other configuration, one at a time on the same GPU: value, ms_per_step, roofline of the dominant
+    kernel, whole-layer roofline fraction and the clocks seen while it was timed."""
+    import gc
+    import torch
+    out = {}
+    shared = None   # the quantised MXFP8 weights, drawn once for mxfp8 and mxfp8_act
+    chosen = [c for c in args.configs.split(",") if c]
+    for c in chosen:
+        if c not in CONFIG_WORKLOADS:
+            raise SystemExit(f"bench.py: unknown configuration {c!r} (known: {', '.join(CONFIG_WORKLOADS)})")
+    for name in CONFIG_WORKLOADS:
+        if name == skip or name not in chosen:
+            continue
+        w = workload_list(name)[0]
+        inst = Instance(w, args.seed, dev, weights=shared if w.weight == "mxfp8" else None)
+        if w.weight == "mxfp8":
+            shared = (inst.W1, inst.s1, inst.W2, inst.s2)
+        flush = l2_flush_buffer([inst], dev)
+        m = measure([inst], args, stream, 1, flush)
+        roof = gemm_roofline([inst], m["g1_ms"], peaks, tensor_bound=(name == "prefill"))
+        sw = layer_sweep([inst], m, peaks)[0]
+        out[name] = {"workload": describe(name, [w]), "value": round(inst.routes * args.steps / (m["ms_total"] / 1e3), 1),
+                     "unit": UNIT, "ms_per_step": round(m["ms_total"] / args.steps, 4),
+                     "routes_per_step": inst.routes, "experts_touched": inst.used_experts,
+                     "layer_roofline_ms": sw["roofline_ms"], "layer_frac": sw["layer_frac"],
+                     "roofline": roof, "clocks": m["clocks"], "timing_stats": m["timing_stats"],
+                     "gpu_launches": inst.launches() * args.steps, "l2": l2_note([inst]), "launch": m["mode"]}
+        del inst, flush, m
+        if name == "mxfp8_act" or (w.weight == "mxfp8" and ("mxfp8_act" == skip or "mxfp8_act" not in chosen)):
+            shared = None
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, insts, dev):
@@ -698,51 +825,106 @@ def run_oracle_samples(samples):
     return routes
 
 
+def host_cores():
+    """Host cores this process may run on (the affinity mask; os.cpu_count() where that is unavailable)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def time_oracle(samples, seconds, threads):
+    """Routes per second of the oracle on `samples` (one token each) for about `seconds`: `threads` host threads
+    each run whole oracle calls, one sample at a time (the oracle's C calls release the GIL); the oracle itself
+    is unchanged."""
+    from concurrent.futures import ThreadPoolExecutor
+    t0 = time.perf_counter()
+    routes, reps = 0, 0
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            # one round: every thread gets len(samples) calls
+            tasks = [[sm] for sm in samples] * threads
+            routes += sum(ex.map(run_oracle_samples, tasks))
+            reps += 1
+            if time.perf_counter() - t0 > seconds or reps >= 50:
+                break
+    dt = time.perf_counter() - t0
+    return routes / dt, routes, dt, reps
+
+
 def cpu_baseline(args, insts):
     import oracle
     oracle.build()
     samples = oracle_sample([i.w for i in insts], args.seed, insts)
-    t0 = time.perf_counter()
-    routes, reps = 0, 0
-    while True:
-        routes += run_oracle_samples(samples)
-        reps += 1
-        if time.perf_counter() - t0 > args.cpu_seconds or reps >= 50:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(routes / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x (one token of each pass of the workload, all its routes; single-threaded C "
-                      f"oracle, fp64), {routes} routes in {dt:.1f} s on the host"}
+    n = host_cores()
+    v1, r1, t1, k1 = time_oracle(samples, args.cpu_seconds / 2, 1)
+    vn, rn, tn, kn = time_oracle(samples, args.cpu_seconds / 2, n)
+    return {"value": round(vn, 3), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"one token of each pass of the workload (all its routes) per oracle call, fp64 C oracle; "
+                      f"{n} host threads: {rn} routes in {tn:.1f} s; 1 thread: {r1} routes in {t1:.1f} s",
+            "single_thread": {"value": round(v1, 3), "cores": 1},
+            "nproc": os.cpu_count()}
 
 
 def run_reference(args, rank):
     if rank != 0:
         return
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     oracle.build()
     ws = workload_list(args.workload)
     samples = oracle_sample(ws, args.seed)
-    # each step: one token of one pass of the workload, rotating through the passes
-    for i in range(args.warmup):
-        run_oracle_samples([samples[i % len(samples)]])
-    t0 = time.perf_counter()
-    routes = 0
-    for i in range(args.steps):
-        routes += run_oracle_samples([samples[i % len(samples)]])
-    dt = time.perf_counter() - t0
+    n = host_cores()
+    # each step: one oracle call per host thread, each on one token (all its routes) of one pass of the
+    # workload, passes in rotation
+    calls = 0
+
+    def one_step(ex):
+        nonlocal calls
+        tasks = [[samples[(calls + i) % len(samples)]] for i in range(n)]
+        calls += n
+        return sum(ex.map(run_oracle_samples, tasks))
+
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        for _ in range(args.warmup):
+            one_step(ex)
+        t0 = time.perf_counter()
+        routes = 0
+        for _ in range(args.steps):
+            routes += one_step(ex)
+        dt = time.perf_counter() - t0
     value = routes / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": describe(args.workload, ws),
-                   "sample": "each step: one token (all its routes) of one pass of the workload, passes in "
-                             "rotation, through the CPU oracle"},
-        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "one token of one pass per step, single-threaded fp64 C oracle"},
+                   "sample": f"each step: {n} oracle calls on {n} host threads, each one token (all its routes) of "
+                             "one pass of the workload, passes in rotation"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": n, "kind": "oracle",
+                         "sample": f"{n} tokens per step, one per host thread, fp64 C oracle"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def replica_launch(args, env):
+    """How `bench.py --gpus N` runs: None when this process is one rank of a launch of N ranks (or N = 1 without
+    a launcher), else the torchrun command that starts N local ranks, one replica per GPU.  A launcher whose
+    world size differs from --gpus is an error."""
+    world = env.get("WORLD_SIZE")
+    if world is not None:
+        if int(world) != args.gpus:
+            raise SystemExit(f"bench.py: --gpus {args.gpus} but the launcher started {world} ranks")
+        return None
+    if args.gpus <= 1:
+        return None
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
 
 
 def main():
@@ -756,6 +938,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only the selected workload (by default every other configuration is timed after it, "
+                         "in the line's `configs`)")
+    ap.add_argument("--configs", default=",".join(CONFIG_WORKLOADS),
+                    help="comma-separated configurations timed after the headline workload")
     ap.add_argument("--eager", action="store_true", help="issue the timed steps from Python, not as a CUDA graph")
     ap.add_argument("--split-experts", action="store_true",
                     help="run GEMM 1 and GEMM 2 as two launches even where the plan uses swap-AB tiles (by default "
@@ -768,6 +955,9 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    cmd = replica_launch(args, os.environ)
+    if cmd is not None:   # --gpus N without a launcher: N local ranks, one replica of the workload per GPU
+        sys.exit(subprocess.call(cmd))
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

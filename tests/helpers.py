@@ -44,3 +44,15 @@ def compact_experts(ids: np.ndarray, W1: torch.Tensor, W2: torch.Tensor, S1=None
     out.append(None if S1 is None else wl.to_numpy(S1.index_select(0, sel)))
     out.append(None if S2 is None else wl.to_numpy(S2.index_select(0, sel)))
     return new_ids, out
+
+
+def oracle_map(fn, tasks, workers=None):
+    """Runs fn(task) for every task on a thread pool and returns the results in task order.
+
+    The oracle's C calls release the GIL (ctypes), so one oracle call per token runs on every host core at
+    once, sharing the host arrays without copies; the oracle itself is unchanged (one plain call per task)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    n = workers or max(1, os.cpu_count() or 1)
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        return list(ex.map(fn, tasks))

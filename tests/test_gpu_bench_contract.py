@@ -24,7 +24,7 @@ def _line(args):
 
 
 def test_bench_line_has_every_key():
-    d = _line(["--workload", "tiny", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1"])
+    d = _line(["--workload", "tiny", "--steps", "3", "--warmup", "3", "--cpu-seconds", "2", "--configs", "prefill"])
     for k in REQUIRED:
         assert k in d, k
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["n_gpus"] == 1 and d["steps"] == 3
@@ -34,6 +34,17 @@ def test_bench_line_has_every_key():
     assert roof["achieved"] > 0 and abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] > 0
+    assert cpu["single_thread"]["cores"] == 1 and cpu["single_thread"]["value"] > 0
+    # the per-pass sweep and the other configurations timed in the same process
+    sw = d["sweep"][0]
+    assert sw["layer_ms"] > 0 and sw["gemm1_ms"] <= sw["layer_ms"] and sw["layer_frac"] > 0
+    assert list(d["configs"]) == ["prefill"]
+    c = d["configs"]["prefill"]
+    for k in ("value", "ms_per_step", "roofline", "clocks", "layer_frac", "routes_per_step", "gpu_launches"):
+        assert k in c, k
+    assert c["value"] > 0 and c["roofline"]["bound"] == "tensor" and 0 < c["roofline"]["frac"] < 1.2
+    assert abs(c["value"] - c["routes_per_step"] / (c["ms_per_step"] / 1e3)) / c["value"] < 1e-3
+    assert "sm_mhz" in c["clocks"]
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0

@@ -57,6 +57,38 @@ def test_single_rank_is_identity():
     assert bench.aggregate_over_ranks(7.5, 42, 1, "cpu") == (7.5, 42.0)
 
 
+def test_replica_launch_plan():
+    """--gpus N: one rank of a launch of N runs as is; without a launcher bench.py starts N local ranks; a
+    launcher whose world size differs from --gpus is refused."""
+    sys.path.insert(0, ROOT)
+    import argparse
+    import bench
+    a1, a4 = argparse.Namespace(gpus=1), argparse.Namespace(gpus=4)
+    assert bench.replica_launch(a1, {}) is None
+    assert bench.replica_launch(a4, {"WORLD_SIZE": "4"}) is None
+    with pytest.raises(SystemExit):
+        bench.replica_launch(a4, {"WORLD_SIZE": "2"})
+    cmd = bench.replica_launch(a4, {})
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"] and "--nproc-per-node=4" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert any(c.endswith("bench.py") for c in cmd)
+
+
+@pytest.mark.slow
+def test_bench_gpus_2_starts_its_own_ranks():
+    """`bench.py --gpus 2` without a launcher starts two local ranks (torchrun); on the reference arm rank 0
+    alone prints, so exactly one JSON line comes out."""
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    env.pop("WORLD_SIZE", None)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "0", "--workload", "tiny"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    assert json.loads(lines[0])["impl"] == "reference"
+
+
 @pytest.mark.slow
 def test_reference_arm_under_torchrun_prints_once():
     """--impl reference under torchrun with two ranks (gloo is enough: no collective is used): one JSON line."""

@@ -406,10 +406,11 @@ def measure(insts, args, stream, world=1, flush=None):
 
     def step_flush(s):
         flush.fill_(s & 127)
+        cur = torch.cuda.current_stream()     # the capture stream while a graph is being recorded
         for n, inst in enumerate(insts):
-            lev[n][s][0].record(stream)
+            lev[n][s][0].record(cur)
             inst.forward()
-            lev[n][s][1].record(stream)
+            lev[n][s][1].record(cur)
 
     timed = step_flush if flush is not None else (lambda s: step(s))
     for s in range(args.warmup):

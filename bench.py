@@ -80,7 +80,7 @@ def read_peaks():
 class Instance:
     """Device inputs and the layer object of one workload."""
 
-    def __init__(self, w, seed, device, fused=True, tiled=True, weights=None):
+    def __init__(self, w, seed, device, fused=True, tiled=True, weights=None, impl=None):
         import torch
         import mixture_experts_layer_permute_gb300 as m
         from mixture_experts_layer_permute_gb300 import workloads as wl
@@ -119,7 +119,8 @@ class Instance:
                                     layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens, device=dev)
         else:
             self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
-                                    act_quant=w.act_quant, fused_experts=fused, device=dev)
+                                    act_quant=w.act_quant, fused_experts=fused, device=dev,
+                                    impl=m.MOE_IMPL_AUTO if impl is None else impl)
         # weights as the kernels stream them: row-major, or (fused decode plan, bf16) re-laid out once into the
         # tile-contiguous layout by moe_tile_weights -- weight preparation, outside every timed region
         self.W1r, self.W2r, self.w1_layout = self.W1, self.W2, w.w1_layout
@@ -559,7 +560,10 @@ def run_ours(args, rank, world, local_rank):
     if args.experts:
         from mixture_experts_layer_permute_gb300 import workloads as wl
         ws = [wl.scaled(w, E=args.experts) for w in ws]
-    insts = [Instance(w, args.seed, dev, fused=not args.split_experts, tiled=not args.row_major_weights)
+    import mixture_experts_layer_permute_gb300 as m
+    impl = {"auto": m.MOE_IMPL_AUTO, "tcgen05": m.MOE_IMPL_TCGEN05, "swap_ab": m.MOE_IMPL_TCGEN05_SWAP_AB,
+            "pair": m.MOE_IMPL_TCGEN05_PAIR, "mixed": m.MOE_IMPL_TCGEN05_MIXED, "simt": m.MOE_IMPL_SIMT}[args.gemm_impl]
+    insts = [Instance(w, args.seed, dev, fused=not args.split_experts, tiled=not args.row_major_weights, impl=impl)
              for w in ws]
     stream = torch.cuda.current_stream()
     peaks = read_peaks()
@@ -951,6 +955,9 @@ def main():
     ap.add_argument("--row-major-weights", action="store_true",
                     help="stream the weights as stored (E, rows, cols); by default the fused decode plan reads them "
                          "re-laid out once by moe_tile_weights")
+    ap.add_argument("--gemm-impl", default="auto", choices=["auto", "tcgen05", "swap_ab", "pair", "mixed", "simt"],
+                    help="GEMM implementation of the headline workload's contiguous layer (default: the library's "
+                         "choice)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: fewer experts than the workload (a small case for ncu)")
     args = ap.parse_args()

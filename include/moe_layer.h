@@ -79,6 +79,8 @@ extern "C" {
 #define MOE_DEVERR_ID_RANGE 1
 #define MOE_DEVERR_CAPACITY 2
 #define MOE_DEVERR_TIMEOUT 4
+#define MOE_DEVERR_INTERNAL 8         /* a kernel's own consistency check failed (the two CTAs of a pair saw
+                                         different tensor-memory addresses); it did no work, outputs unspecified */
 
 /* ---- element types ---- */
 #define MOE_F32 0
@@ -108,6 +110,10 @@ extern "C" {
 #define MOE_IMPL_SIMT 3               /* CUDA-core FMA tiles (fp32 path, any shape) */
 #define MOE_IMPL_TCGEN05_MIXED 4      /* tcgen05: 128-row tiles for experts of 64 rows or more and a swap-AB
                                          tile for each smaller expert, in one launch (bf16 weights) */
+#define MOE_IMPL_TCGEN05_PAIR 5       /* tcgen05 on CTA pairs (cta_group::2, two SMs per tile): 256 weight rows
+                                         on the MMA M side (128 staged by each SM), up to 256 tokens on N;
+                                         bf16 activations and weights, 2I % 256 == 0 (GEMM 1), K % 256 == 0
+                                         (GEMM 2), contraction % 64 == 0 */
 
 /* Message describing the calling thread's last failed call ("" if none). */
 MOE_API const char* moe_last_error(void);

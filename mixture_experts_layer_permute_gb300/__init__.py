@@ -7,8 +7,10 @@ this package does not load the library; ``load()`` does, and raises if it has
 not been built.
 """
 from .binding import (  # noqa: F401
-    EXPORTED, LIB_PATH, MOE_BF16, MOE_DEVERR_CAPACITY, MOE_DEVERR_ID_RANGE, MOE_DEVERR_TIMEOUT, MOE_E4M3, MOE_F32,
-    MOE_IMPL_AUTO, MOE_IMPL_SIMT, MOE_IMPL_TCGEN05, MOE_IMPL_TCGEN05_MIXED, MOE_IMPL_TCGEN05_SWAP_AB,
+    EXPORTED, LIB_PATH, MOE_BF16, MOE_DEVERR_CAPACITY, MOE_DEVERR_ID_RANGE, MOE_DEVERR_INTERNAL, MOE_DEVERR_TIMEOUT,
+    MOE_E4M3, MOE_F32,
+    MOE_IMPL_AUTO, MOE_IMPL_SIMT, MOE_IMPL_TCGEN05, MOE_IMPL_TCGEN05_MIXED, MOE_IMPL_TCGEN05_PAIR,
+    MOE_IMPL_TCGEN05_SWAP_AB,
     MOE_LAYOUT_BATCHED,
     MOE_LAYOUT_CONTIGUOUS, MOE_W1_GATE_UP, MOE_W1_INTERLEAVE16, MOE_W_TILED, MoEError, load, moe_batched_topk_reduce, moe_batched_weight_reduce, moe_experts_fused,
     moe_experts_fused_workspace_size,

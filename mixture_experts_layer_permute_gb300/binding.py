@@ -25,7 +25,8 @@ MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_LAYOUT_CONTIGUOUS, MOE_LAYOUT_BATCHED = 0, 1
 MOE_W1_GATE_UP, MOE_W1_INTERLEAVE16, MOE_W_TILED = 0, 1, 2
 MOE_IMPL_AUTO, MOE_IMPL_TCGEN05, MOE_IMPL_TCGEN05_SWAP_AB, MOE_IMPL_SIMT, MOE_IMPL_TCGEN05_MIXED = 0, 1, 2, 3, 4
-MOE_DEVERR_ID_RANGE, MOE_DEVERR_CAPACITY, MOE_DEVERR_TIMEOUT = 1, 2, 4
+MOE_IMPL_TCGEN05_PAIR = 5
+MOE_DEVERR_ID_RANGE, MOE_DEVERR_CAPACITY, MOE_DEVERR_TIMEOUT, MOE_DEVERR_INTERNAL = 1, 2, 4, 8
 
 EXPORTED = [
     "moe_last_error", "moe_version", "moe_max_padded_rows", "moe_permute_workspace_size", "moe_topk_route",

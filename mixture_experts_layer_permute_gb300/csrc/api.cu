@@ -282,6 +282,10 @@ int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
         }
     }
     if (chosen == MOE_IMPL_SIMT) return launch_status(launch_gemm_simt(g, s), name);
+    if (chosen == MOE_IMPL_TCGEN05_PAIR) {
+        MOE_REQUIRE(device_cc() >= 100, MOE_ERR_UNSUPPORTED, std::string(name) + ": tcgen05 needs an sm_100+ device");
+        return launch_gemm_pair(g, s);
+    }
     MOE_REQUIRE(chosen == MOE_IMPL_TCGEN05 || chosen == MOE_IMPL_TCGEN05_SWAP_AB ||
                     chosen == MOE_IMPL_TCGEN05_MIXED,
                 MOE_ERR_INVALID_ARG, std::string(name) + ": unknown impl");

@@ -853,10 +853,6 @@ struct MapKeyHash {
     }
 };
 
-struct MapSet {
-    CUtensorMap act, w, act_s, w_s;
-};
-
 std::mutex g_map_mu;
 std::unordered_map<MapKey, MapSet, MapKeyHash> g_maps;
 

@@ -2,6 +2,7 @@
 // Arguments are validated in api.cu before any of these is called.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -80,6 +81,15 @@ cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t s);
 enum { TC_NORMAL = 0, TC_SWAP = 1, TC_MIXED = 2 };
 // Returns MOE_OK or a status (with message) when the tcgen05 path cannot run.
 int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s);
+// TMA tensor maps of one tcgen05 launch: activation rows and weight rows (normal or swap-AB boxes), and for
+// mixed launches the swap-AB pair as well; encoded once per (device, pointers, shape) and cached.
+struct MapSet {
+    CUtensorMap act, w, act_s, w_s;
+};
+int cached_maps(const GemmArgs& g, int mode, bool w8, int64_t kdim, int64_t wrows, int w_mode, MapSet* out);
+// bf16 grouped GEMM on CTA pairs (cta_group::2): 256 weight rows across the two SMs of a pair, up to 256 tokens
+// per tile.  Returns MOE_ERR_UNSUPPORTED (nothing launched) for shapes outside its tiles.
+int launch_gemm_pair(const GemmArgs& g, cudaStream_t s);
 // GEMM 1 then GEMM 2 (bf16, swap-AB tiles, contiguous layout) in one cooperative launch; seg_done is the
 // caller's workspace (per token segment counters, cleared by the call).
 size_t experts_fused_workspace_bytes(int64_t rows_cap, int E);

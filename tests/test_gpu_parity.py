@@ -17,12 +17,12 @@ from helpers import TOL_BF16, TOL_F32, assert_close, compact_experts, to_f64
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-IMPLS_BF16 = ["tcgen05", "swap_ab", "mixed", "simt"]
+IMPLS_BF16 = ["tcgen05", "swap_ab", "mixed", "pair", "simt"]
 
 
 def _impl(m, name):
     return {"tcgen05": m.MOE_IMPL_TCGEN05, "swap_ab": m.MOE_IMPL_TCGEN05_SWAP_AB, "simt": m.MOE_IMPL_SIMT,
-            "mixed": m.MOE_IMPL_TCGEN05_MIXED, "auto": m.MOE_IMPL_AUTO}[name]
+            "mixed": m.MOE_IMPL_TCGEN05_MIXED, "pair": m.MOE_IMPL_TCGEN05_PAIR, "auto": m.MOE_IMPL_AUTO}[name]
 
 
 # ----------------------------------------------------------------------------
@@ -432,7 +432,7 @@ def test_gemm2(moe, impl, shape, weighted):
     assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 {impl}")
 
 
-@pytest.mark.parametrize("impl", ["tcgen05", "auto"])
+@pytest.mark.parametrize("impl", ["tcgen05", "pair", "auto"])
 @pytest.mark.parametrize("maxT", [300, 256, 140])
 @pytest.mark.parametrize("w1_layout", [0, 1])
 def test_gemms_batched_layout(moe, impl, maxT, w1_layout):
@@ -462,6 +462,55 @@ def test_gemms_batched_layout(moe, impl, maxT, w1_layout):
         yref = oracle.expert_down(wl.to_numpy(hc[e, :c]), ids, wl.to_numpy(W2))
         yref = yref * rw[e, :c].numpy().astype(np.float64)[:, None]
         assert_close(to_f64(yc[e, :c]), yref, TOL_BF16, f"batched gemm2 expert {e}")
+
+
+@pytest.mark.parametrize("w1_layout", [0, 1])
+def test_pair_tiles_ragged_segments(moe, w1_layout):
+    """CTA-pair tiles on experts of 257, 255, 33 and 1 tokens (a full 256-token segment plus a 1-token one, N
+    rounded up to 32 tokens, one token), several 256-row weight tiles per expert: GEMM 1 and GEMM 2 (weighted,
+    scattered to the routes) against the oracle, and run-to-run bit identity."""
+    counts = [257, 255, 33, 1]
+    E, K, I = len(counts), 512, 384
+    g = torch.Generator().manual_seed(31)
+    ids = torch.cat([torch.full((c,), e, dtype=torch.int32) for e, c in enumerate(counts)])
+    ids = ids[torch.randperm(ids.numel(), generator=g)].reshape(-1, 1)
+    T = ids.shape[0]
+    w = wl.scaled(wl.decode(T), T=T, K=K, I=I, E=E, top_k=1, w_std=0.05)
+    x = wl.activations(w, 31)
+    W1 = wl.expert_weights(w, "W1", 31)
+    W2 = wl.expert_weights(w, "W2", 31)
+    wts = torch.rand(T, 1, generator=g)
+    res = moe.moe_permute_align(ids.to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 128, x=x.to(DEV))
+    pair = moe.MOE_IMPL_TCGEN05_PAIR
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    h = moe.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], W1.to(DEV), I, w1_layout=w1_layout,
+                             impl=pair, err_word=err)
+    y = moe.moe_gemm2(h, res["counts"], res["offsets"], W2.to(DEV), T, row_route=res["row_route"],
+                      route_weights=wts.reshape(-1).to(DEV), impl=pair, err_word=err)
+    y2 = moe.moe_gemm2(h, res["counts"], res["offsets"], W2.to(DEV), T, row_route=res["row_route"],
+                       route_weights=wts.reshape(-1).to(DEV), impl=pair, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    flat = ids.reshape(-1).numpy()
+    href = oracle.expert_gate_up(wl.to_numpy(x), flat, wl.to_numpy(W1), w1_layout=w1_layout)
+    rr = res["route_row"].cpu().reshape(-1).long()
+    assert_close(to_f64(h.cpu()[rr]), href, TOL_BF16, "pair gemm1")
+    yref = oracle.expert_down(wl.to_numpy(h.cpu()[rr]), flat, wl.to_numpy(W2)) * wts.numpy().astype(np.float64)
+    assert_close(to_f64(y.cpu()), yref, TOL_BF16, "pair gemm2")
+
+
+def test_pair_tiles_refuse_other_shapes(moe):
+    """Shapes outside the CTA-pair tiles (weight rows per expert not a multiple of 256) are refused with nothing
+    launched; MOE_IMPL_AUTO never picks them there."""
+    E, K, I = 2, 256, 64                      # GEMM 1: 2I = 128 weight rows per expert
+    x = torch.zeros((8, K), dtype=torch.bfloat16, device=DEV)
+    counts = torch.tensor([4, 4], dtype=torch.int32, device=DEV)
+    offs = torch.tensor([0, 4, 8], dtype=torch.int32, device=DEV)
+    W1 = torch.zeros((E, 2 * I, K), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_gemm1_swiglu(x, counts, offs, W1, I, impl=moe.MOE_IMPL_TCGEN05_PAIR)
+    assert ei.value.status == 2 and "256" in str(ei.value)
 
 
 E4M3_SHAPES = [  # T, k, E, K, I

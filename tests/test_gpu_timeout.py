@@ -10,7 +10,9 @@ tile give up the same way (their wait on the segment counter is bounded too).  T
 batched case runs the 256-row normal tiles (one accumulator, 8 epilogue warps); the
 E4M3 case the MXFP8-weight tiles whose converter warps wait on the code ring; the MX
 case the block-scaled MXFP8 kernel (gemm_mx_kernel), whose MMA waits on the ring
-while its scale writers run ahead.
+while its scale writers run ahead; the PAIR case the CTA-pair tiles, where the leader CTA's MMA waits
+on a stage whose bytes (counted for both CTAs) never all arrive, and both CTAs of every pair must
+still meet at their closing cluster barrier and free their tensor memory.
 """
 import os
 import subprocess
@@ -67,7 +69,7 @@ print("ROUTE_OK", bool(np.array_equal(ids2.cpu().numpy(), rids)))
 """
 
 
-@pytest.mark.parametrize("impl", ["TCGEN05", "TCGEN05_SWAP_AB", "FUSED", "BATCHED", "E4M3", "MX"])
+@pytest.mark.parametrize("impl", ["TCGEN05", "TCGEN05_SWAP_AB", "FUSED", "BATCHED", "E4M3", "MX", "TCGEN05_PAIR"])
 def test_gemm_wait_runs_out_and_reports(moe, impl):
     env = dict(os.environ, MOE_TEST_SKIP_FIRST_COPY="1")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT, impl=impl)], env=env, capture_output=True,

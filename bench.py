@@ -93,7 +93,7 @@ class Instance:
             self.W1 = wl.expert_weights(w, "W1", seed, dev)
             self.W2 = wl.expert_weights(w, "W2", seed, dev)
             self.layer = m.MoELayer(0, w.K, w.I, w.E, 1, layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens,
-                                    device=dev)
+                                    device=dev, impl=m.MOE_IMPL_AUTO if impl is None else impl)
             self.s1 = self.s2 = None
             self.W1r, self.W2r, self.w1_layout = self.W1, self.W2, w.w1_layout
             self.routes = int(self.counts.sum().item())
@@ -116,7 +116,8 @@ class Instance:
             self.s1 = self.s2 = None
         if w.layout == "batched_tokens":
             self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype,
-                                    layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens, device=dev)
+                                    layout=m.MOE_LAYOUT_BATCHED, max_tokens=w.max_tokens, device=dev,
+                                    impl=m.MOE_IMPL_AUTO if impl is None else impl)
         else:
             self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
                                     act_quant=w.act_quant, fused_experts=fused, device=dev,
@@ -524,10 +525,7 @@ def gemm_roofline(insts, g1_ms, peaks, tensor_bound):
         achieved = sum(g1_bytes) / (sum(g1_ms) / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4)}
-    mx = any(i.w.act_quant for i in insts)
-    fused = any(i.fused() for i in insts)
-    roof["kernel"] = ("gemm_mx_kernel" if mx else "gemm_tc_kernel") + (
-        " (moe_experts_fused: GEMM 1 + GEMM 2 in one launch)" if fused else " (moe_gemm1_swiglu)")
+    roof["kernel"] = gemm1_kernel(insts[0])
     roof["peak_source"] = (f"MEASURED_PEAKS.json ({peak_kind}), " +
                            ("bf16_tflops (burst: the GEMM runs inside a timed replay of milliseconds)"
                             if tensor_bound else "hbm_gbs"))
@@ -535,6 +533,23 @@ def gemm_roofline(insts, g1_ms, peaks, tensor_bound):
     roof["launch_ms"] = [round(x, 4) for x in g1_ms]
     roof["timing"] = "CUDA events around each GEMM launch, in a replay of the same K steps right after the timed one"
     return roof
+
+
+def gemm1_kernel(inst):
+    """The kernel behind the timed GEMM 1 launch, by the library's MOE_IMPL_AUTO rule: block-scaled MXFP8 for
+    quantised activations, the fused experts launch in the decode regime, swap-AB tiles for E4M3 weights or
+    few rows per expert, CTA-pair tiles otherwise (bf16)."""
+    w, L = inst.w, inst.layer
+    if w.act_quant:
+        return "gemm_mx_kernel (moe_gemm1_swiglu)"
+    if inst.fused():
+        return "gemm_tc_kernel (moe_experts_fused: GEMM 1 + GEMM 2 in one launch)"
+    if w.weight == "f32":
+        return "gemm_simt_kernel (moe_gemm1_swiglu)"
+    per_expert = (L.max_tokens // 2) if w.layout != "contiguous" else L.rows_cap // max(1, w.E)
+    if w.weight == "mxfp8" or per_expert < 64:
+        return "gemm_tc_kernel (moe_gemm1_swiglu, swap-AB tiles)"
+    return "gemm_pair_kernel (moe_gemm1_swiglu, CTA-pair tiles)"
 
 
 def layer_sweep(insts, m, peaks):

@@ -100,8 +100,9 @@ extern "C" {
                                          written by moe_tile_weights */
 
 /* ---- GEMM implementations ---- */
-#define MOE_IMPL_AUTO 0               /* swap-AB tiles when routes/expert are few, else normal tiles;
-                                         E4M3 weights on swap-AB tiles; CUDA cores for fp32 */
+#define MOE_IMPL_AUTO 0               /* swap-AB tiles when routes/expert are few, else CTA-pair tiles
+                                         (bf16; normal tiles for shapes outside them); E4M3 weights on
+                                         swap-AB tiles; CUDA cores for fp32 */
 #define MOE_IMPL_TCGEN05 1            /* tcgen05 tiles, tokens on the MMA M side (128 rows per tile; 256,
                                          as two MMA halves, for the batched layout) */
 #define MOE_IMPL_TCGEN05_SWAP_AB 2    /* tcgen05 tiles, weight rows on the MMA M side, tokens on N

@@ -278,13 +278,19 @@ int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
             int64_t rows = g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens;
             int64_t per_expert = rows / std::max(1, g.E);
             if (g.layout == MOE_LAYOUT_BATCHED) per_expert = g.max_tokens / 2;
-            chosen = per_expert < 64 ? MOE_IMPL_TCGEN05_SWAP_AB : MOE_IMPL_TCGEN05;
+            // many tokens per expert: CTA-pair tiles (measured faster than 128-row normal tiles on the skewed
+            // prefill, batched and batched-token workloads), normal tiles for shapes outside them
+            chosen = per_expert < 64 ? MOE_IMPL_TCGEN05_SWAP_AB
+                                     : (g.w_dtype == MOE_BF16 ? MOE_IMPL_TCGEN05_PAIR : MOE_IMPL_TCGEN05);
         }
     }
     if (chosen == MOE_IMPL_SIMT) return launch_status(launch_gemm_simt(g, s), name);
     if (chosen == MOE_IMPL_TCGEN05_PAIR) {
         MOE_REQUIRE(device_cc() >= 100, MOE_ERR_UNSUPPORTED, std::string(name) + ": tcgen05 needs an sm_100+ device");
-        return launch_gemm_pair(g, s);
+        const int rc = launch_gemm_pair(g, s);
+        if (rc != MOE_ERR_UNSUPPORTED || impl != MOE_IMPL_AUTO) return rc;
+        g_last_error.clear();   // shape outside the pair tiles: single-SM normal tiles (or CUDA cores) below
+        chosen = MOE_IMPL_TCGEN05;
     }
     MOE_REQUIRE(chosen == MOE_IMPL_TCGEN05 || chosen == MOE_IMPL_TCGEN05_SWAP_AB ||
                     chosen == MOE_IMPL_TCGEN05_MIXED,

@@ -83,6 +83,11 @@ MOE_DEVICE void report(int32_t* err_word, int bit) {
 
 MOE_DEVICE float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// SiLU-and-mul with the fast exponential and division intrinsics (__expf, __fdividef): a few ulp from
+// silu_mul, for epilogues where the full-precision division dominates the instruction count.  For g below
+// about -87 the denominator overflows and the result is 0 (silu_mul gives a value below 1e-36 there).
+MOE_DEVICE float silu_mul_fast(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
 // ---- expert tile schedule -------------------------------------------------
 //
 // A grouped GEMM walks "tiles" that each belong to one expert.  The number of

@@ -16,14 +16,17 @@
 //
 // Per CTA, 192 threads:
 //   warp 0      TMA producer: this CTA's 128 weight rows (128-byte swizzled, through the gate/up view for
-//               GEMM 1 as in the single-SM swap-AB tiles) and N/2 token rows (16-row boxes) of each k-block
-//               into a 6-stage ring; the bytes of BOTH CTAs are counted on the leader CTA's "full" barrier.
+//               GEMM 1 as in the single-SM swap-AB tiles) and its 128-row box of the tile's tokens (of which
+//               the MMA reads N/2) of each k-block into a 6-stage ring; the bytes of BOTH CTAs are counted on
+//               the leader CTA's "full" barrier.
 //   warp 1      TMEM: allocates all 512 columns for the pair (one warp of each CTA, together).  In the
 //               leader CTA (rank 0) one thread issues the pair's MMAs and commits each stage to the "empty"
 //               barriers and each finished accumulator to the "acc_full" barriers of both CTAs (multicast).
-//   warps 2..5  epilogue: tcgen05.ld of this CTA's accumulator (TMEM lane = weight row, column = token),
-//               SiLU-and-mul (GEMM 1) or route weight + scatter to the (token, slot) row (GEMM 2); then one
-//               arrival per warp on the leader's "acc_empty" barrier (8 per tile: both CTAs).
+//   warps 2..9  epilogue, two warps per TMEM lane quarter taking alternate 16-token chunks: tcgen05.ld of
+//               this CTA's accumulator (TMEM lane = weight row, column = token), SiLU-and-mul (GEMM 1) or
+//               route weight + scatter to the (token, slot) row (GEMM 2), each 16-token block transposed
+//               through the warp's own shared-memory tile into 16-byte stores; then one arrival per warp on
+//               the leader's "acc_empty" barrier (16 per tile: both CTAs).
 // Two 256-column accumulators let the epilogue of one tile overlap the MMAs of the next.
 //
 // Every mbarrier wait is bounded (2 s of globaltimer); on expiry the CTA records MOE_DEVERR_TIMEOUT and its
@@ -46,7 +49,6 @@ constexpr int PM = 128;                      // weight rows per CTA (the pair's 
 constexpr int PK = 64;                       // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
 constexpr int PSPAN = 256;                   // tokens per tile (MMA N; N/2 staged by each CTA)
-constexpr int TOK_BOX = 16;                  // token rows per TMA box
 constexpr int STAGES = 6;
 constexpr int A_BYTES = PM * PK * 2;         // 16 KB of weights per CTA per k-block
 constexpr int B_BYTES = (PSPAN / 2) * PK * 2;   // up to 16 KB of tokens per CTA per k-block
@@ -54,18 +56,31 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
 constexpr int ACC_COLS = PSPAN;              // fp32 TMEM columns per accumulator
 constexpr int TMEM_COLS = 512;
-constexpr int THREADS = 192;
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;                 // two per TMEM lane quarter, taking alternate 16-token chunks
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_TOK = PSPAN / 2;           // tokens of a tile one epilogue warp handles
 constexpr uint64_t kWaitNs = 2000000000ull;
+static_assert(SMEM + 13 * 1024 + 2 * EPI_WARPS * EPI_TOK * 4 + EPI_WARPS * 1024 <= 227 * 1024,
+              "shared memory exceeds the opt-in limit");
 static_assert(2 * ACC_COLS <= TMEM_COLS, "accumulators exceed the TMEM allocation");
 static_assert(SMEM + 13 * 1024 <= 227 * 1024, "stage ring exceeds shared memory");
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stage buffers must stay 1024-byte aligned");
+
+// GEMM 2 epilogue: each epilogue warp's copy of the tile's destination rows and route weights (loaded for all
+// tokens at once at the start of a tile instead of two dependent loads per token)
+struct __align__(16) EpiStage {
+    int32_t dst[EPI_WARPS][EPI_TOK];   // indexed by the warp's own chunks: (cb / 2) * 16 + i
+    float wt[EPI_WARPS][EPI_TOK];
+    // per warp, one 16-token block of its results transposed to token-major order for 16-byte stores:
+    // GEMM 1 [16 tokens][16 units] bf16, GEMM 2 [16 tokens][32 columns] bf16
+    uint16_t tr[EPI_WARPS][16 * 32];
+};
 
 struct __align__(8) PairCtrl {
     uint64_t full[STAGES];     // leader: both CTAs' bytes of the stage have landed
     uint64_t empty[STAGES];    // each CTA: the MMAs that read the stage completed (multicast commit)
     uint64_t acc_full[2];      // each CTA: the tile's accumulator is complete (multicast commit)
-    uint64_t acc_empty[2];     // leader: the 8 epilogue warps of the pair have read the accumulator
+    uint64_t acc_empty[2];     // leader: the 16 epilogue warps of the pair have read the accumulator
     uint64_t drain;            // leader: every MMA issued has completed
     uint32_t tmem_base;
     volatile int abort;
@@ -130,6 +145,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ ExpertTable tab;
     __shared__ PairCtrl ctrl;
+    __shared__ EpiStage epi;
 
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
@@ -182,8 +198,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             for (int32_t t = cid; t < total && !ctrl.abort; t += ncl) {
                 const PTile tl = decode_tile(tab, p, t);
                 const int n = pair_n(tl.rows);
-                const int nbox = n / (2 * TOK_BOX);                  // 16-row token boxes per CTA
-                const uint32_t bytes = 2u * uint32_t(A_BYTES + nbox * TOK_BOX * PK * 2);   // both CTAs
+                // one 128-row token box per CTA (rows past the tile are never read by the MMA; past the end of
+                // the activations the box is zero-filled): 2 copies per stage and CTA, a constant byte count
+                const uint32_t bytes = 2u * uint32_t(STAGE_BYTES);   // both CTAs
                 const int wblk = 2 * tl.nb + int(rank);              // this CTA's 128-row weight block
                 const int64_t trow = tl.row0 + int64_t(rank) * (n / 2);
                 bool ok = true;
@@ -201,9 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         ptx::tma_load_5d_pair(sa, &tm_w, fb, k0, 0, 0, wblk * (PM / 32), tl.e, pol);
                     else
                         ptx::tma_load_3d_pair(sa, &tm_w, fb, k0, wblk * PM, tl.e, pol);
-                    for (int b = 0; b < nbox; ++b)
-                        ptx::tma_load_2d_pair(sb + b * TOK_BOX * PK * 2, &tm_act, fb, k0,
-                                              int32_t(trow + b * TOK_BOX), pol);
+                    ptx::tma_load_2d_pair(sb, &tm_act, fb, k0, int32_t(trow), pol);
                 }
                 if (!ok) break;
             }
@@ -256,6 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const int sub = (warp - 2) >> 2;              // chunks cb with cb % 2 == sub
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         uint32_t tc = 0;
         for (int32_t t = cid; t < total; t += ncl, ++tc) {
@@ -269,60 +285,107 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int n_tok = tl.rows;
             const int n_chunks = (n_tok + 15) / 16;
             if (p.gemm == 1) {
-                // lanes 0..15: gate of unit u, lanes 16..31: up of unit u, u = 64*wblk + 16*q + (lane & 15)
-                const int64_t unit = int64_t(wblk) * 64 + q * 16 + (lane & 15);
+                // lane l < 16 holds the gate, lane l + 16 the up value of unit u = 64*wblk + 16*q + (l & 15) for
+                // 16 tokens of a chunk.  Lane l computes the even tokens' h of its unit and lane l + 16 the odd
+                // ones: each sends the partner the value it lacks (one exchange per token pair), so every SiLU
+                // runs on a full warp.  The 16 x 16 block of h goes through this warp's shared-memory tile to
+                // token-major order and leaves as one 16-byte store per lane (two lanes per token row).
+                const int64_t unit0 = int64_t(wblk) * 64 + q * 16;
                 uint16_t* h = static_cast<uint16_t*>(p.out);
+                uint16_t* tr = epi.tr[warp - 2];
+                const bool up_lane = lane >= 16;
+                const int u_local = lane & 15;
                 uint32_t va[16], vb[16];
-                ptx::tmem_ld_32x32b_x16(tacc, va);
+                if (sub < n_chunks) ptx::tmem_ld_32x32b_x16(tacc + sub * 16, va);
 #pragma unroll 1
-                for (int cb = 0; cb < n_chunks; ++cb) {
+                for (int cb = sub; cb < n_chunks; cb += 2) {
                     ptx::tmem_ld_wait_regs16(va);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) vb[i] = va[i];
-                    if (cb + 1 < n_chunks) ptx::tmem_ld_32x32b_x16(tacc + (cb + 1) * 16, va);
+                    if (cb + 2 < n_chunks) ptx::tmem_ld_32x32b_x16(tacc + (cb + 2) * 16, va);
+                    __syncwarp();                                  // the previous block has been read back
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float mine = __uint_as_float(vb[i]);
-                        const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-                        const float g = lane < 16 ? mine : other;
-                        const float u = lane < 16 ? other : mine;
-                        const int n = cb * 16 + i;
-                        // lanes 0..15 store even tokens, 16..31 odd tokens of each pair
-                        if (((i & 1) == (lane >> 4)) && n < n_tok)
-                            h[(tl.row0 + n) * p.I + unit] = float_to_bf16_bits(silu_mul(g, u));
+                    for (int j = 0; j < 8; ++j) {
+                        const float even = __uint_as_float(vb[2 * j]), odd = __uint_as_float(vb[2 * j + 1]);
+                        const float recv = __shfl_xor_sync(0xffffffffu, up_lane ? even : odd, 16);
+                        const float g = up_lane ? recv : even;     // gate of token 2j (+1 for up lanes)
+                        const float u = up_lane ? odd : recv;      // up of the same token
+                        tr[(2 * j + (up_lane ? 1 : 0)) * 16 + u_local] = float_to_bf16_bits(silu_mul_fast(g, u));
                     }
+                    __syncwarp();
+                    const int t = lane >> 1, n = cb * 16 + t;      // token of this lane's half row
+                    const uint4 v = *reinterpret_cast<const uint4*>(tr + t * 16 + (lane & 1) * 8);
+                    if (n < n_tok)
+                        *reinterpret_cast<uint4*>(h + (tl.row0 + n) * p.I + unit0 + (lane & 1) * 8) = v;
                 }
             } else {
                 const int64_t col = int64_t(wblk) * PM + q * 32 + lane;   // output hidden index
+                // destination row (-1: skip) and weight of every token of the tile, 8 per lane, loads in flight
+                // together
+                int32_t* dst_s = epi.dst[warp - 2];
+                float* wt_s = epi.wt[warp - 2];
+                __syncwarp();                                  // this warp's reads of the previous tile are done
+                int32_t dr[EPI_TOK / 32];
+#pragma unroll
+                for (int j = 0; j < EPI_TOK / 32; ++j) {
+                    // entry j*32 + lane: token (cb/2)*16 + i of chunk cb = 2*((j*32+lane)/16) + sub
+                    const int e = j * 32 + lane;
+                    const int n = (2 * (e >> 4) + sub) * 16 + (e & 15);
+                    int32_t d = -1;
+                    if (n < n_tok) {
+                        const int64_t row = tl.row0 + n;
+                        if (p.layout == MOE_LAYOUT_CONTIGUOUS) {
+                            const int32_t route = p.row_route[row];
+                            d = (route >= 0 && route < p.out_rows) ? route : -1;
+                        } else {
+                            d = int32_t(row);
+                        }
+                    }
+                    dr[j] = d;
+                }
+#pragma unroll
+                for (int j = 0; j < EPI_TOK / 32; ++j) {
+                    dst_s[j * 32 + lane] = dr[j];
+                    wt_s[j * 32 + lane] = (p.route_w && dr[j] >= 0) ? p.route_w[dr[j]] : 1.f;
+                }
+                __syncwarp();
+                uint16_t* tr = epi.tr[warp - 2];
+                const int64_t col0 = int64_t(wblk) * PM + q * 32;   // this warp's 32 output columns
                 uint32_t va[16], vb[16];
-                ptx::tmem_ld_32x32b_x16(tacc, va);
+                if (sub < n_chunks) ptx::tmem_ld_32x32b_x16(tacc + sub * 16, va);
 #pragma unroll 1
-                for (int cb = 0; cb < n_chunks; ++cb) {
+                for (int cb = sub; cb < n_chunks; cb += 2) {
                     ptx::tmem_ld_wait_regs16(va);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) vb[i] = va[i];
-                    if (cb + 1 < n_chunks) ptx::tmem_ld_32x32b_x16(tacc + (cb + 1) * 16, va);
+                    if (cb + 2 < n_chunks) ptx::tmem_ld_32x32b_x16(tacc + (cb + 2) * 16, va);
+                    const int base = (cb >> 1) * 16;               // this chunk's entries in dst_s / wt_s
+                    if (p.out_dtype == MOE_BF16) {
+                        // the 16 tokens x 32 columns block goes token-major through this warp's tile and leaves
+                        // as two 16-byte stores per lane (two lanes per token row of 64 bytes)
+                        __syncwarp();                              // the previous block has been read back
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int n = cb * 16 + i;
-                        if (n >= n_tok) break;
-                        const int64_t row = tl.row0 + n;
-                        int64_t dst_row;
-                        float wt = 1.f;
-                        if (p.layout == MOE_LAYOUT_CONTIGUOUS) {
-                            const int32_t route = p.row_route[row];
-                            if (route < 0 || route >= p.out_rows) continue;
-                            dst_row = route;
-                            if (p.route_w) wt = p.route_w[route];
-                        } else {
-                            dst_row = row;
-                            if (p.route_w) wt = p.route_w[row];
+                        for (int i = 0; i < 16; ++i)
+                            tr[i * 32 + lane] = float_to_bf16_bits(wt_s[base + i] * __uint_as_float(vb[i]));
+                        __syncwarp();
+                        // lanes 2t and 2t+1 write token t's 64 bytes as two whole 32-byte sectors: store k holds
+                        // columns 16k..16k+15, 8 per lane
+                        const int t = lane >> 1, h8 = (lane & 1) * 8;
+                        const int32_t d = dst_s[base + t];         // -1 for skipped routes and past the tokens
+                        const uint4 v0 = *reinterpret_cast<const uint4*>(tr + t * 32 + h8);
+                        const uint4 v1 = *reinterpret_cast<const uint4*>(tr + t * 32 + 16 + h8);
+                        if (d >= 0) {
+                            uint16_t* row = static_cast<uint16_t*>(p.out) + int64_t(d) * p.K + col0;
+                            *reinterpret_cast<uint4*>(row + h8) = v0;
+                            *reinterpret_cast<uint4*>(row + 16 + h8) = v1;
                         }
-                        const float val = wt * __uint_as_float(vb[i]);
-                        if (p.out_dtype == MOE_BF16)
-                            static_cast<uint16_t*>(p.out)[dst_row * p.K + col] = float_to_bf16_bits(val);
-                        else
-                            static_cast<float*>(p.out)[dst_row * p.K + col] = val;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int32_t d = dst_s[base + i];
+                            if (d < 0) continue;
+                            static_cast<float*>(p.out)[int64_t(d) * p.K + col] = wt_s[base + i] * __uint_as_float(vb[i]);
+                        }
                     }
                 }
             }
@@ -402,10 +465,13 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t s) {
     if (g.rows_cap >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "CTA-pair tiles: too many rows");
     if (g.rows_cap == 0) return MOE_OK;
 
-    // the swap-AB maps: 16-row token boxes, 128-row weight boxes (gate/up view for GEMM 1 on [gate; up] W1)
+    // token rows in 128-row boxes (the normal tiles' activation map) and weights in 128-row boxes (the swap-AB
+    // tiles' weight map: the gate/up view for GEMM 1 on [gate; up] W1)
     const int w_mode = (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0;
-    MapSet maps;
-    int rc = cached_maps(g, TC_SWAP, false, kdim, wrows, w_mode, &maps);
+    MapSet m_tok, m_w;
+    int rc = cached_maps(g, TC_NORMAL, false, kdim, wrows, w_mode, &m_tok);
+    if (rc) return rc;
+    rc = cached_maps(g, TC_SWAP, false, kdim, wrows, w_mode, &m_w);
     if (rc) return rc;
 
     PairParams p{};
@@ -438,7 +504,7 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t s) {
     const int64_t tiles = segs * p.nt;
     if (tiles == 0) return MOE_OK;
     const int clusters = int(std::min<int64_t>(tiles, pair_clusters()));
-    gemm_pair_kernel<<<2 * clusters, THREADS, SMEM, s>>>(maps.act, maps.w, p);
+    gemm_pair_kernel<<<2 * clusters, THREADS, SMEM, s>>>(m_tok.act, m_w.w, p);
     return check_launch("gemm_pair_kernel");
 }
 

@@ -98,6 +98,8 @@ class Instance:
             self.W1r, self.W2r, self.w1_layout = self.W1, self.W2, w.w1_layout
             self.routes = int(self.counts.sum().item())
             self.used_experts = int((self.counts > 0).sum().item())
+            if tiled and impl in (None, m.MOE_IMPL_AUTO, m.MOE_IMPL_TCGEN05_PAIR) and self._pair_plan():
+                self._tile_weights()
             return
         self.x = wl.activations(w, seed, dev)
         if w.routing == "affine":
@@ -127,16 +129,28 @@ class Instance:
         self.W1r, self.W2r, self.w1_layout = self.W1, self.W2, w.w1_layout
         self.forward()
         torch.cuda.synchronize()
-        if tiled and w.weight == "bf16" and w.layout == "contiguous" and self.fused():
-            self.W1r = m.moe_tile_weights(self.W1, 1, w.w1_layout)
-            self.W2r = m.moe_tile_weights(self.W2, 2)
-            self.w1_layout = m.MOE_W_TILED
+        if tiled and w.weight == "bf16" and (
+                (w.layout == "contiguous" and self.fused())
+                or (impl in (None, m.MOE_IMPL_AUTO, m.MOE_IMPL_TCGEN05_PAIR) and self._pair_plan())):
+            self._tile_weights()
             self.forward()
             torch.cuda.synchronize()
         ids = self.layer.ids if self.logits is not None else self.ids
         kept = self.layer.route_row >= 0      # batched: routes beyond the capacity are dropped
         self.routes = int(kept.sum().item())
         self.used_experts = int(torch.unique(ids[kept]).numel())
+
+    def _pair_plan(self):
+        """True where the layer's GEMMs run on CTA-pair tiles (bf16, many rows per expert)."""
+        return "CTA-pair" in gemm1_kernel(self)
+
+    def _tile_weights(self):
+        """Weights re-laid out once into the tile-contiguous layout the kernels stream (moe_tile_weights): weight
+        preparation, outside every timed region."""
+        m = self.m
+        self.W1r = m.moe_tile_weights(self.W1, 1, self.w.w1_layout)
+        self.W2r = m.moe_tile_weights(self.W2, 2)
+        self.w1_layout = m.MOE_W_TILED
 
     def _mxfp8(self, w, which, seed, dev):
         import torch

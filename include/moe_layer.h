@@ -96,8 +96,9 @@ extern "C" {
 #define MOE_W1_INTERLEAVE16 1         /* rows in groups of 32: 16 gate rows then the 16 matching up rows
                                          ("Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2,
                                          _interleave_gate_up_16 "After") */
-#define MOE_W_TILED 2                 /* moe_experts_fused only: W1 AND W2 in the tile-contiguous layout
-                                         written by moe_tile_weights */
+#define MOE_W_TILED 2                 /* tile-contiguous layout written by moe_tile_weights: W1 and W2 of
+                                         moe_experts_fused, W1 of moe_gemm1_swiglu / W2 of moe_gemm2 on
+                                         CTA-pair tiles (bf16) */
 
 /* ---- GEMM implementations ---- */
 #define MOE_IMPL_AUTO 0               /* swap-AB tiles when routes/expert are few, else CTA-pair tiles
@@ -252,7 +253,10 @@ MOE_API int moe_permute_align_static(const int32_t* topk_ids, int64_t T, int top
  *                 same rows as `a`, K/32 per row, 4-byte aligned; NULL otherwise.
  *                 E4M3 activations need E4M3 weights and run on block-scaled tcgen05
  *                 swap-AB tiles (K % 128 == 0, 2I % 128 == 0) or MOE_IMPL_SIMT.
- *   w1            (E, 2I, K) of w_dtype (F32, BF16 or E4M3); rows per w1_layout
+ *   w1            (E, 2I, K) of w_dtype (F32, BF16 or E4M3); rows per w1_layout: MOE_W1_GATE_UP,
+ *                 MOE_W1_INTERLEAVE16, or MOE_W_TILED (bf16 weights from moe_tile_weights, which = 1;
+ *                 CTA-pair tiles only: MOE_IMPL_AUTO or MOE_IMPL_TCGEN05_PAIR, else
+ *                 MOE_ERR_UNSUPPORTED)
  *   w1_scale      (E, 2I, K/32) E8M0 bytes when w_dtype == MOE_E4M3, else NULL
  *   h             same row indexing as `a`, (rows, I) of h_dtype (F32, BF16, or E4M3 codes);
  *                 only valid rows are written.
@@ -287,6 +291,8 @@ MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale,
  *                 As for GEMM 1, E4M3 h needs E4M3 weights (I % 128 == 0, K % 128 == 0
  *                 on tcgen05 tiles).
  *   w2            (E, K, I) of w_dtype; w2_scale (E, K, I/32) E8M0 for E4M3, else NULL
+ *   w2_layout     MOE_W1_GATE_UP (row-major, as above) or MOE_W_TILED (bf16 W2 from
+ *                 moe_tile_weights, which = 2; CTA-pair tiles only, as for moe_gemm1_swiglu)
  *   contiguous:   row s goes to y[row_route[s]] (rows with row_route -1 are skipped);
  *                 y is (y_rows, K) with y_rows = T*top_k; route_weights, if not NULL,
  *                 is (T*top_k) fp32 indexed by route.
@@ -297,7 +303,7 @@ MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale,
 MOE_API int moe_gemm2(const void* h, int h_dtype, const uint8_t* h_scale, int layout,
               const int32_t* expert_counts, const int32_t* expert_offsets,
               int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
-              const void* w2, const uint8_t* w2_scale, int w_dtype,
+              const void* w2, const uint8_t* w2_scale, int w_dtype, int w2_layout,
               const int32_t* row_route, const float* route_weights,
               int impl, void* y, int y_dtype, int64_t y_rows, int32_t* err_word, void* stream);
 

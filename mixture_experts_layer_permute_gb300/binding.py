@@ -76,8 +76,8 @@ def load(path: Optional[str] = None):
                                                P, P]),
             "moe_gemm1_swiglu": (I32, [P, I32, P, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, I32, I32, P,
                                        I32, P, P, P]),
-            "moe_gemm2": (I32, [P, I32, P, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, P, P, I32, P, I32, I64,
-                                P, P]),
+            "moe_gemm2": (I32, [P, I32, P, I32, P, P, I32, I64, I32, I64, I64, P, P, I32, I32, P, P, I32, P, I32,
+                                I64, P, P]),
             "moe_unpermute_topk_reduce": (I32, [P, I32, P, P, I64, I32, I32, I64, P, I32, P]),
             "moe_batched_weight_reduce": (I32, [P, I32, P, P, I32, I32, I64, P, I32, P]),
             "moe_batched_topk_reduce": (I32, [P, I32, I64, P, P, I64, I32, I64, P, I32, P, P]),
@@ -294,8 +294,9 @@ def moe_gemm1_swiglu(a, expert_counts, expert_offsets, w1, I, layout=MOE_LAYOUT_
 
 def moe_gemm2(h, expert_counts, expert_offsets, w2, y_rows, layout=MOE_LAYOUT_CONTIGUOUS, max_tokens=0,
               w2_scale=None, row_route=None, route_weights=None, impl=MOE_IMPL_AUTO, y=None, y_dtype=None,
-              err_word=None, stream=None, h_scale=None):
-    """h_scale: E8M0 scales when `h` holds E4M3 codes (uint8) of an MXFP8 intermediate."""
+              err_word=None, stream=None, h_scale=None, w2_layout=MOE_W1_GATE_UP):
+    """h_scale: E8M0 scales when `h` holds E4M3 codes (uint8) of an MXFP8 intermediate.
+    w2_layout: MOE_W1_GATE_UP (row-major) or MOE_W_TILED (W2 from moe_tile_weights)."""
     E, K, I = w2.shape
     rows_cap = h.shape[0] if layout == MOE_LAYOUT_CONTIGUOUS else E * max_tokens
     h_dt = dtype_code(h, e4m3=h_scale is not None)
@@ -307,8 +308,8 @@ def moe_gemm2(h, expert_counts, expert_offsets, w2, y_rows, layout=MOE_LAYOUT_CO
     _check(load().moe_gemm2(
         _ptr(h), h_dt, _ptr(h_scale), layout, _ptr(expert_counts), _ptr(expert_offsets), max_tokens, rows_cap, E,
         K, I,
-        _ptr(w2), _ptr(w2_scale), dtype_code(w2, e4m3=w2_scale is not None), _ptr(row_route), _ptr(route_weights),
-        impl, _ptr(y), y_dtype, y_rows, _ptr(err_word), _stream(stream)))
+        _ptr(w2), _ptr(w2_scale), dtype_code(w2, e4m3=w2_scale is not None), w2_layout, _ptr(row_route),
+        _ptr(route_weights), impl, _ptr(y), y_dtype, y_rows, _ptr(err_word), _stream(stream)))
     return y
 
 

@@ -264,6 +264,15 @@ int run_gemm_mx(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
 
 int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
     if ((g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens) == 0) return MOE_OK;
+    if (g.w1_layout == MOE_W_TILED) {
+        // tile-contiguous weights (moe_tile_weights) are read by the CTA-pair tiles only
+        MOE_REQUIRE(impl == MOE_IMPL_AUTO || impl == MOE_IMPL_TCGEN05_PAIR, MOE_ERR_UNSUPPORTED,
+                    std::string(name) + ": tile-contiguous weights run on CTA-pair tiles (MOE_IMPL_TCGEN05_PAIR) only");
+        MOE_REQUIRE(g.a_dtype == MOE_BF16 && g.w_dtype == MOE_BF16, MOE_ERR_UNSUPPORTED,
+                    std::string(name) + ": tile-contiguous weights need bf16 activations and weights");
+        MOE_REQUIRE(device_cc() >= 100, MOE_ERR_UNSUPPORTED, std::string(name) + ": tcgen05 needs an sm_100+ device");
+        return launch_gemm_pair(g, s);
+    }
     if (g.a_dtype == MOE_E4M3) return run_gemm_mx(g, impl, s, name);
     const bool tc_ok = g.a_dtype == MOE_BF16 && (g.w_dtype == MOE_BF16 || g.w_dtype == MOE_E4M3) &&
                        g.out_dtype == MOE_BF16 && device_cc() >= 100;
@@ -337,8 +346,8 @@ int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale, int lay
     g.err_word = err_word;
     int rc = validate_gemm(g, "moe_gemm1_swiglu");
     if (rc) return rc;
-    MOE_REQUIRE(w1_layout == MOE_W1_GATE_UP || w1_layout == MOE_W1_INTERLEAVE16, MOE_ERR_INVALID_ARG,
-                "moe_gemm1_swiglu: unknown w1_layout");
+    MOE_REQUIRE(w1_layout == MOE_W1_GATE_UP || w1_layout == MOE_W1_INTERLEAVE16 || w1_layout == MOE_W_TILED,
+                MOE_ERR_INVALID_ARG, "moe_gemm1_swiglu: unknown w1_layout");
     MOE_REQUIRE(w1_layout != MOE_W1_INTERLEAVE16 || I % 16 == 0, MOE_ERR_ALIGNMENT,
                 "moe_gemm1_swiglu: interleave-16 needs I % 16 == 0");
     return run_gemm(g, impl, as_stream(stream), "moe_gemm1_swiglu");
@@ -346,7 +355,7 @@ int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale, int lay
 
 int moe_gemm2(const void* hh, int h_dtype, const uint8_t* h_scale, int layout, const int32_t* expert_counts,
               const int32_t* expert_offsets, int max_tokens, int64_t rows_cap, int E, int64_t K, int64_t I,
-              const void* w2, const uint8_t* w2_scale, int w_dtype, const int32_t* row_route,
+              const void* w2, const uint8_t* w2_scale, int w_dtype, int w2_layout, const int32_t* row_route,
               const float* route_weights, int impl, void* y, int y_dtype, int64_t y_rows, int32_t* err_word,
               void* stream) {
     g_last_error.clear();
@@ -366,6 +375,7 @@ int moe_gemm2(const void* hh, int h_dtype, const uint8_t* h_scale, int layout, c
     g.w = w2;
     g.w_scale = w2_scale;
     g.w_dtype = w_dtype;
+    g.w1_layout = w2_layout;   // MOE_W1_GATE_UP (row-major) or MOE_W_TILED
     g.row_route = row_route;
     g.route_w = route_weights;
     g.out = y;
@@ -376,6 +386,8 @@ int moe_gemm2(const void* hh, int h_dtype, const uint8_t* h_scale, int layout, c
     if (rc) return rc;
     MOE_REQUIRE(layout == MOE_LAYOUT_BATCHED || row_route, MOE_ERR_INVALID_ARG,
                 "moe_gemm2: contiguous layout needs row_route");
+    MOE_REQUIRE(w2_layout == MOE_W1_GATE_UP || w2_layout == MOE_W_TILED, MOE_ERR_INVALID_ARG,
+                "moe_gemm2: w2_layout must be MOE_W1_GATE_UP (row-major) or MOE_W_TILED");
     MOE_REQUIRE(y_rows >= 0, MOE_ERR_INVALID_ARG, "moe_gemm2: y_rows < 0");
     return run_gemm(g, impl, as_stream(stream), "moe_gemm2");
 }

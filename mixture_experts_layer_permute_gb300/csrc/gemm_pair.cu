@@ -16,7 +16,8 @@
 //
 // Per CTA, 192 threads:
 //   warp 0      TMA producer: this CTA's 128 weight rows (128-byte swizzled, through the gate/up view for
-//               GEMM 1 as in the single-SM swap-AB tiles) and its 128-row box of the tile's tokens (of which
+//               GEMM 1 as in the single-SM swap-AB tiles, or one contiguous 16 KB block of weights re-laid out
+//               by moe_tile_weights) and its 128-row box of the tile's tokens (of which
 //               the MMA reads N/2) of each k-block into a 6-stage ring; the bytes of BOTH CTAs are counted on
 //               the leader CTA's "full" barrier.
 //   warp 1      TMEM: allocates all 512 columns for the pair (one warp of each CTA, together).  In the
@@ -94,7 +95,9 @@ struct PairParams {
     int64_t rows_cap;
     int nkb;             // k-blocks per tile
     int nt;              // 256-row weight tiles per expert
-    int w_mode;          // weights map: 0 = 3-D (k, rows, E), 1 = 5-D gate/up interleaving view
+    int w_mode;          // weights map: 0 = 3-D (k, rows, E), 1 = 5-D gate/up interleaving view,
+                         // 2 = 4-D tile-contiguous (64, 128, k-blocks, E x 128-row blocks), from moe_tile_weights
+    int wblocks;         // 128-row weight blocks per expert
     int64_t I, K;
     const int32_t* counts;
     const int32_t* offsets;
@@ -216,6 +219,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     const int k0 = kb * PK;
                     if (p.w_mode == 1)
                         ptx::tma_load_5d_pair(sa, &tm_w, fb, k0, 0, 0, wblk * (PM / 32), tl.e, pol);
+                    else if (p.w_mode == 2)   // one contiguous 16 KB block per k-block
+                        ptx::tma_load_4d_pair(sa, &tm_w, fb, 0, 0, kb, tl.e * p.wblocks + wblk, pol);
                     else
                         ptx::tma_load_3d_pair(sa, &tm_w, fb, k0, wblk * PM, tl.e, pol);
                     ptx::tma_load_2d_pair(sb, &tm_act, fb, k0, int32_t(trow), pol);
@@ -461,13 +466,12 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t s) {
         return fail(MOE_ERR_UNSUPPORTED, "CTA-pair tiles: weight rows per expert must be a multiple of 256");
     if (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP && g.I % 16 != 0)
         return fail(MOE_ERR_UNSUPPORTED, "CTA-pair tiles: I must be a multiple of 16");
-    if (g.w1_layout == MOE_W_TILED) return fail(MOE_ERR_UNSUPPORTED, "CTA-pair tiles: row-major weights only");
     if (g.rows_cap >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "CTA-pair tiles: too many rows");
     if (g.rows_cap == 0) return MOE_OK;
 
     // token rows in 128-row boxes (the normal tiles' activation map) and weights in 128-row boxes (the swap-AB
     // tiles' weight map: the gate/up view for GEMM 1 on [gate; up] W1)
-    const int w_mode = (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0;
+    const int w_mode = g.w1_layout == MOE_W_TILED ? 2 : ((g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0);
     MapSet m_tok, m_w;
     int rc = cached_maps(g, TC_NORMAL, false, kdim, wrows, w_mode, &m_tok);
     if (rc) return rc;
@@ -483,6 +487,7 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t s) {
     p.nkb = int(kdim / PK);
     p.nt = int(wrows / (2 * PM));
     p.w_mode = w_mode;
+    p.wblocks = int(wrows / PM);
     p.I = g.I;
     p.K = g.K;
     p.counts = g.counts;

@@ -328,6 +328,15 @@ MOE_DEVICE void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar, 
         : "memory");
 }
 
+MOE_DEVICE void tma_load_4d_pair(void* dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1, int32_t c2,
+                                 int32_t c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 MOE_DEVICE void tma_load_5d_pair(void* dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1, int32_t c2,
                                  int32_t c3, int32_t c4, uint64_t policy) {
     asm volatile(

@@ -131,6 +131,8 @@ class MoELayer:
         adt = B.dtype_code(x)
         wdt = B.dtype_code(w1, e4m3=w1_scale is not None)
         I, K, E, T, k = self.I, self.K, self.E, self.T, self.top_k
+        # MOE_W_TILED: W1 and W2 both from moe_tile_weights (the fused decode launch or CTA-pair tiles)
+        w2_layout = B.MOE_W_TILED if w1_layout == B.MOE_W_TILED else B.MOE_W1_GATE_UP
         calls = []
         if self.layout == B.MOE_LAYOUT_BATCHED and T > 0:
             return self._token_batched_plan(x, w1, w2, logits, topk_ids, topk_weights, w1_scale, w2_scale,
@@ -143,7 +145,8 @@ class MoELayer:
                                                  self.err.data_ptr(), stream), "gemm1"))
             rw = row_weights if self.weight_in_gemm2 else None
             calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, None, self.layout, counts.data_ptr(), None, mt,
-                                          self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, None, _p(rw),
+                                          self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, w2_layout,
+                                          None, _p(rw),
                                           self.impl, self.out.data_ptr(), adt, self.rows_cap, self.err.data_ptr(),
                                           stream), "gemm2"))
             if not self.weight_in_gemm2:
@@ -183,8 +186,6 @@ class MoELayer:
             calls.append((lib.moe_unpermute_topk_reduce, (self.y.data_ptr(), adt, ids.data_ptr(), None, T, k, E,
                                                           K, self.out.data_ptr(), adt, stream), "reduce"))
             return calls
-        if w1_layout == B.MOE_W_TILED:
-            raise ValueError("MOE_W_TILED weights run on the fused decode plan only (bf16, swap-AB regime)")
         if self.act_quant:   # GEMM 1's epilogue writes h as MXFP8 (codes + scales)
             hout, hdt, hs = self.h_codes.data_ptr(), B.MOE_E4M3, self.h_scales.data_ptr()
         else:
@@ -197,7 +198,7 @@ class MoELayer:
         rw = weights if self.weight_in_gemm2 else None
         calls.append((lib.moe_gemm2, (a2, a2dt, a2s, self.layout, self.counts.data_ptr(),
                                       self.offsets.data_ptr(), 0, self.rows_cap, E, K, I, w2.data_ptr(),
-                                      _p(w2_scale), wdt, self.row_route.data_ptr(), _p(rw), self.impl,
+                                      _p(w2_scale), wdt, w2_layout, self.row_route.data_ptr(), _p(rw), self.impl,
                                       self.y.data_ptr(), adt, T * k, self.err.data_ptr(), stream), "gemm2"))
         calls.append((lib.moe_unpermute_topk_reduce, (self.y.data_ptr(), adt, ids.data_ptr(),
                                                       None if self.weight_in_gemm2 else weights.data_ptr(), T, k,
@@ -224,8 +225,9 @@ class MoELayer:
                                              mt, self.rows_cap, E, K, I, w1.data_ptr(), _p(w1_scale), wdt,
                                              w1_layout, self.impl, self.h.data_ptr(), adt, None,
                                              self.err.data_ptr(), stream), "gemm1"))
+        w2_layout = B.MOE_W_TILED if w1_layout == B.MOE_W_TILED else B.MOE_W1_GATE_UP
         calls.append((lib.moe_gemm2, (self.h.data_ptr(), adt, None, self.layout, self.counts.data_ptr(), None, mt,
-                                      self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, None, None,
+                                      self.rows_cap, E, K, I, w2.data_ptr(), _p(w2_scale), wdt, w2_layout, None, None,
                                       self.impl, self.y.data_ptr(), adt, self.rows_cap, self.err.data_ptr(),
                                       stream), "gemm2"))
         calls.append((lib.moe_batched_topk_reduce, (self.y.data_ptr(), adt, self.rows_cap,
@@ -247,7 +249,8 @@ class MoELayer:
         Batched layout with T = 0: x (E, max_tokens, K), `expert_num_tokens` (E,), optional `row_weights`
         (E, max_tokens).
         ``w1_layout``: MOE_W1_GATE_UP or MOE_W1_INTERLEAVE16 for row-major W1, or MOE_W_TILED when W1 and W2 come
-        from moe_tile_weights (the fused decode plan only; other plans raise ValueError).
+        from moe_tile_weights (bf16: the fused decode launch, or CTA-pair tiles where there are many rows per
+        expert; the library refuses other plans with MOE_ERR_UNSUPPORTED).
         ``gemm1_events`` = (start, end) CUDA events recorded around the gate/up GEMM.
         """
         s = stream if stream is not None else torch.cuda.current_stream()

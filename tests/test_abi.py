@@ -146,11 +146,11 @@ def test_gemm_validation(lib):
                               fake, 1, None, None, None)
     assert rc == 3
     # contiguous gemm2 needs row_route
-    rc = lib.moe_gemm2(fake, 1, None, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, None, None, 0, fake, 1, 10, None,
+    rc = lib.moe_gemm2(fake, 1, None, 0, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, 0, None, None, 0, fake, 1, 10, None,
                        None)
     assert rc == 1 and "row_route" in lib_error()
     # unknown layout
-    rc = lib.moe_gemm2(fake, 1, None, 7, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, fake, None, 0, fake, 1, 10, None,
+    rc = lib.moe_gemm2(fake, 1, None, 7, fake, fake, 0, 64, 4, 128, 64, fake, None, 1, 0, fake, None, 0, fake, 1, 10, None,
                        None)
     assert rc == 1
     # E4M3 activations: scales required, E4M3 weights required, normal tiles refused
@@ -163,7 +163,7 @@ def test_gemm_validation(lib):
     rc = lib.moe_gemm1_swiglu(fake, 2, ctypes.c_void_p(0x1001), 0, fake, fake, 0, 64, 4, 128, 64, fake, fake, 2, 0,
                               0, fake, 1, None, None, None)
     assert rc == 3
-    rc = lib.moe_gemm2(fake, 2, fake, 0, fake, fake, 0, 64, 4, 128, 128, fake, fake, 2, fake, None, 1, fake, 1, 10,
+    rc = lib.moe_gemm2(fake, 2, fake, 0, fake, fake, 0, 64, 4, 128, 128, fake, fake, 2, 0, fake, None, 1, fake, 1, 10,
                        None, None)
     assert rc == 2 and "swap-AB" in lib_error()
     # E4M3 h needs its scale output
@@ -224,3 +224,18 @@ def test_permute_static_validation(lib):
     rc = call(T=70000, k=8, E=128, rows_cap=70000 * 8)
     assert rc == 4
     assert "2097152" in lib_error() and "moe_permute_align" in lib_error()
+
+
+def test_tiled_weight_layout_validation(lib):
+    fake = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
+    # moe_gemm2: an unknown W2 layout
+    rc = lib.moe_gemm2(fake, 1, None, 0, fake, fake, 0, 64, 4, 256, 128, fake, None, 1, 7, fake, None, 0, fake, 1,
+                       10, None, None)
+    assert rc == 1 and "w2_layout" in lib_error()
+    # tile-contiguous weights on an implementation other than the CTA-pair tiles
+    rc = lib.moe_gemm2(fake, 1, None, 0, fake, fake, 0, 64, 4, 256, 128, fake, None, 1, 2, fake, None,
+                       m.MOE_IMPL_TCGEN05_SWAP_AB, fake, 1, 10, None, None)
+    assert rc == 2 and "CTA-pair" in lib_error()
+    rc = lib.moe_gemm1_swiglu(fake, 1, None, 0, fake, fake, 0, 64, 4, 256, 128, fake, None, 1, 2, m.MOE_IMPL_SIMT,
+                              fake, 1, None, None, None)
+    assert rc == 2 and "CTA-pair" in lib_error()

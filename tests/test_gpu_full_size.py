@@ -94,6 +94,24 @@ def test_decode_sweep_every_token(moe):
         _release()
 
 
+@pytest.mark.parametrize("seed", [1, 2])
+def test_decode_t64_other_seeds(moe, seed):
+    """The T=64 decode pass (the largest of the sweep) drawn from seeds 1 and 2: every token."""
+    w = wl.decode(64)
+    inst = bench.Instance(w, seed, DEV)
+    assert inst.fused() and inst.w1_layout == moe.MOE_W_TILED
+    out = inst.forward()
+    torch.cuda.synchronize()
+    assert inst.layer.device_errors() == 0
+    ids, weights = _routing_exact(inst, w)
+    x, w1h, w2h = wl.to_numpy(inst.x), wl.to_numpy(inst.W1), wl.to_numpy(inst.W2)
+    refs = oracle_map(lambda t: oracle.moe_layer(x[t:t + 1], ids[t:t + 1], weights[t:t + 1], w1h, w2h)[0],
+                      range(w.T))
+    _check_tokens(to_f64(out), refs, range(w.T), TOL_BF16, f"decode T=64 seed {seed}")
+    del inst, out
+    _release()
+
+
 def _prefill_tokens(ids, E, block_m, k, at_least=64):
     routes = ids.reshape(-1)
     tokens = set()
@@ -111,10 +129,11 @@ def _prefill_tokens(ids, E, block_m, k, at_least=64):
     return sorted(tokens)
 
 
-def test_prefill_tail_tiles(moe):
+@pytest.mark.parametrize("seed", [0, 1])
+def test_prefill_tail_tiles(moe, seed):
     """Skewed prefill: tokens covering every touched expert's ragged last 128-row tile and its coldest experts."""
     w = wl.prefill()
-    inst = bench.Instance(w, 0, DEV)
+    inst = bench.Instance(w, seed, DEV)
     out = inst.forward()
     torch.cuda.synchronize()
     assert inst.layer.device_errors() == 0

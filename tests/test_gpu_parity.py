@@ -500,6 +500,52 @@ def test_pair_tiles_ragged_segments(moe, w1_layout):
     assert_close(to_f64(y.cpu()), yref, TOL_BF16, "pair gemm2")
 
 
+@pytest.mark.parametrize("w1_layout", [0, 1])
+@pytest.mark.parametrize("layout", ["contiguous", "batched"])
+def test_pair_tiles_tiled_weights(moe, w1_layout, layout):
+    """CTA-pair tiles on tile-contiguous W1 and W2 (moe_tile_weights, MOE_W_TILED) give h and y bit for bit equal
+    to the row-major weights (same tiles, same accumulation order)."""
+    E, K, I = 4, 512, 384
+    pair = moe.MOE_IMPL_TCGEN05_PAIR
+    w = wl.scaled(wl.decode(64), T=300, K=K, I=I, E=E, top_k=2, w_std=0.05)
+    W1 = wl.expert_weights(w, "W1", 41).to(DEV)
+    W2 = wl.expert_weights(w, "W2", 41).to(DEV)
+    W1t, W2t = moe.moe_tile_weights(W1, 1, w1_layout), moe.moe_tile_weights(W2, 2)
+    if layout == "contiguous":
+        _, x, ids, weights = _routed(300, 2, E, K, seed=41)
+        res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 128, x=x.to(DEV))
+        a, counts, offs, kw = res["x_out"], res["counts"], res["offsets"], {}
+        g2 = dict(row_route=res["row_route"], route_weights=torch.from_numpy(weights).to(DEV).reshape(-1))
+        y_rows = 600
+    else:
+        maxT = 200
+        counts = torch.tensor([200, 131, 77, 0], dtype=torch.int32, device=DEV)
+        offs = torch.arange(E + 1, dtype=torch.int32, device=DEV) * maxT
+        a = wl._normal((E * maxT, K), 1.0, 41, "x", 0, DEV, torch.bfloat16)
+        kw = dict(layout=moe.MOE_LAYOUT_BATCHED, max_tokens=maxT)
+        g2 = dict(route_weights=torch.rand(E * maxT, generator=torch.Generator().manual_seed(41)).to(DEV))
+        y_rows = E * maxT
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = []
+    for W1x, W2x, l1, l2 in ((W1, W2, w1_layout, moe.MOE_W1_GATE_UP), (W1t, W2t, moe.MOE_W_TILED, moe.MOE_W_TILED)):
+        h = moe.moe_gemm1_swiglu(a, counts, offs, W1x, I, w1_layout=l1, impl=pair, err_word=err, **kw)
+        y = moe.moe_gemm2(h, counts, offs, W2x, y_rows, w2_layout=l2, impl=pair, err_word=err, **kw, **g2)
+        outs.append((h, y))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    (h1, y1), (h2, y2) = outs
+    if layout == "contiguous":
+        rr = res["route_row"].view(-1).long()
+        assert torch.equal(h1[rr].view(torch.int16), h2[rr].view(torch.int16))
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    else:
+        for e in range(E):
+            c = int(counts[e])
+            rows = slice(e * maxT, e * maxT + c)
+            assert torch.equal(h1.reshape(-1, I)[rows].view(torch.int16), h2.reshape(-1, I)[rows].view(torch.int16))
+            assert torch.equal(y1.reshape(-1, K)[rows].view(torch.int16), y2.reshape(-1, K)[rows].view(torch.int16))
+
+
 def test_pair_tiles_refuse_other_shapes(moe):
     """Shapes outside the CTA-pair tiles (weight rows per expert not a multiple of 256) are refused with nothing
     launched; MOE_IMPL_AUTO never picks them there."""
@@ -706,10 +752,11 @@ def test_layer_tiny_fp32(moe):
 
 @pytest.mark.parametrize("impl", IMPLS_BF16 + ["auto"])
 @pytest.mark.parametrize("bm", [1, 128])
-def test_layer_bf16_small(moe, impl, bm):
+@pytest.mark.parametrize("seed", [3, 1, 2])
+def test_layer_bf16_small(moe, impl, bm, seed):
     w = wl.scaled(wl.decode(64), T=200, K=512, I=256, E=16, top_k=4)
-    x, logits = wl.activations(w, 3), wl.router_logits(w, 3)
-    W1, W2 = wl.expert_weights(w, "W1", 3), wl.expert_weights(w, "W2", 3)
+    x, logits = wl.activations(w, seed), wl.router_logits(w, seed)
+    W1, W2 = wl.expert_weights(w, "W1", seed), wl.expert_weights(w, "W2", seed)
     layer = moe.MoELayer(w.T, w.K, w.I, w.E, w.top_k, block_m=bm, impl=_impl(moe, impl), device=DEV)
     out = layer.forward(x.to(DEV), W1.to(DEV), W2.to(DEV), logits=logits.to(DEV))
     ids, weights = oracle.topk_route(logits.numpy(), w.top_k)
@@ -1007,7 +1054,7 @@ def test_experts_fused_tiled_weights(moe, shape):
 
 def test_layer_decode_tiled_weights_full_size(moe):
     """The decode layer at full size on tile-contiguous weights equals the layer on row-major weights bit for
-    bit; a plan that is not the fused decode plan refuses tiled weights."""
+    bit; so does a prefill-sized layer (CTA-pair tiles), and single-SM normal tiles refuse tiled weights."""
     w = wl.decode(64)
     x, logits = wl.activations(w, 1, DEV), wl.router_logits(w, 1, DEV)
     W1, W2 = wl.expert_weights(w, "W1", 1, DEV), wl.expert_weights(w, "W2", 1, DEV)
@@ -1018,10 +1065,17 @@ def test_layer_decode_tiled_weights_full_size(moe):
     torch.cuda.synchronize()
     assert layer.device_errors() == 0
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
-    big = moe.MoELayer(4096, w.K, w.I, w.E, w.top_k, block_m=128, device=DEV)     # normal tiles
-    with pytest.raises(ValueError):
-        big.forward(wl._normal((4096, w.K), 1.0, 3, "x", 0, DEV, torch.bfloat16), W1t, W2t,
-                    logits=wl._normal((4096, w.E), 1.0, 3, "l", 0, DEV, torch.float32), w1_layout=moe.MOE_W_TILED)
+    xb = wl._normal((4096, w.K), 1.0, 3, "x", 0, DEV, torch.bfloat16)
+    lb = wl._normal((4096, w.E), 1.0, 3, "l", 0, DEV, torch.float32)
+    big = moe.MoELayer(4096, w.K, w.I, w.E, w.top_k, block_m=128, device=DEV)     # CTA-pair tiles
+    big_a = big.forward(xb, W1, W2, logits=lb).clone()
+    big_b = big.forward(xb, W1t, W2t, logits=lb, w1_layout=moe.MOE_W_TILED)
+    torch.cuda.synchronize()
+    assert big.device_errors() == 0
+    assert torch.equal(big_a.view(torch.int16), big_b.view(torch.int16))
+    normal = moe.MoELayer(4096, w.K, w.I, w.E, w.top_k, block_m=128, impl=moe.MOE_IMPL_TCGEN05, device=DEV)
+    with pytest.raises(moe.MoEError):
+        normal.forward(xb, W1t, W2t, logits=lb, w1_layout=moe.MOE_W_TILED)
 
 
 def test_layer_decode_fused_experts_full_size(moe):

@@ -168,7 +168,7 @@ class Instance:
         w1_layout = self.w1_layout
         if self.w.layout == "batched":
             return L.forward(self.xb, self.W1r, self.W2r, expert_num_tokens=self.counts, row_weights=self.rw,
-                             gemm1_events=gemm1_events)
+                             w1_layout=w1_layout, gemm1_events=gemm1_events)
         x = self.x if x is None else x
         if self.logits is not None:
             lg = self.logits if logits is None else logits
@@ -727,7 +727,7 @@ def run_e2e(args, insts, dev):
 
     def kwargs_of(inst, dl):
         if inst.w.layout == "batched":
-            return dict(expert_num_tokens=inst.counts, row_weights=inst.rw)
+            return dict(expert_num_tokens=inst.counts, row_weights=inst.rw, w1_layout=inst.w1_layout)
         if dl is not None:
             return dict(logits=dl, w1_scale=inst.s1, w2_scale=inst.s2, w1_layout=inst.w1_layout)
         return dict(topk_ids=inst.ids, topk_weights=inst.tw, w1_scale=inst.s1, w2_scale=inst.s2,

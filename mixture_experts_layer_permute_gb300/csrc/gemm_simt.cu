@@ -76,8 +76,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     float acc[4][4] = {};
 
-    for (int64_t k0 = 0; k0 < kdim; k0 += BK) {
-        // A: 64 rows x 16 k, 4 elements per thread
+    // This thread's 4 A and 4 B elements of the k-step at k0 (A: 64 rows x 16 k; B: 64 weight rows x 16 k).
+    auto load_step = [&](int64_t k0, float (&ra)[4], float (&rb)[4]) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * 256, r = idx / BK, kk = idx % BK;
@@ -86,9 +86,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
                 if constexpr (ADT == MOE_E4M3) v = load_weight<MOE_E4M3>(g.a, g.a_scale, row0 + r, k0 + kk, kdim);
                 else v = load_as_float<ADT>(g.a, (row0 + r) * kdim + k0 + kk);
             }
-            As[kk][r] = v;
+            ra[q] = v;
         }
-        // B: 64 weight rows x 16 k
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * 256, c = idx / BK, kk = idx % BK;
@@ -104,20 +103,42 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
                 ok = wr < g.K;
             }
             if (ok) v = load_weight<WDT>(g.w, g.w_scale, wbase_row + wr, k0 + kk, kdim);
-            Bs[kk][c] = v;
+            rb[q] = v;
         }
-        __syncthreads();
+    };
+
+    // The k-steps' loads are issued PF steps ahead into registers, so a small layer (few k-steps, nothing in
+    // cache) waits for memory once per PF steps instead of once per step; the sums run in the same order.
+    constexpr int PF = 4;
+    float ra[PF][4], rb[PF][4];
 #pragma unroll
-        for (int kk = 0; kk < BK; ++kk) {
-            float a[4], b[4];
+    for (int f = 0; f < PF; ++f)
+        if (int64_t(f) * BK < kdim) load_step(int64_t(f) * BK, ra[f], rb[f]);
+    for (int64_t k0 = 0; k0 < kdim; k0 += PF * BK) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; b[i] = Bs[kk][tx * 4 + i]; }
+        for (int f = 0; f < PF; ++f) {
+            const int64_t ks = k0 + int64_t(f) * BK;
+            if (ks >= kdim) break;                         // the same for every thread of the block
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int q = 0; q < 4; ++q) {
+                const int idx = tid + q * 256;
+                As[idx % BK][idx / BK] = ra[f][q];
+                Bs[idx % BK][idx / BK] = rb[f][q];
+            }
+            __syncthreads();
+            if (ks + PF * BK < kdim) load_step(ks + PF * BK, ra[f], rb[f]);   // refill this slot
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            for (int kk = 0; kk < BK; ++kk) {
+                float a[4], b[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; b[i] = Bs[kk][tx * 4 + i]; }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
 
     if constexpr (GEMM == 1) {

@@ -21,8 +21,9 @@
 //               the MMA reads N/2) of each k-block into a 6-stage ring; the bytes of BOTH CTAs are counted on
 //               the leader CTA's "full" barrier.
 //   warp 1      TMEM: allocates all 512 columns for the pair (one warp of each CTA, together).  In the
-//               leader CTA (rank 0) one thread issues the pair's MMAs and commits each stage to the "empty"
-//               barriers and each finished accumulator to the "acc_full" barriers of both CTAs (multicast).
+//               leader CTA (rank 0) the warp runs the MMA loop and lane 0 issues the pair's MMAs and commits
+//               each stage to the "empty" barriers and each finished accumulator to the "acc_full" barriers of
+//               both CTAs (multicast).
 //   warps 2..9  epilogue, two warps per TMEM lane quarter taking alternate 16-token chunks: tcgen05.ld of
 //               this CTA's accumulator (TMEM lane = weight row, column = token), SiLU-and-mul (GEMM 1) or
 //               route weight + scatter to the (token, slot) row (GEMM 2), each 16-token block transposed
@@ -239,13 +240,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader CTA only)
-        if (leader && lane == 0) {
+        // the whole warp runs the loop (waits, addresses and descriptors are warp-uniform) and lane 0 issues
+        // every MMA and commit
+        if (leader) {
+            const uint32_t issue = lane == 0;
             uint32_t it = 0, tc = 0;
             for (int32_t t = cid; t < total && !ctrl.abort; t += ncl, ++tc) {
                 const PTile tl = decode_tile(tab, p, t);
                 const int buf = int(tc & 1);
                 const uint32_t aph = (tc >> 1) & 1;
-                if (!wait_bar(&ctrl.acc_empty[buf], aph ^ 1, ctrl, p.err_word)) break;
+                if (!__all_sync(0xffffffffu, wait_bar(&ctrl.acc_empty[buf], aph ^ 1, ctrl, p.err_word))) break;
                 ptx::tc_fence_after();
                 const uint32_t idesc = ptx::idesc_bf16(2 * PM, pair_n(tl.rows));
                 const uint32_t d_tmem = tmem_base + uint32_t(buf * ACC_COLS);
@@ -253,21 +257,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 for (int kb = 0; kb < p.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
-                    if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
+                    if (!__all_sync(0xffffffffu, wait_bar(&ctrl.full[s], ph, ctrl, p.err_word))) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < PK / UMMA_K; ++kk)
-                        ptx::mma_f16_pair(d_tmem, ptx::smem_desc_sw128(sa + kk * UMMA_K * 2),
-                                          ptx::smem_desc_sw128(sb + kk * UMMA_K * 2), idesc, (kb | kk) != 0);
-                    ptx::mma_commit_pair(&ctrl.empty[s], 0x3);
+                        ptx::mma_f16_pair_by(issue, d_tmem, ptx::smem_desc_sw128(sa + kk * UMMA_K * 2),
+                                             ptx::smem_desc_sw128(sb + kk * UMMA_K * 2), idesc, (kb | kk) != 0);
+                    ptx::mma_commit_pair_by(issue, &ctrl.empty[s], 0x3);
                 }
                 if (!ok) break;
-                ptx::mma_commit_pair(&ctrl.acc_full[buf], 0x3);
+                ptx::mma_commit_pair_by(issue, &ctrl.acc_full[buf], 0x3);
             }
             // all MMAs issued (and the commits before this one) complete before TMEM is released
-            ptx::mma_commit_pair(&ctrl.drain, 0x1);
+            ptx::mma_commit_pair_by(issue, &ctrl.drain, 0x1);
             const uint64_t deadline = ptx::globaltimer() + kWaitNs / 4;
             volatile int never = 0;
             ptx::mbar_wait_bounded(&ctrl.drain, 0, deadline, &never);

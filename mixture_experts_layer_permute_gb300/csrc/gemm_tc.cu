@@ -4,7 +4,7 @@
 //   warp 0      TMA producer: one thread streams 64-wide k-blocks of the A and
 //               B tiles into a 4-stage shared-memory ring (128-byte swizzle),
 //               completing a "full" mbarrier per stage.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (kind::f16, bf16 in,
+//   warp 1      MMA issuer: lane 0 issues tcgen05.mma (kind::f16, bf16 in,
 //               fp32 accumulate) into one of two TMEM accumulators and frees
 //               each stage with tcgen05.commit on its "empty" mbarrier.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
@@ -30,9 +30,13 @@
 //   weight, each read once, full 128-byte lines, 128-byte swizzled) into a
 //   9-stage code ring that is freed as soon as a slice is decoded; four A
 //   slots hold decoded tiles in tensor memory plus the matching token tiles
-//   (loaded by a token-producer warp once the MMA has released the slot).
-//   Sixteen converter warps in four groups take slices in turn (group = slice
-//   index mod 4 = A slot), so four slices are in conversion at once.  Warp w
+//   in shared memory.  Sixteen converter warps in four groups take slices in
+//   turn (group = slice index mod 4 = A slot), so four slices are in
+//   conversion at once.  Once the MMA has released its slot, a group starts
+//   16-byte cp.async copies of the slice's token rows into the slot (128-byte
+//   swizzled, as the MMA reads them) and decodes while they land: a TMA copy
+//   per slot issued by one more warp took about 0.35 us to issue under the
+//   converters' load and put its latency on the slot's critical path.  Warp w
 //   may only reach TMEM lanes 32*(w%4)..+31, so in its group thread (w, lane)
 //   owns row 32*(w%4)+lane of the slice: 128 codes and four scales.  Decoding
 //   needs no conversion instruction: the E4M3 bits placed into bf16 bit
@@ -40,7 +44,12 @@
 //   exactly code * 2^-120 for normal, subnormal and zero codes alike, and one
 //   bf16x2 multiply by 2^(scale-7) restores the value (two multiplies when that
 //   factor would leave bf16's range).  The MMA takes its A operand from TMEM.
-//   Tokens per tile are capped at 64.
+//   Tokens per tile are capped at 64.  Two warps issue the MMAs, the even and
+//   the odd k slices of a tile, each into its own accumulator, and the
+//   epilogue adds the two: with the converter warps competing for issue slots
+//   one issuing warp sustains only about one M=128, K=16 MMA per 65-100 ns
+//   whatever N is (measured on GB300), which for 1-byte weights (128 x 16
+//   bytes per MMA) is at or below the HBM rate; two warps double it.
 //
 // Wide tiles (bf16, batched layout): 256 token rows x 256 weight rows as two
 // 128-row MMA halves that share each B stage, so an expert of up to 256 rows
@@ -62,6 +71,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mx_codec.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -85,8 +95,9 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 //   V_SWAP64: bf16 swap-AB tiles of up to 64 tokens: smem [A 16 KB][B 8 KB] x 8 stages (twice the
 //             weight bytes in flight of V_BF16); TMEM: two 64-column accumulators; 192 threads
 //   V_E4M3:   smem: 9 code stages of 128 rows x 128 B, then 4 token slots of 2 x 8 KB;
-//             TMEM: two 64-column accumulators, then 4 bf16 A tiles of 64 columns;
-//             736 threads (+ 16 converter warps, + 1 token warp); up to 64 tokens per tile
+//             TMEM: two buffers of two 64-column accumulators (one per MMA issuer), then 4 bf16 A tiles
+//             of 64 columns; 736 threads (+ 16 converter warps, + a second MMA warp); up to 64 tokens per
+//             tile
 //   V_WIDE:   batched-layout normal tiles of 256 token rows (two 128-row MMA halves sharing each B stage):
 //             smem [A rows 0..127 16 KB][A rows 128..255 16 KB][B 32 KB] x 3 stages; TMEM: one accumulator of
 //             two 256-column halves (the whole 512 columns, so no second buffer); 320 threads (8 epilogue
@@ -111,12 +122,14 @@ struct Cfg {
     static constexpr int TOK_OFF = STAGES * STAGE_BYTES;        // E4M3: token slots after the code ring
     static constexpr int TOK_SLOT = B_SUB * KSUB;
     static constexpr int EPI_WARPS = WIDE ? 8 : 4;
-    static constexpr int THREADS = W8 ? 192 + kConvThreads + 32 : 64 + 32 * EPI_WARPS;   // E4M3: + converters + token warp
-    static constexpr int TOK_WARP = 6 + kConvThreads / 32;
+    static constexpr int ISSUERS = W8 ? 2 : 1;                  // MMA-issuing threads, one accumulator each
+    static constexpr int THREADS = W8 ? 192 + kConvThreads + 32 : 64 + 32 * EPI_WARPS;   // E4M3: + converters,
+                                                                                         // second MMA warp
+    static constexpr int MMA2_WARP = 6 + kConvThreads / 32;     // E4M3: second MMA issuer (odd k slices)
     static constexpr int SMEM = STAGES * STAGE_BYTES + (W8 ? A_SLOTS * TOK_SLOT : 0) + 1024;
     static constexpr int ACC_STRIDE = (W8 || NARROW) ? TOK_SPAN : ACC_COLS; // TMEM columns per accumulator (half)
     static constexpr int NBUF = WIDE ? 1 : 2;                   // accumulators (the wide one fills TMEM)
-    static constexpr int A_TMEM = 2 * ACC_STRIDE;               // E4M3: first A tile column
+    static constexpr int A_TMEM = 2 * ISSUERS * ACC_STRIDE;     // E4M3: first A tile column
     static constexpr int A_COLS = KSUB * BK / 2;                // E4M3: TMEM columns per A tile
     static constexpr int TMEM_USED = W8 ? A_TMEM + A_SLOTS * A_COLS : (WIDE ? 2 * ACC_COLS : 2 * ACC_STRIDE);
 };
@@ -136,7 +149,7 @@ static_assert(Cfg<V_E4M3>::A_SLOTS == 4, "converter groups take A slot (stage in
 struct __align__(8) Ctrl {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
-    uint64_t conv[MAX_STAGES];   // E4M3: A slot converted and its tokens landed
+    uint64_t conv[MAX_STAGES];   // E4M3: A slot converted and its tokens copied
     uint64_t a_empty[4];         // E4M3: A slot free (MMA done)
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
@@ -169,6 +182,8 @@ struct TcParams {
     int mixed;           // 1: normal tiles plus a swap-AB tile for each expert's short tail
     int nt_n, nt_s;      // mixed: weight tiles per m-tile (normal, 256 rows) and per segment (swap, 128 rows)
     const uint8_t* w_scale;   // E4M3 weights: E8M0 scales (E, wrows, kdim/32)
+    const uint16_t* act;      // E4M3 weights: bf16 activation rows (rows_cap, act_ld), copied by the converters
+    int64_t act_ld;
     int64_t wrows;       // weight rows per expert
     int64_t nsb;         // scale bytes per weight row (kdim / 32)
     int skip_first_copy; // test hook: CTA 0 never issues its first weight copy (see timeout_test_hook)
@@ -291,20 +306,6 @@ MOE_DEVICE int64_t tile_weight_row(const TcParams& p, int nb, int r) {
     return int64_t(nb) * 128 + r;
 }
 
-// 4 E4M3 codes (one 32-bit word) -> 2 bf16x2 words (codes 0,1 and 2,3) times f1.
-// prmt copies each code into the low byte of a 16-bit half and its sign into the high byte;
-// shifting by 4 moves exponent+mantissa to bits 10..4 and the sign bits to 15..12 (and 19..16,
-// outside the half); the mask keeps bits 15 and 10..4 of each half.
-MOE_DEVICE void dequant4(uint32_t w, uint32_t f1, uint32_t& lo, uint32_t& hi) {
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));   // [sx(c1) c1 sx(c0) c0]
-    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));   // [sx(c3) c3 sx(c2) c2]
-    a = (a << 4) & 0x87F087F0u;
-    b = (b << 4) & 0x87F087F0u;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(f1));
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(f1));
-}
-
 // Normal-tile GEMM 1 epilogue, one 32-column chunk c of a row: columns [gate16, up16] of units
 // 128*nb + 16*c .. +15 -> 16 bf16 values of h.
 MOE_DEVICE void store_h_chunk(const TcParams& p, const uint32_t (&v)[32], bool valid, int64_t row, int nb, int c) {
@@ -343,12 +344,6 @@ MOE_DEVICE void store_y_chunk(const TcParams& p, const uint32_t (&v)[32], int64_
     }
 }
 
-MOE_DEVICE uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
 template <int V>
 __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
@@ -381,14 +376,14 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             ptx::mbar_init(&ctrl.empty[s], W8 ? 4 : 1);   // E4M3: freed by the 4 warps of the converting group
         }
         for (int a = 0; a < Cfg<V>::A_SLOTS; ++a) {
-            ptx::mbar_init(&ctrl.conv[a], 5);             // 4 converter warps + the token producer
+            ptx::mbar_init(&ctrl.conv[a], 4);             // the 4 converter warps of the slot's group
             ptx::mbar_init(&ctrl.a_empty[a], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(&ctrl.acc_full[b], 1);
+            ptx::mbar_init(&ctrl.acc_full[b], Cfg<V>::ISSUERS);   // one commit per MMA issuer
             ptx::mbar_init(&ctrl.acc_empty[b], Cfg<V>::EPI_WARPS);
         }
-        ptx::mbar_init(&ctrl.drain, 1);
+        ptx::mbar_init(&ctrl.drain, Cfg<V>::ISSUERS);
         ctrl.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -456,7 +451,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                     if (p.skip_first_copy && blockIdx.x == 0 && it == 0) continue;   // bytes that never arrive
                     const int k0 = kb * BK * KSUB;
                     // weights: normal -> B operand (256 rows); swap -> A operand (128 rows);
-                    // E4M3 codes -> row-major 64-byte rows for the converters
+                    // E4M3 codes -> 128-byte rows for the converters
                     uint8_t* wdst = W8 ? sa : (tl.swap ? sa : sb);
                     const int wrows = tl.swap ? 128 : 256;
                     const int row_w = tl.nb * wrows;          // first weight row (interleaved order)
@@ -467,7 +462,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                     else
                         ptx::tma_load_3d(wdst, mw, &ctrl.full[s], k0, row_w, tl.e, pol_w);
                     if (W8) {
-                        // E4M3 tokens come from the token producer
+                        // E4M3: the converters copy the tokens
                     } else if (tl.swap) {
                         for (int b = 0; b < nbox; ++b)
                             ptx::tma_load_2d(sb + b * TOK_BOX * BK * 2, mact, &ctrl.full[s], k0,
@@ -489,116 +484,85 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || (W8 && warp == Cfg<V>::MMA2_WARP)) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t it = 0, tc = 0;
-            for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x, ++tc) {
-                const Tile tl = decode_tile(tab, p, t);
-                const int buf = Cfg<V>::NBUF == 2 ? int(tc & 1) : 0;
-                const uint32_t aph = Cfg<V>::NBUF == 2 ? (tc >> 1) & 1 : tc & 1;
-                if (!wait_bar(&ctrl.acc_empty[buf], aph ^ 1, ctrl, p.err_word)) break;
-                ptx::tc_fence_after();
-                const bool half2 = Cfg<V>::WIDE && tl.rows > BM;   // wide tiles: MMAs for rows 128..255
-                int n_mma = 256;
-                if (tl.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
-                const uint32_t idesc = ptx::idesc_bf16(BM, n_mma);
-                const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg<V>::ACC_STRIDE);
-                const int nkb = tl.gemm == 2 && p.fused ? p.nkb2 : p.nkb;
-                bool ok = true;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    if constexpr (W8) {
-                        // A slot a: decoded weights in TMEM, tokens in the slot's smem tile
-                        const int a = it % Cfg<V>::A_SLOTS;
-                        const uint32_t ph = (it / Cfg<V>::A_SLOTS) & 1;
-                        if (!wait_bar(&ctrl.conv[a], ph, ctrl, p.err_word)) { ok = false; break; }
-                        ptx::tc_fence_after();
-                        const uint32_t sb = ptx::smem_addr(smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT);
+        // E4M3: issuer j (warp 1: j = 0, the second MMA warp: j = 1) takes the k slices kb = j (mod 2) of every
+        // tile into accumulator j of the buffer; bf16 variants have one issuer.  The whole warp runs the loop
+        // (waits, addresses and descriptors are warp-uniform) and lane 0 issues every MMA and commit.
+        const int j = warp == 1 ? 0 : 1;
+        const uint32_t issue = lane == 0;
+        uint32_t it = 0, tc = 0;
+        for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x, ++tc) {
+            const Tile tl = decode_tile(tab, p, t);
+            const int buf = Cfg<V>::NBUF == 2 ? int(tc & 1) : 0;
+            const uint32_t aph = Cfg<V>::NBUF == 2 ? (tc >> 1) & 1 : tc & 1;
+            if (!__all_sync(0xffffffffu, wait_bar(&ctrl.acc_empty[buf], aph ^ 1, ctrl, p.err_word))) break;
+            ptx::tc_fence_after();
+            const bool half2 = Cfg<V>::WIDE && tl.rows > BM;   // wide tiles: MMAs for rows 128..255
+            int n_mma = 256;
+            if (tl.swap) n_mma = max(16, (tl.rows + 15) / 16 * 16);
+            const uint32_t idesc = ptx::idesc_bf16(BM, n_mma);
+            const uint32_t d_tmem = tmem_base + uint32_t((buf * Cfg<V>::ISSUERS + j) * Cfg<V>::ACC_STRIDE);
+            const int nkb = tl.gemm == 2 && p.fused ? p.nkb2 : p.nkb;
+            bool ok = true;
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                if constexpr (W8) {
+                    if ((kb & 1) != j) continue;   // the other issuer's slice
+                    // A slot a: decoded weights in TMEM, tokens in the slot's smem tile
+                    const int a = it % Cfg<V>::A_SLOTS;
+                    const uint32_t ph = (it / Cfg<V>::A_SLOTS) & 1;
+                    if (!__all_sync(0xffffffffu, wait_bar(&ctrl.conv[a], ph, ctrl, p.err_word))) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t sb = ptx::smem_addr(smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT);
 #pragma unroll
-                        for (int kk = 0; kk < Cfg<V>::KSUB * BK / UMMA_K; ++kk) {
-                            const int sub = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
-                            const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<V>::B_SUB + kq * UMMA_K * 2);
-                            // 16 bf16 of a row = 8 TMEM columns per k step
-                            const uint32_t a_tmem =
-                                tmem_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS + kk * 8);
-                            ptx::mma_f16_tmem_a(d_tmem, a_tmem, bd, idesc, (kb | kk) != 0);
-                        }
-                        ptx::mma_commit(&ctrl.a_empty[a]);
-                    } else {
-                        const int s = it % STAGES;
-                        const uint32_t ph = (it / STAGES) & 1;
-                        if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
-                        ptx::tc_fence_after();
-                        const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
-                        const uint32_t sb = sa + Cfg<V>::B_OFF;
-#pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                            const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
-                            const uint64_t bd = ptx::smem_desc_sw128(sb + kk * UMMA_K * 2);
-                            ptx::mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
-                            if (half2) {
-                                const uint64_t ad2 = ptx::smem_desc_sw128(sa + A_BYTES + kk * UMMA_K * 2);
-                                ptx::mma_f16(d_tmem + ACC_COLS, ad2, bd, idesc, (kb | kk) != 0);
-                            }
-                        }
-                        ptx::mma_commit(&ctrl.empty[s]);
+                    for (int kk = 0; kk < Cfg<V>::KSUB * BK / UMMA_K; ++kk) {
+                        const int sub = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
+                        const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<V>::B_SUB + kq * UMMA_K * 2);
+                        // 16 bf16 of a row = 8 TMEM columns per k step
+                        const uint32_t a_tmem = tmem_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS + kk * 8);
+                        ptx::mma_f16_tmem_a_by(issue, d_tmem, a_tmem, bd, idesc, kb != j || kk != 0);
                     }
+                    ptx::mma_commit_by(issue, &ctrl.a_empty[a]);
+                } else {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!__all_sync(0xffffffffu, wait_bar(&ctrl.full[s], ph, ctrl, p.err_word))) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_addr(smem + s * STAGE_BYTES);
+                    const uint32_t sb = sa + Cfg<V>::B_OFF;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t ad = ptx::smem_desc_sw128(sa + kk * UMMA_K * 2);
+                        const uint64_t bd = ptx::smem_desc_sw128(sb + kk * UMMA_K * 2);
+                        ptx::mma_f16_by(issue, d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        if (half2) {
+                            const uint64_t ad2 = ptx::smem_desc_sw128(sa + A_BYTES + kk * UMMA_K * 2);
+                            ptx::mma_f16_by(issue, d_tmem + ACC_COLS, ad2, bd, idesc, (kb | kk) != 0);
+                        }
+                    }
+                    ptx::mma_commit_by(issue, &ctrl.empty[s]);
                 }
-                if (!ok) break;
-                ptx::mma_commit(&ctrl.acc_full[buf]);
             }
-            // all MMAs issued by this thread complete before TMEM is released
-            ptx::mma_commit(&ctrl.drain);
-            const uint64_t deadline = ptx::globaltimer() + kWaitNs / 4;
-            volatile int never = 0;
-            ptx::mbar_wait_bounded(&ctrl.drain, 0, deadline, &never);
+            if (!ok) break;
+            ptx::mma_commit_by(issue, &ctrl.acc_full[buf]);
         }
+        // all MMAs issued by lane 0 complete before TMEM is released
+        ptx::mma_commit_by(issue, &ctrl.drain);
+        const uint64_t deadline = ptx::globaltimer() + kWaitNs / 4;
+        volatile int never = 0;
+        ptx::mbar_wait_bounded(&ctrl.drain, 0, deadline, &never);
         __syncwarp();
     } else if (W8 && warp >= 6) {
-        // ------------------------------------------------------------ E4M3 converters and token producer
-        if (warp == Cfg<V>::TOK_WARP) {
-            // token producer: one lane loads each stage's token rows into A slot (stage % 4) once the MMA
-            // has released that slot
-            if (lane == 0) {
-                const uint64_t pol_keep = ptx::policy_evict_last();
-                uint32_t it = 0;
-                for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
-                    const Tile tl = decode_tile(tab, p, t);
-                    const int nbox = (tl.rows + TOK_BOX - 1) / TOK_BOX;
-                    const uint32_t bytes = uint32_t(Cfg<V>::KSUB * nbox * TOK_BOX * BK * 2);
-                    bool ok = true;
-                    for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                        const int a = it % Cfg<V>::A_SLOTS;
-                        const uint32_t ph = (it / Cfg<V>::A_SLOTS) & 1;
-                        if (!wait_bar(&ctrl.a_empty[a], ph ^ 1, ctrl, p.err_word)) { ok = false; break; }
-                        ptx::mbar_arrive_expect_tx(&ctrl.conv[a], bytes);
-                        uint8_t* dst = smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT;
-                        const int k0 = kb * BK * Cfg<V>::KSUB;
-                        for (int sub = 0; sub < Cfg<V>::KSUB; ++sub)
-                            for (int b = 0; b < nbox; ++b)
-                                ptx::tma_load_2d(dst + sub * Cfg<V>::B_SUB + b * TOK_BOX * BK * 2, &tm_act,
-                                                 &ctrl.conv[a], k0 + sub * BK, int32_t(tl.row0 + b * TOK_BOX),
-                                                 pol_keep);
-                    }
-                    if (!ok) break;
-                }
-                // token copies in flight land before the CTA can exit (bounded)
-                for (uint32_t j = it > 4u ? it - 4u : 0u; j < it; ++j) {
-                    const uint64_t deadline = ptx::globaltimer() + kWaitNs / 8;
-                    volatile int never = 0;
-                    ptx::mbar_wait_bounded(&ctrl.conv[j % 4], (j / 4) & 1, deadline, &never);
-                }
-            }
-            __syncwarp();
-        } else {
+        // ------------------------------------------------------------ E4M3 converters
         // Four groups of 4 warps take stages in turn (group = stage index mod 4 = its A slot), so four
         // stages are in conversion at once.  In a group, thread (warp w, lane) owns row r = 32*(w%4) + lane
         // of the 128-row weight tile: its 128 codes of the slice (scale blocks 0..3) go to TMEM lane r, the
-        // slot's 64 A-tile columns.
+        // slot's 64 A-tile columns.  The group also copies the slice's token rows into the slot.
         const int cw = warp - 6, grp = cw >> 2;
         const int q = warp & 3, r = q * 32 + lane;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows (4 slices per 16 B)
+        const uint64_t pol_keep = ptx::policy_evict_last();   // token rows are read by every weight block
         uint32_t it = 0;
         for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
             const Tile tl = decode_tile(tab, p, t);
@@ -616,9 +580,28 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                 if (kb + 16 < p.nkb) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 4 * (kb + 16)));
                 const int s = it % STAGES, a = grp;
                 const uint32_t ph = (it / STAGES) & 1, pha = (it / Cfg<V>::A_SLOTS) & 1;
-                if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) { ok = false; break; }
                 if (!wait_bar(&ctrl.a_empty[a], pha ^ 1, ctrl, p.err_word)) { ok = false; break; }
                 ptx::tc_fence_after();   // the MMA that last read this A slot has completed
+                {
+                    // the slice's token rows (16-row boxes) -> the slot's two 64-wide k-blocks, rows of 128
+                    // bytes, 16-byte chunk c of row n at chunk c ^ (n % 8) (the 128-byte swizzle of the MMA's
+                    // B operand); rows past the tile's tokens are zero-filled without a global read
+                    const int nchunk = (tl.rows + TOK_BOX - 1) / TOK_BOX * TOK_BOX * 16;
+                    uint8_t* slot = smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT;
+                    const int64_t k0 = int64_t(kb) * BK * Cfg<V>::KSUB;
+                    for (int idx = r; idx < nchunk; idx += 128) {
+                        const int n = idx >> 4, sub = (idx >> 3) & 1, c = idx & 7;
+                        const bool valid = n < tl.rows;
+                        const uint16_t* src = p.act + (tl.row0 + (valid ? n : 0)) * p.act_ld + k0 + sub * BK + c * 8;
+                        ptx::cp_async_16(ptx::smem_addr(slot + sub * Cfg<V>::B_SUB + n * (BK * 2) + ((c ^ (n & 7)) << 4)),
+                                         src, valid ? 16u : 0u, pol_keep);
+                    }
+                }
+                if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) {
+                    ptx::cp_async_wait_all();   // no copy of this thread is left in flight
+                    ok = false;
+                    break;
+                }
                 // the code tile lands 128-byte swizzled: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
                 const uint8_t* row = smem + s * STAGE_BYTES + r * (BK * 2);
 #pragma unroll
@@ -627,11 +610,8 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
 #pragma unroll
                     for (int b2 = 0; b2 < 2; ++b2) {
                         const int b = 2 * half + b2;     // scale block of the slice
-                        const uint32_t sc = (quad >> (8 * b)) & 0xFFu;
-                        // bf16x2 factor 2^(sc-7) turns code*2^-120 into code*2^(sc-127); above sc = 134 that
-                        // factor leaves bf16's range, so 2^(sc-127) is applied first and 2^120 after
-                        const uint32_t e1 = sc <= 134u ? sc + 120u : sc;
-                        const uint32_t f1 = (e1 << 7) | (e1 << 23);
+                        bool second;                     // the factor 2^120 still to apply (large scales)
+                        const uint32_t f1 = mx_e4m3_factor((quad >> (8 * b)) & 0xFFu, second);
                         const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * b) ^ (r & 7)) << 4));
                         const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * b + 1) ^ (r & 7)) << 4));
                         uint32_t* ob = o + 16 * b2;
@@ -643,25 +623,25 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                         dequant4(v1.y, f1, ob[10], ob[11]);
                         dequant4(v1.z, f1, ob[12], ob[13]);
                         dequant4(v1.w, f1, ob[14], ob[15]);
-                        if (sc > 134u) {
-                            const uint32_t f2 = (247u << 7) | (247u << 23);   // 2^120
+                        if (second) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], f2);
+                            for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], kBf16x2Pow2_120);
                         }
                     }
                     ptx::tmem_st_32x32b_x32(
                         tmem_base + lane_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS + half * 32), o);
                 }
                 ptx::tmem_st_wait();
+                ptx::cp_async_wait_all();           // this thread's token copies have landed
+                ptx::fence_proxy_async_smem();      // and are visible to the MMA's operand reads
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     ptx::mbar_arrive(&ctrl.empty[s]);   // the code stage can be refilled
-                    ptx::mbar_arrive(&ctrl.conv[a]);    // the A slot is ready for the MMA
+                    ptx::mbar_arrive(&ctrl.conv[a]);    // the A slot and its tokens are ready for the MMA
                 }
             }
             if (!ok) break;
-        }
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -675,7 +655,8 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             const uint32_t aph = Cfg<V>::NBUF == 2 ? (tc >> 1) & 1 : tc & 1;
             if (!wait_bar(&ctrl.acc_full[buf], aph, ctrl, p.err_word)) break;
             ptx::tc_fence_after();
-            const uint32_t tacc = tmem_base + lane_base + uint32_t(buf * Cfg<V>::ACC_STRIDE + half * ACC_COLS);
+            const uint32_t tacc =
+                tmem_base + lane_base + uint32_t(buf * Cfg<V>::ISSUERS * Cfg<V>::ACC_STRIDE + half * ACC_COLS);
             if (!tl.swap) {
               if constexpr (V == V_BF16 || V == V_WIDE) {   // the other variants run swap-AB tiles only
                if (half * BM < tl.rows) {                     // (a wide tile may have no second half)
@@ -717,6 +698,23 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                 // swap-AB: TMEM lane = weight row of the tile, column = token
                 const int n_tok = tl.rows;
                 const int n_chunks = (n_tok + 15) / 16;
+                // 16 token columns of this thread's row; E4M3: the second issuer's accumulator (odd k slices,
+                // present when the tile has two or more) added to the first's
+                const bool two = Cfg<V>::ISSUERS == 2 && p.nkb >= 2;
+                auto load16 = [&](int cb, uint32_t (&v)[16]) {
+                    ptx::tmem_ld_32x32b_x16(tacc + cb * 16, v);
+                    if (two) {
+                        uint32_t w[16];
+                        ptx::tmem_ld_32x32b_x16(tacc + Cfg<V>::ACC_STRIDE + cb * 16, w);
+                        ptx::tmem_ld_wait_regs16(v);
+                        ptx::tmem_ld_wait_regs16(w);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
+                    } else {
+                        ptx::tmem_ld_wait_regs16(v);
+                    }
+                };
                 if (tl.gemm == 1) {
                     // lanes 0..15: gate of unit u, lanes 16..31: up of unit u, u = 64*nb + 16*q + (lane & 15)
                     const int64_t unit = int64_t(tl.nb) * 64 + q * 16 + (lane & 15);
@@ -724,8 +722,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
 #pragma unroll 1
                     for (int cb = 0; cb < n_chunks; ++cb) {
                         uint32_t v[16];
-                        ptx::tmem_ld_32x32b_x16(tacc + cb * 16, v);
-                        ptx::tmem_ld_wait();
+                        load16(cb, v);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const float mine = __uint_as_float(v[i]);
@@ -753,8 +750,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
 #pragma unroll 1
                     for (int cb = 0; cb < n_chunks; ++cb) {
                         uint32_t v[16];
-                        ptx::tmem_ld_32x32b_x16(tacc + cb * 16, v);
-                        ptx::tmem_ld_wait();
+                        load16(cb, v);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int n = cb * 16 + i;
@@ -1012,6 +1008,8 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     p.span = swap ? (variant == V_E4M3 ? Cfg<V_E4M3>::TOK_SPAN : Cfg<V_SWAP64>::TOK_SPAN)
                   : (variant == V_WIDE ? 2 * BM : BM);
     p.w_scale = g.w_scale;
+    p.act = static_cast<const uint16_t*>(g.a);
+    p.act_ld = kdim;
     p.wrows = wrows;
     p.nsb = kdim / 32;
     p.skip_first_copy = timeout_test_hook() ? 1 : 0;

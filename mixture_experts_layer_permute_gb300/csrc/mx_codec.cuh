@@ -48,4 +48,39 @@ MOE_DEVICE float mx_pow2(int k) {   // 2^k for -149 <= k <= 127, exact
 // The factor that maps a block with scale code `code` onto the E4M3 grid.
 MOE_DEVICE float mx_inv_scale(int code) { return mx_pow2(127 - code); }
 
+// ---- E4M3 weights decoded to bf16 for the kind::f16 MMA ----
+//
+// Placing an E4M3 code's sign in bf16 bit 15 and its exponent and mantissa in bits 10..4 gives exactly
+// code * 2^-120 for normal, subnormal and zero codes alike; one bf16x2 multiply by 2^(scale-7) then yields
+// code * 2^(scale-127).  mx_e4m3_factor gives that factor for scale code sc and whether the result still needs
+// the second factor 2^120 (above sc = 134, 2^(sc-7) leaves bf16's range, so 2^(sc-127) is applied first).
+
+// 4 E4M3 codes (one 32-bit word) -> 2 bf16x2 words (codes 0,1 and 2,3) times f1.
+// prmt copies each code into the low byte of a 16-bit half and its sign into the high byte;
+// shifting by 4 moves exponent+mantissa to bits 10..4 and the sign bits to 15..12 (and 19..16,
+// outside the half); the mask keeps bits 15 and 10..4 of each half.
+MOE_DEVICE void dequant4(uint32_t w, uint32_t f1, uint32_t& lo, uint32_t& hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));   // [sx(c1) c1 sx(c0) c0]
+    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));   // [sx(c3) c3 sx(c2) c2]
+    a = (a << 4) & 0x87F087F0u;
+    b = (b << 4) & 0x87F087F0u;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(f1));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(f1));
+}
+
+MOE_DEVICE uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+MOE_DEVICE uint32_t mx_e4m3_factor(uint32_t sc, bool& second) {
+    second = sc > 134u;
+    const uint32_t e1 = second ? sc : sc + 120u;
+    return (e1 << 7) | (e1 << 23);
+}
+
+constexpr uint32_t kBf16x2Pow2_120 = (247u << 7) | (247u << 23);   // 2^120 in both halves
+
 }  // namespace moe

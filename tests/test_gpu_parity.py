@@ -563,6 +563,7 @@ E4M3_SHAPES = [  # T, k, E, K, I
     (96, 4, 8, 512, 256),            # ~48 tokens per expert
     (300, 1, 2, 256, 128),           # ~150 tokens per expert: three 64-token segments
     (5, 8, 64, 512, 128),            # decode-like
+    (40, 2, 4, 384, 384),            # three k slices in both GEMMs (the second MMA issuer takes one)
 ]
 
 
@@ -595,7 +596,7 @@ def test_gemm1_swiglu_e4m3(moe, impl, shape, w1_layout):
     assert_close(to_f64(h.cpu()[torch.from_numpy(rr).long()]), href, TOL_BF16, f"gemm1 e4m3 {impl}")
 
 
-@pytest.mark.parametrize("impl", ["swap_ab", "simt"])
+@pytest.mark.parametrize("impl", ["swap_ab", "auto", "simt"])
 @pytest.mark.parametrize("shape", E4M3_SHAPES)
 def test_gemm2_e4m3(moe, impl, shape):
     T, k, E, K, I = shape

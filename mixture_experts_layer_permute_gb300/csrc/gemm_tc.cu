@@ -297,6 +297,15 @@ MOE_DEVICE Tile decode_tile(const ExpertTable& tab, const TcParams& p, int32_t t
     return tl;
 }
 
+// The k-th tile of CTA b among G CTAs.  Fused launches walk the tiles serpentine (b, 2G-1-b, 2G+b, ...): their
+// list holds all GEMM 1 tiles (K-long weight rows) before the GEMM 2 tiles (I-long rows), so plain round-robin
+// hands the CTAs of low index more bytes; measured on the decode sweep, the serpentine order is 0.6 % faster
+// (1.5 % at T=8), while on the MXFP8-weight tiles, all of one size, it was 1.4 % slower.
+MOE_DEVICE int32_t nth_tile(const TcParams& p, int32_t k) {
+    const int32_t G = int32_t(gridDim.x), b = int32_t(blockIdx.x);
+    return k * G + ((p.fused && (k & 1)) ? G - 1 - b : b);
+}
+
 // Weight row (within the expert) held by row r of a 128-row swap-AB weight tile nb.
 MOE_DEVICE int64_t tile_weight_row(const TcParams& p, int nb, int r) {
     if (p.w_mode == 1) {   // [gate; up] rows seen through the interleave-16 view
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             const uint64_t pol_keep = ptx::policy_evict_last();
             const uint64_t pol_a = pol_keep;
             uint32_t it = 0;
-            for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
+            for (int32_t k_ = 0, t = blockIdx.x; t < total && !ctrl.abort; t = nth_tile(p, ++k_)) {
                 const Tile tl = decode_tile(tab, p, t);
                 const int nbox = tl.swap ? (tl.rows + TOK_BOX - 1) / TOK_BOX : 0;
                 const bool second = (p.mixed && tl.swap) || (tl.gemm == 2 && p.fused);   // maps of the second kind
@@ -492,7 +501,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
         const int j = warp == 1 ? 0 : 1;
         const uint32_t issue = lane == 0;
         uint32_t it = 0, tc = 0;
-        for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x, ++tc) {
+        for (int32_t k_ = 0, t = blockIdx.x; t < total && !ctrl.abort; t = nth_tile(p, ++k_), ++tc) {
             const Tile tl = decode_tile(tab, p, t);
             const int buf = Cfg<V>::NBUF == 2 ? int(tc & 1) : 0;
             const uint32_t aph = Cfg<V>::NBUF == 2 ? (tc >> 1) & 1 : tc & 1;
@@ -564,7 +573,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows (4 slices per 16 B)
         const uint64_t pol_keep = ptx::policy_evict_last();   // token rows are read by every weight block
         uint32_t it = 0;
-        for (int32_t t = blockIdx.x; t < total && !ctrl.abort; t += gridDim.x) {
+        for (int32_t k_ = 0, t = blockIdx.x; t < total && !ctrl.abort; t = nth_tile(p, ++k_)) {
             const Tile tl = decode_tile(tab, p, t);
             const uint8_t* srow = p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb;
             bool ok = true;
@@ -649,7 +658,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
         const int half = Cfg<V>::WIDE ? (warp - 2) >> 2 : 0;   // wide tiles: row half of this warp
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         uint32_t tc = 0;
-        for (int32_t t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+        for (int32_t k_ = 0, t = blockIdx.x; t < total; t = nth_tile(p, ++k_), ++tc) {
             const Tile tl = decode_tile(tab, p, t);
             const int buf = Cfg<V>::NBUF == 2 ? int(tc & 1) : 0;
             const uint32_t aph = Cfg<V>::NBUF == 2 ? (tc >> 1) & 1 : tc & 1;

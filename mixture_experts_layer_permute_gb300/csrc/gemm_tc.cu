@@ -98,23 +98,28 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 //             TMEM: two buffers of two 64-column accumulators (one per MMA issuer), then 4 bf16 A tiles
 //             of 64 columns; 736 threads (+ 16 converter warps, + a second MMA warp); up to 64 tokens per
 //             tile
+//   V_E4M3N:  as V_E4M3 with up to 32 tokens per tile (chosen when the routed rows average 16 or fewer per
+//             expert): 11 code stages, token slots of 2 x 4 KB; TMEM: two buffers of four 32-column
+//             accumulators; four MMA warps (800 threads), two per slice parity, each issuing 4 of a slice's 8
+//             MMAs, so a slot's MMAs are issued in half the time and the SM issues twice as many
 //   V_WIDE:   batched-layout normal tiles of 256 token rows (two 128-row MMA halves sharing each B stage):
 //             smem [A rows 0..127 16 KB][A rows 128..255 16 KB][B 32 KB] x 3 stages; TMEM: one accumulator of
 //             two 256-column halves (the whole 512 columns, so no second buffer); 320 threads (8 epilogue
 //             warps, one per TMEM lane quarter and half).  Each stage carries twice the MMA work of a V_BF16
 //             stage for 4/3 of its bytes.
-enum { V_BF16 = 0, V_E4M3 = 1, V_SWAP64 = 2, V_WIDE = 3 };
+enum { V_BF16 = 0, V_E4M3 = 1, V_SWAP64 = 2, V_WIDE = 3, V_E4M3N = 4 };
 
 template <int V>
 struct Cfg {
-    static constexpr bool W8 = V == V_E4M3;
+    static constexpr bool W8 = V == V_E4M3 || V == V_E4M3N;
+    static constexpr bool E4N = V == V_E4M3N;
     static constexpr bool NARROW = V == V_SWAP64;
     static constexpr bool WIDE = V == V_WIDE;
     static constexpr int KSUB = W8 ? 2 : 1;                     // 64-wide k-blocks per stage
-    static constexpr int STAGES = W8 ? 9 : (NARROW ? 8 : (WIDE ? 3 : 4));   // bf16: operand stages; E4M3: code stages
+    static constexpr int STAGES = W8 ? (E4N ? 11 : 9) : (NARROW ? 8 : (WIDE ? 3 : 4));   // E4M3: code stages
     static constexpr int A_PARTS = WIDE ? 2 : 1;                // 128-row A tiles per stage
     static constexpr int A_SLOTS = 4;                           // E4M3: TMEM A tiles (+ token tiles)
-    static constexpr int TOK_SPAN = (W8 || NARROW) ? 64 : 256;  // swap-AB tokens per tile
+    static constexpr int TOK_SPAN = E4N ? 32 : ((W8 || NARROW) ? 64 : 256);   // swap-AB tokens per tile
     static constexpr int B_OFF = W8 ? 0 : A_PARTS * A_BYTES;    // bf16: B operand offset in a stage
     static constexpr int B_SUB = TOK_SPAN * BK * 2;             // token bytes per 64-wide k-block (swap)
     static constexpr int B_BYTES = W8 ? 0 : (NARROW ? B_SUB : 256 * BK * 2);
@@ -122,10 +127,10 @@ struct Cfg {
     static constexpr int TOK_OFF = STAGES * STAGE_BYTES;        // E4M3: token slots after the code ring
     static constexpr int TOK_SLOT = B_SUB * KSUB;
     static constexpr int EPI_WARPS = WIDE ? 8 : 4;
-    static constexpr int ISSUERS = W8 ? 2 : 1;                  // MMA-issuing threads, one accumulator each
-    static constexpr int THREADS = W8 ? 192 + kConvThreads + 32 : 64 + 32 * EPI_WARPS;   // E4M3: + converters,
-                                                                                         // second MMA warp
-    static constexpr int MMA2_WARP = 6 + kConvThreads / 32;     // E4M3: second MMA issuer (odd k slices)
+    static constexpr int ISSUERS = E4N ? 4 : (W8 ? 2 : 1);     // MMA-issuing warps, one accumulator each
+    static constexpr int PER_SLICE = W8 ? ISSUERS / 2 : 1;      // E4M3: issuers sharing a slice's MMAs
+    static constexpr int THREADS = W8 ? 192 + kConvThreads + 32 * (ISSUERS - 1) : 64 + 32 * EPI_WARPS;
+    static constexpr int MMA2_WARP = 6 + kConvThreads / 32;     // E4M3: first MMA warp after warp 1
     static constexpr int SMEM = STAGES * STAGE_BYTES + (W8 ? A_SLOTS * TOK_SLOT : 0) + 1024;
     static constexpr int ACC_STRIDE = (W8 || NARROW) ? TOK_SPAN : ACC_COLS; // TMEM columns per accumulator (half)
     static constexpr int NBUF = WIDE ? 1 : 2;                   // accumulators (the wide one fills TMEM)
@@ -138,6 +143,9 @@ static_assert(Cfg<V_SWAP64>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed t
 static_assert(Cfg<V_WIDE>::TMEM_USED <= TMEM_COLS, "bf16 accumulators exceed the TMEM allocation");
 static_assert(Cfg<V_WIDE>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
 static_assert(Cfg<V_E4M3>::TMEM_USED <= TMEM_COLS, "E4M3 accumulators and A tiles exceed the TMEM allocation");
+static_assert(Cfg<V_E4M3N>::TMEM_USED <= TMEM_COLS, "E4M3 accumulators and A tiles exceed the TMEM allocation");
+static_assert(Cfg<V_E4M3N>::SMEM + 13 * 1024 <= 227 * 1024, "E4M3 stage ring exceeds shared memory");
+static_assert(Cfg<V_E4M3N>::STAGES <= MAX_STAGES, "too many stages");
 static_assert(Cfg<V_BF16>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
 static_assert(Cfg<V_SWAP64>::SMEM + 13 * 1024 <= 227 * 1024, "bf16 stage ring exceeds shared memory");
 static_assert(Cfg<V_E4M3>::SMEM + 13 * 1024 <= 227 * 1024, "E4M3 stage ring exceeds shared memory");
@@ -386,7 +394,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
         }
         for (int a = 0; a < Cfg<V>::A_SLOTS; ++a) {
             ptx::mbar_init(&ctrl.conv[a], 4);             // the 4 converter warps of the slot's group
-            ptx::mbar_init(&ctrl.a_empty[a], 1);
+            ptx::mbar_init(&ctrl.a_empty[a], Cfg<V>::PER_SLICE);   // E4M3: each issuer of the slice commits
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&ctrl.acc_full[b], Cfg<V>::ISSUERS);   // one commit per MMA issuer
@@ -493,12 +501,14 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1 || (W8 && warp == Cfg<V>::MMA2_WARP)) {
+    } else if (warp == 1 || (W8 && warp >= Cfg<V>::MMA2_WARP && warp < Cfg<V>::MMA2_WARP + Cfg<V>::ISSUERS - 1)) {
         // ------------------------------------------------------------ MMA issuer
-        // E4M3: issuer j (warp 1: j = 0, the second MMA warp: j = 1) takes the k slices kb = j (mod 2) of every
-        // tile into accumulator j of the buffer; bf16 variants have one issuer.  The whole warp runs the loop
-        // (waits, addresses and descriptors are warp-uniform) and lane 0 issues every MMA and commit.
-        const int j = warp == 1 ? 0 : 1;
+        // E4M3: issuer j (warp 1: j = 0, the further MMA warps: j = 1, 2, ...) takes the k slices of parity
+        // j / PER_SLICE of every tile, and of each such slice the MMAs of part j % PER_SLICE, into accumulator j
+        // of the buffer; bf16 variants have one issuer.  The whole warp runs the loop (waits, addresses and
+        // descriptors are warp-uniform) and lane 0 issues every MMA and commit.
+        const int j = warp == 1 ? 0 : warp - Cfg<V>::MMA2_WARP + 1;
+        const int par = j / Cfg<V>::PER_SLICE, part = j % Cfg<V>::PER_SLICE;
         const uint32_t issue = lane == 0;
         uint32_t it = 0, tc = 0;
         for (int32_t k_ = 0, t = blockIdx.x; t < total && !ctrl.abort; t = nth_tile(p, ++k_), ++tc) {
@@ -516,20 +526,22 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             bool ok = true;
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 if constexpr (W8) {
-                    if ((kb & 1) != j) continue;   // the other issuer's slice
+                    if ((kb & 1) != par) continue;   // the other parity's slice
                     // A slot a: decoded weights in TMEM, tokens in the slot's smem tile
                     const int a = it % Cfg<V>::A_SLOTS;
                     const uint32_t ph = (it / Cfg<V>::A_SLOTS) & 1;
                     if (!__all_sync(0xffffffffu, wait_bar(&ctrl.conv[a], ph, ctrl, p.err_word))) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t sb = ptx::smem_addr(smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT);
+                    constexpr int KK = Cfg<V>::KSUB * BK / UMMA_K / Cfg<V>::PER_SLICE;   // MMAs per issuer
 #pragma unroll
-                    for (int kk = 0; kk < Cfg<V>::KSUB * BK / UMMA_K; ++kk) {
+                    for (int k2 = 0; k2 < KK; ++k2) {
+                        const int kk = part * KK + k2;   // k step of the slice
                         const int sub = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
                         const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<V>::B_SUB + kq * UMMA_K * 2);
                         // 16 bf16 of a row = 8 TMEM columns per k step
                         const uint32_t a_tmem = tmem_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS + kk * 8);
-                        ptx::mma_f16_tmem_a_by(issue, d_tmem, a_tmem, bd, idesc, kb != j || kk != 0);
+                        ptx::mma_f16_tmem_a_by(issue, d_tmem, a_tmem, bd, idesc, kb != par || k2 != 0);
                     }
                     ptx::mma_commit_by(issue, &ctrl.a_empty[a]);
                 } else {
@@ -707,21 +719,20 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                 // swap-AB: TMEM lane = weight row of the tile, column = token
                 const int n_tok = tl.rows;
                 const int n_chunks = (n_tok + 15) / 16;
-                // 16 token columns of this thread's row; E4M3: the second issuer's accumulator (odd k slices,
-                // present when the tile has two or more) added to the first's
-                const bool two = Cfg<V>::ISSUERS == 2 && p.nkb >= 2;
+                // 16 token columns of this thread's row; E4M3: the accumulators of all issuers added (those of
+                // the odd-slice issuers hold something when the tile has two or more slices)
+                const int n_acc = (Cfg<V>::ISSUERS > 1 && p.nkb < 2) ? Cfg<V>::PER_SLICE : Cfg<V>::ISSUERS;
                 auto load16 = [&](int cb, uint32_t (&v)[16]) {
                     ptx::tmem_ld_32x32b_x16(tacc + cb * 16, v);
-                    if (two) {
+                    ptx::tmem_ld_wait_regs16(v);
+#pragma unroll 1
+                    for (int jj = 1; jj < n_acc; ++jj) {
                         uint32_t w[16];
-                        ptx::tmem_ld_32x32b_x16(tacc + Cfg<V>::ACC_STRIDE + cb * 16, w);
-                        ptx::tmem_ld_wait_regs16(v);
+                        ptx::tmem_ld_32x32b_x16(tacc + jj * Cfg<V>::ACC_STRIDE + cb * 16, w);
                         ptx::tmem_ld_wait_regs16(w);
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
-                    } else {
-                        ptx::tmem_ld_wait_regs16(v);
                     }
                 };
                 if (tl.gemm == 1) {
@@ -1011,10 +1022,15 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     // are 256 rows, so one tile covers an expert of up to max_tokens = 256 and streams each weight tile once;
     // the contiguous layout keeps 128-row tiles, whose second accumulator hides the epilogue (measured on the
     // skewed prefill: 256-row tiles took GEMM 1 from 0.629 to 0.665 ms)
-    const int variant = w8 ? V_E4M3
+    // E4M3 weights: 32-token tiles with four MMA warps when the routed rows average 16 or fewer per expert (the
+    // decode regime; an expert with more tokens takes several tiles), else 64-token tiles with two
+    const int64_t rows_all = g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens;
+    const int variant = w8 ? (rows_all <= 16 * int64_t(g.E) ? V_E4M3N : V_E4M3)
                            : (swap ? V_SWAP64
                                    : ((mixed || g.layout == MOE_LAYOUT_CONTIGUOUS) ? V_BF16 : V_WIDE));
-    p.span = swap ? (variant == V_E4M3 ? Cfg<V_E4M3>::TOK_SPAN : Cfg<V_SWAP64>::TOK_SPAN)
+    p.span = swap ? (variant == V_E4M3    ? Cfg<V_E4M3>::TOK_SPAN
+                     : variant == V_E4M3N ? Cfg<V_E4M3N>::TOK_SPAN
+                                          : Cfg<V_SWAP64>::TOK_SPAN)
                   : (variant == V_WIDE ? 2 * BM : BM);
     p.w_scale = g.w_scale;
     p.act = static_cast<const uint16_t*>(g.a);
@@ -1024,6 +1040,7 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     p.skip_first_copy = timeout_test_hook() ? 1 : 0;
 
     int rc = variant == V_E4M3     ? set_smem_attr<V_E4M3>()
+             : variant == V_E4M3N  ? set_smem_attr<V_E4M3N>()
              : variant == V_SWAP64 ? set_smem_attr<V_SWAP64>()
              : variant == V_WIDE   ? set_smem_attr<V_WIDE>()
                                    : set_smem_attr<V_BF16>();
@@ -1039,6 +1056,9 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     if (variant == V_E4M3)
         gemm_tc_kernel<V_E4M3><<<grid, Cfg<V_E4M3>::THREADS, Cfg<V_E4M3>::SMEM, s>>>(maps.act, maps.w, maps.act_s,
                                                                                      maps.w_s, p);
+    else if (variant == V_E4M3N)
+        gemm_tc_kernel<V_E4M3N><<<grid, Cfg<V_E4M3N>::THREADS, Cfg<V_E4M3N>::SMEM, s>>>(
+            maps.act, maps.w, maps.act_s, maps.w_s, p);
     else if (variant == V_SWAP64)
         gemm_tc_kernel<V_SWAP64><<<grid, Cfg<V_SWAP64>::THREADS, Cfg<V_SWAP64>::SMEM, s>>>(
             maps.act, maps.w, maps.act_s, maps.w_s, p);

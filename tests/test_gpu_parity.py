@@ -564,6 +564,9 @@ E4M3_SHAPES = [  # T, k, E, K, I
     (300, 1, 2, 256, 128),           # ~150 tokens per expert: three 64-token segments
     (5, 8, 64, 512, 128),            # decode-like
     (40, 2, 4, 384, 384),            # three k slices in both GEMMs (the second MMA issuer takes one)
+    # 16 or fewer rows per expert on average: 32-token tiles with four MMA warps
+    (90, 1, 6, 384, 256),            # steep bias: the first expert needs several 32-token tiles; 3 k slices
+    (64, 2, 16, 256, 384),           # GEMM 2 with three k slices
 ]
 
 

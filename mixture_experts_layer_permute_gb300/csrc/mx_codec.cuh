@@ -1,6 +1,7 @@
-// MXFP8 encoding helpers shared by the quantiser and the GEMM epilogues that
-// emit MXFP8 directly, so that every producer of E4M3 codes + E8M0 scales
-// makes the same decisions bit for bit.
+// MXFP8 helpers of the CUDA path: the encoding shared by the quantiser and the
+// GEMM epilogues that emit MXFP8 directly, so that every producer of E4M3
+// codes + E8M0 scales makes the same decisions bit for bit, and the decoding
+// of E4M3 weights to bf16 used by the tcgen05 kernels (end of this file).
 //
 // Scale code of a block from its maximum magnitude m, with integer arithmetic
 // on the fp32 bits (exact, no logarithm): writing m = f * 2^p with f in [1, 2),

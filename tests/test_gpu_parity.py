@@ -599,6 +599,38 @@ def test_gemm1_swiglu_e4m3(moe, impl, shape, w1_layout):
     assert_close(to_f64(h.cpu()[torch.from_numpy(rr).long()]), href, TOL_BF16, f"gemm1 e4m3 {impl}")
 
 
+@pytest.mark.parametrize("impl", ["swap_ab", "auto"])
+@pytest.mark.parametrize("maxT", [12, 48])
+def test_gemms_batched_layout_e4m3(moe, impl, maxT):
+    """MXFP8 weights on the batched (E, max_tokens, K) layout: max_tokens = 12 runs the 32-token tiles with four
+    MMA warps (16 or fewer rows per expert), 48 the 64-token tiles with two; full, ragged, empty and one-token
+    experts, GEMM 2 with the per-row weight."""
+    E, K, I = 5, 256, 256
+    w = wl.scaled(wl.tiny(), T=1, K=K, I=I, E=E, top_k=1, x_std=1.0, w_std=0.05, weight="mxfp8")
+    counts = torch.tensor([maxT, maxT - 1, maxT // 2 + 1, 0, 1], dtype=torch.int32)
+    x = wl._normal((E, maxT, K), 1.0, 17, "x", 0, "cpu", torch.bfloat16)
+    rw = torch.rand((E, maxT), generator=torch.Generator().manual_seed(maxT))
+    c1, s1, rc1, rs1 = _e4m3_weights(moe, wl.expert_weights(w, "W1", 8))
+    c2, s2, rc2, rs2 = _e4m3_weights(moe, wl.expert_weights(w, "W2", 8))
+    offs = torch.arange(E + 1, dtype=torch.int32) * maxT
+    kw = dict(layout=moe.MOE_LAYOUT_BATCHED, max_tokens=maxT, impl=_impl(moe, impl))
+    h = moe.moe_gemm1_swiglu(x.to(DEV).reshape(E * maxT, K), counts.to(DEV), offs.to(DEV), c1, I, w1_scale=s1, **kw)
+    y = moe.moe_gemm2(h, counts.to(DEV), offs.to(DEV), c2, E * maxT, w2_scale=s2,
+                      route_weights=rw.to(DEV).reshape(-1), **kw)
+    torch.cuda.synchronize()
+    hc, yc = h.cpu().reshape(E, maxT, I), y.cpu().reshape(E, maxT, K)
+    for e in range(E):
+        c = int(counts[e])
+        if c == 0:
+            continue
+        ids = np.full(c, e, dtype=np.int32)
+        href = oracle.expert_gate_up(wl.to_numpy(x[e, :c]), ids, rc1, w1_scale=rs1)
+        assert_close(to_f64(hc[e, :c]), href, TOL_BF16, f"batched e4m3 gemm1 expert {e}")
+        yref = oracle.expert_down(wl.to_numpy(hc[e, :c]), ids, rc2, w2_scale=rs2)
+        yref = yref * rw[e, :c].numpy().astype(np.float64)[:, None]
+        assert_close(to_f64(yc[e, :c]), yref, TOL_BF16, f"batched e4m3 gemm2 expert {e}")
+
+
 @pytest.mark.parametrize("impl", ["swap_ab", "auto", "simt"])
 @pytest.mark.parametrize("shape", E4M3_SHAPES)
 def test_gemm2_e4m3(moe, impl, shape):

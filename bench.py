@@ -124,14 +124,17 @@ class Instance:
             self.layer = m.MoELayer(w.T, w.K, w.I, w.E, w.top_k, act_dtype=self.x.dtype, block_m=w.block_m,
                                     act_quant=w.act_quant, fused_experts=fused, device=dev,
                                     impl=m.MOE_IMPL_AUTO if impl is None else impl)
-        # weights as the kernels stream them: row-major, or (fused decode plan, bf16) re-laid out once into the
-        # tile-contiguous layout by moe_tile_weights -- weight preparation, outside every timed region
+        # weights as the kernels stream them: row-major, or re-laid out once into the tile-contiguous layout by
+        # moe_tile_weights (bf16 on the fused decode launch and CTA-pair tiles; MXFP8 codes with an interleave-16
+        # W1 on swap-AB tiles) -- weight preparation, outside every timed region
         self.W1r, self.W2r, self.w1_layout = self.W1, self.W2, w.w1_layout
         self.forward()
         torch.cuda.synchronize()
-        if tiled and w.weight == "bf16" and (
+        codes_tileable = (w.weight == "mxfp8" and w.layout == "contiguous" and w.w1_layout == m.MOE_W1_INTERLEAVE16
+                          and impl in (None, m.MOE_IMPL_AUTO, m.MOE_IMPL_TCGEN05_SWAP_AB))
+        if tiled and (codes_tileable or (w.weight == "bf16" and (
                 (w.layout == "contiguous" and self.fused())
-                or (impl in (None, m.MOE_IMPL_AUTO, m.MOE_IMPL_TCGEN05_PAIR) and self._pair_plan())):
+                or (impl in (None, m.MOE_IMPL_AUTO, m.MOE_IMPL_TCGEN05_PAIR) and self._pair_plan())))):
             self._tile_weights()
             self.forward()
             torch.cuda.synchronize()
@@ -673,10 +676,14 @@ def run_configs(args, dev, stream, peaks, skip=None):
         flush = l2_flush_buffer([inst], dev)
         m = measure([inst], args, stream, 1, flush)
         roof = gemm_roofline([inst], m["g1_ms"], peaks, tensor_bound=(name == "prefill"))
+        tiled = inst.w1_layout == inst.m.MOE_W_TILED
+        roof["traffic"] = recorded_traffic(name, inst.fused(), tiled)
         sw = layer_sweep([inst], m, peaks)[0]
         out[name] = {"workload": describe(name, [w]), "value": round(inst.routes * args.steps / (m["ms_total"] / 1e3), 1),
                      "unit": UNIT, "ms_per_step": round(m["ms_total"] / args.steps, 4),
                      "routes_per_step": inst.routes, "experts_touched": inst.used_experts,
+                     "weights": ("tile-contiguous (moe_tile_weights, prepared once, untimed)" if tiled
+                                 else "as stored"),
                      "layer_roofline_ms": sw["roofline_ms"], "layer_frac": sw["layer_frac"],
                      "roofline": roof, "clocks": m["clocks"], "timing_stats": m["timing_stats"],
                      "gpu_launches": inst.launches() * args.steps, "l2": l2_note([inst]), "launch": m["mode"]}

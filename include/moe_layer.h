@@ -98,7 +98,7 @@ extern "C" {
                                          _interleave_gate_up_16 "After") */
 #define MOE_W_TILED 2                 /* tile-contiguous layout written by moe_tile_weights: W1 and W2 of
                                          moe_experts_fused, W1 of moe_gemm1_swiglu / W2 of moe_gemm2 on
-                                         CTA-pair tiles (bf16) */
+                                         CTA-pair tiles (bf16) or on swap-AB tiles (E4M3 codes) */
 
 /* ---- GEMM implementations ---- */
 #define MOE_IMPL_AUTO 0               /* swap-AB tiles when routes/expert are few, else CTA-pair tiles
@@ -254,8 +254,9 @@ MOE_API int moe_permute_align_static(const int32_t* topk_ids, int64_t T, int top
  *                 E4M3 activations need E4M3 weights and run on block-scaled tcgen05
  *                 swap-AB tiles (K % 128 == 0, 2I % 128 == 0) or MOE_IMPL_SIMT.
  *   w1            (E, 2I, K) of w_dtype (F32, BF16 or E4M3); rows per w1_layout: MOE_W1_GATE_UP,
- *                 MOE_W1_INTERLEAVE16, or MOE_W_TILED (bf16 weights from moe_tile_weights, which = 1;
- *                 CTA-pair tiles only: MOE_IMPL_AUTO or MOE_IMPL_TCGEN05_PAIR, else
+ *                 MOE_W1_INTERLEAVE16, or MOE_W_TILED (from moe_tile_weights, which = 1: bf16
+ *                 weights on CTA-pair tiles, MOE_IMPL_AUTO or MOE_IMPL_TCGEN05_PAIR; E4M3 codes on
+ *                 swap-AB tiles, MOE_IMPL_AUTO or MOE_IMPL_TCGEN05_SWAP_AB; else
  *                 MOE_ERR_UNSUPPORTED)
  *   w1_scale      (E, 2I, K/32) E8M0 bytes when w_dtype == MOE_E4M3, else NULL
  *   h             same row indexing as `a`, (rows, I) of h_dtype (F32, BF16, or E4M3 codes);
@@ -291,8 +292,9 @@ MOE_API int moe_gemm1_swiglu(const void* a, int a_dtype, const uint8_t* a_scale,
  *                 As for GEMM 1, E4M3 h needs E4M3 weights (I % 128 == 0, K % 128 == 0
  *                 on tcgen05 tiles).
  *   w2            (E, K, I) of w_dtype; w2_scale (E, K, I/32) E8M0 for E4M3, else NULL
- *   w2_layout     MOE_W1_GATE_UP (row-major, as above) or MOE_W_TILED (bf16 W2 from
- *                 moe_tile_weights, which = 2; CTA-pair tiles only, as for moe_gemm1_swiglu)
+ *   w2_layout     MOE_W1_GATE_UP (row-major, as above) or MOE_W_TILED (W2 from
+ *                 moe_tile_weights, which = 2: bf16 on CTA-pair tiles, E4M3 codes on swap-AB
+ *                 tiles, as for moe_gemm1_swiglu)
  *   contiguous:   row s goes to y[row_route[s]] (rows with row_route -1 are skipped);
  *                 y is (y_rows, K) with y_rows = T*top_k; route_weights, if not NULL,
  *                 is (T*top_k) fp32 indexed by route.
@@ -334,22 +336,25 @@ MOE_API int moe_gemm2(const void* h, int h_dtype, const uint8_t* h_scale, int la
 MOE_API size_t moe_experts_fused_workspace_size(int64_t rows_cap, int E);
 
 /*
- * moe_tile_weights -- offline re-layout of bf16 expert weights into the
- * tile-contiguous layout that moe_experts_fused streams with MOE_W_TILED (a
+ * moe_tile_weights -- offline re-layout of expert weights (bf16, or E4M3 codes) into the
+ * tile-contiguous layout that the GEMMs stream with MOE_W_TILED (a
  * weight-preparation step, like the gate/up interleave of the "Cake MegaMoE
  * EP16" FlashInfer PR 5148 analysis, section 2, or the MXFP8 quantisation):
- * every 128-row x 64-column block that one pipeline stage loads is stored as
- * one contiguous 16 KB run, so each stage reads whole DRAM pages instead of
- * 128 pieces of 128 bytes one weight row apart.
- *     out[e][b][c][r][j] = w[e][row(b, r)][64*c + j]
- *     (b < rows/128 row blocks, c < cols/64 column blocks, r < 128, j < 64)
+ * every 128-row x 128-byte block that one pipeline stage loads (64 bf16 or 128
+ * E4M3 codes per row) is stored as one contiguous 16 KB run, so each stage
+ * reads whole DRAM pages instead of 128 pieces of 128 bytes one weight row apart.
+ *     out[e][b][c][r][j] = w[e][row(b, r)][n*c + j]
+ *     (n = 64 for bf16, 128 for E4M3; b < rows/128, c < cols/n, r < 128, j < n)
  *   which = 1: w is W1 (E, 2I, K) in layout w1_layout; rows = 2I, cols = K; each
  *              block holds 64 gate/up units as [16 gate rows, the 16 matching
  *              up rows] x 4: row(b, r) = unit u = 64b + 16(r/32) + r%16, its gate
  *              row (r%32 < 16) or up row (r%32 >= 16) -- for MOE_W1_GATE_UP
  *              rows u and I + u, for MOE_W1_INTERLEAVE16 row 128b + r.
  *   which = 2: w is W2 (E, K, I); rows = K, cols = I; row(b, r) = 128b + r.
- *   w_dtype    MOE_BF16.  rows % 128 == 0 and cols % 64 == 0.
+ *   w_dtype    MOE_BF16 (cols % 64 == 0), or MOE_E4M3 codes (cols % 128 == 0; W1
+ *              only in MOE_W1_INTERLEAVE16, so that the rows keep their stored order
+ *              and the E8M0 scale arrays are used as they are; MOE_ERR_UNSUPPORTED
+ *              for [gate; up] codes).  rows % 128 == 0.
  *   w, out     device, 16-byte aligned, E*rows*cols elements each, not overlapping.
  */
 MOE_API int moe_tile_weights(const void* w, int w_dtype, int which, int w1_layout, int E, int64_t rows,

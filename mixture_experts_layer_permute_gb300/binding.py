@@ -185,13 +185,13 @@ def moe_permute_align(topk_ids, E, layout=MOE_LAYOUT_CONTIGUOUS, block_m=1, max_
 
 
 def moe_tile_weights(w, which, w1_layout=MOE_W1_GATE_UP, out=None, stream=None):
-    """Offline re-layout of bf16 W1 (which=1, (E, 2I, K) in w1_layout) or W2 (which=2, (E, K, I)) into the
-    tile-contiguous layout moe_experts_fused reads with w1_layout=MOE_W_TILED.  Returns a tensor of w's shape
-    holding the tiled bytes."""
+    """Offline re-layout of W1 (which=1, (E, 2I, K) in w1_layout) or W2 (which=2, (E, K, I)) into the
+    tile-contiguous layout the GEMMs read with MOE_W_TILED: bf16 weights, or E4M3 codes (uint8; W1 in the
+    interleave-16 layout, the E8M0 scales unchanged).  Returns a tensor of w's shape holding the tiled bytes."""
     E, rows, cols = w.shape
     if out is None:
         out = torch.empty_like(w)
-    _check(load().moe_tile_weights(_ptr(w), dtype_code(w), which, w1_layout, E, rows, cols, _ptr(out),
+    _check(load().moe_tile_weights(_ptr(w), dtype_code(w, e4m3=True), which, w1_layout, E, rows, cols, _ptr(out),
                                    _stream(stream)))
     return out
 

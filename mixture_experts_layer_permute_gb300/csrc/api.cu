@@ -264,8 +264,18 @@ int run_gemm_mx(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
 
 int run_gemm(const GemmArgs& g, int impl, cudaStream_t s, const char* name) {
     if ((g.layout == MOE_LAYOUT_CONTIGUOUS ? g.rows_cap : int64_t(g.E) * g.max_tokens) == 0) return MOE_OK;
+    if (g.w1_layout == MOE_W_TILED && g.w_dtype == MOE_E4M3) {
+        // tile-contiguous E4M3 codes are read by the swap-AB tiles: bf16 activations decode them into TMEM, E4M3
+        // activations take the block-scaled MMA
+        MOE_REQUIRE(impl == MOE_IMPL_AUTO || impl == MOE_IMPL_TCGEN05_SWAP_AB, MOE_ERR_UNSUPPORTED,
+                    std::string(name) + ": tile-contiguous E4M3 codes run on swap-AB tiles (MOE_IMPL_TCGEN05_SWAP_AB)");
+        MOE_REQUIRE(g.a_dtype == MOE_BF16 || g.a_dtype == MOE_E4M3, MOE_ERR_UNSUPPORTED,
+                    std::string(name) + ": tile-contiguous E4M3 codes need bf16 or E4M3 activations");
+        MOE_REQUIRE(device_cc() >= 100, MOE_ERR_UNSUPPORTED, std::string(name) + ": tcgen05 needs an sm_100+ device");
+        return g.a_dtype == MOE_E4M3 ? launch_gemm_mx(g, s) : launch_gemm_tc(g, TC_SWAP, s);
+    }
     if (g.w1_layout == MOE_W_TILED) {
-        // tile-contiguous weights (moe_tile_weights) are read by the CTA-pair tiles only
+        // tile-contiguous bf16 weights (moe_tile_weights) are read by the CTA-pair tiles
         MOE_REQUIRE(impl == MOE_IMPL_AUTO || impl == MOE_IMPL_TCGEN05_PAIR, MOE_ERR_UNSUPPORTED,
                     std::string(name) + ": tile-contiguous weights run on CTA-pair tiles (MOE_IMPL_TCGEN05_PAIR) only");
         MOE_REQUIRE(g.a_dtype == MOE_BF16 && g.w_dtype == MOE_BF16, MOE_ERR_UNSUPPORTED,
@@ -449,20 +459,28 @@ int moe_experts_fused(const void* a, int a_dtype, const int32_t* expert_counts, 
 int moe_tile_weights(const void* w, int w_dtype, int which, int w1_layout, int E, int64_t rows, int64_t cols,
                      void* out, void* stream) {
     g_last_error.clear();
-    MOE_REQUIRE(w_dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_tile_weights: bf16 weights only");
+    MOE_REQUIRE(w_dtype == MOE_BF16 || w_dtype == MOE_E4M3, MOE_ERR_UNSUPPORTED,
+                "moe_tile_weights: bf16 weights or E4M3 codes only");
     MOE_REQUIRE(which == 1 || which == 2, MOE_ERR_INVALID_ARG, "moe_tile_weights: which must be 1 (W1) or 2 (W2)");
     MOE_REQUIRE(which == 2 || w1_layout == MOE_W1_GATE_UP || w1_layout == MOE_W1_INTERLEAVE16, MOE_ERR_INVALID_ARG,
                 "moe_tile_weights: unknown w1_layout");
+    const bool codes = w_dtype == MOE_E4M3;   // 1-byte elements: a 128 x 128-code block is 16 KB
+    MOE_REQUIRE(!codes || which == 2 || w1_layout == MOE_W1_INTERLEAVE16, MOE_ERR_UNSUPPORTED,
+                "moe_tile_weights: E4M3 W1 codes must be in the interleave-16 layout (their E8M0 scales keep the "
+                "stored row order)");
     MOE_REQUIRE(E >= 1 && rows > 0 && cols > 0, MOE_ERR_INVALID_ARG, "moe_tile_weights: bad sizes");
-    MOE_REQUIRE(rows % 128 == 0 && cols % 64 == 0, MOE_ERR_ALIGNMENT,
-                "moe_tile_weights: rows % 128 and cols % 64 must be 0");
+    MOE_REQUIRE(rows % 128 == 0 && cols % (codes ? 128 : 64) == 0, MOE_ERR_ALIGNMENT,
+                codes ? "moe_tile_weights: rows % 128 and cols % 128 must be 0"
+                      : "moe_tile_weights: rows % 128 and cols % 64 must be 0");
     MOE_REQUIRE(w && out, MOE_ERR_INVALID_ARG, "moe_tile_weights: null pointer");
     MOE_REQUIRE(aligned16(w) && aligned16(out), MOE_ERR_ALIGNMENT, "moe_tile_weights: w and out must be 16-byte aligned");
-    const int64_t bytes = int64_t(E) * rows * cols * 2;
+    const int64_t bytes = int64_t(E) * rows * cols * (codes ? 1 : 2);
     const uintptr_t a = reinterpret_cast<uintptr_t>(w), b = reinterpret_cast<uintptr_t>(out);
     MOE_REQUIRE(a + uintptr_t(bytes) <= b || b + uintptr_t(bytes) <= a, MOE_ERR_INVALID_ARG,
                 "moe_tile_weights: w and out overlap");
-    return launch_status(launch_tile_weights(w, which, w1_layout, E, rows, cols, out, as_stream(stream)),
+    // E4M3 codes move as pairs: the same 128-byte row pieces as 64 bf16 columns
+    return launch_status(launch_tile_weights(w, which, w1_layout, E, rows, codes ? cols / 2 : cols, out,
+                                             as_stream(stream)),
                          "moe_tile_weights");
 }
 

@@ -88,7 +88,8 @@ struct MxParams {
     int64_t rows_cap;
     int nks;             // k slices per tile
     int nt;              // weight blocks (128 rows) per expert
-    int w_mode;          // weights map: 0 = 3-D (k, rows, E), 1 = 5-D gate/up interleaving view
+    int w_mode;          // weights map: 0 = 3-D (k, rows, E), 1 = 5-D gate/up interleaving view,
+                         // 2 = 4-D tile-contiguous codes (128, 128, slices, E x 128-row blocks)
     int64_t I, K;
     const int32_t* counts;
     const int32_t* offsets;
@@ -211,6 +212,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int row_w = tl.nb * BM;
                     if (p.w_mode == 1)
                         ptx::tma_load_5d(sa, &tm_w, &ctrl.full[s], k0, 0, 0, row_w / 32, tl.e, pol_stream);
+                    else if (p.w_mode == 2)   // one contiguous 16 KB block per slice
+                        ptx::tma_load_4d(sa, &tm_w, &ctrl.full[s], 0, 0, kb, tl.e * p.nt + tl.nb, pol_stream);
                     else
                         ptx::tma_load_3d(sa, &tm_w, &ctrl.full[s], k0, row_w, tl.e, pol_stream);
                     for (int b = 0; b < nbox; ++b)
@@ -507,6 +510,13 @@ int build_maps(const GemmArgs& g, int64_t kdim, int64_t wrows, int w_mode, MapPa
         int rc = make_byte_map(&mp->act, g.a, 2, dims, str, box, "MXFP8 activation codes");
         if (rc) return rc;
     }
+    if (w_mode == 2) {
+        // tile-contiguous codes (moe_tile_weights): [E x 128-row blocks][slices][128 rows][128 codes]
+        cuuint64_t dims[4] = {cuuint64_t(KS), 128, cuuint64_t(kdim / KS), cuuint64_t(g.E * (wrows / 128))};
+        cuuint64_t str[3] = {cuuint64_t(KS), cuuint64_t(128 * KS), cuuint64_t(kdim / KS * 128 * KS)};
+        cuuint32_t box[4] = {KS, 128, 1, 1};
+        return make_byte_map(&mp->w, g.w, 4, dims, str, box, g.gemm == 1 ? "W1 codes (tiled)" : "W2 codes (tiled)");
+    }
     if (w_mode == 1) {
         // W1[e] (2I, K) seen as (K, 16, 2, I/16): row = half*I + 16*blk + q
         cuuint64_t dims[5] = {cuuint64_t(g.K), 16, 2, cuuint64_t(g.I / 16), cuuint64_t(g.E)};
@@ -555,7 +565,7 @@ int launch_gemm_mx(const GemmArgs& g, cudaStream_t s) {
     if (g.rows_cap >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "block-scaled MXFP8 path: too many rows");
     if (g.rows_cap == 0) return MOE_OK;
 
-    const int w_mode = (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0;
+    const int w_mode = g.w1_layout == MOE_W_TILED ? 2 : ((g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0);
     int dev_id = 0;
     cudaGetDevice(&dev_id);
     const MapKey key{dev_id, g.a, g.w, kdim, g.rows_cap, wrows, g.I, g.K, g.E, g.gemm, w_mode};

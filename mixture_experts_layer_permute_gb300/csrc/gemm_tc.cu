@@ -917,11 +917,13 @@ int build_maps(const GemmArgs& g, bool swap, bool w8, int64_t kdim, int64_t wrow
     const int64_t es = w8 ? 1 : 2;
     const cuuint32_t kbox = cuuint32_t(w8 ? BK * Cfg<V_E4M3>::KSUB : BK);
     if (g.w1_layout == MOE_W_TILED) {
-        // tile-contiguous weights (moe_tile_weights): [E x 128-row blocks][k-blocks][128 rows][64 columns]
-        cuuint64_t dims[4] = {cuuint64_t(BK), 128, cuuint64_t(kdim / BK), cuuint64_t(g.E * (wrows / 128))};
-        cuuint64_t str[3] = {cuuint64_t(BK * 2), cuuint64_t(128 * BK * 2), cuuint64_t(kdim / BK * 128 * BK * 2)};
-        cuuint32_t box[4] = {BK, 128, 1, 1};
-        return make_map(w, g.w, 4, dims, str, box, g.gemm == 1 ? "W1 (tiled)" : "W2 (tiled)");
+        // tile-contiguous weights (moe_tile_weights): [E x 128-row blocks][k-blocks][128 rows][128 bytes] (64 bf16
+        // or 128 E4M3 codes per row piece, one 16 KB block per stage)
+        const cuuint64_t kb = cuuint64_t(128 / es);
+        cuuint64_t dims[4] = {kb, 128, cuuint64_t(kdim) / kb, cuuint64_t(g.E * (wrows / 128))};
+        cuuint64_t str[3] = {128, 128 * 128, cuuint64_t(kdim) / kb * 128 * 128};
+        cuuint32_t box[4] = {cuuint32_t(kb), 128, 1, 1};
+        return make_map(w, g.w, 4, dims, str, box, g.gemm == 1 ? "W1 (tiled)" : "W2 (tiled)", w8);
     }
     if (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) {
         // view W1[e] (2I, K) as (K, 16, 2, I/16): row = half*I + 16*blk + q
@@ -990,7 +992,7 @@ int launch_gemm_tc(const GemmArgs& g, int mode, cudaStream_t s) {
     if (g.rows_cap >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "tcgen05 path: too many rows");
     if (g.rows_cap == 0) return MOE_OK;   // no rows, nothing to do
 
-    const int w_mode = (g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0;
+    const int w_mode = g.w1_layout == MOE_W_TILED ? 2 : ((g.gemm == 1 && g.w1_layout == MOE_W1_GATE_UP) ? 1 : 0);
     MapSet maps;
     int rc0 = cached_maps(g, mode, w8, kdim, wrows, w_mode, &maps);
     if (rc0) return rc0;

@@ -131,7 +131,8 @@ class MoELayer:
         adt = B.dtype_code(x)
         wdt = B.dtype_code(w1, e4m3=w1_scale is not None)
         I, K, E, T, k = self.I, self.K, self.E, self.T, self.top_k
-        # MOE_W_TILED: W1 and W2 both from moe_tile_weights (the fused decode launch or CTA-pair tiles)
+        # MOE_W_TILED: W1 and W2 both from moe_tile_weights (the fused decode launch, CTA-pair tiles, or MXFP8
+        # codes on swap-AB tiles)
         w2_layout = B.MOE_W_TILED if w1_layout == B.MOE_W_TILED else B.MOE_W1_GATE_UP
         calls = []
         if self.layout == B.MOE_LAYOUT_BATCHED and T > 0:
@@ -250,7 +251,8 @@ class MoELayer:
         (E, max_tokens).
         ``w1_layout``: MOE_W1_GATE_UP or MOE_W1_INTERLEAVE16 for row-major W1, or MOE_W_TILED when W1 and W2 come
         from moe_tile_weights (bf16: the fused decode launch, or CTA-pair tiles where there are many rows per
-        expert; the library refuses other plans with MOE_ERR_UNSUPPORTED).
+        expert; MXFP8 codes: the swap-AB tiles, scales as stored; the library refuses other plans with
+        MOE_ERR_UNSUPPORTED).
         ``gemm1_events`` = (start, end) CUDA events recorded around the gate/up GEMM.
         """
         s = stream if stream is not None else torch.cuda.current_stream()

@@ -131,6 +131,11 @@ def test_tile_weights_validation(lib):
     assert lib.moe_tile_weights(fake, 1, 2, 0, 2, 256, 128, ctypes.c_void_p(0x100100), None) == 1   # overlap
     assert lib.moe_tile_weights(None, 1, 2, 0, 2, 256, 128, other, None) == 1      # null
     assert lib.moe_tile_weights(ctypes.c_void_p(0x100008), 1, 2, 0, 2, 256, 128, other, None) == 3  # alignment
+    # E4M3 codes: W1 only in the interleave-16 layout (the scales keep the stored row order), 128-code columns
+    assert lib.moe_tile_weights(fake, 2, 1, 0, 2, 256, 128, other, None) == 2      # [gate; up] codes
+    assert "interleave-16" in lib_error()
+    assert lib.moe_tile_weights(fake, 2, 2, 0, 2, 256, 64, other, None) == 3       # cols % 128
+    assert lib.moe_tile_weights(fake, 2, 1, 1, 2, 256, 192, other, None) == 3     # cols % 128 (W1)
 
 
 def test_gemm_validation(lib):

@@ -704,6 +704,52 @@ def test_gemm2_mxf8(moe, impl, shape):
     assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 mxf8 {impl}")
 
 
+@pytest.mark.parametrize("act", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("shape", [(5, 8, 64, 512, 128), (96, 4, 8, 512, 256), (64, 2, 16, 384, 384)])
+@pytest.mark.parametrize("impl", ["swap_ab", "auto"])
+def test_e4m3_tiled_codes_bit_identical(moe, act, shape, impl):
+    """E4M3 codes re-laid out by moe_tile_weights (interleave-16 W1, W2; scales as stored) give the same h and y,
+    bit for bit, as the codes as stored: bf16 activations on both E4M3 tile forms (the first and last shape run
+    the 32-token tiles, the second the 64-token ones), MXFP8 activations on the block-scaled tiles."""
+    T, k, E, K, I = shape
+    w, x, ids, weights = _routed(T, k, E, K, seed=T + 9 * E)
+    W1 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8"), "W1", 12)
+    W2 = wl.expert_weights(wl.scaled(w, I=I, weight="mxfp8"), "W2", 12)
+    c1, s1 = moe.mxfp8_quantize_block32(W1.to(DEV))
+    c2, s2 = moe.mxfp8_quantize_block32(W2.to(DEV))
+    c1t = moe.moe_tile_weights(c1, 1, moe.MOE_W1_INTERLEAVE16)
+    c2t = moe.moe_tile_weights(c2, 2)
+    assert not torch.equal(c1t, c1)                            # the layout did change
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    R = T * k
+    wt = torch.from_numpy(weights).to(DEV).reshape(-1)
+    a, a_scale = res["x_out"], None
+    if act == "mxfp8":
+        a, a_scale = moe.mxfp8_quantize_block32(a)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = []
+    for w1x, w2x, l1, l2 in ((c1, c2, moe.MOE_W1_INTERLEAVE16, moe.MOE_W1_GATE_UP),
+                             (c1t, c2t, moe.MOE_W_TILED, moe.MOE_W_TILED)):
+        h = moe.moe_gemm1_swiglu(a, res["counts"], res["offsets"], w1x, I, w1_scale=s1, a_scale=a_scale,
+                                 w1_layout=l1, impl=_impl(moe, impl), err_word=err)
+        h2, h2s = (h, None) if act == "bf16" else moe.mxfp8_quantize_block32(h)
+        y = moe.moe_gemm2(h2, res["counts"], res["offsets"], w2x, R, w2_scale=s2, h_scale=h2s,
+                          row_route=res["row_route"], route_weights=wt, w2_layout=l2, impl=_impl(moe, impl),
+                          err_word=err)
+        outs.append((h, y))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    (h1, y1), (h2_, y2) = outs
+    rr = res["route_row"].view(-1).long()
+    assert torch.equal(h1[rr].view(torch.int16), h2_[rr].view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    if act == "bf16":   # and the tiled result against the oracle
+        rc1, rs1 = oracle.mxfp8_quantize(W1.numpy())
+        href = oracle.expert_gate_up(wl.to_numpy(x)[np.arange(R) // k], ids.reshape(-1), rc1, w1_scale=rs1,
+                                     w1_layout=moe.MOE_W1_INTERLEAVE16)
+        assert_close(to_f64(h2_.cpu()[rr.cpu()]), href, TOL_BF16, "gemm1 e4m3 tiled codes")
+
+
 @pytest.mark.parametrize("impl", ["swap_ab", "simt"])
 @pytest.mark.parametrize("shape", MX_SHAPES)
 @pytest.mark.parametrize("w1_layout", [0, 1])

@@ -585,12 +585,15 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
         const bool vec_scales = (p.nsb & 15) == 0;       // 16-byte aligned scale rows (4 slices per 16 B)
         const uint64_t pol_keep = ptx::policy_evict_last();   // token rows are read by every weight block
         uint32_t it = 0;
+        // this group's slices are it = grp, grp + 4, ...: their code stage (it % STAGES) and the parities of the
+        // code ring and of the A slot advance incrementally
+        int s_own = grp;
+        uint32_t ph_own = 0, pha_own = 0, it_next = uint32_t(grp);
         for (int32_t k_ = 0, t = blockIdx.x; t < total && !ctrl.abort; t = nth_tile(p, ++k_)) {
             const Tile tl = decode_tile(tab, p, t);
             const uint8_t* srow = p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb;
             bool ok = true;
-            for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-                if (int(it & 3) != grp) continue;   // another group's stage
+            for (int kb = int(it_next - it); kb < p.nkb; kb += 4) {
                 uint32_t quad;                      // this row's four scale bytes of the slice
                 if (vec_scales) {
                     quad = __ldg(reinterpret_cast<const uint32_t*>(srow + 4 * kb));
@@ -599,8 +602,15 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                     for (int b = 0; b < 4; ++b) quad |= uint32_t(__ldg(srow + 4 * kb + b)) << (8 * b);
                 }
                 if (kb + 16 < p.nkb) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + 4 * (kb + 16)));
-                const int s = it % STAGES, a = grp;
-                const uint32_t ph = (it / STAGES) & 1, pha = (it / Cfg<V>::A_SLOTS) & 1;
+                const int s = s_own, a = grp;
+                const uint32_t ph = ph_own, pha = pha_own;
+                s_own += 4;
+                if (s_own >= STAGES) {
+                    s_own -= STAGES;
+                    ph_own ^= 1;
+                }
+                pha_own ^= 1;
+                it_next += 4;
                 if (!wait_bar(&ctrl.a_empty[a], pha ^ 1, ctrl, p.err_word)) { ok = false; break; }
                 ptx::tc_fence_after();   // the MMA that last read this A slot has completed
                 {
@@ -662,6 +672,7 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                     ptx::mbar_arrive(&ctrl.conv[a]);    // the A slot and its tokens are ready for the MMA
                 }
             }
+            it += uint32_t(p.nkb);
             if (!ok) break;
         }
     } else {

@@ -524,27 +524,33 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
             const uint32_t d_tmem = tmem_base + uint32_t((buf * Cfg<V>::ISSUERS + j) * Cfg<V>::ACC_STRIDE);
             const int nkb = tl.gemm == 2 && p.fused ? p.nkb2 : p.nkb;
             bool ok = true;
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
-                if constexpr (W8) {
-                    if ((kb & 1) != par) continue;   // the other parity's slice
-                    // A slot a: decoded weights in TMEM, tokens in the slot's smem tile
-                    const int a = it % Cfg<V>::A_SLOTS;
-                    const uint32_t ph = (it / Cfg<V>::A_SLOTS) & 1;
+            if constexpr (W8) {
+                // this issuer's slices of the tile: kb = par, par + 2, ...; A slot and parity of slice it0 + kb
+                const uint32_t it0 = it;
+                for (int kb = par; kb < nkb; kb += 2) {
+                    const uint32_t itk = it0 + uint32_t(kb);
+                    const int a = int(itk & 3u);
+                    const uint32_t ph = (itk >> 2) & 1u;
                     if (!__all_sync(0xffffffffu, wait_bar(&ctrl.conv[a], ph, ctrl, p.err_word))) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t sb = ptx::smem_addr(smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT);
+                    // tokens in the slot's smem tile (descriptor start addresses step by 16 bytes), decoded weights in
+                    // the slot's TMEM columns
+                    const uint64_t bd0 = ptx::smem_desc_sw128(ptx::smem_addr(smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT));
+                    const uint32_t a0 = tmem_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS);
                     constexpr int KK = Cfg<V>::KSUB * BK / UMMA_K / Cfg<V>::PER_SLICE;   // MMAs per issuer
 #pragma unroll
                     for (int k2 = 0; k2 < KK; ++k2) {
                         const int kk = part * KK + k2;   // k step of the slice
                         const int sub = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
-                        const uint64_t bd = ptx::smem_desc_sw128(sb + sub * Cfg<V>::B_SUB + kq * UMMA_K * 2);
+                        const uint64_t bd = bd0 + uint64_t((sub * Cfg<V>::B_SUB + kq * UMMA_K * 2) >> 4);
                         // 16 bf16 of a row = 8 TMEM columns per k step
-                        const uint32_t a_tmem = tmem_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS + kk * 8);
-                        ptx::mma_f16_tmem_a_by(issue, d_tmem, a_tmem, bd, idesc, kb != par || k2 != 0);
+                        ptx::mma_f16_tmem_a_by(issue, d_tmem, a0 + uint32_t(kk * 8), bd, idesc, kb != par || k2 != 0);
                     }
                     ptx::mma_commit_by(issue, &ctrl.a_empty[a]);
-                } else {
+                }
+                it += uint32_t(nkb);
+            } else {
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!__all_sync(0xffffffffu, wait_bar(&ctrl.full[s], ph, ctrl, p.err_word))) { ok = false; break; }

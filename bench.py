@@ -343,9 +343,16 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 
 def kernel_source_hash(name="gemm_tc.cu"):
+    """Hash of a kernel source's code: comments, trailing blanks and empty lines are left out, so that a record
+    taken on a kernel stays valid across edits of its comments only."""
+    import re
     p = os.path.join(ROOT, "mixture_experts_layer_permute_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(p) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)            # block comments
+    text = re.sub(r"//[^\n]*", "", text)                          # line comments (none sit inside strings here)
+    code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def recorded_traffic(workload, fused=False, tiled=False):

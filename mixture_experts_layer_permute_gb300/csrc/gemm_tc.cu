@@ -4,9 +4,11 @@
 //   warp 0      TMA producer: one thread streams 64-wide k-blocks of the A and
 //               B tiles into a 4-stage shared-memory ring (128-byte swizzle),
 //               completing a "full" mbarrier per stage.
-//   warp 1      MMA issuer: lane 0 issues tcgen05.mma (kind::f16, bf16 in,
-//               fp32 accumulate) into one of two TMEM accumulators and frees
-//               each stage with tcgen05.commit on its "empty" mbarrier.
+//   warp 1      MMA issuer: the whole warp runs the issue loop (warp-uniform
+//               addresses and descriptors) and lane 0 issues tcgen05.mma
+//               (kind::f16, bf16 in, fp32 accumulate) into one of two TMEM
+//               accumulators and frees each stage with tcgen05.commit on its
+//               "empty" mbarrier.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
 //               32*(w%4)...), apply SiLU-and-mul (GEMM 1) or route weight +
 //               scatter to the (token, slot) row (GEMM 2), store to global.
@@ -47,9 +49,14 @@
 //   Tokens per tile are capped at 64.  Two warps issue the MMAs, the even and
 //   the odd k slices of a tile, each into its own accumulator, and the
 //   epilogue adds the two: with the converter warps competing for issue slots
-//   one issuing warp sustains only about one M=128, K=16 MMA per 65-100 ns
+//   one issuing warp sustains only about one M=128, K=16 MMA per 65-120 ns
 //   whatever N is (measured on GB300), which for 1-byte weights (128 x 16
-//   bytes per MMA) is at or below the HBM rate; two warps double it.
+//   bytes per MMA) is at or below the HBM rate; two warps double it.  When the
+//   routed rows average 16 or fewer per expert, tiles hold up to 32 tokens and
+//   four warps issue, two per slice parity, each half of a slice's MMAs (the
+//   narrower accumulators leave TMEM room for them).  Every instruction the
+//   converter and MMA warps save is an issue slot for the others, so both walk
+//   only their own slices, with stage indices and parities kept incrementally.
 //
 // Wide tiles (bf16, batched layout): 256 token rows x 256 weight rows as two
 // 128-row MMA halves that share each B stage, so an expert of up to 256 rows

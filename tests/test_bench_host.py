@@ -19,16 +19,25 @@ def test_decode_traffic_record_matches_its_plan_only():
     assert bench.recorded_traffic("prefill", fused=False, tiled=False) is None
 
 
-def test_traffic_record_dropped_when_the_kernel_source_changes(tmp_path, monkeypatch):
-    # a copy of the repository layout whose gemm_tc.cu differs by one byte
+def _copy_with_gemm_tc(tmp_path, monkeypatch, extra):
+    # a copy of the repository layout whose gemm_tc.cu has `extra` appended
     src = os.path.join(ROOT, "mixture_experts_layer_permute_gb300", "csrc", "gemm_tc.cu")
     csrc = tmp_path / "mixture_experts_layer_permute_gb300" / "csrc"
     csrc.mkdir(parents=True)
     with open(src, "rb") as f:
-        (csrc / "gemm_tc.cu").write_bytes(f.read() + b"\n")
+        (csrc / "gemm_tc.cu").write_bytes(f.read() + extra)
     shutil.copytree(os.path.join(ROOT, "profiles"), tmp_path / "profiles")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+
+
+def test_traffic_record_dropped_when_the_kernel_code_changes(tmp_path, monkeypatch):
+    _copy_with_gemm_tc(tmp_path, monkeypatch, b"static int moe_extra_symbol;\n")
     assert bench.recorded_traffic("decode", fused=True, tiled=True) is None
+
+
+def test_traffic_record_kept_across_comment_edits(tmp_path, monkeypatch):
+    _copy_with_gemm_tc(tmp_path, monkeypatch, b"\n// a remark\n/* and a block\n   comment */\n\n")
+    assert bench.recorded_traffic("decode", fused=True, tiled=True) is not None
 
 
 def test_describe_names_the_workload():

@@ -368,6 +368,41 @@ MOE_DEVICE void store_y_chunk(const TcParams& p, const uint32_t (&v)[32], int64_
     }
 }
 
+// E4M3 converter, one weight row of a slice: its 128 codes (at `row`, landed 128-byte swizzled: 16-byte chunk c
+// of row r at chunk c ^ (r % 8)) times the four block scales in `quad` (block b in byte b) -> 64 bf16x2 words
+// in TMEM columns tmem .. tmem + 63 of this thread's lane.  BIG: a scale code of the warp is above 134, so a
+// block may need the second multiply by 2^120; otherwise the four factors come from the scale word at once.
+template <bool BIG>
+MOE_DEVICE void decode_row_slice(const uint8_t* row, int r, uint32_t quad, uint32_t tmem) {
+    const uint32_t q120 = quad + 0x78787878u;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t o[32];
+#pragma unroll
+        for (int b2 = 0; b2 < 2; ++b2) {
+            const int b = 2 * half + b2;     // scale block of the slice
+            bool second = false;             // the factor 2^120 still to apply (large scales)
+            const uint32_t f1 = BIG ? mx_e4m3_factor((quad >> (8 * b)) & 0xFFu, second) : mx_e4m3_factor_small(q120, b);
+            const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * b) ^ (r & 7)) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * b + 1) ^ (r & 7)) << 4));
+            uint32_t* ob = o + 16 * b2;
+            dequant4(v0.x, f1, ob[0], ob[1]);
+            dequant4(v0.y, f1, ob[2], ob[3]);
+            dequant4(v0.z, f1, ob[4], ob[5]);
+            dequant4(v0.w, f1, ob[6], ob[7]);
+            dequant4(v1.x, f1, ob[8], ob[9]);
+            dequant4(v1.y, f1, ob[10], ob[11]);
+            dequant4(v1.z, f1, ob[12], ob[13]);
+            dequant4(v1.w, f1, ob[14], ob[15]);
+            if (BIG && second) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], kBf16x2Pow2_120);
+            }
+        }
+        ptx::tmem_st_32x32b_x32(tmem + uint32_t(half * 32), o);
+    }
+}
+
 template <int V>
 __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
@@ -605,6 +640,13 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
         for (int32_t k_ = 0, t = blockIdx.x; t < total && !ctrl.abort; t = nth_tile(p, ++k_)) {
             const Tile tl = decode_tile(tab, p, t);
             const uint8_t* srow = p.w_scale + (int64_t(tl.e) * p.wrows + tile_weight_row(p, tl.nb, r)) * p.nsb;
+            // this thread's 16-byte token chunks of a slice: column chunk r % 8 of k-block half (r / 8) % 2, rows
+            // n = r / 16 + 8j of the tile (the slot's chunks in order, 128 threads apart), so only the row and
+            // the slice's k offset change from chunk to chunk
+            const int n0 = r >> 4, tsub = (r >> 3) & 1, tcc = r & 7;
+            const int nrow16 = (tl.rows + TOK_BOX - 1) / TOK_BOX * TOK_BOX;   // rows past tl.rows are zero-filled
+            const uint16_t* tok0 = p.act + tl.row0 * p.act_ld + tsub * BK + tcc * 8;   // tile row 0
+            const uint32_t tok_dst = uint32_t(tsub * Cfg<V>::B_SUB + n0 * (BK * 2) + ((tcc ^ (n0 & 7)) << 4));
             bool ok = true;
             for (int kb = int(it_next - it); kb < p.nkb; kb += 4) {
                 uint32_t quad;                      // this row's four scale bytes of the slice
@@ -627,18 +669,20 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                 if (!wait_bar(&ctrl.a_empty[a], pha ^ 1, ctrl, p.err_word)) { ok = false; break; }
                 ptx::tc_fence_after();   // the MMA that last read this A slot has completed
                 {
-                    // the slice's token rows (16-row boxes) -> the slot's two 64-wide k-blocks, rows of 128
-                    // bytes, 16-byte chunk c of row n at chunk c ^ (n % 8) (the 128-byte swizzle of the MMA's
-                    // B operand); rows past the tile's tokens are zero-filled without a global read
-                    const int nchunk = (tl.rows + TOK_BOX - 1) / TOK_BOX * TOK_BOX * 16;
-                    uint8_t* slot = smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT;
-                    const int64_t k0 = int64_t(kb) * BK * Cfg<V>::KSUB;
-                    for (int idx = r; idx < nchunk; idx += 128) {
-                        const int n = idx >> 4, sub = (idx >> 3) & 1, c = idx & 7;
-                        const bool valid = n < tl.rows;
-                        const uint16_t* src = p.act + (tl.row0 + (valid ? n : 0)) * p.act_ld + k0 + sub * BK + c * 8;
-                        ptx::cp_async_16(ptx::smem_addr(slot + sub * Cfg<V>::B_SUB + n * (BK * 2) + ((c ^ (n & 7)) << 4)),
-                                         src, valid ? 16u : 0u, pol_keep);
+                    // the slice's token rows -> the slot's two 64-wide k-blocks, rows of 128 bytes, 16-byte chunk
+                    // c of row n at chunk c ^ (n % 8) (the 128-byte swizzle of the MMA's B operand; n % 8 is the
+                    // same for all of this thread's rows); rows past the tile's tokens are zero-filled without a
+                    // global read
+                    const uint32_t dst = ptx::smem_addr(smem + Cfg<V>::TOK_OFF + a * Cfg<V>::TOK_SLOT) + tok_dst;
+                    const uint16_t* src0 = tok0 + int64_t(kb) * BK * Cfg<V>::KSUB;
+#pragma unroll
+                    for (int j = 0; j < Cfg<V>::TOK_SPAN / 8; ++j) {
+                        const int n = n0 + 8 * j;
+                        if (n < nrow16) {
+                            const bool valid = n < tl.rows;
+                            ptx::cp_async_16(dst + uint32_t(j * 8 * BK * 2), valid ? src0 + int64_t(n) * p.act_ld : src0,
+                                             valid ? 16u : 0u, pol_keep);
+                        }
                     }
                 }
                 if (!wait_bar(&ctrl.full[s], ph, ctrl, p.err_word)) {
@@ -646,35 +690,12 @@ __global__ void __launch_bounds__(Cfg<V>::THREADS, 1)
                     ok = false;
                     break;
                 }
-                // the code tile lands 128-byte swizzled: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
                 const uint8_t* row = smem + s * STAGE_BYTES + r * (BK * 2);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t o[32];
-#pragma unroll
-                    for (int b2 = 0; b2 < 2; ++b2) {
-                        const int b = 2 * half + b2;     // scale block of the slice
-                        bool second;                     // the factor 2^120 still to apply (large scales)
-                        const uint32_t f1 = mx_e4m3_factor((quad >> (8 * b)) & 0xFFu, second);
-                        const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * b) ^ (r & 7)) << 4));
-                        const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * b + 1) ^ (r & 7)) << 4));
-                        uint32_t* ob = o + 16 * b2;
-                        dequant4(v0.x, f1, ob[0], ob[1]);
-                        dequant4(v0.y, f1, ob[2], ob[3]);
-                        dequant4(v0.z, f1, ob[4], ob[5]);
-                        dequant4(v0.w, f1, ob[6], ob[7]);
-                        dequant4(v1.x, f1, ob[8], ob[9]);
-                        dequant4(v1.y, f1, ob[10], ob[11]);
-                        dequant4(v1.z, f1, ob[12], ob[13]);
-                        dequant4(v1.w, f1, ob[14], ob[15]);
-                        if (second) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) ob[i] = bf16x2_mul(ob[i], kBf16x2Pow2_120);
-                        }
-                    }
-                    ptx::tmem_st_32x32b_x32(
-                        tmem_base + lane_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS + half * 32), o);
-                }
+                const uint32_t a_cols = tmem_base + lane_base + uint32_t(Cfg<V>::A_TMEM + a * Cfg<V>::A_COLS);
+                if (__any_sync(0xffffffffu, mx_scale_above_134(quad) != 0))
+                    decode_row_slice<true>(row, r, quad, a_cols);
+                else
+                    decode_row_slice<false>(row, r, quad, a_cols);
                 ptx::tmem_st_wait();
                 ptx::cp_async_wait_all();           // this thread's token copies have landed
                 ptx::fence_proxy_async_smem();      // and are visible to the MMA's operand reads

@@ -84,4 +84,17 @@ MOE_DEVICE uint32_t mx_e4m3_factor(uint32_t sc, bool& second) {
 
 constexpr uint32_t kBf16x2Pow2_120 = (247u << 7) | (247u << 23);   // 2^120 in both halves
 
+// Nonzero when a byte (scale code) of `quad` is above 134: its bit 7 set and its low 7 bits at least 7 (the
+// per-byte sums stay below 256, so no carry crosses a byte).
+MOE_DEVICE uint32_t mx_scale_above_134(uint32_t quad) {
+    return ((quad & 0x7F7F7F7Fu) + 0x79797979u) & quad & 0x80808080u;
+}
+
+// mx_e4m3_factor of byte b of a scale word whose codes are all at most 134, from q120 = quad + 0x78787878
+// (sc + 120 in each byte, no carry): byte b placed in bytes 1 and 3, shifted down by one bit, lands in both
+// bf16 exponent fields.
+MOE_DEVICE uint32_t mx_e4m3_factor_small(uint32_t q120, int b) {
+    return __byte_perm(q120, 0u, 0x0404u | (uint32_t(b) << 4) | (uint32_t(b) << 12)) >> 1;
+}
+
 }  // namespace moe

@@ -651,6 +651,61 @@ def test_gemm2_e4m3(moe, impl, shape):
     assert_close(to_f64(y.cpu()), yref, TOL_BF16, f"gemm2 e4m3 {impl}")
 
 
+def _exp_classes(n):
+    """Power-of-two exponents for n weight units or output columns: whole 64-unit blocks at 2^0, 2^30 and 2^48
+    in turn (so some 128-row weight tiles hold ordinary scales only and others large ones), and every fifth unit
+    of the 2^0 blocks at 2^40 (large scale codes next to ordinary ones in one warp)."""
+    s = np.array([0, 30, 48])[(np.arange(n) // 64) % 3]
+    s[(s == 0) & (np.arange(n) % 5 == 2)] = 40
+    return s
+
+
+@pytest.mark.parametrize("shape", [(96, 4, 8, 512, 256), (5, 8, 64, 512, 256)])   # 64- / 32-token tiles
+@pytest.mark.parametrize("impl", ["swap_ab", "simt"])
+@pytest.mark.parametrize("w1_layout", [0, 1])
+def test_e4m3_large_scale_codes(moe, shape, impl, w1_layout):
+    """E8M0 scale codes above 134, for which the decoding's factor 2^(sc-7) leaves bf16's range and is applied as
+    2^(sc-127) then 2^120, beside ordinary codes in the same tiles and warps (the MXFP8 block format, "Cake
+    MegaMoE EP16" FlashInfer PR 5148 analysis, section 2): W1 units and W2 output columns scaled by 2^0, 2^30,
+    2^40 and 2^48 (scale codes about 116 to 164), each class compared with the oracle on its own columns."""
+    T, k, E, K, I = shape
+    w, x, ids, weights = _routed(T, k, E, K, seed=T + 5 * E)
+    wm = wl.scaled(w, I=I, weight="mxfp8")
+    W1 = wl.expert_weights(wm, "W1", 9)
+    units = np.arange(2 * I)
+    units = units % I if w1_layout == 0 else 16 * (units // 32) + units % 16   # the unit of each W1 row
+    s1 = _exp_classes(I)
+    W1 *= torch.from_numpy(2.0 ** s1[units]).float()[None, :, None]
+    W2 = wl.expert_weights(wm, "W2", 9)
+    s2 = _exp_classes(K)
+    W2 *= torch.from_numpy(2.0 ** s2).float()[None, :, None]
+    c1, sc1, rc1, rs1 = _e4m3_weights(moe, W1)
+    c2, sc2, rc2, rs2 = _e4m3_weights(moe, W2)
+    assert rs1.max() > 134 and rs1.min() <= 134 and rs2.max() > 134
+    res = moe.moe_permute_align(torch.from_numpy(ids).to(DEV), E, moe.MOE_LAYOUT_CONTIGUOUS, 1, x=x.to(DEV))
+    h = moe.moe_gemm1_swiglu(res["x_out"], res["counts"], res["offsets"], c1, I, w1_scale=sc1,
+                             w1_layout=w1_layout, impl=_impl(moe, impl))
+    rr = res["route_row"].view(-1).long()
+    href = oracle.expert_gate_up(wl.to_numpy(x)[np.arange(T * k) // k], ids.reshape(-1), rc1, w1_scale=rs1,
+                                 w1_layout=w1_layout)
+    # GEMM 2 on ordinary h rows (h above reaches 2^96, which times 2^48 would leave bf16's range)
+    hsrc = wl._normal((T * k, I), 1.0, 10, "h", 0, "cpu", torch.bfloat16)
+    hperm = torch.zeros((res["rows_cap"], I), dtype=torch.bfloat16, device=DEV)
+    hperm[rr] = hsrc.to(DEV)
+    wt = torch.from_numpy(weights).to(DEV).reshape(-1)
+    y = moe.moe_gemm2(hperm, res["counts"], res["offsets"], c2, T * k, w2_scale=sc2, row_route=res["row_route"],
+                      route_weights=wt, impl=_impl(moe, impl))
+    yref = oracle.expert_down(wl.to_numpy(hsrc), ids.reshape(-1), rc2, w2_scale=rs2)
+    yref = yref * weights.reshape(-1, 1).astype(np.float64)
+    hg, yg = to_f64(h[rr].cpu()), to_f64(y.cpu())
+    for c in np.unique(s1):
+        cols = np.nonzero(s1 == c)[0]
+        assert_close(hg[:, cols], href[:, cols], TOL_BF16, f"gemm1 e4m3 {impl} units at 2^{c}")
+    for c in np.unique(s2):
+        cols = np.nonzero(s2 == c)[0]
+        assert_close(yg[:, cols], yref[:, cols], TOL_BF16, f"gemm2 e4m3 {impl} columns at 2^{c}")
+
+
 MX_SHAPES = E4M3_SHAPES + [(700, 2, 6, 256, 128)]   # + skewed: full, long and short token segments
 
 

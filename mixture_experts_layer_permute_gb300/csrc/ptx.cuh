@@ -83,15 +83,6 @@ MOE_DEVICE uint64_t policy_evict_last() {
     return p;
 }
 
-// Contiguous global -> shared bulk copy (no tensor map) completing on an mbarrier: both addresses 16-byte
-// aligned, bytes a multiple of 16.
-MOE_DEVICE void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
 MOE_DEVICE void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t c0, int32_t c1,
                             uint64_t policy) {
     asm volatile(

@@ -596,9 +596,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
     ws = workload_list(args.workload)
-    if args.experts:
+    if args.experts or args.tokens:
         from mixture_experts_layer_permute_gb300 import workloads as wl
-        ws = [wl.scaled(w, E=args.experts) for w in ws]
+        ws = [wl.scaled(w, E=args.experts or w.E, T=args.tokens or w.T) for w in ws]
     import mixture_experts_layer_permute_gb300 as m
     impl = {"auto": m.MOE_IMPL_AUTO, "tcgen05": m.MOE_IMPL_TCGEN05, "swap_ab": m.MOE_IMPL_TCGEN05_SWAP_AB,
             "pair": m.MOE_IMPL_TCGEN05_PAIR, "mixed": m.MOE_IMPL_TCGEN05_MIXED, "simt": m.MOE_IMPL_SIMT}[args.gemm_impl]
@@ -1003,6 +1003,9 @@ def main():
                          "choice)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: fewer experts than the workload (a small case for ncu)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: another token count than the workload (with --experts, the routed rows "
+                         "per expert of the full workload at a small size)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

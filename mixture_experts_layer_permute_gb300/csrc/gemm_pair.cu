@@ -62,7 +62,7 @@ constexpr int EPI_WARPS = 8;                 // two per TMEM lane quarter, takin
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int EPI_TOK = PSPAN / 2;           // tokens of a tile one epilogue warp handles
 constexpr uint64_t kWaitNs = 2000000000ull;
-static_assert(SMEM + 13 * 1024 + 2 * EPI_WARPS * EPI_TOK * 4 + EPI_WARPS * 1024 <= 227 * 1024,
+static_assert(SMEM + 13 * 1024 + 2 * EPI_WARPS * EPI_TOK * 4 + EPI_WARPS * 1024 + 4 * kMaxExperts <= 227 * 1024,
               "shared memory exceeds the opt-in limit");
 static_assert(2 * ACC_COLS <= TMEM_COLS, "accumulators exceed the TMEM allocation");
 static_assert(SMEM + 13 * 1024 <= 227 * 1024, "stage ring exceeds shared memory");
@@ -129,10 +129,41 @@ struct PTile {
     int nb;         // 256-row weight tile
 };
 
-MOE_DEVICE PTile decode_tile(const ExpertTable& tab, const PairParams& p, int32_t t) {
+// Tile order.  An expert of one token segment streams its weights for a handful of tokens, so its tiles are
+// bound by memory while the segments of a busy expert are bound by the tensor cores.  Listed expert by expert,
+// the single-segment experts (the cold ones, which come last under a skewed routing) would share the last waves
+// and wait on HBM together while earlier waves left it idle, so the order spreads their tiles evenly: tile slot t
+// holds a single-segment tile when floor((t+1) n1 / T) > floor(t n1 / T) (n1 of the T tiles are single-segment),
+// and the two kinds keep expert order among themselves, each multi-segment expert's segments together so that
+// its weight tiles are reused through L2.  `single` is the inclusive prefix of single-segment tiles over experts.
+// Every role of both CTAs decodes the same tile from the same table.
+MOE_DEVICE PTile decode_tile(const ExpertTable& tab, const int32_t* single, int32_t n1, const PairParams& p,
+                             int32_t t) {
+    const int64_t T = tab.total;
+    int lo = 0, hi = p.E - 1;
+    int32_t local;
+    if (n1 == 0 || n1 == T) {   // one kind only (e.g. every batched expert fits a segment): expert order
+        lo = find_expert(tab, p.E, t);
+        local = t - tiles_before(tab, lo);
+    } else if (int32_t(int64_t(t + 1) * n1 / T) > int32_t(int64_t(t) * n1 / T)) {   // a single-segment tile
+        const int32_t b0 = int32_t(int64_t(t) * n1 / T);
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (single[mid] > b0) hi = mid;
+            else lo = mid + 1;
+        }
+        local = b0 - (lo > 0 ? single[lo - 1] : 0);
+    } else {         // the (t - floor(t n1 / T))-th tile of the multi-segment experts
+        const int32_t a = t - int32_t(int64_t(t) * n1 / T);
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (tab.tile_end[mid] - single[mid] > a) hi = mid;
+            else lo = mid + 1;
+        }
+        local = a - (lo > 0 ? tab.tile_end[lo - 1] - single[lo - 1] : 0);
+    }
     PTile tl;
-    tl.e = find_expert(tab, p.E, t);
-    const int32_t local = t - tiles_before(tab, tl.e);
+    tl.e = lo;
     const int32_t seg = local / p.nt;
     tl.nb = local - seg * p.nt;
     tl.row0 = int64_t(tab.start[tl.e]) + int64_t(seg) * PSPAN;
@@ -150,6 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     __shared__ ExpertTable tab;
     __shared__ PairCtrl ctrl;
     __shared__ EpiStage epi;
+    __shared__ int32_t single[kMaxExperts];   // inclusive prefix of single-segment experts' tiles (tile order)
 
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
@@ -181,6 +213,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int nt = p.nt;
     build_expert_table(tab, p.E, p.counts, p.offsets, p.max_tokens, p.rows_cap,
                        [nt](int32_t c) { return ((c + PSPAN - 1) / PSPAN) * nt; });
+    if (warp == 2) {   // one warp scans the single-segment tiles over the experts, 32 at a time
+        int32_t run = 0;
+        for (int e0 = 0; e0 < p.E; e0 += 32) {
+            const int e = e0 + lane;
+            const int32_t c = e < p.E ? tab.count[e] : 0;
+            int32_t v = (c > 0 && c <= PSPAN) ? nt : 0;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t n = __shfl_up_sync(0xffffffffu, v, d);
+                if (lane >= d) v += n;
+            }
+            if (e < p.E) single[e] = run + v;
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::cluster_sync();     // barriers initialised and TMEM allocated in both CTAs before any cross-CTA use
@@ -192,6 +239,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (!pair_ok && threadIdx.x == 0) report(p.err_word, MOE_DEVERR_INTERNAL);
     const int32_t total = pair_ok ? tab.total : 0;
     const int32_t cid = int32_t(ptx::cluster_id_x()), ncl = int32_t(ptx::cluster_count_x());
+    const int32_t n1 = p.E > 0 ? single[p.E - 1] : 0;   // single-segment tiles in all
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
@@ -200,7 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const uint64_t pol = ptx::policy_evict_last();
             uint32_t it = 0;
             for (int32_t t = cid; t < total && !ctrl.abort; t += ncl) {
-                const PTile tl = decode_tile(tab, p, t);
+                const PTile tl = decode_tile(tab, single, n1, p, t);
                 const int n = pair_n(tl.rows);
                 // one 128-row token box per CTA (rows past the tile are never read by the MMA; past the end of
                 // the activations the box is zero-filled): 2 copies per stage and CTA, a constant byte count
@@ -246,7 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const uint32_t issue = lane == 0;
             uint32_t it = 0, tc = 0;
             for (int32_t t = cid; t < total && !ctrl.abort; t += ncl, ++tc) {
-                const PTile tl = decode_tile(tab, p, t);
+                const PTile tl = decode_tile(tab, single, n1, p, t);
                 const int buf = int(tc & 1);
                 const uint32_t aph = (tc >> 1) & 1;
                 if (!__all_sync(0xffffffffu, wait_bar(&ctrl.acc_empty[buf], aph ^ 1, ctrl, p.err_word))) break;
@@ -284,7 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         uint32_t tc = 0;
         for (int32_t t = cid; t < total; t += ncl, ++tc) {
-            const PTile tl = decode_tile(tab, p, t);
+            const PTile tl = decode_tile(tab, single, n1, p, t);
             const int buf = int(tc & 1);
             const uint32_t aph = (tc >> 1) & 1;
             if (!wait_bar(&ctrl.acc_full[buf], aph, ctrl, p.err_word)) break;

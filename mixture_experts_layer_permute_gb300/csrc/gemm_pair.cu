@@ -12,7 +12,9 @@
 // 128-row token tiles padded each expert to a multiple of 128 rows, and a pair of such tiles would pad it to
 // 256 (a fifth of the executed rows on the skewed prefill routing); here about 3 %.  Each weight tile is
 // reused by every 256-token segment of its expert through L2 ("Cake MegaMoE EP16" FlashInfer PR 5148
-// analysis, section 3: weight-tile reuse across an expert's tokens).
+// analysis, section 3: weight-tile reuse across an expert's tokens).  The tiles of experts with a single
+// segment, which stream their weights for few tokens, are spread evenly among the other experts' tiles rather
+// than left to run together at the end (decode_tile).
 //
 // Per CTA, 192 threads:
 //   warp 0      TMA producer: this CTA's 128 weight rows (128-byte swizzled, through the gate/up view for

@@ -45,7 +45,10 @@
 //   positions (sign to bit 15, exponent and mantissa to bits 10..4) give
 //   exactly code * 2^-120 for normal, subnormal and zero codes alike, and one
 //   bf16x2 multiply by 2^(scale-7) restores the value (two multiplies when that
-//   factor would leave bf16's range).  The MMA takes its A operand from TMEM.
+//   factor would leave bf16's range, scale codes above 134: a warp whose slice
+//   has one takes that path for all its rows, so the common slice carries no
+//   per-block test; the four factors of an ordinary scale word are formed at
+//   once).  The MMA takes its A operand from TMEM.
 //   Tokens per tile are capped at 64.  Two warps issue the MMAs, the even and
 //   the odd k slices of a tile, each into its own accumulator, and the
 //   epilogue adds the two: with the converter warps competing for issue slots

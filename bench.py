@@ -358,10 +358,10 @@ def kernel_source_hash(name="gemm_tc.cu"):
 def recorded_traffic(workload, fused=False, tiled=False):
     """GEMM 1 DRAM bytes per launch from the committed ncu summary, if taken on this kernel source.
 
-    profiles/gemm_{tc,mx}_traffic_<workload>.txt holds `source <file>`, `source_sha <hash>` (or the older
+    profiles/gemm_{tc,mx,pair}_traffic_<workload>.txt holds `source <file>`, `source_sha <hash>` (or the older
     `gemm_tc_sha`), `workload` and `gemm1_traffic_bytes` lines."""
     tag = "decode_sweep" if workload == "decode" else workload
-    for kind in ("tc", "mx"):
+    for kind in ("tc", "mx", "pair"):
         p = os.path.join(ROOT, "profiles", f"gemm_{kind}_traffic_{tag}.txt")
         fields = {}
         try:

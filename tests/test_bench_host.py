@@ -19,6 +19,16 @@ def test_decode_traffic_record_matches_its_plan_only():
     assert bench.recorded_traffic("prefill", fused=False, tiled=False) is None
 
 
+def test_config_traffic_records_match_their_plans_only():
+    # one record per configuration the bench times on a kernel it has a record for: the tiled GEMM 1 of each
+    for name in ("prefill", "mxfp8", "mxfp8_act", "batched", "batched_tokens"):
+        rec = bench.recorded_traffic(name, fused=False, tiled=True)
+        assert rec is not None and len(rec) == 1 and rec[0] > 0, name
+        assert bench.recorded_traffic(name, fused=False, tiled=False) is None, name
+        assert bench.recorded_traffic(name, fused=True, tiled=True) is None, name
+    assert bench.recorded_traffic("tiny", fused=False, tiled=False) is None
+
+
 def _copy_with_gemm_tc(tmp_path, monkeypatch, extra):
     # a copy of the repository layout whose gemm_tc.cu has `extra` appended
     src = os.path.join(ROOT, "mixture_experts_layer_permute_gb300", "csrc", "gemm_tc.cu")

@@ -397,6 +397,42 @@ def test_mxfp8_dequantize_matches_torch(oracle_mod):
     assert np.array_equal(got, _torch_dequant(codes, scales).numpy())
 
 
+@pytest.mark.parametrize("w1_layout", [0, 1])
+def test_expert_gemms_decode_every_scale_code(oracle_mod, w1_layout):
+    """The oracle's W1 and W2 products on E4M3 codes with E8M0 scale codes drawn over the whole range 0..254 (the
+    MXFP8 block format, "Cake MegaMoE EP16" FlashInfer PR 5148 analysis, section 2: value = code x 2^(scale-127)),
+    against a dense fp64 product of the weights decoded by torch's float8_e4m3fn and ldexp: every block's factor,
+    from 2^-127 to 2^127, reaches the sums the GPU tests compare with."""
+    g = torch.Generator().manual_seed(23)
+    E, K, I, n = 2, 96, 32, 5
+    c1 = torch.randint(0, 256, (E, 2 * I, K), generator=g, dtype=torch.int32)
+    c1[(c1 & 0x7F) == 0x7F] = 0x31                         # no NaN codes
+    c1 = c1.to(torch.uint8).numpy()
+    s1 = torch.randint(0, 255, (E, 2 * I, K // 32), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    c2 = torch.randint(0, 256, (E, K, I), generator=g, dtype=torch.int32)
+    c2[(c2 & 0x7F) == 0x7F] = 0x2C
+    c2 = c2.to(torch.uint8).numpy()
+    s2 = torch.randint(0, 255, (E, K, I // 32), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    assert s1.min() < 7 and s1.max() > 240                  # both ends of the factor range
+    x = torch.randn((n, K), generator=g, dtype=torch.float64)
+    ids = np.array([0, 1, 1, 0, 1], np.int32)
+    h = oracle_mod.expert_gate_up(x.numpy(), ids, c1, w1_scale=s1, w1_layout=w1_layout)
+    D1 = _torch_dequant(c1, s1)
+    units = np.arange(2 * I)
+    gate_rows = units[:I] if w1_layout == 0 else np.array([32 * (u // 16) + u % 16 for u in range(I)])
+    up_rows = units[I:] if w1_layout == 0 else gate_rows + 16
+    for r in range(n):
+        e = int(ids[r])
+        ref = F.silu(D1[e, gate_rows] @ x[r]) * (D1[e, up_rows] @ x[r])
+        assert np.allclose(h[r], ref.numpy(), rtol=1e-12, atol=0), r
+    hin = torch.randn((n, I), generator=g, dtype=torch.float64)
+    y = oracle_mod.expert_down(hin.numpy(), ids, c2, w2_scale=s2)
+    D2 = _torch_dequant(c2, s2)
+    for r in range(n):
+        ref = D2[int(ids[r])] @ hin[r]
+        assert np.allclose(y[r], ref.numpy(), rtol=1e-12, atol=0), r
+
+
 def test_quantised_activations_and_bf16_intermediate(oracle_mod):
     """quant_x: each x row MXFP8 round-tripped before W1; quant_h="bf16": h rounded to bf16, then round-tripped
     before W2 -- against torch fp64 matmuls with the round trips written out (torch float8 casts)."""

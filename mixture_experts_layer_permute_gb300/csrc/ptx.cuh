@@ -19,14 +19,6 @@ MOE_DEVICE uint64_t globaltimer() {
     return t;
 }
 
-MOE_DEVICE bool elect_one() {
-    uint32_t pred = 0;
-    asm volatile(
-        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(pred));
-    return pred != 0;
-}
-
 // ---- mbarrier ----
 MOE_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
@@ -152,26 +144,6 @@ MOE_DEVICE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {   // whole warp
 MOE_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MOE_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16/fp16 in, fp32 accumulate).
-MOE_DEVICE void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A is M rows in TMEM lanes, K packed two
-// 16-bit values per 32-bit column (8 columns per 16-element k step).
-MOE_DEVICE void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                               uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // D[tmem] (+)= (A * 2^(SFA-127)) * (B * 2^(SFB-127))^T, kind::mxf8f6f4 with one E8M0 scale per 32 along K
 // (scale_vec::1X): A and B E4M3 in shared memory (descriptors), K = 32 per instruction.  The scale factors
 // sit in TMEM at sfa_tmem / sfb_tmem; the byte of each 32-bit column used by this instruction is the
@@ -196,6 +168,7 @@ MOE_DEVICE void mma_commit(uint64_t* bar) {
 // and only the lane with `issue` != 0 executes the instruction (predicated, no branch).  Always pass the same
 // lane: a commit tracks the MMAs issued by its own thread.  On GB300 an M=128, K=16, N<=128 MMA issued this
 // way took about 29 ns against 50 ns from a loop that only lane 0 runs.
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16/fp16 in, fp32 accumulate).
 MOE_DEVICE void mma_f16_by(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                            uint32_t accumulate) {
     asm volatile(
@@ -205,6 +178,8 @@ MOE_DEVICE void mma_f16_by(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A is M rows in TMEM lanes, K packed two
+// 16-bit values per 32-bit column (8 columns per 16-element k step).
 MOE_DEVICE void mma_f16_tmem_a_by(uint32_t issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                   uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -279,13 +254,6 @@ MOE_DEVICE void tmem_st_32x32b_x4(uint32_t taddr, uint32_t r0, uint32_t r1, uint
                  : "memory");
 }
 
-// 32 lanes x 8 consecutive 32-bit columns: thread i writes columns [col, col+8) of lane (base + i).
-MOE_DEVICE void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-
 // 32 lanes x 32 consecutive 32-bit columns: thread i writes columns [col, col+32) of lane (base + i).
 MOE_DEVICE void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -296,16 +264,6 @@ MOE_DEVICE void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit columns: thread i writes columns [col, col+16) of lane (base + i).
-MOE_DEVICE void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
@@ -406,20 +364,10 @@ MOE_DEVICE void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// Warp-wide pair forms (see mma_f16_by): every lane runs them, only the lane with `issue` != 0 executes.
 // D[tmem] (+)= A * B^T over the CTA pair, kind::f16: A's M = 256 rows are 128 in each CTA's shared memory and
 // B's N rows are N/2 in each, at the same offsets as the descriptors give in the issuing CTA; each CTA's TMEM
 // holds its 128 rows of D.  Issued by one thread of the pair.
-MOE_DEVICE void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on the mbarrier at the same shared-memory offset in every CTA of `cta_mask` when all tcgen05.mma
-// issued by this thread have completed.
-// Warp-wide pair forms (see mma_f16_by): every lane runs them, only the lane with `issue` != 0 executes.
 MOE_DEVICE void mma_f16_pair_by(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                 uint32_t accumulate) {
     asm volatile(
@@ -428,18 +376,13 @@ MOE_DEVICE void mma_f16_pair_by(uint32_t issue, uint32_t d_tmem, uint64_t a_desc
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
         : "memory");
 }
+// Arrive once on the mbarrier at the same shared-memory offset in every CTA of `cta_mask` when all tcgen05.mma
+// issued by this thread have completed.
 MOE_DEVICE void mma_commit_pair_by(uint32_t issue, uint64_t* bar, uint16_t cta_mask) {
     asm volatile(
         "{\n .reg .pred i;\n setp.ne.b32 i, %2, 0;\n"
         " @i tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}\n"
         ::"r"(smem_addr(bar)), "h"(cta_mask), "r"(issue)
-        : "memory");
-}
-MOE_DEVICE void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_addr(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 
